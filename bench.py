@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the int4 routed-expert MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl coli|reference]
+
+A step is one pass of the whole layer (prep + router/top-K/union + gate/up SwiGLU + down/combine)
+over one batch of synthetic tokens that already sit in HBM; the token changes every step (a pool
+of 4096 seeded tokens), and L2 is flushed between steps by writing a 256 MB buffer, so expert
+weights always come from HBM.  Each step is timed with CUDA events on the stream the kernels run
+on; the per-kernel events give the roofline of the dominant kernel (gate/up).  With --gpus N under
+torchrun every rank runs its own replica on its own tokens (weak scaling, no collective on the
+data path) and the slowest rank's time is used.  Prints one JSON line.
+
+--impl reference times the plain CPU oracle (oracle/) on the host cores instead, on the same
+workload and metric; each of its steps is one token with the expert rows sampled so the whole
+run stays within a few minutes.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gen import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and int4 expert-weight GB/s as % of GB300 HBM peak"
+POOL = 4096
+FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--workload", default="glm_decode_t1", choices=sorted(W.WORKLOADS))
+    p.add_argument("--impl", default="coli", choices=["coli", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--reference-budget", type=float, default=150.0,
+                   help="seconds the reference arm may spend on its timed steps")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ bytes and peaks --------
+
+def expert_bytes(wl, n_union_total):
+    """nibbles + f32 row scales read per forward (union experts incl. the shared one)"""
+    return n_union_total * wl.expert_bytes
+
+
+def gateup_bytes(wl, n_union_total):
+    return n_union_total * (wl.f * wl.d + 8 * wl.f)
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM, "fallback"
+
+
+def recorded_traffic(kernel, workload):
+    """per-launch DRAM bytes from the committed ncu summary of this kernel, if it is current"""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(f"{kernel}:{workload}")
+    except Exception:
+        return None
+    if not rec:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "int4_routed_expert_quantize_gb300", "csrc", rec["source"])
+    with open(src, "rb") as fh:
+        digest = hashlib.sha256(fh.read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if digest == rec["source_sha256_16"] else None
+
+
+# ------------------------------------------------------------------ distributed ------------
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value, world):
+    """slowest rank's value (host-side timing collective only)"""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks -----------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for ln in fh:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle -------------
+
+def oracle_layer(wl, layer=0):
+    from oracle import oracle as O
+    return O.Layer(wl, layer)
+
+
+def oracle_sample_step(OL, x_tok, phi):
+    """One token through the oracle with a fraction phi of every expert's rows: full router,
+    top-K and union; gate/up on the first phi*f rows (the rest of h is zero), h re-quantised,
+    down on the first phi*d rows; combine in rank order.  phi = 1 is the whole layer."""
+    import numpy as np
+
+    from oracle import oracle as O
+    wl = OL.wl
+    if phi >= 1.0:
+        return OL.forward(x_tok, want_dump=False, want_y64=False)["y"]
+    d, f = wl.d, wl.f
+    xn, ids, w = O.route_only(wl, x_tok, OL.Wr, OL.bias, OL.gamma)
+    fr = max(32, int(round(phi * f / 32)) * 32)
+    dr = max(1, int(round(phi * d)))
+    y = np.zeros((x_tok.shape[0], dr), dtype=np.float32)
+    for t in range(x_tok.shape[0]):
+        qx, dx = O.quantize_q8(xn[t])
+        experts = ([(wl.E, 1.0)] if wl.n_shared else []) + list(zip(ids[t], w[t]))
+        for k, (ex, wk) in enumerate(experts):
+            rec, sc = OL.recs[int(ex)]
+            Wg = rec[: f * d // 2].reshape(f, d // 2)
+            Wu = rec[f * d // 2: f * d].reshape(f, d // 2)
+            Wd = rec[f * d:].reshape(d, f // 2)
+            g, _ = O.i4_matvec(np.ascontiguousarray(Wg[:fr]), np.ascontiguousarray(sc[:fr]), d, qx, dx)
+            u, _ = O.i4_matvec(np.ascontiguousarray(Wu[:fr]), np.ascontiguousarray(sc[f:f + fr]), d, qx, dx)
+            h = np.zeros(f, dtype=np.float32)
+            h[:fr] = [O.lib().orc_silu_mul(float(a), float(b)) for a, b in zip(g, u)]
+            qh, dh = O.quantize_q8(h)
+            e, _ = O.i4_matvec(np.ascontiguousarray(Wd[:dr]), np.ascontiguousarray(sc[2 * f:2 * f + dr]),
+                               f, qh, dh)
+            y[t] = e if k == 0 else (np.float32(wk) * e + y[t])
+    return y
+
+
+def cpu_baseline(wl, seconds):
+    """the oracle as it stands, whole layer per token, on a bounded sample of tokens"""
+    from oracle import oracle as O
+    OL = oracle_layer(wl)
+    ntok = 2
+    x = W.x_host(wl, 64 * wl.T)
+    # generate the experts of the candidate sample outside the timing
+    _, ids, _ = O.route_only(wl, x[: 16 * wl.T], OL.Wr, OL.bias, OL.gamma)
+    OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        OL.forward(x[done * wl.T:(done + 1) * wl.T], want_dump=False, want_y64=False)
+        done += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and done >= ntok) or done >= 16:
+            break
+    return {"value": done * wl.T / el, "unit": "tokens/s", "cores": O.lib().orc_num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} batches of T={wl.T} token(s) of {wl.name} through the full layer "
+                      f"(experts pre-generated), {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return None
+    from oracle import oracle as O
+    wl = W.WORKLOADS[args.workload]
+    if wl.layers > 1:
+        wl = W.WORKLOADS["glm_decode_t1"] if wl.d == 6144 else wl
+    OL = oracle_layer(wl)
+    x = W.x_host(wl, 64 * wl.T)
+    _, ids, _ = O.route_only(wl, x, OL.Wr, OL.bias, OL.gamma)
+    OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
+    # size the per-step sample: a full token if it fits the budget, else a row fraction
+    t0 = time.perf_counter()
+    oracle_sample_step(OL, x[: wl.T], 1.0)
+    full = time.perf_counter() - t0
+    phi = min(1.0, args.reference_budget / max(1, args.steps + args.warmup) / max(full, 1e-6))
+    phi = max(phi, 1.0 / 64)
+    for i in range(args.warmup):
+        j = i % 64
+        oracle_sample_step(OL, x[j * wl.T:(j + 1) * wl.T], phi)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        j = i % 64
+        oracle_sample_step(OL, x[j * wl.T:(j + 1) * wl.T], phi)
+    el = time.perf_counter() - t0
+    value = args.steps * wl.T * phi / el
+    cores = O.lib().orc_num_threads()
+    sample = (f"one batch of T={wl.T} of {wl.name} per step with {phi:.4f} of every expert's rows "
+              f"(full router and union); tokens/s scaled by that fraction")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "i4xi8->i32,f32", "data": "synthetic",
+            "config": {"workload": wl.name, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
+                       "n_shared": wl.n_shared, "T": wl.T, "layers": 1},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ GPU arm ----------------
+
+def run_coli(args):
+    import torch
+
+    from int4_routed_expert_quantize_gb300 import coli, synthetic
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_index = torch.cuda.current_device()
+    wl = W.WORKLOADS[args.workload]
+    T = wl.T
+    layers = [synthetic.build_layer(wl, layer=l, max_tokens=T) for l in range(wl.layers)]
+    stacked = wl.layers > 1
+    pool = synthetic.x_tokens(wl, POOL * T, token0=rank * POOL * T).view(POOL, T, wl.d)
+    y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+    xs = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")  # stack works in place
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i, evs):
+        flush.fill_(float(i & 1023))
+        if stacked:
+            xs.copy_(pool[i % POOL])
+            evs[0].record(stream)
+            coli.stack_forward(layers, xs)
+            evs[4].record(stream)
+        else:
+            layers[0].forward_profiled(pool[i % POOL], y, evs)
+
+    n_ev = 5
+    for i in range(args.warmup):
+        step(i, [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)])
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev_index) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i, events[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    for L in layers:
+        st = L.status()
+        if st != 0:
+            raise RuntimeError(f"device status {st}")
+    fwd_ms = [ev[0].elapsed_time(ev[4]) for ev in events]
+    mean_fwd_ms = statistics.fmean(fwd_ms)
+    total_fwd_s = reduce_max(sum(fwd_ms) / 1000.0, world)
+    tokens = world * args.steps * T
+    value = tokens / total_fwd_s
+    n_union = None
+    gu_ms = dn_ms = None
+    if not stacked:
+        gu_ms = statistics.fmean(ev[2].elapsed_time(ev[3]) for ev in events)
+        dn_ms = statistics.fmean(ev[3].elapsed_time(ev[4]) for ev in events)
+        rt_ms = statistics.fmean(ev[1].elapsed_time(ev[2]) for ev in events)
+        pp_ms = statistics.fmean(ev[0].elapsed_time(ev[1]) for ev in events)
+    # union size of each step (T=1: always K+1); averaged over the pool for T>1
+    if T == 1:
+        n_union = wl.K + wl.n_shared
+    else:
+        sizes = []
+        for i in range(min(args.steps, 256)):
+            dmp = layers[0].forward_debug(pool[i % POOL])
+            sizes.append(int(dmp["n_union"].item()))
+        n_union = statistics.fmean(sizes)
+    ebytes = expert_bytes(wl, n_union) * wl.layers
+    peak, peak_kind = hbm_peak()
+    mean_s = total_fwd_s / (args.steps)
+    expert_gbs = ebytes / mean_s / 1e9
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_fwd_ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "i4xi8->i32,f32", "data": "synthetic",
+           "config": {"workload": wl.name, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
+                      "n_shared": wl.n_shared, "T": T, "layers": wl.layers,
+                      "resident_expert_gb": round(wl.layers * (wl.E + wl.n_shared) * wl.expert_bytes / 1e9, 2),
+                      "l2": "flushed between steps (256 MB write, outside the timed events)",
+                      "tokens": f"pool of {POOL} seeded batches, one per step"},
+           "expert_bytes_per_step": ebytes, "mean_union_experts": n_union,
+           "expert_gbs": expert_gbs, "expert_hbm_frac": expert_gbs / peak,
+           "wall_s": wall, "gpu_launches": 4 * wl.layers * args.steps}
+    if not stacked:
+        gb = gateup_bytes(wl, n_union)
+        ach = gb / (gu_ms / 1000.0) / 1e9
+        out["roofline"] = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": ach,
+                           "peak": peak, "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                           "frac": ach / peak, "algorithmic_bytes": gb,
+                           "traffic": recorded_traffic("gateup_decode_kernel", wl.name)}
+        out["kernel_ms"] = {"prep": pp_ms, "router": rt_ms, "gateup": gu_ms, "down": dn_ms}
+        out["down_gbs"] = expert_bytes(wl, n_union) * (wl.d * wl.f // 2 + 4 * wl.d) / wl.expert_bytes / (dn_ms / 1000.0) / 1e9
+    if clk:
+        out["clocks"] = clk
+    # end to end through the host-buffer entry point (pinned buffers, copies in the region)
+    if not args.no_e2e and not stacked:
+        xh = pool[:64].cpu().pin_memory()
+        yh = torch.empty((T, wl.d), dtype=torch.float32).pin_memory()
+        n_e2e = min(args.steps, 2000)
+        for i in range(20):
+            layers[0].forward_host(xh[i % 64], yh)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            layers[0].forward_host(xh[i % 64], yh)
+        el = reduce_max(time.perf_counter() - t0, world)
+        out["e2e"] = {"value": world * n_e2e * T / el, "unit": "tokens/s",
+                      "h2d_bytes_per_step": T * wl.d * 4, "d2h_bytes_per_step": T * wl.d * 4,
+                      "steps": n_e2e, "note": "coli_moe_forward_host: H2D x, forward, D2H y, sync"}
+    elif not args.no_e2e and stacked:
+        xh = pool[:64].cpu().pin_memory()
+        n_e2e = min(args.steps, 500)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            xs.copy_(xh[i % 64], non_blocking=True)
+            coli.stack_forward(layers, xs)
+            yh = xs.to("cpu")
+        el = reduce_max(time.perf_counter() - t0, world)
+        out["e2e"] = {"value": world * n_e2e * T / el, "unit": "tokens/s",
+                      "h2d_bytes_per_step": T * wl.d * 4, "d2h_bytes_per_step": T * wl.d * 4,
+                      "steps": n_e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl if not stacked else W.WORKLOADS["glm_decode_t1"],
+                                           args.cpu_seconds)
+        if stacked:
+            out["cpu_baseline"]["value"] /= wl.layers
+            out["cpu_baseline"]["sample"] += f"; divided by {wl.layers} layers per token"
+    for L in layers:
+        L.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    out = run_reference(args) if args.impl == "reference" else run_coli(args)
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

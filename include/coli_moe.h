@@ -1,0 +1,167 @@
+/* coli_moe -- one int4 routed-expert MoE layer on an NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The layer is the MoE step of a GLM-5.2-style decoder as the colibrì pages describe it
+ * ("colibrì 架构概述" §5, the moe step of each layer; §3.1 int4 experts and the IDOT integer
+ * dot path; the colibrì README "絕不為同一次硬碟讀取等待兩遍" for the batch union):
+ *
+ *   x_n  = RMSNorm(x)                    (only with has_norm; then y = x + MoE(x_n))
+ *   q8   = int8 blocks of 32 of x_n      (Q8_0-style: d = max|x|/127, q = round(x/d))
+ *   route: logits = W_r x_n (fp32), score = sigmoid(logit), top-K by score + bias
+ *          (bias selects only; ties go to the lower expert id), w_k = score_k / sum(score)
+ *   union: the T*K (token, expert) pairs grouped by expert so each distinct expert's
+ *          weights are read once per call; the shared expert (id E) takes every token
+ *   expert: g = W_g x, u = W_u x (int4 weights x int8 codes, int32 block dots, per-row f32
+ *          scale, per-block activation scale), h = SiLU(g) * u, h re-quantised to int8
+ *          blocks of 32, e = W_d h
+ *   combine: y_t = e(shared, t), then y_t = fma(w_{t,k}, e(t,k), y_t) for k = 0..K-1
+ *
+ * All fp32 steps follow one canonical order of operations (fma chains over 32 contiguous
+ * groups, then a pairwise tree; an own exp), so results are reproducible bit for bit and a
+ * token's output does not depend on the batch it is in.
+ *
+ * Formats.  An expert record is [gate f x d | up f x d | down d x f] int4 nibbles, row
+ * major, two's complement, element 2i in the low nibble of byte i of its row, followed by
+ * the f32 row scales [s_gate (f) | s_up (f) | s_down (d)] ("colibrì 架构概述" §3.1: two
+ * 4-bit values per byte, one f32 scale per row; README: the three matrices of an expert
+ * are stored next to each other).  The library repacks records into its own device layout
+ * at load time; the weights are never expanded to floats.
+ *
+ * Conventions.  Every call returns COLI_OK (0) or a negative COLI_E* status; nothing aborts,
+ * throws or traps.  Pointers named *_dev are device pointers owned by the caller; the
+ * library owns everything it allocates in coli_moe_create and frees it in coli_moe_destroy.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  Calls on one handle must not
+ * overlap in time (they share its workspace).  All calls use the CUDA device that is
+ * current on the calling thread; it must be the device the handle was created on.
+ */
+#ifndef COLI_MOE_H
+#define COLI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define COLI_OK 0
+#define COLI_EINVAL (-1)       /* bad argument (NULL pointer, size out of range, ...)      */
+#define COLI_ENOMEM (-2)       /* device or host allocation failed                         */
+#define COLI_ESTATE (-3)       /* call out of order (e.g. forward before weights loaded)   */
+#define COLI_ECUDA (-4)        /* a CUDA runtime call or kernel launch failed              */
+#define COLI_ETIMEOUT (-5)     /* a bounded device-side wait gave up (see coli_moe_status) */
+#define COLI_EUNSUPPORTED (-6) /* shape the kernels do not cover (see coli_moe_create)     */
+
+typedef struct coli_moe coli_moe; /* opaque; owned by the library */
+
+typedef struct {
+  int d;            /* model width; multiple of 128, d/32 divisible by ceil(d/1024), <= 16384 */
+  int f;            /* expert hidden width (routed and shared); same rules as d              */
+  int n_experts;    /* E routed experts, 1..1024                                              */
+  int top_k;        /* K experts per token, 1..min(E, 32)                                      */
+  int n_shared;     /* 0 or 1 always-on shared expert (id E), weight 1                        */
+  int qblock;       /* activation block length; must be 32                                    */
+  int max_tokens;   /* largest T accepted by forward; workspace is sized for it, 1..4096      */
+  float routed_scale; /* multiplies every routing weight (1.0 = plain renormalisation)       */
+  float rms_eps;    /* RMSNorm epsilon (used only with has_norm)                               */
+  int has_norm;     /* 1: forward computes y = x + MoE(RMSNorm(x)) with the loaded gamma      */
+} coli_moe_config;
+
+/* Optional per-step outputs of coli_moe_forward_debug.  Device pointers owned by the caller;
+ * NULL entries are skipped.  P = T*K + n_shared*T pairs, ordered as in the batch union. */
+typedef struct {
+  float* xn;          /* [T,d]   layer input after RMSNorm (copy of x without norm)       */
+  int8_t* qx;         /* [T,d]   activation q8 codes                                      */
+  float* dx;          /* [T,d/32] activation block scales                                  */
+  float* logits;      /* [T,E]                                                             */
+  float* scores;      /* [T,E]   sigmoid(logits)                                           */
+  int32_t* ids;       /* [T,K]   selected experts, rank order                              */
+  float* w;           /* [T,K]   routing weights                                           */
+  int32_t* n_union;   /* [1]     union slots (distinct routed experts + shared)            */
+  int32_t* union_ids; /* [E+1]   expert id per union slot, ascending, shared (= E) last     */
+  int32_t* offsets;   /* [E+2]   first pair of each union slot; offsets[n_union] = P        */
+  int32_t* pair_token;/* [P]     token of each pair                                        */
+  int32_t* pair_rank; /* [P]     k of each pair (-1 for the shared expert)                 */
+  int32_t* inv;       /* [T,K]   pair index of (t, ids[t,k])                               */
+  float* g;           /* [P,f]   gate projection                                           */
+  float* u;           /* [P,f]   up projection                                             */
+  float* h;           /* [P,f]   SiLU(g)*u                                                 */
+  int8_t* qh;         /* [P,f]   h q8 codes                                                */
+  float* dh;          /* [P,f/32] h block scales                                           */
+  float* e;           /* [P,d]   expert outputs                                            */
+  int32_t* Ag;        /* [P,f,d/32] int32 block dots of the gate projection                */
+  int32_t* Au;        /* [P,f,d/32] up                                                     */
+  int32_t* Ad;        /* [P,d,f/32] down                                                   */
+} coli_moe_dump;
+
+/* Validates cfg and allocates, on the current device, the expert store ((E+n_shared) expert
+ * records in the library's layout), the router and the workspace for max_tokens.
+ * EINVAL: bad cfg or out == NULL.  EUNSUPPORTED: a shape rule above is broken.  ENOMEM.
+ * ECUDA: no usable device.  On error *out is left NULL. */
+int coli_moe_create(const coli_moe_config* cfg, coli_moe** out);
+
+/* Frees everything the handle owns (synchronises the device first).  NULL is a no-op. */
+void coli_moe_destroy(coli_moe* h);
+
+/* Copies the router W_r [E,d] (fp32, row major), the optional selection bias [E] and, for
+ * has_norm, the RMSNorm gamma [d] into the handle.  Host or device pointers.  Returns when
+ * the copies are complete on `stream`.  EINVAL: NULL W_r, or gamma NULL while has_norm. */
+int coli_moe_load_router(coli_moe* h, const float* W_r, const float* bias, const float* gamma,
+                         void* stream);
+
+/* Loads `count` consecutive expert records, ids first..first+count-1 (id E = the shared
+ * expert), from `packed` (count records of 3*d*f/2 bytes, format above) and `scales` (count
+ * records of 2f+d floats).  Host or device pointers; repacked on the device.  The host
+ * buffers may be freed on return (the call synchronises `stream`).  EINVAL: ids out of range. */
+int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* packed,
+                          const float* scales, void* stream);
+
+/* y_dev[T,d] = layer(x_dev[T,d]), asynchronous on `stream`, no host synchronisation and no
+ * allocation (safe to capture in a CUDA graph).  T == 0 is a no-op.  x_dev may equal y_dev
+ * only with has_norm (residual update in place).  EINVAL: T < 0 or T > max_tokens, NULL
+ * pointers, forbidden aliasing.  ESTATE: router or some expert not loaded yet. */
+int coli_moe_forward(coli_moe* h, const float* x_dev, int T, float* y_dev, void* stream);
+
+/* coli_moe_forward plus the intermediates selected in `dump` (slower; for verification). */
+int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
+                           const coli_moe_dump* dump, void* stream);
+
+/* coli_moe_forward that also records `events[0..4]` (cudaEvent_t handles created by the
+ * caller) on `stream`: before the prep kernel, then after prep, after the router, after the
+ * gate/up kernel and after the down kernel -- so the caller can time each launch.
+ * T <= 4 (one launch of each kernel).  EINVAL: n_events < 5 or T out of range. */
+int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
+                              void* const* events, int n_events, void* stream);
+
+/* Host-buffer form: copies x_host [T,d] to the device, runs forward, copies y back to
+ * y_host [T,d] and synchronises `stream`.  Pinned host memory gives the fastest copies. */
+int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host, void* stream);
+
+/* Runs n_layers has_norm layers in sequence on x_dev [T,d] in place:
+ * x <- x + MoE_l(RMSNorm_l(x)) for l = 0..n_layers-1.  Asynchronous on `stream`. */
+int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, int T,
+                           void* stream);
+
+/* Device status word of the handle: COLI_OK, or COLI_ETIMEOUT if a bounded device-side wait
+ * of an earlier forward gave up (the word is then cleared).  Synchronises `stream`. */
+int coli_moe_status(coli_moe* h, void* stream);
+
+/* Bytes of one expert record in the canonical format (3*d*f/2 + 4*(2f+d)). */
+int64_t coli_moe_expert_record_bytes(int d, int f);
+
+/* Standalone pack of fp32 rows into the canonical int4 format ("colibrì 架构概述" §3.1):
+ * s[r] = max|w[r,:]|/7, q = round(w/s) clamped to [-7,7], two nibbles per byte.
+ * w_dev [rows,cols] -> packed_dev [rows,cols/2], scales_dev [rows].  cols even, <= 65536. */
+int coli_quantize_i4_rows(const float* w_dev, int64_t rows, int cols, uint8_t* packed_dev,
+                          float* scales_dev, void* stream);
+
+/* Standalone Q8_0-style activation quantisation: blocks of 32, d = max|x|/127,
+ * q = round(x/d).  x_dev [n] -> q_dev [n], d_dev [n/32]; n a multiple of 32. */
+int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_dev,
+                         void* stream);
+
+const char* coli_moe_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLI_MOE_H */

@@ -1,0 +1,37 @@
+"""Build of libcoli_moe.so: nvcc for sm_103a, one object per source compiled in parallel."""
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+SO = os.path.join(PKG, "libcoli_moe.so")
+SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "runtime.cu"]
+
+
+def nvcc_flags(arch="sm_103a"):
+    cc = arch.split("_")[1]
+    return ["-O3", "-std=c++17", f"-gencode=arch=compute_{cc},code={arch}", "-lineinfo",
+            "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+
+
+def build(arch="sm_103a", verbose=False, extra=()):
+    os.makedirs(BUILD, exist_ok=True)
+    flags = nvcc_flags(arch) + list(extra)
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        cmd = ["nvcc"] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            print(" ".join(cmd))
+        subprocess.check_call(cmd)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    subprocess.check_call(["nvcc", "-shared", "-cudart", "static", "-Xlinker",
+                           "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", SO] + objs)
+    return SO

@@ -1,0 +1,211 @@
+"""Thin ctypes binding of libcoli_moe.so (include/coli_moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.  If the shared library is missing the import of
+`lib()` raises: there is no CPU fallback.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+from . import _build
+
+_i, _f, _vp, _i64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int64
+
+STATUS = {0: "COLI_OK", -1: "COLI_EINVAL", -2: "COLI_ENOMEM", -3: "COLI_ESTATE", -4: "COLI_ECUDA",
+          -5: "COLI_ETIMEOUT", -6: "COLI_EUNSUPPORTED"}
+HEADER = os.path.join(_build.INCLUDE, "coli_moe.h")
+
+
+class ColiError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({lib().coli_moe_strerror(status).decode()})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("d", _i), ("f", _i), ("n_experts", _i), ("top_k", _i), ("n_shared", _i),
+                ("qblock", _i), ("max_tokens", _i), ("routed_scale", _f), ("rms_eps", _f),
+                ("has_norm", _i)]
+
+
+DUMP_FIELDS = ["xn", "qx", "dx", "logits", "scores", "ids", "w", "n_union", "union_ids", "offsets",
+               "pair_token", "pair_rank", "inv", "g", "u", "h", "qh", "dh", "e", "Ag", "Au", "Ad"]
+
+
+class Dump(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in DUMP_FIELDS]
+
+
+_lib = None
+
+
+def header_functions():
+    """names of the functions include/coli_moe.h declares"""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(coli_\w+)\s*\(", text, re.M)))
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.SO):
+            raise RuntimeError(f"{_build.SO} is missing: build the CUDA extension first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(_build.SO)
+        L.coli_moe_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(_vp)]
+        L.coli_moe_destroy.argtypes = [_vp]
+        L.coli_moe_destroy.restype = None
+        L.coli_moe_load_router.argtypes = [_vp, _vp, _vp, _vp, _vp]
+        L.coli_moe_load_experts.argtypes = [_vp, _i, _i, _vp, _vp, _vp]
+        L.coli_moe_forward.argtypes = [_vp, _vp, _i, _vp, _vp]
+        L.coli_moe_forward_debug.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(Dump), _vp]
+        L.coli_moe_forward_host.argtypes = [_vp, _vp, _i, _vp, _vp]
+        L.coli_moe_forward_profiled.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(_vp), _i, _vp]
+        L.coli_moe_stack_forward.argtypes = [ctypes.POINTER(_vp), _i, _vp, _i, _vp]
+        L.coli_moe_status.argtypes = [_vp, _vp]
+        L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
+        L.coli_moe_expert_record_bytes.restype = _i64
+        L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
+        L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
+        L.coli_moe_strerror.argtypes = [_i]
+        L.coli_moe_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise ColiError(rc, where)
+
+
+def _ptr(a):
+    """device or host address of a torch tensor / numpy array (None -> NULL)"""
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        assert a.is_contiguous()
+        return a.data_ptr()
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else stream
+
+
+def expert_record_bytes(d, f):
+    return int(lib().coli_moe_expert_record_bytes(d, f))
+
+
+class MoeLayer:
+    """One int4 routed-expert MoE layer resident on the current CUDA device."""
+
+    def __init__(self, d, f, n_experts, top_k, n_shared=1, max_tokens=4, routed_scale=1.0,
+                 rms_eps=1e-6, has_norm=False):
+        self.cfg = Config(d, f, n_experts, top_k, n_shared, 32, max_tokens, routed_scale, rms_eps,
+                          int(has_norm))
+        h = _vp()
+        _check(lib().coli_moe_create(ctypes.byref(self.cfg), ctypes.byref(h)), "coli_moe_create")
+        self.h = h
+        self.d, self.f, self.E, self.K, self.n_shared = d, f, n_experts, top_k, n_shared
+        self.max_tokens, self.has_norm = max_tokens, has_norm
+
+    @classmethod
+    def for_workload(cls, wl, max_tokens=None):
+        return cls(wl.d, wl.f, wl.E, wl.K, wl.n_shared, max_tokens or wl.T, 1.0, wl.rms_eps,
+                   wl.has_norm)
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            lib().coli_moe_destroy(self.h)
+            self.h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load_router(self, W_r, bias=None, gamma=None, stream=None):
+        _check(lib().coli_moe_load_router(self.h, _ptr(W_r), _ptr(bias), _ptr(gamma), _stream(stream)),
+               "coli_moe_load_router")
+
+    def load_experts(self, first, count, packed, scales, stream=None):
+        _check(lib().coli_moe_load_experts(self.h, first, count, _ptr(packed), _ptr(scales),
+                                           _stream(stream)), "coli_moe_load_experts")
+
+    def forward(self, x, y=None, stream=None):
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        _check(lib().coli_moe_forward(self.h, _ptr(x), T, _ptr(y), _stream(stream)), "coli_moe_forward")
+        return y
+
+    def forward_profiled(self, x, y, events, stream=None):
+        """forward recording 5 torch.cuda.Event objects around prep, router, gate/up, down"""
+        arr = (_vp * len(events))(*[e.cuda_event for e in events])
+        _check(lib().coli_moe_forward_profiled(self.h, _ptr(x), x.shape[0], _ptr(y), arr, len(events),
+                                               _stream(stream)), "coli_moe_forward_profiled")
+        return y
+
+    def forward_host(self, x, y, stream=None):
+        _check(lib().coli_moe_forward_host(self.h, _ptr(x), x.shape[0], _ptr(y), _stream(stream)),
+               "coli_moe_forward_host")
+        return y
+
+    def forward_debug(self, x, want_A=False, stream=None):
+        """forward plus every intermediate, as torch tensors on the device"""
+        T, d, f, E, K = x.shape[0], self.d, self.f, self.E, self.K
+        P = T * K + (T if self.n_shared else 0)
+        dev = x.device
+        f32, i32, i8 = torch.float32, torch.int32, torch.int8
+        shapes = dict(xn=((T, d), f32), qx=((T, d), i8), dx=((T, d // 32), f32),
+                      logits=((T, E), f32), scores=((T, E), f32), ids=((T, K), i32),
+                      w=((T, K), f32), n_union=((1,), i32), union_ids=((E + 1,), i32),
+                      offsets=((E + 2,), i32), pair_token=((P,), i32), pair_rank=((P,), i32),
+                      inv=((T, K), i32), g=((P, f), f32), u=((P, f), f32), h=((P, f), f32),
+                      qh=((P, f), i8), dh=((P, f // 32), f32), e=((P, d), f32))
+        if want_A:
+            shapes.update(Ag=((P, f, d // 32), i32), Au=((P, f, d // 32), i32),
+                          Ad=((P, d, f // 32), i32))
+        out = {k: torch.zeros(s, dtype=t, device=dev) for k, (s, t) in shapes.items()}
+        dump = Dump(**{k: v.data_ptr() for k, v in out.items()})
+        y = torch.empty_like(x)
+        _check(lib().coli_moe_forward_debug(self.h, _ptr(x), T, _ptr(y), ctypes.byref(dump),
+                                            _stream(stream)), "coli_moe_forward_debug")
+        out["y"] = y
+        return out
+
+    def status(self, stream=None):
+        return int(lib().coli_moe_status(self.h, _stream(stream)))
+
+
+def stack_forward(layers, x, stream=None):
+    arr = (_vp * len(layers))(*[l.h.value for l in layers])
+    _check(lib().coli_moe_stack_forward(arr, len(layers), _ptr(x), x.shape[0], _stream(stream)),
+           "coli_moe_stack_forward")
+    return x
+
+
+def quantize_i4_rows(w, packed=None, scales=None, stream=None):
+    rows, cols = w.shape
+    if packed is None:
+        packed = torch.empty((rows, cols // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().coli_quantize_i4_rows(_ptr(w), rows, cols, _ptr(packed), _ptr(scales), _stream(stream)),
+           "coli_quantize_i4_rows")
+    return packed, scales
+
+
+def quantize_act_q8(x, stream=None):
+    q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    d = torch.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=torch.float32, device=x.device)
+    _check(lib().coli_quantize_act_q8(_ptr(x), x.numel(), _ptr(q), _ptr(d), _stream(stream)),
+           "coli_quantize_act_q8")
+    return q, d

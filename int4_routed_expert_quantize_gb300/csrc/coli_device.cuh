@@ -1,0 +1,188 @@
+// Device helpers of the coli_moe kernels (sm_103a): inline PTX for the bulk-copy engine and
+// mbarriers, the mixed-sign dp4a, and the canonical fp32 operations (explicitly rounded
+// intrinsics, so nvcc cannot contract or reorder them).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coli_internal.h"
+
+namespace coli {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ------------------------------------------------------------------ canonical fp32 -------
+// exp(x) = 2^k * e^r: k the nearest integer to x*log2(e) (rounded with the 1.5*2^23 shifter),
+// r = x - k*ln2 by Cody-Waite reduction (ln2 = hi + lo, hi with 12 fractional bits so k*hi is
+// exact), e^r by the degree-7 Taylor polynomial in Horner form, then two exact power-of-two
+// multiplies (only a subnormal result rounds).  Coefficients are 1/n! rounded to fp32.
+__device__ __forceinline__ float canon_exp(float x) {
+  if (x != x) return __fadd_rn(x, x);
+  if (x > 89.0f) return __int_as_float(0x7f800000);
+  if (x < -104.0f) return 0.0f;
+  const float t = __fmul_rn(x, 0x1.715476p+0f);
+  const float kf = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+  float r = __fmaf_rn(-kf, 0x1.62ep-1f, x);
+  r = __fmaf_rn(-kf, 0x1.0bfbe8p-15f, r);
+  float p = __fmaf_rn(0x1.a01a02p-13f, r, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int k = (int)kf;
+  const int k1 = k / 2, k2 = k - k1;
+  return __fmul_rn(__fmul_rn(p, __int_as_float((k1 + 127) << 23)), __int_as_float((k2 + 127) << 23));
+}
+
+__device__ __forceinline__ float canon_sigmoid(float x) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, canon_exp(-x)));
+}
+
+// SiLU(g) * u, SiLU(g) = g / (1 + exp(-g))
+__device__ __forceinline__ float canon_silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, canon_exp(-g))), u);
+}
+
+// xor butterfly over the 32 lanes; every lane ends with the pairwise-tree sum of the lane
+// values in lane order (fp32 addition is commutative, so both partners compute the same sum)
+__device__ __forceinline__ float warp_tree_sum(float v) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, off));
+  return v;
+}
+
+__device__ __forceinline__ int warp_isum(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(FULL, v, off);
+  return v;
+}
+
+// Q8_0-style code of one element of a 32-block held one element per lane:
+// d = max|x| / 127, q = round(x / d) (half away from zero), clamped to [-127, 127].
+__device__ __forceinline__ int q8_code(float x, float d) {
+  if (d == 0.0f) return 0;
+  int q = (int)roundf(__fdiv_rn(x, d));
+  return max(-127, min(127, q));
+}
+
+// ------------------------------------------------------------------ integer dots ---------
+// a: four unsigned bytes, b: four signed bytes -> c + sum a_i*b_i
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// int32 dot of one 32-element block.  w: the block's 16 bytes in the store layout (word k
+// covers elements 8k..8k+7; byte m holds element 8k+m in its low nibble and 8k+m+4 in its
+// high nibble, both offset by +8).  x: the 32 int8 codes as 8 words in element order.
+// neg8sx = -8 * (sum of the 32 codes) removes the +8 offset exactly.
+__device__ __forceinline__ int block_dot(const uint4 w, const uint32_t (&x)[8], int neg8sx) {
+  int a1 = 0, a16 = 0;
+  a1 = dp4a_us(w.x & 0x0F0F0F0Fu, x[0], a1);
+  a16 = dp4a_us(w.x & 0xF0F0F0F0u, x[1], a16);
+  a1 = dp4a_us(w.y & 0x0F0F0F0Fu, x[2], a1);
+  a16 = dp4a_us(w.y & 0xF0F0F0F0u, x[3], a16);
+  a1 = dp4a_us(w.z & 0x0F0F0F0Fu, x[4], a1);
+  a16 = dp4a_us(w.z & 0xF0F0F0F0u, x[5], a16);
+  a1 = dp4a_us(w.w & 0x0F0F0F0Fu, x[6], a1);
+  a16 = dp4a_us(w.w & 0xF0F0F0F0u, x[7], a16);
+  return a1 + (a16 >> 4) + neg8sx;
+}
+
+// ------------------------------------------------------------------ mbarrier / bulk copy ---
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// make barrier initialisation visible to the async (bulk-copy) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Gives up after kWaitLimitNs, records
+// COLI_ETIMEOUT in the device status word and raises the CTA's abort flag; once the flag is
+// up every later wait returns false at once, so no thread of the CTA can block forever.
+static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status) {
+  if (*abort_flag) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicExch(status, COLI_ETIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// one bulk copy global -> shared (the TMA engine's non-tensor form), completing on `bar`.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace coli

@@ -1,0 +1,113 @@
+// Internal types of the coli_moe library: device layout of the expert store, the per-handle
+// workspace and the kernel launchers.  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coli_moe.h"
+
+namespace coli {
+
+constexpr int kQB = 32;                         // activation block length
+constexpr int kDecodeTmax = 4;                  // tokens per call on the smem-staged path
+constexpr int kNW = 8;                          // consumer warps per CTA of the expert kernels
+constexpr int kThreads = (kNW + 1) * 32;        // + one producer warp
+constexpr int kGuRps = 8;                       // gate/up row pairs per pipeline stage
+constexpr int kDownRowsPerWarp = 2;             // output rows per warp per down stage
+constexpr int kDownRd = kNW * kDownRowsPerWarp; // output rows per down stage
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
+
+// Store layout (built by the repack kernel at load time):
+//  * a matrix row of n int4 values is n/32 blocks of 16 bytes.  With nb = n/32 blocks,
+//    G = ceil(nb/32) blocks per lane group and A = nb/G active groups, block b = g*G + i is
+//    stored at chunk position i*A + g, so that step i of a warp (lane g) reads A consecutive
+//    chunks.  Inside a chunk, word k holds elements 8k..8k+7: byte m has element 8k+m in the
+//    low nibble and 8k+m+4 in the high nibble, each as code + 8 (0..15).
+//  * wgu: per expert slot, f rows of [gate row r | up row r] (d bytes per row pair).
+//  * wd : per expert slot, d rows of the down matrix (f/2 bytes each).
+//  * sc : per expert slot, the canonical scales [s_gate f | s_up f | s_down d].
+//  * wr : router rows with 4-float chunks permuted the same way (lane g's 4*i..4*i+3 of its
+//    d/32 contiguous elements at chunk i*32 + g).
+struct Store {
+  uint8_t* wgu = nullptr;
+  uint8_t* wd = nullptr;
+  float* sc = nullptr;
+  float* wr = nullptr;
+  float* bias = nullptr;   // nullptr: no selection bias
+  float* gamma = nullptr;  // has_norm only
+};
+
+struct Work {
+  float* xn = nullptr;       // [Tm,d]  normalised input (natural layout)
+  float* xnp = nullptr;      // [Tm,d]  same, router chunk layout
+  int8_t* qx = nullptr;      // [Tm,d]
+  float* dx = nullptr;       // [Tm,d/32]
+  int32_t* sx = nullptr;     // [Tm,d/32] sum of the codes of each block
+  float* logits = nullptr;   // [Tm,E]
+  float* scores = nullptr;   // [Tm,E]
+  int32_t* ids = nullptr;    // [Tm,K]
+  float* w = nullptr;        // [Tm,K]
+  int32_t* n_union = nullptr;
+  int32_t* union_ids = nullptr;  // [E+1]
+  int32_t* offsets = nullptr;    // [E+2]
+  int32_t* pair_token = nullptr; // [Pm]
+  int32_t* pair_rank = nullptr;  // [Pm]
+  int32_t* inv = nullptr;        // [Tm,K]
+  int8_t* qh = nullptr;      // [Pm,f]
+  float* dh = nullptr;       // [Pm,f/32]
+  int32_t* sh = nullptr;     // [Pm,f/32]
+  int32_t* counter = nullptr;  // last-CTA ticket of the router (returns to 0 after each use)
+  int32_t* status = nullptr;   // COLI_OK or COLI_ETIMEOUT
+};
+
+struct Shape {
+  int d, f, E, K, n_shared, T;
+  float routed_scale, rms_eps;
+  int has_norm;
+};
+
+// optional debug outputs of the expert kernels (device pointers, may be null)
+struct ExpertDebug {
+  float* g = nullptr;
+  float* u = nullptr;
+  float* h = nullptr;
+  float* e = nullptr;
+  int32_t* Ag = nullptr;
+  int32_t* Au = nullptr;
+  int32_t* Ad = nullptr;
+};
+
+// ---- launchers (return the launch's cudaError_t) ----
+cudaError_t launch_prep(const float* x, const Shape& s, const Store& st, const Work& w,
+                        cudaStream_t stream);
+cudaError_t launch_router(const Shape& s, const Store& st, const Work& w, int num_sms,
+                          cudaStream_t stream);
+cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
+                                 const ExpertDebug& dbg, int num_sms, cudaStream_t stream);
+cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
+                               const Work& w, const ExpertDebug& dbg, int num_sms,
+                               cudaStream_t stream);
+cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
+                                 int64_t dst_row_stride, cudaStream_t stream);
+cudaError_t launch_permute_router(const float* src, float* dst, int E, int d,
+                                  cudaStream_t stream);
+cudaError_t launch_quantize_i4_rows(const float* w, int64_t rows, int cols, uint8_t* packed,
+                                    float* scales, cudaStream_t stream);
+cudaError_t launch_quantize_q8(const float* x, int64_t n, int8_t* q, float* d,
+                               cudaStream_t stream);
+cudaError_t configure_expert_kernels();
+
+// shared-memory plans (host and device agree on the carve-up)
+struct GateupPlan {
+  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, total;
+};
+struct DownPlan {
+  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, total;
+};
+GateupPlan gateup_plan(int d, int f, int T);
+DownPlan down_plan(int d, int f, int T, int K, int n_shared);
+
+}  // namespace coli

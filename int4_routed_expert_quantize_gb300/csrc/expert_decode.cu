@@ -1,0 +1,480 @@
+// Expert kernels of the decode path (a few tokens per call): the fused int4 x int8 gate/up
+// projection with SwiGLU and h re-quantisation, and the down projection with the fixed-order
+// routing-weighted combine.  Both are HBM-bound streams over the union experts' weights
+// ("colibrì 架构概述" §5: gate/up/SiLU/down on the IDOT fast path, then the shared expert;
+// README: each distinct expert of a batch is read once).
+//
+// Structure of both kernels: a persistent grid (one CTA per SM) splits the work into equal
+// contiguous ranges; in each CTA one producer lane streams the weight rows of its range
+// through a ring of shared-memory stages with bulk copies (cp.async.bulk, mbarrier
+// completion, L2 evict-first), and 8 consumer warps reduce each row: lane g owns the g-th of
+// 32 contiguous groups of 32-element blocks, computes exact int32 block dots with dp4a, folds
+// them with fma in block order, and the warp's xor butterfly adds the 32 group partials in
+// pairwise-tree order.  All waits are bounded (see coli_device.cuh).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coli_device.cuh"
+#include "coli_internal.h"
+
+namespace coli {
+
+static inline int align16(int x) { return (x + 15) & ~15; }
+
+GateupPlan gateup_plan(int d, int f, int T) {
+  (void)f;
+  GateupPlan p;
+  const int nbd = d / kQB;
+  p.stage_bytes = kGuRps * d;
+  p.xs_bytes = align16(T * d);
+  p.aux_bytes = align16(T * nbd * 8);
+  p.hs_bytes = align16(2 * 32 * T * 4);
+  const int fixed = 2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes;
+  int nst = (kSmemLimit - fixed) / p.stage_bytes;
+  p.nst = nst > kMaxStages ? kMaxStages : nst;
+  p.total = p.nst * p.stage_bytes + fixed;
+  return p;
+}
+
+DownPlan down_plan(int d, int f, int T, int K, int n_shared) {
+  (void)d;
+  DownPlan p;
+  const int P = T * K + (n_shared ? T : 0);
+  const int nbf = f / kQB;
+  p.stage_bytes = kDownRd * (f / 2);
+  p.hq_bytes = align16(P * f);
+  p.aux_bytes = align16(P * nbf * 8);
+  p.es_bytes = align16(kDownRd * P * 4);
+  const int fixed = 2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes;
+  int nst = (kSmemLimit - fixed) / p.stage_bytes;
+  p.nst = nst > kMaxStages ? kMaxStages : nst;
+  p.total = p.nst * p.stage_bytes + fixed;
+  return p;
+}
+
+struct GateupArgs {
+  Shape s;
+  Store st;
+  Work w;
+  ExpertDebug dbg;
+  GateupPlan pl;
+};
+
+struct DownArgs {
+  Shape s;
+  Store st;
+  Work w;
+  ExpertDebug dbg;
+  DownPlan pl;
+  const float* x;
+  float* y;
+};
+
+// After an abort, wait (bounded, ignoring the abort flag) for the last fills the producer
+// issued, so no bulk copy is still writing shared memory when the CTA exits.
+__device__ __noinline__ void drain_fills(uint64_t* full, int nst, long issued) {
+  const long first = issued > nst ? issued - nst : 0;
+  for (long it = first; it < issued; ++it) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(&full[it % nst], (uint32_t)((it / nst) & 1))) {
+      if (global_ns() - t0 > kWaitLimitNs / 8) break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ gate/up + SwiGLU ------
+// Work unit = (union slot, 32-row block of h): 32 row pairs [gate row | up row] of one
+// expert, which yields one int8 block of h for every token of the slot's bucket.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const GateupArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int abort_flag;
+  const int d = a.s.d, f = a.s.f, T = a.s.T;
+  const int nbd = d >> 5, A = nbd / G, nhb = f >> 5;
+  const GateupPlan& pl = a.pl;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint8_t* xs = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [T][2 halves][chunks][16]
+  float* dxs = reinterpret_cast<float*>(xs + pl.xs_bytes);         // [T][nbd]
+  int* nsx = reinterpret_cast<int*>(dxs + T * nbd);                // [T][nbd]  -8*sum(codes)
+  float* hs = reinterpret_cast<float*>(xs + pl.xs_bytes + pl.aux_bytes);  // [2][32][T]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int nu = *a.w.n_union;
+  const long units = (long)nu * nhb;
+  const long u0 = units * blockIdx.x / gridDim.x;
+  const long u1 = units * (blockIdx.x + 1) / gridDim.x;
+  constexpr int SPU = 32 / kGuRps;
+  const long nstage = (u1 - u0) * SPU;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < pl.nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kNW);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of a
+  // chunk live in separate planes so a warp's 16-byte loads are consecutive
+  for (int idx = threadIdx.x; idx < T * nbd; idx += blockDim.x) {
+    const int t = idx / nbd, b = idx - t * nbd;
+    const int g = b / G, i = b - g * G;
+    const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
+    uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
+    *reinterpret_cast<uint4*>(base) = src[0];
+    *reinterpret_cast<uint4*>(base + nbd * 16) = src[1];
+    dxs[idx] = a.w.dx[(long)t * nbd + b];
+    nsx[idx] = -8 * a.w.sx[(long)t * nbd + b];
+  }
+  __syncthreads();
+
+  if (warp == kNW) {
+    // ---------------- producer: one lane streams row-pair stages
+    if (lane == 0 && nstage > 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      long issued = 0;
+      for (long it = 0; it < nstage; ++it) {
+        const int s = (int)(it % pl.nst);
+        const long n = it / pl.nst;
+        if (n > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((n - 1) & 1), &abort_flag, a.w.status))
+          break;
+        const long unit = u0 + it / SPU;
+        const int sub = (int)(it % SPU);
+        const int slot = (int)(unit / nhb), hb = (int)(unit - (long)slot * nhb);
+        const int ex = a.w.union_ids[slot];
+        const uint8_t* src = a.st.wgu + ((long)ex * f + hb * 32 + sub * kGuRps) * (long)d;
+        mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
+        bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
+        ++issued;
+      }
+      if (abort_flag) drain_fills(full, pl.nst, issued);
+    }
+  } else {
+    // ---------------- consumers: warp `warp` takes row pair `warp` of every stage
+    uint32_t xr[G][8];
+    float dr[G];
+    int nr[G];
+    int cached_tok = -1;
+    for (long it = 0; it < nstage; ++it) {
+      const long unit = u0 + it / SPU;
+      const int sub = (int)(it % SPU);
+      const int slot = (int)(unit / nhb), hb = (int)(unit - (long)slot * nhb);
+      const int ex = a.w.union_ids[slot];
+      const int p0 = a.w.offsets[slot], np = a.w.offsets[slot + 1] - p0;
+      const int s = (int)(it % pl.nst);
+      mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
+      const int rr = sub * kGuRps + warp;
+      const int row = hb * 32 + rr;
+      const uint8_t* grow = ring + (long)s * pl.stage_bytes + (long)warp * d;
+      const float* scx = a.st.sc + (long)ex * (2 * f + d);
+      const float sg = scx[row], su = scx[f + row];
+      for (int q = 0; q < np; ++q) {
+        const int p = p0 + q;
+        const int t = a.w.pair_token[p];
+        if (t != cached_tok) {
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            if (lane < A) {
+              const uint8_t* base = xs + (long)t * d + (i * A + lane) * 16;
+              const uint4 v0 = *reinterpret_cast<const uint4*>(base);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(base + nbd * 16);
+              xr[i][0] = v0.x; xr[i][1] = v0.y; xr[i][2] = v0.z; xr[i][3] = v0.w;
+              xr[i][4] = v1.x; xr[i][5] = v1.y; xr[i][6] = v1.z; xr[i][7] = v1.w;
+              dr[i] = dxs[t * nbd + lane * G + i];
+              nr[i] = nsx[t * nbd + lane * G + i];
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) xr[i][k] = 0u;
+              dr[i] = 0.0f;
+              nr[i] = 0;
+            }
+          }
+          cached_tok = (np == 1) ? t : -1;
+        }
+        float pg = 0.0f, pu = 0.0f;
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          uint4 wg = make_uint4(0, 0, 0, 0), wu = make_uint4(0, 0, 0, 0);
+          if (lane < A) {
+            wg = *reinterpret_cast<const uint4*>(grow + (i * A + lane) * 16);
+            wu = *reinterpret_cast<const uint4*>(grow + d / 2 + (i * A + lane) * 16);
+          }
+          const int ag = block_dot(wg, xr[i], nr[i]);
+          const int au = block_dot(wu, xr[i], nr[i]);
+          pg = __fmaf_rn(dr[i], __int2float_rn(ag), pg);
+          pu = __fmaf_rn(dr[i], __int2float_rn(au), pu);
+          if (a.dbg.Ag != nullptr && lane < A) {
+            const long o = ((long)p * f + row) * nbd + lane * G + i;
+            a.dbg.Ag[o] = ag;
+            a.dbg.Au[o] = au;
+          }
+        }
+        pg = warp_tree_sum(pg);
+        pu = warp_tree_sum(pu);
+        const float g = __fmul_rn(sg, pg), u = __fmul_rn(su, pu);
+        const float hv = canon_silu_mul(g, u);
+        if (lane == 0) {
+          hs[((unit & 1) * 32 + rr) * T + q] = hv;
+          if (a.dbg.g != nullptr) {
+            a.dbg.g[(long)p * f + row] = g;
+            a.dbg.u[(long)p * f + row] = u;
+            a.dbg.h[(long)p * f + row] = hv;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with its row pair
+      if (sub == SPU - 1) {
+        // the unit's 32 rows of h are complete: quantise one int8 block per token
+        named_bar_sync(1, kNW * 32);
+        for (int q = warp; q < np; q += kNW) {
+          const float hv = hs[((unit & 1) * 32 + lane) * T + q];
+          const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
+          const int code = q8_code(hv, dd);
+          const int p = p0 + q;
+          a.w.qh[(long)p * f + hb * 32 + lane] = (int8_t)code;
+          const int sq = warp_isum(code);
+          if (lane == 0) {
+            a.w.dh[(long)p * nhb + hb] = dd;
+            a.w.sh[(long)p * nhb + hb] = sq;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ down + combine --------
+// Work unit = 16 output rows of y; a stage is those rows of one union expert's down matrix.
+// Warp w owns rows 2w, 2w+1 of the unit; once every union expert has been seen it combines
+// them for every token in the fixed order: shared expert first, then ranks 0..K-1.
+template <int GF>
+__global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int abort_flag;
+  const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
+  const int nbf = f >> 5, A = nbf / GF;
+  const DownPlan& pl = a.pl;
+  const int nu = *a.w.n_union;
+  const int P = a.w.offsets[nu];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][2 halves][chunks][16]
+  float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf]
+  int* hn = reinterpret_cast<int*>(hd + P * nbf);                  // [P][nbf]  -8*sum(codes)
+  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [kDownRd][P]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const long units = d / kDownRd;
+  const long u0 = units * blockIdx.x / gridDim.x;
+  const long u1 = units * (blockIdx.x + 1) / gridDim.x;
+  const long nstage = (u1 - u0) * nu;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < pl.nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kNW);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (int idx = threadIdx.x; idx < P * nbf; idx += blockDim.x) {
+    const int p = idx / nbf, b = idx - p * nbf;
+    const int g = b / GF, i = b - g * GF;
+    const uint4* src = reinterpret_cast<const uint4*>(a.w.qh + (long)p * f + b * 32);
+    uint8_t* base = hq + (long)p * f + (i * A + g) * 16;
+    *reinterpret_cast<uint4*>(base) = src[0];
+    *reinterpret_cast<uint4*>(base + nbf * 16) = src[1];
+    hd[idx] = a.w.dh[(long)p * nbf + b];
+    hn[idx] = -8 * a.w.sh[(long)p * nbf + b];
+  }
+  __syncthreads();
+
+  if (warp == kNW) {
+    if (lane == 0 && nstage > 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      long issued = 0;
+      for (long it = 0; it < nstage; ++it) {
+        const int s = (int)(it % pl.nst);
+        const long n = it / pl.nst;
+        if (n > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((n - 1) & 1), &abort_flag, a.w.status))
+          break;
+        const long unit = u0 + it / nu;
+        const int slot = (int)(it % nu);
+        const int ex = a.w.union_ids[slot];
+        const uint8_t* src = a.st.wd + ((long)ex * d + unit * kDownRd) * (long)(f / 2);
+        mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
+        bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
+        ++issued;
+      }
+      if (abort_flag) drain_fills(full, pl.nst, issued);
+    }
+  } else {
+    for (long it = 0; it < nstage; ++it) {
+      const long unit = u0 + it / nu;
+      const int slot = (int)(it % nu);
+      const int ex = a.w.union_ids[slot];
+      const int p0 = a.w.offsets[slot], np = a.w.offsets[slot + 1] - p0;
+      const int s = (int)(it % pl.nst);
+      mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
+      const int lr = warp * kDownRowsPerWarp;  // local row within the unit
+      const int r0 = (int)unit * kDownRd + lr;
+      const uint8_t* srow = ring + (long)s * pl.stage_bytes + (long)lr * (f / 2);
+      uint4 w0[GF], w1[GF];
+#pragma unroll
+      for (int i = 0; i < GF; ++i) {
+        if (lane < A) {
+          w0[i] = *reinterpret_cast<const uint4*>(srow + (i * A + lane) * 16);
+          w1[i] = *reinterpret_cast<const uint4*>(srow + f / 2 + (i * A + lane) * 16);
+        } else {
+          w0[i] = make_uint4(0, 0, 0, 0);
+          w1[i] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
+      const float* sdx = a.st.sc + (long)ex * (2 * f + d) + 2 * f;
+      const float sd0 = sdx[r0], sd1 = sdx[r0 + 1];
+      for (int q = 0; q < np; ++q) {
+        const int p = p0 + q;
+        uint32_t hr[GF][8];
+        float hdr[GF];
+        int hnr[GF];
+#pragma unroll
+        for (int i = 0; i < GF; ++i) {
+          if (lane < A) {
+            const uint8_t* base = hq + (long)p * f + (i * A + lane) * 16;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(base);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(base + nbf * 16);
+            hr[i][0] = v0.x; hr[i][1] = v0.y; hr[i][2] = v0.z; hr[i][3] = v0.w;
+            hr[i][4] = v1.x; hr[i][5] = v1.y; hr[i][6] = v1.z; hr[i][7] = v1.w;
+            hdr[i] = hd[p * nbf + lane * GF + i];
+            hnr[i] = hn[p * nbf + lane * GF + i];
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) hr[i][k] = 0u;
+            hdr[i] = 0.0f;
+            hnr[i] = 0;
+          }
+        }
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < GF; ++i) {
+          const int a0 = block_dot(w0[i], hr[i], hnr[i]);
+          const int a1 = block_dot(w1[i], hr[i], hnr[i]);
+          s0 = __fmaf_rn(hdr[i], __int2float_rn(a0), s0);
+          s1 = __fmaf_rn(hdr[i], __int2float_rn(a1), s1);
+          if (a.dbg.Ad != nullptr && lane < A) {
+            a.dbg.Ad[((long)p * d + r0) * nbf + lane * GF + i] = a0;
+            a.dbg.Ad[((long)p * d + r0 + 1) * nbf + lane * GF + i] = a1;
+          }
+        }
+        s0 = warp_tree_sum(s0);
+        s1 = warp_tree_sum(s1);
+        const float e0 = __fmul_rn(sd0, s0), e1 = __fmul_rn(sd1, s1);
+        if (lane == 0) {
+          es[lr * P + p] = e0;
+          es[(lr + 1) * P + p] = e1;
+          if (a.dbg.e != nullptr) {
+            a.dbg.e[(long)p * d + r0] = e0;
+            a.dbg.e[(long)p * d + r0 + 1] = e1;
+          }
+        }
+      }
+      if (slot == nu - 1) {
+        __syncwarp();
+        for (int t = lane; t < T; t += 32) {
+#pragma unroll
+          for (int j = 0; j < kDownRowsPerWarp; ++j) {
+            const float* er = es + (lr + j) * P;
+            float y = a.s.n_shared ? er[T * K + t] : 0.0f;
+            for (int k = 0; k < K; ++k) y = __fmaf_rn(a.w.w[t * K + k], er[a.w.inv[t * K + k]], y);
+            if (a.s.has_norm) y = __fadd_rn(a.x[(long)t * d + r0 + j], y);
+            a.y[(long)t * d + r0 + j] = y;
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ launchers -------------
+template <int G>
+static cudaError_t gateup_launch_g(const GateupArgs& args, int grid, cudaStream_t stream) {
+  gateup_decode_kernel<G><<<grid, kThreads, args.pl.total, stream>>>(args);
+  return cudaGetLastError();
+}
+
+template <int G>
+static cudaError_t down_launch_g(const DownArgs& args, int grid, cudaStream_t stream) {
+  down_decode_kernel<G><<<grid, kThreads, args.pl.total, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t configure_expert_kernels() {
+  cudaError_t e = cudaSuccess;
+#define COLI_SET(KERN)                                                                      \
+  if (e == cudaSuccess)                                                                     \
+    e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  COLI_SET(gateup_decode_kernel<1>) COLI_SET(gateup_decode_kernel<2>)
+  COLI_SET(gateup_decode_kernel<3>) COLI_SET(gateup_decode_kernel<4>)
+  COLI_SET(gateup_decode_kernel<5>) COLI_SET(gateup_decode_kernel<6>)
+  COLI_SET(gateup_decode_kernel<7>) COLI_SET(gateup_decode_kernel<8>)
+  COLI_SET(down_decode_kernel<1>) COLI_SET(down_decode_kernel<2>)
+  COLI_SET(down_decode_kernel<3>) COLI_SET(down_decode_kernel<4>)
+  COLI_SET(down_decode_kernel<5>) COLI_SET(down_decode_kernel<6>)
+  COLI_SET(down_decode_kernel<7>) COLI_SET(down_decode_kernel<8>)
+#undef COLI_SET
+  return e;
+}
+
+cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
+                                 const ExpertDebug& dbg, int num_sms, cudaStream_t stream) {
+  GateupArgs args{s, st, w, dbg, gateup_plan(s.d, s.f, s.T)};
+  const int G = (s.d / kQB + 31) / 32;
+  // the unit count depends on the union size, known only on the device: size the grid for
+  // the largest possible union and let idle CTAs exit
+  const long max_units = (long)(s.T * s.K < s.E ? s.T * s.K : s.E) + s.n_shared;
+  long grid = max_units * (s.f / kQB);
+  if (grid > num_sms) grid = num_sms;
+  switch (G) {
+    case 1: return gateup_launch_g<1>(args, (int)grid, stream);
+    case 2: return gateup_launch_g<2>(args, (int)grid, stream);
+    case 3: return gateup_launch_g<3>(args, (int)grid, stream);
+    case 4: return gateup_launch_g<4>(args, (int)grid, stream);
+    case 5: return gateup_launch_g<5>(args, (int)grid, stream);
+    case 6: return gateup_launch_g<6>(args, (int)grid, stream);
+    case 7: return gateup_launch_g<7>(args, (int)grid, stream);
+    case 8: return gateup_launch_g<8>(args, (int)grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
+                               const Work& w, const ExpertDebug& dbg, int num_sms,
+                               cudaStream_t stream) {
+  DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.n_shared), x, y};
+  const int GF = (s.f / kQB + 31) / 32;
+  long grid = s.d / kDownRd;
+  if (grid > num_sms) grid = num_sms;
+  switch (GF) {
+    case 1: return down_launch_g<1>(args, (int)grid, stream);
+    case 2: return down_launch_g<2>(args, (int)grid, stream);
+    case 3: return down_launch_g<3>(args, (int)grid, stream);
+    case 4: return down_launch_g<4>(args, (int)grid, stream);
+    case 5: return down_launch_g<5>(args, (int)grid, stream);
+    case 6: return down_launch_g<6>(args, (int)grid, stream);
+    case 7: return down_launch_g<7>(args, (int)grid, stream);
+    case 8: return down_launch_g<8>(args, (int)grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace coli

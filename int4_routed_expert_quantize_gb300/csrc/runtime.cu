@@ -1,0 +1,463 @@
+// Host runtime of the coli_moe C ABI: argument checks, allocation of the expert store and
+// workspace, weight loading (with the repack into the store layout) and the launch sequence
+// of one forward: prep -> router (+ top-K, union) -> gate/up SwiGLU -> down + combine.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "coli_internal.h"
+#include "coli_moe.h"
+
+using namespace coli;
+
+struct coli_moe {
+  coli_moe_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int slots = 0;  // E + n_shared
+  Store st;
+  Work w;
+  float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
+  bool router_loaded = false;
+  std::vector<uint8_t> loaded;
+  int n_loaded = 0;
+  std::vector<void*> allocs;
+};
+
+namespace {
+
+int64_t rec_bytes(int d, int f) { return 3LL * d * f / 2; }
+
+bool shape_ok(int n) {
+  if (n < 128 || n > 8192 || n % 128) return false;
+  const int nb = n / 32, G = (nb + 31) / 32;
+  return nb % G == 0;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? COLI_OK : COLI_ECUDA; }
+
+template <class T>
+int dalloc(coli_moe* h, T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  void* q = nullptr;
+  if (cudaMalloc(&q, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return COLI_ENOMEM;
+  }
+  h->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return COLI_OK;
+}
+
+void free_all(coli_moe* h) {
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char *pa = (const char*)a, *pb = (const char*)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+int check_device(const coli_moe* h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return COLI_ECUDA;
+  return dev == h->device ? COLI_OK : COLI_ESTATE;
+}
+
+Shape shape_of(const coli_moe* h, int T) {
+  const coli_moe_config& c = h->cfg;
+  return Shape{c.d, c.f, c.n_experts, c.top_k, c.n_shared, T, c.routed_scale, c.rms_eps,
+               c.has_norm};
+}
+
+std::once_flag g_cfg_once;
+cudaError_t g_cfg_err = cudaSuccess;
+
+int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump* dump,
+               cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
+  const Shape s = shape_of(h, T);
+  ExpertDebug dbg;
+  if (dump) {
+    dbg.g = dump->g;
+    dbg.u = dump->u;
+    dbg.h = dump->h;
+    dbg.e = dump->e;
+    dbg.Ag = dump->Ag;
+    dbg.Au = dump->Au;
+    dbg.Ad = dump->Ad;
+    if ((dbg.g || dbg.u || dbg.h) && !(dbg.g && dbg.u && dbg.h)) return COLI_EINVAL;
+    if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
+  }
+  cudaError_t e = ev ? cudaEventRecord(ev[0], stream) : cudaSuccess;
+  if (e == cudaSuccess) e = launch_prep(x, s, h->st, h->w, stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], stream);
+  if (e == cudaSuccess) e = launch_router(s, h->st, h->w, h->num_sms, stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
+  if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], stream);
+  if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], stream);
+  if (e != cudaSuccess) return COLI_ECUDA;
+  if (dump) {
+    const coli_moe_config& c = h->cfg;
+    const long P = (long)T * c.top_k + (c.n_shared ? T : 0);
+    struct Cp {
+      void* dst;
+      const void* src;
+      size_t bytes;
+    } cps[] = {
+        {dump->xn, h->w.xn, sizeof(float) * T * c.d},
+        {dump->qx, h->w.qx, (size_t)T * c.d},
+        {dump->dx, h->w.dx, sizeof(float) * T * (c.d / 32)},
+        {dump->logits, h->w.logits, sizeof(float) * T * c.n_experts},
+        {dump->scores, h->w.scores, sizeof(float) * T * c.n_experts},
+        {dump->ids, h->w.ids, sizeof(int32_t) * T * c.top_k},
+        {dump->w, h->w.w, sizeof(float) * T * c.top_k},
+        {dump->n_union, h->w.n_union, sizeof(int32_t)},
+        {dump->union_ids, h->w.union_ids, sizeof(int32_t) * (c.n_experts + 1)},
+        {dump->offsets, h->w.offsets, sizeof(int32_t) * (c.n_experts + 2)},
+        {dump->pair_token, h->w.pair_token, sizeof(int32_t) * P},
+        {dump->pair_rank, h->w.pair_rank, sizeof(int32_t) * P},
+        {dump->inv, h->w.inv, sizeof(int32_t) * T * c.top_k},
+        {dump->qh, h->w.qh, (size_t)P * c.f},
+        {dump->dh, h->w.dh, sizeof(float) * P * (c.f / 32)},
+    };
+    for (const Cp& cp : cps)
+      if (cp.dst && cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToDevice, stream) !=
+                        cudaSuccess)
+        return COLI_ECUDA;
+  }
+  return COLI_OK;
+}
+
+int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump* dump,
+                 void* stream) {
+  if (!h || T < 0 || T > h->cfg.max_tokens) return COLI_EINVAL;
+  if (T == 0) return COLI_OK;
+  if (!x || !y) return COLI_EINVAL;
+  const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
+  if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
+  if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
+  if (dump && T > kDecodeTmax) return COLI_EUNSUPPORTED;
+  if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the smem-staged kernels take up to kDecodeTmax tokens; larger batches run in chunks,
+  // which gives the same result per token (each token's output depends on itself only)
+  for (int c0 = 0; c0 < T; c0 += kDecodeTmax) {
+    const int Tc = T - c0 < kDecodeTmax ? T - c0 : kDecodeTmax;
+    rc = run_decode(h, x + (size_t)c0 * h->cfg.d, Tc, y + (size_t)c0 * h->cfg.d, dump, st);
+    if (rc) return rc;
+  }
+  return COLI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* coli_moe_strerror(int status) {
+  switch (status) {
+    case COLI_OK: return "ok";
+    case COLI_EINVAL: return "invalid argument";
+    case COLI_ENOMEM: return "out of memory";
+    case COLI_ESTATE: return "call out of order (weights not loaded, or wrong device)";
+    case COLI_ECUDA: return "CUDA runtime error";
+    case COLI_ETIMEOUT: return "a bounded device wait timed out";
+    case COLI_EUNSUPPORTED: return "unsupported shape";
+    default: return "unknown status";
+  }
+}
+
+int64_t coli_moe_expert_record_bytes(int d, int f) {
+  return rec_bytes(d, f) + 4LL * (2LL * f + d);
+}
+
+int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
+  if (!out) return COLI_EINVAL;
+  *out = nullptr;
+  if (!cfg) return COLI_EINVAL;
+  const coli_moe_config c = *cfg;
+  if (c.qblock != 32 || c.n_experts < 1 || c.n_experts > 1024 || c.top_k < 1 ||
+      c.top_k > c.n_experts || c.top_k > 32 || (c.n_shared != 0 && c.n_shared != 1) ||
+      c.max_tokens < 1 || c.max_tokens > 4096 || !std::isfinite(c.routed_scale) ||
+      !(c.rms_eps >= 0.0f) || !std::isfinite(c.rms_eps) || c.d <= 0 || c.f <= 0)
+    return COLI_EINVAL;
+  if (!shape_ok(c.d) || !shape_ok(c.f)) return COLI_EUNSUPPORTED;
+  const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
+  if (gateup_plan(c.d, c.f, Tc).nst < 2 || down_plan(c.d, c.f, Tc, c.top_k, c.n_shared).nst < 2)
+    return COLI_EUNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return COLI_ECUDA;
+  }
+  std::call_once(g_cfg_once, [] { g_cfg_err = configure_expert_kernels(); });
+  if (g_cfg_err != cudaSuccess) return COLI_ECUDA;
+
+  coli_moe* h = new (std::nothrow) coli_moe();
+  if (!h) return COLI_ENOMEM;
+  h->cfg = c;
+  h->device = dev;
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete h;
+    return COLI_ECUDA;
+  }
+  h->slots = c.n_experts + c.n_shared;
+  h->loaded.assign(h->slots, 0);
+  const long S = h->slots, d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
+  const long Pm = Tm * K + (c.n_shared ? Tm : 0);
+  int rc = COLI_OK;
+#define ALLOC(ptr, bytes) \
+  if (rc == COLI_OK) rc = dalloc(h, &(ptr), (size_t)(bytes));
+  ALLOC(h->st.wgu, S * f * d)
+  ALLOC(h->st.wd, S * d * (f / 2))
+  ALLOC(h->st.sc, sizeof(float) * S * (2 * f + d))
+  ALLOC(h->st.wr, sizeof(float) * E * d)
+  if (c.has_norm) ALLOC(h->st.gamma, sizeof(float) * d)
+  ALLOC(h->w.xn, sizeof(float) * Tm * d)
+  ALLOC(h->w.xnp, sizeof(float) * Tm * d)
+  ALLOC(h->w.qx, Tm * d)
+  ALLOC(h->w.dx, sizeof(float) * Tm * (d / 32))
+  ALLOC(h->w.sx, sizeof(int32_t) * Tm * (d / 32))
+  ALLOC(h->w.logits, sizeof(float) * Tm * E)
+  ALLOC(h->w.scores, sizeof(float) * Tm * E)
+  ALLOC(h->w.ids, sizeof(int32_t) * Tm * K)
+  ALLOC(h->w.w, sizeof(float) * Tm * K)
+  ALLOC(h->w.n_union, sizeof(int32_t) * 4)
+  ALLOC(h->w.union_ids, sizeof(int32_t) * (E + 1))
+  ALLOC(h->w.offsets, sizeof(int32_t) * (E + 2))
+  ALLOC(h->w.pair_token, sizeof(int32_t) * Pm)
+  ALLOC(h->w.pair_rank, sizeof(int32_t) * Pm)
+  ALLOC(h->w.inv, sizeof(int32_t) * Tm * K)
+  ALLOC(h->w.qh, Pm * f)
+  ALLOC(h->w.dh, sizeof(float) * Pm * (f / 32))
+  ALLOC(h->w.sh, sizeof(int32_t) * Pm * (f / 32))
+  ALLOC(h->w.counter, sizeof(int32_t) * 4)
+  ALLOC(h->w.status, sizeof(int32_t) * 4)
+  ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
+#undef ALLOC
+  if (rc == COLI_OK && (cudaMemset(h->w.counter, 0, 16) != cudaSuccess ||
+                        cudaMemset(h->w.status, 0, 16) != cudaSuccess ||
+                        cudaDeviceSynchronize() != cudaSuccess))
+    rc = COLI_ECUDA;
+  if (rc != COLI_OK) {
+    free_all(h);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return COLI_OK;
+}
+
+void coli_moe_destroy(coli_moe* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+int coli_moe_load_router(coli_moe* h, const float* W_r, const float* bias, const float* gamma,
+                         void* stream) {
+  if (!h || !W_r) return COLI_EINVAL;
+  if (h->cfg.has_norm && !gamma) return COLI_EINVAL;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t E = h->cfg.n_experts, d = h->cfg.d;
+  float* tmp = nullptr;
+  if (cudaMalloc(&tmp, sizeof(float) * E * d) != cudaSuccess) {
+    cudaGetLastError();
+    return COLI_ENOMEM;
+  }
+  cudaError_t e = cudaMemcpyAsync(tmp, W_r, sizeof(float) * E * d, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = launch_permute_router(tmp, h->st.wr, (int)E, (int)d, st);
+  if (e == cudaSuccess && bias) {
+    if (!h->st.bias) {
+      if (dalloc(h, &h->st.bias, sizeof(float) * E) != COLI_OK) {
+        cudaStreamSynchronize(st);
+        cudaFree(tmp);
+        return COLI_ENOMEM;
+      }
+    }
+    e = cudaMemcpyAsync(h->st.bias, bias, sizeof(float) * E, cudaMemcpyDefault, st);
+  }
+  if (e == cudaSuccess && h->cfg.has_norm)
+    e = cudaMemcpyAsync(h->st.gamma, gamma, sizeof(float) * d, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(tmp);
+  if (e != cudaSuccess) return COLI_ECUDA;
+  if (!bias && h->st.bias) {
+    // a later load without bias removes it
+    for (size_t i = 0; i < h->allocs.size(); ++i)
+      if (h->allocs[i] == h->st.bias) {
+        cudaFree(h->st.bias);
+        h->allocs.erase(h->allocs.begin() + i);
+        break;
+      }
+    h->st.bias = nullptr;
+  }
+  h->router_loaded = true;
+  return COLI_OK;
+}
+
+int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* packed,
+                          const float* scales, void* stream) {
+  if (!h || !packed || !scales || first < 0 || count < 0 || first + count > h->slots)
+    return COLI_EINVAL;
+  if (count == 0) return COLI_OK;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int d = h->cfg.d, f = h->cfg.f;
+  const size_t rb = (size_t)rec_bytes(d, f);
+  const bool on_device = is_device_ptr(packed);
+  uint8_t* staging = nullptr;
+  if (!on_device && cudaMalloc(&staging, rb) != cudaSuccess) {
+    cudaGetLastError();
+    return COLI_ENOMEM;
+  }
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < count && e == cudaSuccess; ++i) {
+    const int slot = first + i;
+    const uint8_t* rec = packed + (size_t)i * rb;
+    if (!on_device) {
+      e = cudaMemcpyAsync(staging, rec, rb, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+      rec = staging;
+    }
+    uint8_t* gu = h->st.wgu + (size_t)slot * f * d;
+    uint8_t* dn = h->st.wd + (size_t)slot * d * (f / 2);
+    if (e == cudaSuccess) e = launch_repack_matrix(rec, gu, f, d, d, st);
+    if (e == cudaSuccess) e = launch_repack_matrix(rec + (size_t)f * d / 2, gu + d / 2, f, d, d, st);
+    if (e == cudaSuccess) e = launch_repack_matrix(rec + (size_t)f * d, dn, d, f, f / 2, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->st.sc + (size_t)slot * (2 * f + d), scales + (size_t)i * (2 * f + d),
+                          sizeof(float) * (2 * f + d), cudaMemcpyDefault, st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (staging) cudaFree(staging);
+  if (e != cudaSuccess) return COLI_ECUDA;
+  for (int i = 0; i < count; ++i)
+    if (!h->loaded[first + i]) {
+      h->loaded[first + i] = 1;
+      ++h->n_loaded;
+    }
+  return COLI_OK;
+}
+
+int coli_moe_forward(coli_moe* h, const float* x_dev, int T, float* y_dev, void* stream) {
+  return forward_impl(h, x_dev, T, y_dev, nullptr, stream);
+}
+
+int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
+                           const coli_moe_dump* dump, void* stream) {
+  if (!dump) return COLI_EINVAL;
+  return forward_impl(h, x_dev, T, y_dev, dump, stream);
+}
+
+int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
+                              void* const* events, int n_events, void* stream) {
+  if (!h || !events || n_events < 5 || T < 1 || T > kDecodeTmax || T > h->cfg.max_tokens)
+    return COLI_EINVAL;
+  for (int i = 0; i < 5; ++i)
+    if (!events[i]) return COLI_EINVAL;
+  if (!x_dev || !y_dev) return COLI_EINVAL;
+  const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
+  if (x_dev != y_dev && overlap(x_dev, bytes, y_dev, bytes)) return COLI_EINVAL;
+  if (x_dev == y_dev && !h->cfg.has_norm) return COLI_EINVAL;
+  if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaEvent_t ev[5];
+  for (int i = 0; i < 5; ++i) ev[i] = (cudaEvent_t)events[i];
+  return run_decode(h, x_dev, T, y_dev, nullptr, (cudaStream_t)stream, ev);
+}
+
+int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host, void* stream) {
+  if (!h || T < 0 || T > h->cfg.max_tokens) return COLI_EINVAL;
+  if (T == 0) return COLI_OK;
+  if (!x_host || !y_host) return COLI_EINVAL;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t n = (size_t)T * h->cfg.d;
+  float* dx = h->dev_io;
+  float* dy = h->cfg.has_norm ? h->dev_io : h->dev_io + (size_t)h->cfg.max_tokens * h->cfg.d;
+  if (cudaMemcpyAsync(dx, x_host, sizeof(float) * n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return COLI_ECUDA;
+  rc = forward_impl(h, dx, T, dy, nullptr, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(y_host, dy, sizeof(float) * n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return COLI_ECUDA;
+  return cuda_status(cudaStreamSynchronize(st));
+}
+
+int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, int T,
+                           void* stream) {
+  if (!layers || n_layers < 0 || !x_dev) return COLI_EINVAL;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!layers[l] || !layers[l]->cfg.has_norm || layers[l]->cfg.d != layers[0]->cfg.d)
+      return COLI_EINVAL;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = forward_impl(layers[l], x_dev, T, x_dev, nullptr, stream);
+    if (rc) return rc;
+  }
+  return COLI_OK;
+}
+
+int coli_moe_status(coli_moe* h, void* stream) {
+  if (!h) return COLI_EINVAL;
+  int rc = check_device(h);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, h->w.status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return COLI_ECUDA;
+  if (v != COLI_OK) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(h->w.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return COLI_ECUDA;
+    return v;
+  }
+  return COLI_OK;
+}
+
+int coli_quantize_i4_rows(const float* w_dev, int64_t rows, int cols, uint8_t* packed_dev,
+                          float* scales_dev, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 2 || cols > 65536) return COLI_EINVAL;
+  if (rows == 0) return COLI_OK;
+  if (!w_dev || !packed_dev || !scales_dev) return COLI_EINVAL;
+  return cuda_status(
+      launch_quantize_i4_rows(w_dev, rows, cols, packed_dev, scales_dev, (cudaStream_t)stream));
+}
+
+int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_dev,
+                         void* stream) {
+  if (n < 0 || n % 32) return COLI_EINVAL;
+  if (n == 0) return COLI_OK;
+  if (!x_dev || !q_dev || !d_dev) return COLI_EINVAL;
+  return cuda_status(launch_quantize_q8(x_dev, n, q_dev, d_dev, (cudaStream_t)stream));
+}
+
+}  // extern "C"
