@@ -116,19 +116,20 @@ int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* pack
                           const float* scales, void* stream);
 
 /* y_dev[T,d] = layer(x_dev[T,d]), asynchronous on `stream`, no host synchronisation and no
- * allocation (safe to capture in a CUDA graph).  T == 0 is a no-op.  x_dev may equal y_dev
- * only with has_norm (residual update in place).  EINVAL: T < 0 or T > max_tokens, NULL
- * pointers, forbidden aliasing.  ESTATE: router or some expert not loaded yet. */
+ * allocation (safe to capture in a CUDA graph).  T == 0 is a no-op.  x_dev must be 16-byte
+ * aligned.  x_dev may equal y_dev only with has_norm (residual update in place).  EINVAL:
+ * T < 0 or T > max_tokens, NULL or misaligned pointers, forbidden aliasing.  ESTATE: router or
+ * some expert not loaded yet. */
 int coli_moe_forward(coli_moe* h, const float* x_dev, int T, float* y_dev, void* stream);
 
 /* coli_moe_forward plus the intermediates selected in `dump` (slower; for verification). */
 int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
                            const coli_moe_dump* dump, void* stream);
 
-/* coli_moe_forward that also records `events[0..4]` (cudaEvent_t handles created by the
- * caller) on `stream`: before the prep kernel, then after prep, after the router, after the
- * gate/up kernel and after the down kernel -- so the caller can time each launch.
- * T <= 4 (one launch of each kernel).  EINVAL: n_events < 5 or T out of range. */
+/* coli_moe_forward that also records `events[0..3]` (cudaEvent_t handles created by the
+ * caller) on `stream`: before the routing kernel, after it, after the gate/up kernel and after
+ * the down kernel -- so the caller can time each launch.  The events serialise the launches
+ * (no programmatic overlap between them).  T <= 4.  EINVAL: n_events < 4 or T out of range. */
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream);
 

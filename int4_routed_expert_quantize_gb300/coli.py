@@ -147,7 +147,11 @@ class MoeLayer:
         return y
 
     def forward_profiled(self, x, y, events, stream=None):
-        """forward recording 5 torch.cuda.Event objects around prep, router, gate/up, down"""
+        """forward recording 4 torch.cuda.Event objects: before/after routing, after gate/up,
+        after down"""
+        for e in events:  # torch creates the CUDA event on its first record
+            if not e.cuda_event:
+                e.record()
         arr = (_vp * len(events))(*[e.cuda_event for e in events])
         _check(lib().coli_moe_forward_profiled(self.h, _ptr(x), x.shape[0], _ptr(y), arr, len(events),
                                                _stream(stream)), "coli_moe_forward_profiled")

@@ -99,6 +99,15 @@ __device__ __forceinline__ int block_dot(const uint4 w, const uint32_t (&x)[8], 
   return a1 + (a16 >> 4) + neg8sx;
 }
 
+// Position, within a stored row, of block b = g*G + i (G blocks per lane group): the groups are
+// contiguous and a group's blocks are rotated by one for groups 4..7 mod 8, so that the
+// 16-byte loads of 8 consecutive lanes fall in distinct shared-memory banks.
+__device__ __forceinline__ int store_chunk(int g, int i, int G) {
+  int c = i + ((g >> 2) & 1);
+  if (c >= G) c -= G;
+  return g * G + c;
+}
+
 // ------------------------------------------------------------------ mbarrier / bulk copy ---
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -179,6 +188,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// programmatic dependent launch: wait for the preceding grid (no-op without the attribute) /
+// allow the next grid in the stream to start its prologue
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// bring [src, src+bytes) into L2 (bulk prefetch; src 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

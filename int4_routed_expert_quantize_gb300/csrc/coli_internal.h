@@ -18,14 +18,17 @@ constexpr int kDownRowsPerWarp = 2;             // output rows per warp per down
 constexpr int kDownRd = kNW * kDownRowsPerWarp; // output rows per down stage
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
+constexpr int kGateupSmem = 160 * 1024;         // gate/up ring budget: leaves room on the SM for
+                                                // a routing CTA while its prefetch runs
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
 
 // Store layout (built by the repack kernel at load time):
-//  * a matrix row of n int4 values is n/32 blocks of 16 bytes.  With nb = n/32 blocks,
-//    G = ceil(nb/32) blocks per lane group and A = nb/G active groups, block b = g*G + i is
-//    stored at chunk position i*A + g, so that step i of a warp (lane g) reads A consecutive
-//    chunks.  Inside a chunk, word k holds elements 8k..8k+7: byte m has element 8k+m in the
-//    low nibble and 8k+m+4 in the high nibble, each as code + 8 (0..15).
+//  * a matrix row of n int4 values is n/32 blocks of 16 bytes.  With nb = n/32 blocks and
+//    G = ceil(nb/32) blocks per lane group, block b = g*G + i is stored at chunk position
+//    g*G + ((i + ((g>>2)&1)) mod G): each group's blocks stay contiguous (a K-range a matrix
+//    engine can load whole) and the rotation keeps a warp's loads free of bank conflicts.
+//    Inside a chunk, word k holds elements 8k..8k+7: byte m has element 8k+m in the low
+//    nibble and 8k+m+4 in the high nibble, each as code + 8 (0..15).
 //  * wgu: per expert slot, f rows of [gate row r | up row r] (d bytes per row pair).
 //  * wd : per expert slot, d rows of the down matrix (f/2 bytes each).
 //  * sc : per expert slot, the canonical scales [s_gate f | s_up f | s_down d].
@@ -56,6 +59,7 @@ struct Work {
   int32_t* pair_token = nullptr; // [Pm]
   int32_t* pair_rank = nullptr;  // [Pm]
   int32_t* inv = nullptr;        // [Tm,K]
+  float* hf = nullptr;       // [Pm,f]  SwiGLU output h (fp32) before re-quantisation
   int8_t* qh = nullptr;      // [Pm,f]
   float* dh = nullptr;       // [Pm,f/32]
   int32_t* sh = nullptr;     // [Pm,f/32]
@@ -73,7 +77,6 @@ struct Shape {
 struct ExpertDebug {
   float* g = nullptr;
   float* u = nullptr;
-  float* h = nullptr;
   float* e = nullptr;
   int32_t* Ag = nullptr;
   int32_t* Au = nullptr;
@@ -81,15 +84,17 @@ struct ExpertDebug {
 };
 
 // ---- launchers (return the launch's cudaError_t) ----
-cudaError_t launch_prep(const float* x, const Shape& s, const Store& st, const Work& w,
-                        cudaStream_t stream);
-cudaError_t launch_router(const Shape& s, const Store& st, const Work& w, int num_sms,
-                          cudaStream_t stream);
+// `pdl`: launch as a programmatic dependent of the previous kernel in the stream (the kernel
+// prefetches weights before waiting for its predecessor's results)
+cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const Work& w,
+                         cudaStream_t stream);
 cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
-                                 const ExpertDebug& dbg, int num_sms, cudaStream_t stream);
+                                 const ExpertDebug& dbg, int num_sms, bool pdl,
+                                 cudaStream_t stream);
 cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
-                               const Work& w, const ExpertDebug& dbg, int num_sms,
+                               const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream);
+cudaError_t configure_route_kernels();
 cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
                                  int64_t dst_row_stride, cudaStream_t stream);
 cudaError_t launch_permute_router(const float* src, float* dst, int E, int d,

@@ -30,7 +30,7 @@ GateupPlan gateup_plan(int d, int f, int T) {
   p.aux_bytes = align16(T * nbd * 8);
   p.hs_bytes = align16(2 * 32 * T * 4);
   const int fixed = 2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes;
-  int nst = (kSmemLimit - fixed) / p.stage_bytes;
+  int nst = ((kGateupSmem > fixed + 2 * p.stage_bytes ? kGateupSmem : kSmemLimit) - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
   return p;
@@ -83,8 +83,12 @@ __device__ __noinline__ void drain_fills(uint64_t* full, int nst, long issued) {
 }
 
 // ------------------------------------------------------------------ gate/up + SwiGLU ------
-// Work unit = (union slot, 32-row block of h): 32 row pairs [gate row | up row] of one
-// expert, which yields one int8 block of h for every token of the slot's bucket.
+// Work unit = (union slot, 32-row block of h): 32 row pairs [gate row | up row] of one expert,
+// streamed as 4 stages of 8 row pairs, which yields one int8 block of h for every token of the
+// slot's bucket.  The units are split evenly over the CTAs with the shared expert's units first
+// in every CTA that has some: those are known before routing, so they are prefetched before
+// the kernel waits for the routing grid.  Warp w reduces row pair w of every stage; when a
+// unit's 32 rows are done the CTA re-quantises them (one warp per token).
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const GateupArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -100,13 +104,13 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   int* nsx = reinterpret_cast<int*>(dxs + T * nbd);                // [T][nbd]  -8*sum(codes)
   float* hs = reinterpret_cast<float*>(xs + pl.xs_bytes + pl.aux_bytes);  // [2][32][T]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int nu = *a.w.n_union;
-  const long units = (long)nu * nhb;
-  const long u0 = units * blockIdx.x / gridDim.x;
-  const long u1 = units * (blockIdx.x + 1) / gridDim.x;
   constexpr int SPU = 32 / kGuRps;
-  const long nstage = (u1 - u0) * SPU;
+  const int G_ = gridDim.x, c = blockIdx.x;
+
+  // shared-expert units of this CTA: [a0, a1) of the nhb units of store slot E
+  const long UA = a.s.n_shared ? nhb : 0;
+  const long a0 = UA * c / G_, a1 = UA * (c + 1) / G_;
+  const long na = a1 - a0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < pl.nst; ++i) {
@@ -116,6 +120,39 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     abort_flag = 0;
     fence_barrier_init();
   }
+  __syncthreads();
+  const uint64_t pol = l2_evict_first_policy();
+  const bool producer = (warp == kNW && lane == 0);
+  long issued = 0;
+  if (producer) {
+    for (; issued < na * SPU && issued < pl.nst; ++issued) {
+      const long unit = a0 + issued / SPU;
+      const int sub = (int)(issued % SPU);
+      const uint8_t* src = a.st.wgu + ((long)a.s.E * f + unit * 32 + sub * kGuRps) * (long)d;
+      mbar_expect_tx(&full[issued], (uint32_t)pl.stage_bytes);
+      bulk_g2s(ring + issued * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[issued], pol);
+    }
+  }
+  // the routing grid is complete and its results visible from here on
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // routed units of this CTA: the total U = UA + UB is split evenly (each CTA's shared units
+  // count towards its share) when there are at least as many routed units as CTAs
+  const int nu = __ldcg(a.w.n_union);
+  const long UB = (long)(nu - (a.s.n_shared ? 1 : 0)) * nhb;
+  long b0, b1;
+  if (UB >= G_) {
+    const long U = UA + UB;
+    b0 = U * c / G_ - a0;
+    b1 = U * (c + 1) / G_ - a1;
+  } else {
+    b0 = UB * c / G_;
+    b1 = UB * (c + 1) / G_;
+  }
+  const long nunit = na + (b1 - b0);
+  const long nstage = nunit * SPU;
+
   // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of a
   // chunk live in separate planes so a warp's 16-byte loads are consecutive
   for (int idx = threadIdx.x; idx < T * nbd; idx += blockDim.x) {
@@ -123,31 +160,40 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     const int g = b / G, i = b - g * G;
     const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
     uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
-    *reinterpret_cast<uint4*>(base) = src[0];
-    *reinterpret_cast<uint4*>(base + nbd * 16) = src[1];
-    dxs[idx] = a.w.dx[(long)t * nbd + b];
-    nsx[idx] = -8 * a.w.sx[(long)t * nbd + b];
+    *reinterpret_cast<uint4*>(base) = __ldcg(src);
+    *reinterpret_cast<uint4*>(base + nbd * 16) = __ldcg(src + 1);
+    dxs[idx] = __ldcg(a.w.dx + (long)t * nbd + b);
+    nsx[idx] = -8 * __ldcg(a.w.sx + (long)t * nbd + b);
   }
   __syncthreads();
 
+  // local unit index -> (union slot, 32-row block)
+  auto unit_of = [&](long lu, int& slot, int& hb) {
+    if (lu < na) {
+      slot = nu - 1;
+      hb = (int)(a0 + lu);
+    } else {
+      const long r = b0 + (lu - na);
+      slot = (int)(r / nhb);
+      hb = (int)(r - (long)slot * nhb);
+    }
+  };
+
   if (warp == kNW) {
-    // ---------------- producer: one lane streams row-pair stages
-    if (lane == 0 && nstage > 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      long issued = 0;
-      for (long it = 0; it < nstage; ++it) {
+    // ---------------- producer: one lane streams the remaining stages
+    if (producer) {
+      for (long it = issued; it < nstage; ++it) {
         const int s = (int)(it % pl.nst);
         const long n = it / pl.nst;
         if (n > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((n - 1) & 1), &abort_flag, a.w.status))
           break;
-        const long unit = u0 + it / SPU;
-        const int sub = (int)(it % SPU);
-        const int slot = (int)(unit / nhb), hb = (int)(unit - (long)slot * nhb);
-        const int ex = a.w.union_ids[slot];
-        const uint8_t* src = a.st.wgu + ((long)ex * f + hb * 32 + sub * kGuRps) * (long)d;
+        int slot, hb;
+        unit_of(it / SPU, slot, hb);
+        const int ex = __ldcg(a.w.union_ids + slot);
+        const uint8_t* src = a.st.wgu + ((long)ex * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
-        ++issued;
+        issued = it + 1;
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
@@ -158,11 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     int nr[G];
     int cached_tok = -1;
     for (long it = 0; it < nstage; ++it) {
-      const long unit = u0 + it / SPU;
+      const long lu = it / SPU;
       const int sub = (int)(it % SPU);
-      const int slot = (int)(unit / nhb), hb = (int)(unit - (long)slot * nhb);
-      const int ex = a.w.union_ids[slot];
-      const int p0 = a.w.offsets[slot], np = a.w.offsets[slot + 1] - p0;
+      int slot, hb;
+      unit_of(lu, slot, hb);
+      const int ex = __ldcg(a.w.union_ids + slot);
+      const int p0 = __ldcg(a.w.offsets + slot), np = __ldcg(a.w.offsets + slot + 1) - p0;
       const int s = (int)(it % pl.nst);
       mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
       const int rr = sub * kGuRps + warp;
@@ -172,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       const float sg = scx[row], su = scx[f + row];
       for (int q = 0; q < np; ++q) {
         const int p = p0 + q;
-        const int t = a.w.pair_token[p];
+        const int t = __ldcg(a.w.pair_token + p);
         if (t != cached_tok) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -198,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         for (int i = 0; i < G; ++i) {
           uint4 wg = make_uint4(0, 0, 0, 0), wu = make_uint4(0, 0, 0, 0);
           if (lane < A) {
-            wg = *reinterpret_cast<const uint4*>(grow + (i * A + lane) * 16);
-            wu = *reinterpret_cast<const uint4*>(grow + d / 2 + (i * A + lane) * 16);
+            const int off = store_chunk(lane, i, G) * 16;
+            wg = *reinterpret_cast<const uint4*>(grow + off);
+            wu = *reinterpret_cast<const uint4*>(grow + d / 2 + off);
           }
           const int ag = block_dot(wg, xr[i], nr[i]);
           const int au = block_dot(wu, xr[i], nr[i]);
@@ -214,13 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         pg = warp_tree_sum(pg);
         pu = warp_tree_sum(pu);
         const float g = __fmul_rn(sg, pg), u = __fmul_rn(su, pu);
-        const float hv = canon_silu_mul(g, u);
         if (lane == 0) {
-          hs[((unit & 1) * 32 + rr) * T + q] = hv;
+          hs[((lu & 1) * 32 + rr) * T + q] = canon_silu_mul(g, u);
           if (a.dbg.g != nullptr) {
             a.dbg.g[(long)p * f + row] = g;
             a.dbg.u[(long)p * f + row] = u;
-            a.dbg.h[(long)p * f + row] = hv;
           }
         }
       }
@@ -230,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         // the unit's 32 rows of h are complete: quantise one int8 block per token
         named_bar_sync(1, kNW * 32);
         for (int q = warp; q < np; q += kNW) {
-          const float hv = hs[((unit & 1) * 32 + lane) * T + q];
+          const float hv = hs[((lu & 1) * 32 + lane) * T + q];
           const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
           const int code = q8_code(hv, dd);
           const int p = p0 + q;
+          a.w.hf[(long)p * f + hb * 32 + lane] = hv;
           a.w.qh[(long)p * f + hb * 32 + lane] = (int8_t)code;
           const int sq = warp_isum(code);
           if (lane == 0) {
@@ -249,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
 
 // ------------------------------------------------------------------ down + combine --------
 // Work unit = 16 output rows of y; a stage is those rows of one union expert's down matrix.
-// Warp w owns rows 2w, 2w+1 of the unit; once every union expert has been seen it combines
-// them for every token in the fixed order: shared expert first, then ranks 0..K-1.
+// The union is known when this grid starts (the router finished before the gate/up grid let
+// it launch), so the first stages are prefetched before waiting for the h codes.  Warp w owns
+// rows 2w, 2w+1 of the unit; once every union expert has been seen it combines them for every
+// token in the fixed order: shared expert first, then ranks 0..K-1.
 template <int GF>
 __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -258,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
   const int nbf = f >> 5, A = nbf / GF;
   const DownPlan& pl = a.pl;
-  const int nu = *a.w.n_union;
-  const int P = a.w.offsets[nu];
+  const int nu = __ldcg(a.w.n_union);
+  const int P = __ldcg(a.w.offsets + nu);
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -282,34 +331,45 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
     abort_flag = 0;
     fence_barrier_init();
   }
+  __syncthreads();
+  const uint64_t pol = l2_evict_first_policy();
+  const bool producer = (warp == kNW && lane == 0);
+  long issued = 0;
+  auto issue = [&](long it) {
+    const int s = (int)(it % pl.nst);
+    const long unit = u0 + it / nu;
+    const int slot = (int)(it % nu);
+    const int ex = __ldcg(a.w.union_ids + slot);
+    const uint8_t* src = a.st.wd + ((long)ex * d + unit * kDownRd) * (long)(f / 2);
+    mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
+    bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
+  };
+  if (producer)
+    for (; issued < nstage && issued < pl.nst; ++issued) issue(issued);
+  // gate/up grid complete: h codes visible from here on
+  griddep_wait();
+
   for (int idx = threadIdx.x; idx < P * nbf; idx += blockDim.x) {
     const int p = idx / nbf, b = idx - p * nbf;
     const int g = b / GF, i = b - g * GF;
     const uint4* src = reinterpret_cast<const uint4*>(a.w.qh + (long)p * f + b * 32);
     uint8_t* base = hq + (long)p * f + (i * A + g) * 16;
-    *reinterpret_cast<uint4*>(base) = src[0];
-    *reinterpret_cast<uint4*>(base + nbf * 16) = src[1];
-    hd[idx] = a.w.dh[(long)p * nbf + b];
-    hn[idx] = -8 * a.w.sh[(long)p * nbf + b];
+    *reinterpret_cast<uint4*>(base) = __ldcg(src);
+    *reinterpret_cast<uint4*>(base + nbf * 16) = __ldcg(src + 1);
+    hd[idx] = __ldcg(a.w.dh + (long)p * nbf + b);
+    hn[idx] = -8 * __ldcg(a.w.sh + (long)p * nbf + b);
   }
   __syncthreads();
 
   if (warp == kNW) {
-    if (lane == 0 && nstage > 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      long issued = 0;
-      for (long it = 0; it < nstage; ++it) {
-        const int s = (int)(it % pl.nst);
+    if (producer) {
+      for (long it = issued; it < nstage; ++it) {
         const long n = it / pl.nst;
-        if (n > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((n - 1) & 1), &abort_flag, a.w.status))
+        if (n > 0 && !mbar_wait_bounded(&empty[it % pl.nst], (uint32_t)((n - 1) & 1), &abort_flag,
+                                        a.w.status))
           break;
-        const long unit = u0 + it / nu;
-        const int slot = (int)(it % nu);
-        const int ex = a.w.union_ids[slot];
-        const uint8_t* src = a.st.wd + ((long)ex * d + unit * kDownRd) * (long)(f / 2);
-        mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
-        bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
-        ++issued;
+        issue(it);
+        issued = it + 1;
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
@@ -317,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
     for (long it = 0; it < nstage; ++it) {
       const long unit = u0 + it / nu;
       const int slot = (int)(it % nu);
-      const int ex = a.w.union_ids[slot];
-      const int p0 = a.w.offsets[slot], np = a.w.offsets[slot + 1] - p0;
+      const int ex = __ldcg(a.w.union_ids + slot);
+      const int p0 = __ldcg(a.w.offsets + slot), np = __ldcg(a.w.offsets + slot + 1) - p0;
       const int s = (int)(it % pl.nst);
       mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
       const int lr = warp * kDownRowsPerWarp;  // local row within the unit
@@ -328,8 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
 #pragma unroll
       for (int i = 0; i < GF; ++i) {
         if (lane < A) {
-          w0[i] = *reinterpret_cast<const uint4*>(srow + (i * A + lane) * 16);
-          w1[i] = *reinterpret_cast<const uint4*>(srow + f / 2 + (i * A + lane) * 16);
+          const int off = store_chunk(lane, i, GF) * 16;
+          w0[i] = *reinterpret_cast<const uint4*>(srow + off);
+          w1[i] = *reinterpret_cast<const uint4*>(srow + f / 2 + off);
         } else {
           w0[i] = make_uint4(0, 0, 0, 0);
           w1[i] = make_uint4(0, 0, 0, 0);
@@ -393,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
           for (int j = 0; j < kDownRowsPerWarp; ++j) {
             const float* er = es + (lr + j) * P;
             float y = a.s.n_shared ? er[T * K + t] : 0.0f;
-            for (int k = 0; k < K; ++k) y = __fmaf_rn(a.w.w[t * K + k], er[a.w.inv[t * K + k]], y);
+            for (int k = 0; k < K; ++k)
+              y = __fmaf_rn(__ldcg(a.w.w + t * K + k), er[__ldcg(a.w.inv + t * K + k)], y);
             if (a.s.has_norm) y = __fadd_rn(a.x[(long)t * d + r0 + j], y);
             a.y[(long)t * d + r0 + j] = y;
           }
@@ -406,16 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
 }
 
 // ------------------------------------------------------------------ launchers -------------
-template <int G>
-static cudaError_t gateup_launch_g(const GateupArgs& args, int grid, cudaStream_t stream) {
-  gateup_decode_kernel<G><<<grid, kThreads, args.pl.total, stream>>>(args);
-  return cudaGetLastError();
-}
-
-template <int G>
-static cudaError_t down_launch_g(const DownArgs& args, int grid, cudaStream_t stream) {
-  down_decode_kernel<G><<<grid, kThreads, args.pl.total, stream>>>(args);
-  return cudaGetLastError();
+template <class Args>
+static cudaError_t launch_ex(void (*kern)(const Args), const Args& args, int grid, int smem,
+                             bool pdl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 cudaError_t configure_expert_kernels() {
@@ -436,45 +502,50 @@ cudaError_t configure_expert_kernels() {
 }
 
 cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
-                                 const ExpertDebug& dbg, int num_sms, cudaStream_t stream) {
+                                 const ExpertDebug& dbg, int num_sms, bool pdl,
+                                 cudaStream_t stream) {
   GateupArgs args{s, st, w, dbg, gateup_plan(s.d, s.f, s.T)};
   const int G = (s.d / kQB + 31) / 32;
   // the unit count depends on the union size, known only on the device: size the grid for
-  // the largest possible union and let idle CTAs exit
-  const long max_units = (long)(s.T * s.K < s.E ? s.T * s.K : s.E) + s.n_shared;
-  long grid = max_units * (s.f / kQB);
+  // the largest possible union (CTAs without work exit)
+  const long max_slots = (long)(s.T * s.K < s.E ? s.T * s.K : s.E) + s.n_shared;
+  long grid = max_slots * (s.f / 32);
   if (grid > num_sms) grid = num_sms;
+  void (*k)(const GateupArgs) = nullptr;
   switch (G) {
-    case 1: return gateup_launch_g<1>(args, (int)grid, stream);
-    case 2: return gateup_launch_g<2>(args, (int)grid, stream);
-    case 3: return gateup_launch_g<3>(args, (int)grid, stream);
-    case 4: return gateup_launch_g<4>(args, (int)grid, stream);
-    case 5: return gateup_launch_g<5>(args, (int)grid, stream);
-    case 6: return gateup_launch_g<6>(args, (int)grid, stream);
-    case 7: return gateup_launch_g<7>(args, (int)grid, stream);
-    case 8: return gateup_launch_g<8>(args, (int)grid, stream);
+    case 1: k = gateup_decode_kernel<1>; break;
+    case 2: k = gateup_decode_kernel<2>; break;
+    case 3: k = gateup_decode_kernel<3>; break;
+    case 4: k = gateup_decode_kernel<4>; break;
+    case 5: k = gateup_decode_kernel<5>; break;
+    case 6: k = gateup_decode_kernel<6>; break;
+    case 7: k = gateup_decode_kernel<7>; break;
+    case 8: k = gateup_decode_kernel<8>; break;
     default: return cudaErrorInvalidValue;
   }
+  return launch_ex(k, args, (int)grid, args.pl.total, pdl, stream);
 }
 
 cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
-                               const Work& w, const ExpertDebug& dbg, int num_sms,
+                               const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream) {
   DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.n_shared), x, y};
   const int GF = (s.f / kQB + 31) / 32;
   long grid = s.d / kDownRd;
   if (grid > num_sms) grid = num_sms;
+  void (*k)(const DownArgs) = nullptr;
   switch (GF) {
-    case 1: return down_launch_g<1>(args, (int)grid, stream);
-    case 2: return down_launch_g<2>(args, (int)grid, stream);
-    case 3: return down_launch_g<3>(args, (int)grid, stream);
-    case 4: return down_launch_g<4>(args, (int)grid, stream);
-    case 5: return down_launch_g<5>(args, (int)grid, stream);
-    case 6: return down_launch_g<6>(args, (int)grid, stream);
-    case 7: return down_launch_g<7>(args, (int)grid, stream);
-    case 8: return down_launch_g<8>(args, (int)grid, stream);
+    case 1: k = down_decode_kernel<1>; break;
+    case 2: k = down_decode_kernel<2>; break;
+    case 3: k = down_decode_kernel<3>; break;
+    case 4: k = down_decode_kernel<4>; break;
+    case 5: k = down_decode_kernel<5>; break;
+    case 6: k = down_decode_kernel<6>; break;
+    case 7: k = down_decode_kernel<7>; break;
+    case 8: k = down_decode_kernel<8>; break;
     default: return cudaErrorInvalidValue;
   }
+  return launch_ex(k, args, (int)grid, args.pl.total, pdl, stream);
 }
 
 }  // namespace coli

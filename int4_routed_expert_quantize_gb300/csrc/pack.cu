@@ -69,8 +69,9 @@ cudaError_t launch_quantize_q8(const float* x, int64_t n, int8_t* q, float* d,
 }
 
 // Canonical row (two's-complement nibbles, element 2m low / 2m+1 high in byte m of a block)
-// -> store layout: block b = g*G + i of the row goes to chunk i*A + g, and inside the chunk
-// word k byte m holds element 8k+m (low nibble) and 8k+m+4 (high nibble) as code + 8.
+// -> store layout: block b = g*G + i of the row goes to chunk store_chunk(g, i, G) (groups
+// contiguous, rotated inside), and inside the chunk word k byte m holds element 8k+m (low
+// nibble) and 8k+m+4 (high nibble) as code + 8.
 // For a 4-bit two's-complement nibble, code + 8 is the nibble with its top bit flipped.
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__ src,
                                                      uint8_t* __restrict__ dst, int rows, int cols,
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__
   if (idx >= (long)rows * nb) return;
   const long r = idx / nb;
   const int b = (int)(idx - r * nb);
-  const int G = (nb + 31) / 32, A = nb / G;
+  const int G = (nb + 31) / 32;
   const int g = b / G, i = b - g * G;
   const uint4 c = *reinterpret_cast<const uint4*>(src + r * (cols / 2) + (long)b * 16);
   const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__
     for (int m = 0; m < 4; ++m) v |= (nib[8 * k + m] | (nib[8 * k + m + 4] << 4)) << (8 * m);
     out[k] = v;
   }
-  *reinterpret_cast<uint4*>(dst + r * dst_row_stride + (long)(i * A + g) * 16) =
+  *reinterpret_cast<uint4*>(dst + r * dst_row_stride + (long)store_chunk(g, i, G) * 16) =
       make_uint4(out[0], out[1], out[2], out[3]);
 }
 

@@ -1,5 +1,5 @@
-// Routing half of the layer: activation preparation (optional RMSNorm, Q8_0-style int8
-// blocks of 32) and the sigmoid top-K router with the batch union.
+// Routing half of the layer in one launch: activation preparation (optional RMSNorm,
+// Q8_0-style int8 blocks of 32) and the sigmoid top-K router with the batch union.
 //   "colibrì 架构概述" §3.1 (IDOT: decode activations quantised to int8), §5 (moe step:
 //   sigmoid routing, top-8), the ai4coding.ru page (DeepSeek-V3-style sigmoid router,
 //   Q8_0-style int8 activations) and the README's batch union (each distinct expert of a
@@ -11,62 +11,6 @@
 #include "coli_internal.h"
 
 namespace coli {
-
-// ------------------------------------------------------------------ prep -----------------
-// One CTA per token: x_n = RMSNorm(x) (or x), written in natural order and in the router's
-// chunk order; then int8 codes, block scales and block code sums.
-__global__ void __launch_bounds__(256) prep_kernel(const float* __restrict__ x, const Shape s,
-                                                   const Store st, const Work w) {
-  extern __shared__ float xs[];  // [d]
-  __shared__ float rinv;
-  const int t = blockIdx.x, d = s.d, nbd = d >> 5, Gd = d >> 5;  // Gd: elements per lane group
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
-  const float* xt = x + (long)t * d;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) xs[j] = xt[j];
-  __syncthreads();
-  if (s.has_norm) {
-    if (warp == 0) {
-      float p = 0.0f;
-      for (int j = lane * Gd; j < lane * Gd + Gd; ++j) p = __fmaf_rn(xs[j], xs[j], p);
-      p = warp_tree_sum(p);
-      if (lane == 0) {
-        const float ms = __fdiv_rn(p, (float)d);
-        rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, s.rms_eps)));
-      }
-    }
-    __syncthreads();
-    const float r = rinv;
-    for (int j = threadIdx.x; j < d; j += blockDim.x)
-      xs[j] = __fmul_rn(__fmul_rn(xs[j], r), st.gamma[j]);
-    __syncthreads();
-  }
-  float* xn = w.xn + (long)t * d;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) xn[j] = xs[j];
-  // router order: lane g's elements g*Gd + 4*i4 .. +3 at 4-float chunk i4*32 + g
-  float4* xp = reinterpret_cast<float4*>(w.xnp + (long)t * d);
-  for (int c = threadIdx.x; c < d / 4; c += blockDim.x) {
-    const int i4 = c >> 5, g = c & 31;
-    const float* src = xs + g * Gd + 4 * i4;
-    xp[c] = make_float4(src[0], src[1], src[2], src[3]);
-  }
-  for (int b = warp; b < nbd; b += nwarp) {
-    const float v = xs[b * 32 + lane];
-    const float dd = __fdiv_rn(warp_max(fabsf(v)), 127.0f);
-    const int q = q8_code(v, dd);
-    w.qx[(long)t * d + b * 32 + lane] = (int8_t)q;
-    const int sq = warp_isum(q);
-    if (lane == 0) {
-      w.dx[(long)t * nbd + b] = dd;
-      w.sx[(long)t * nbd + b] = sq;
-    }
-  }
-}
-
-cudaError_t launch_prep(const float* x, const Shape& s, const Store& st, const Work& w,
-                        cudaStream_t stream) {
-  prep_kernel<<<s.T, 256, s.d * sizeof(float), stream>>>(x, s, st, w);
-  return cudaGetLastError();
-}
 
 // ------------------------------------------------------------------ router ---------------
 constexpr int kRouterEpc = 2;  // experts per CTA
@@ -187,24 +131,95 @@ __device__ void union_bucket(const Shape& s, const Work& w, int* cnt, int* curso
   }
 }
 
-// Each CTA computes the logits of kRouterEpc experts for every token (one warp per
-// (expert, token): lane g runs the fma chain over its d/32 contiguous elements, the warp
-// butterfly adds the 32 partials); the last CTA to finish selects the experts and builds
-// the union (last-block pattern: fence, ticket, no waiting).
-__global__ void __launch_bounds__(256) router_kernel(const Shape s, const Store st, const Work w) {
+// One launch does the whole routing half.  Every CTA: bulk-prefetches its kRouterEpc router
+// rows into L2, lets the gate/up grid start its weight prefetch, normalises the tokens
+// (RMSNorm, one warp per token) into shared memory in the router's chunk order, writes its share
+// of the int8 activation blocks (one warp per block of 32), then computes the logits of its
+// experts for every token (one warp per (expert, token): lane g runs the fma chain over its d/32
+// contiguous elements, the warp butterfly adds the 32 partials).  The last CTA to finish
+// (ticket counter, no waiting) selects the experts and builds the union.
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x, const Shape s,
+                                                    const Store st, const Work w) {
+  extern __shared__ __align__(16) float xsm[];  // [T][d] normalised tokens, router chunk order
+  __shared__ float rinv[kDecodeTmax];
   __shared__ int cnt[kMaxE];
   __shared__ int cursor[kMaxE];
   __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
-  const int d = s.d, E = s.E, T = s.T;
+  const int d = s.d, E = s.E, T = s.T, Gd = d >> 5, nbd = d >> 5;
   const int e0 = blockIdx.x * kRouterEpc;
   const int ne = min(kRouterEpc, E - e0);
+  if (threadIdx.x == 0)
+    for (int r = 0; r < ne; ++r) bulk_prefetch_l2(st.wr + (long)(e0 + r) * d, (uint32_t)d * 4u);
+  griddep_launch_dependents();
+
+  // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
+  // i4*32 + g (coalesced float4 loads; conflict-free reads by lane)
+  for (int c = threadIdx.x; c < T * (d / 4); c += blockDim.x) {
+    const int t = c / (d / 4), pos = c - t * (d / 4);
+    const int i4 = pos >> 5, g = pos & 31;
+    reinterpret_cast<float4*>(xsm + (long)t * d)[pos] =
+        *reinterpret_cast<const float4*>(x + (long)t * d + g * Gd + 4 * i4);
+  }
+  __syncthreads();
+  if (s.has_norm) {
+    // mean of squares in the canonical order (lane g: fma chain over its d/32 elements)
+    for (int t = warp; t < T; t += nwarp) {
+      const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
+      float p = 0.0f;
+      for (int i4 = 0; i4 < d / 128; ++i4) {
+        const float4 v = xp[i4 * 32 + lane];
+        p = __fmaf_rn(v.x, v.x, p);
+        p = __fmaf_rn(v.y, v.y, p);
+        p = __fmaf_rn(v.z, v.z, p);
+        p = __fmaf_rn(v.w, v.w, p);
+      }
+      p = warp_tree_sum(p);
+      if (lane == 0) {
+        const float ms = __fdiv_rn(p, (float)d);
+        rinv[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, s.rms_eps)));
+      }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < T * (d / 4); c += blockDim.x) {
+      const int t = c / (d / 4), pos = c - t * (d / 4);
+      const int i4 = pos >> 5, g = pos & 31;
+      const float r = rinv[t];
+      const float4 gm = *reinterpret_cast<const float4*>(st.gamma + g * Gd + 4 * i4);
+      float4 v = reinterpret_cast<float4*>(xsm + (long)t * d)[pos];
+      v.x = __fmul_rn(__fmul_rn(v.x, r), gm.x);
+      v.y = __fmul_rn(__fmul_rn(v.y, r), gm.y);
+      v.z = __fmul_rn(__fmul_rn(v.z, r), gm.z);
+      v.w = __fmul_rn(__fmul_rn(v.w, r), gm.w);
+      reinterpret_cast<float4*>(xsm + (long)t * d)[pos] = v;
+    }
+    __syncthreads();
+  }
+
+  // this CTA's share of the activation blocks: x_n (natural order), int8 codes, scale, code sum
+  for (int b = blockIdx.x * nwarp + warp; b < T * nbd; b += gridDim.x * nwarp) {
+    const int t = b / nbd, bb = b - t * nbd;
+    const int j = bb * 32 + lane;
+    const int g = j / Gd, m = j - g * Gd;
+    const float v = xsm[(long)t * d + ((m >> 2) * 32 + g) * 4 + (m & 3)];
+    w.xn[(long)t * d + j] = v;
+    const float dd = __fdiv_rn(warp_max(fabsf(v)), 127.0f);
+    const int q = q8_code(v, dd);
+    w.qx[(long)t * d + j] = (int8_t)q;
+    const int sq = warp_isum(q);
+    if (lane == 0) {
+      w.dx[(long)t * nbd + bb] = dd;
+      w.sx[(long)t * nbd + bb] = sq;
+    }
+  }
+
   const int nchunk = d / 128;  // 4-float chunks per lane
   for (int pi = warp; pi < ne * T; pi += nwarp) {
     const int e = e0 + pi / T, t = pi % T;
     const float4* wr = reinterpret_cast<const float4*>(st.wr + (long)e * d);
-    const float4* xp = reinterpret_cast<const float4*>(w.xnp + (long)t * d);
+    const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
     float p = 0.0f;
+#pragma unroll 8
     for (int i4 = 0; i4 < nchunk; ++i4) {
       const float4 a = __ldg(wr + i4 * 32 + lane);
       const float4 b = xp[i4 * 32 + lane];
@@ -231,11 +246,18 @@ __global__ void __launch_bounds__(256) router_kernel(const Shape s, const Store 
   if (threadIdx.x == 0) *w.counter = 0;  // ready for the next call
 }
 
-cudaError_t launch_router(const Shape& s, const Store& st, const Work& w, int num_sms,
-                          cudaStream_t stream) {
-  (void)num_sms;
+constexpr int kRouteSmemMax = kDecodeTmax * 8192 * 4;
+
+cudaError_t configure_route_kernels() {
+  return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kRouteSmemMax);
+}
+
+cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const Work& w,
+                         cudaStream_t stream) {
+  // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work
   const int grid = (s.E + kRouterEpc - 1) / kRouterEpc;
-  router_kernel<<<grid, 256, 0, stream>>>(s, st, w);
+  route_kernel<<<grid, 256, (size_t)s.T * s.d * sizeof(float), stream>>>(x, s, st, w);
   return cudaGetLastError();
 }
 

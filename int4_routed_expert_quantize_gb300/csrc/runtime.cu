@@ -96,23 +96,23 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
   if (dump) {
     dbg.g = dump->g;
     dbg.u = dump->u;
-    dbg.h = dump->h;
     dbg.e = dump->e;
     dbg.Ag = dump->Ag;
     dbg.Au = dump->Au;
     dbg.Ad = dump->Ad;
-    if ((dbg.g || dbg.u || dbg.h) && !(dbg.g && dbg.u && dbg.h)) return COLI_EINVAL;
+    if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
     if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
   }
+  // route (ordinary launch) -> gate/up -> down; the expert kernels are programmatic dependents
+  // that prefetch weights before waiting, unless events are recorded between the launches
+  const bool pdl = (ev == nullptr);
   cudaError_t e = ev ? cudaEventRecord(ev[0], stream) : cudaSuccess;
-  if (e == cudaSuccess) e = launch_prep(x, s, h->st, h->w, stream);
+  if (e == cudaSuccess) e = launch_route(x, s, h->st, h->w, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], stream);
-  if (e == cudaSuccess) e = launch_router(s, h->st, h->w, h->num_sms, stream);
+  if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, pdl, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
-  if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, stream);
+  if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], stream);
-  if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, stream);
-  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], stream);
   if (e != cudaSuccess) return COLI_ECUDA;
   if (dump) {
     const coli_moe_config& c = h->cfg;
@@ -135,6 +135,7 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
         {dump->pair_token, h->w.pair_token, sizeof(int32_t) * P},
         {dump->pair_rank, h->w.pair_rank, sizeof(int32_t) * P},
         {dump->inv, h->w.inv, sizeof(int32_t) * T * c.top_k},
+        {dump->h, h->w.hf, sizeof(float) * P * c.f},
         {dump->qh, h->w.qh, (size_t)P * c.f},
         {dump->dh, h->w.dh, sizeof(float) * P * (c.f / 32)},
     };
@@ -150,7 +151,7 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
                  void* stream) {
   if (!h || T < 0 || T > h->cfg.max_tokens) return COLI_EINVAL;
   if (T == 0) return COLI_OK;
-  if (!x || !y) return COLI_EINVAL;
+  if (!x || !y || ((uintptr_t)x & 15u) || ((uintptr_t)y & 3u)) return COLI_EINVAL;
   const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
   if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
   if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
@@ -210,7 +211,10 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     cudaGetLastError();
     return COLI_ECUDA;
   }
-  std::call_once(g_cfg_once, [] { g_cfg_err = configure_expert_kernels(); });
+  std::call_once(g_cfg_once, [] {
+    g_cfg_err = configure_expert_kernels();
+    if (g_cfg_err == cudaSuccess) g_cfg_err = configure_route_kernels();
+  });
   if (g_cfg_err != cudaSuccess) return COLI_ECUDA;
 
   coli_moe* h = new (std::nothrow) coli_moe();
@@ -248,6 +252,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.pair_token, sizeof(int32_t) * Pm)
   ALLOC(h->w.pair_rank, sizeof(int32_t) * Pm)
   ALLOC(h->w.inv, sizeof(int32_t) * Tm * K)
+  ALLOC(h->w.hf, sizeof(float) * Pm * f)
   ALLOC(h->w.qh, Pm * f)
   ALLOC(h->w.dh, sizeof(float) * Pm * (f / 32))
   ALLOC(h->w.sh, sizeof(int32_t) * Pm * (f / 32))
@@ -376,19 +381,19 @@ int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
 
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream) {
-  if (!h || !events || n_events < 5 || T < 1 || T > kDecodeTmax || T > h->cfg.max_tokens)
+  if (!h || !events || n_events < 4 || T < 1 || T > kDecodeTmax || T > h->cfg.max_tokens)
     return COLI_EINVAL;
-  for (int i = 0; i < 5; ++i)
+  for (int i = 0; i < 4; ++i)
     if (!events[i]) return COLI_EINVAL;
-  if (!x_dev || !y_dev) return COLI_EINVAL;
+  if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15u) || ((uintptr_t)y_dev & 3u)) return COLI_EINVAL;
   const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
   if (x_dev != y_dev && overlap(x_dev, bytes, y_dev, bytes)) return COLI_EINVAL;
   if (x_dev == y_dev && !h->cfg.has_norm) return COLI_EINVAL;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
   int rc = check_device(h);
   if (rc) return rc;
-  cudaEvent_t ev[5];
-  for (int i = 0; i < 5; ++i) ev[i] = (cudaEvent_t)events[i];
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = (cudaEvent_t)events[i];
   return run_decode(h, x_dev, T, y_dev, nullptr, (cudaStream_t)stream, ev);
 }
 
@@ -435,8 +440,9 @@ int coli_moe_status(coli_moe* h, void* stream) {
       cudaStreamSynchronize(st) != cudaSuccess)
     return COLI_ECUDA;
   if (v != COLI_OK) {
-    const int32_t zero = 0;
-    if (cudaMemcpy(h->w.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    // an aborted call may leave the router's ticket counter mid-count: clear it with the status
+    if (cudaMemset(h->w.status, 0, 16) != cudaSuccess || cudaMemset(h->w.counter, 0, 16) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
       return COLI_ECUDA;
     return v;
   }

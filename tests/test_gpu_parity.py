@@ -147,6 +147,17 @@ def test_tiny_host_buffers(tiny):
     assert L.status() == 0
 
 
+def test_tiny_profiled_matches_forward(tiny):
+    wl, L, OL = tiny
+    x = synthetic.x_tokens(wl, 3, token0=55)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    y = torch.empty_like(x)
+    L.forward_profiled(x, y, ev)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(y), to_np(L.forward(x)))
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(3))
+
+
 def test_tiny_edge_cases(tiny):
     wl, L, OL = tiny
     x = synthetic.x_tokens(wl, 2)
@@ -159,6 +170,7 @@ def test_tiny_edge_cases(tiny):
     assert lib.coli_moe_forward(L.h, x.data_ptr(), 2, x[1:].data_ptr(), None) == -1  # overlap
     assert lib.coli_moe_forward(L.h, x.data_ptr(), 2, y.data_ptr(), None) == 0
     assert lib.coli_moe_load_experts(L.h, 30, 5, x.data_ptr(), x.data_ptr(), None) == -1  # ids > E
+    assert lib.coli_moe_forward(L.h, x.data_ptr() + 4, 1, y.data_ptr(), None) == -1  # misaligned x
 
 
 def test_forward_before_load_is_state_error():
