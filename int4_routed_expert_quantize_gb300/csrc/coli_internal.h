@@ -2,6 +2,8 @@
 // workspace and the kernel launchers.  Not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +23,7 @@ constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for
 constexpr int kGateupSmem = 160 * 1024;         // gate/up ring budget: leaves room on the SM for
                                                 // a routing CTA while its prefetch runs
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
+constexpr int kPrefillTileN = 64;               // pairs per tensor-core tile
 
 // Store layout (built by the repack kernel at load time):
 //  * a matrix row of n int4 values is n/32 blocks of 16 bytes.  With nb = n/32 blocks and
@@ -67,6 +70,19 @@ struct Work {
   int32_t* status = nullptr;   // COLI_OK or COLI_ETIMEOUT
 };
 
+// workspace of the batched (tensor-core) path; rows padded by one tile for the copies
+struct PrefillWork {
+  __nv_bfloat16* xb = nullptr;  // [Pm+64][d] every pair's activation codes as bf16
+  float* dxp = nullptr;         // [Pm+64][d/32] their block scales
+  __nv_bfloat16* hb = nullptr;  // [Pm+64][f] h codes as bf16 (down projection operand)
+  float* e = nullptr;           // [Pm][d] expert outputs per pair
+  int32_t* tile_prefix = nullptr;  // [E+2] per union slot: 64-pair tiles before it
+};
+
+struct PrefillMaps {
+  CUtensorMap wgu, wd, xb, hb;
+};
+
 struct Shape {
   int d, f, E, K, n_shared, T;
   float routed_scale, rms_eps;
@@ -95,6 +111,16 @@ cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const S
                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream);
 cudaError_t configure_route_kernels();
+cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, const Work& w,
+                               int32_t* tile_prefix, int tile_n, __nv_bfloat16* xb, float* dxp,
+                               cudaStream_t stream);
+cudaError_t configure_prefill_kernels(int d, int f, int E);
+int prefill_smem_bytes(int d, int f, int E, int down);
+bool prefill_make_maps(PrefillMaps* maps, const Store& st, const PrefillWork& pw, int d, int f,
+                       int slots, int prow);
+cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, const Store& st,
+                                   const Work& w, const PrefillWork& pw, const PrefillMaps& maps,
+                                   const ExpertDebug& dbg, int num_sms, cudaStream_t stream);
 cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
                                  int64_t dst_row_stride, cudaStream_t stream);
 cudaError_t launch_permute_router(const float* src, float* dst, int E, int d,
@@ -107,12 +133,12 @@ cudaError_t configure_expert_kernels();
 
 // shared-memory plans (host and device agree on the carve-up)
 struct GateupPlan {
-  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, total;
+  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, tab_bytes, max_units, total;
 };
 struct DownPlan {
-  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, total;
+  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, tab_bytes, max_rows, max_slots, total;
 };
-GateupPlan gateup_plan(int d, int f, int T);
-DownPlan down_plan(int d, int f, int T, int K, int n_shared);
+GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
+DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 
 }  // namespace coli

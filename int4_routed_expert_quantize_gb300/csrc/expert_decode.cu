@@ -21,23 +21,35 @@ namespace coli {
 
 static inline int align16(int x) { return (x + 15) & ~15; }
 
-GateupPlan gateup_plan(int d, int f, int T) {
-  (void)f;
+// per-CTA unit table of the gate/up kernel: slot, expert, first pair, pair count, the pairs'
+// tokens (T at most) and the 32 gate + 32 up row scales
+constexpr int kGuTabInts = 4 + kDecodeTmax;
+constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
+
+static long max_union_slots(int T, int K, int E, int n_shared) {
+  return (long)(T * K < E ? T * K : E) + (n_shared ? 1 : 0);
+}
+
+GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   GateupPlan p;
   const int nbd = d / kQB;
   p.stage_bytes = kGuRps * d;
   p.xs_bytes = align16(T * d);
   p.aux_bytes = align16(T * nbd * 8);
   p.hs_bytes = align16(2 * 32 * T * 4);
-  const int fixed = 2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes;
+  const long units = max_union_slots(T, K, E, n_shared) * (f / 32);
+  p.max_units = (int)((units + grid - 1) / grid) + 2;
+  p.tab_bytes = align16(p.max_units * kGuTabBytes);
+  const int fixed = 2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes + p.tab_bytes;
   int nst = ((kGateupSmem > fixed + 2 * p.stage_bytes ? kGateupSmem : kSmemLimit) - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
   return p;
 }
 
-DownPlan down_plan(int d, int f, int T, int K, int n_shared) {
-  (void)d;
+// per-CTA tables of the down kernel: union slots (expert, first pair), routing weights and pair
+// indices, and the down-row scales of this CTA's rows for every slot
+DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   DownPlan p;
   const int P = T * K + (n_shared ? T : 0);
   const int nbf = f / kQB;
@@ -45,7 +57,11 @@ DownPlan down_plan(int d, int f, int T, int K, int n_shared) {
   p.hq_bytes = align16(P * f);
   p.aux_bytes = align16(P * nbf * 8);
   p.es_bytes = align16(kDownRd * P * 4);
-  const int fixed = 2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes;
+  p.max_slots = (int)max_union_slots(T, K, E, n_shared);
+  const long units = d / kDownRd;
+  p.max_rows = (int)((units + grid - 1) / grid) * kDownRd;
+  p.tab_bytes = align16((2 * (p.max_slots + 1) + 2 * T * K) * 4 + p.max_slots * p.max_rows * 4);
+  const int fixed = 2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes + p.tab_bytes;
   int nst = (kSmemLimit - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
@@ -103,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   float* dxs = reinterpret_cast<float*>(xs + pl.xs_bytes);         // [T][nbd]
   int* nsx = reinterpret_cast<int*>(dxs + T * nbd);                // [T][nbd]  -8*sum(codes)
   float* hs = reinterpret_cast<float*>(xs + pl.xs_bytes + pl.aux_bytes);  // [2][32][T]
+  int* tab = reinterpret_cast<int*>(xs + pl.xs_bytes + pl.aux_bytes + pl.hs_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int SPU = 32 / kGuRps;
   const int G_ = gridDim.x, c = blockIdx.x;
@@ -165,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     dxs[idx] = __ldcg(a.w.dx + (long)t * nbd + b);
     nsx[idx] = -8 * __ldcg(a.w.sx + (long)t * nbd + b);
   }
-  __syncthreads();
 
   // local unit index -> (union slot, 32-row block)
   auto unit_of = [&](long lu, int& slot, int& hb) {
@@ -178,6 +194,32 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       hb = (int)(r - (long)slot * nhb);
     }
   };
+  auto unit_hb = [&](long lu) {
+    int slot, hb;
+    unit_of(lu, slot, hb);
+    return hb;
+  };
+  // unit table: every value a stage needs, loaded once (one round of memory latency)
+  for (int lu = warp; lu < nunit && lu < pl.max_units; lu += kNW + 1) {
+    int slot, hb;
+    unit_of(lu, slot, hb);
+    int* tu = tab + lu * (kGuTabInts + 64);
+    const int ex = __ldcg(a.w.union_ids + slot);
+    const int p0 = __ldcg(a.w.offsets + slot);
+    const int np = __ldcg(a.w.offsets + slot + 1) - p0;
+    if (lane == 0) {
+      tu[0] = slot;
+      tu[1] = ex;
+      tu[2] = p0;
+      tu[3] = np;
+    }
+    if (lane < np && lane < kDecodeTmax) tu[4 + lane] = __ldcg(a.w.pair_token + p0 + lane);
+    const float* scx = a.st.sc + (long)ex * (2 * f + d);
+    float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
+    tsc[lane] = scx[hb * 32 + lane];
+    tsc[32 + lane] = scx[f + hb * 32 + lane];
+  }
+  __syncthreads();
 
   if (warp == kNW) {
     // ---------------- producer: one lane streams the remaining stages
@@ -189,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
           break;
         int slot, hb;
         unit_of(it / SPU, slot, hb);
-        const int ex = __ldcg(a.w.union_ids + slot);
+        const int ex = tab[(it / SPU) * (kGuTabInts + 64) + 1];
         const uint8_t* src = a.st.wgu + ((long)ex * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
@@ -206,20 +248,19 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     for (long it = 0; it < nstage; ++it) {
       const long lu = it / SPU;
       const int sub = (int)(it % SPU);
-      int slot, hb;
-      unit_of(lu, slot, hb);
-      const int ex = __ldcg(a.w.union_ids + slot);
-      const int p0 = __ldcg(a.w.offsets + slot), np = __ldcg(a.w.offsets + slot + 1) - p0;
+      const int* tu = tab + lu * (kGuTabInts + 64);
+      const int hb = unit_hb(lu);
+      const int p0 = tu[2], np = tu[3];
       const int s = (int)(it % pl.nst);
       mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
       const int rr = sub * kGuRps + warp;
       const int row = hb * 32 + rr;
       const uint8_t* grow = ring + (long)s * pl.stage_bytes + (long)warp * d;
-      const float* scx = a.st.sc + (long)ex * (2 * f + d);
-      const float sg = scx[row], su = scx[f + row];
+      const float* tsc = reinterpret_cast<const float*>(tu + kGuTabInts);
+      const float sg = tsc[rr], su = tsc[32 + rr];
       for (int q = 0; q < np; ++q) {
         const int p = p0 + q;
-        const int t = __ldcg(a.w.pair_token + p);
+        const int t = tu[4 + q];
         if (t != cached_tok) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -316,6 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf]
   int* hn = reinterpret_cast<int*>(hd + P * nbf);                  // [P][nbf]  -8*sum(codes)
   float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [kDownRd][P]
+  int* t_ex = reinterpret_cast<int*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
+  int* t_off = t_ex + pl.max_slots + 1;
+  float* t_w = reinterpret_cast<float*>(t_off + pl.max_slots + 1);  // [T*K]
+  int* t_inv = reinterpret_cast<int*>(t_w + T * K);                 // [T*K]
+  float* t_sd = reinterpret_cast<float*>(t_inv + T * K);            // [slot][max_rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const long units = d / kDownRd;
@@ -335,17 +381,33 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
   long issued = 0;
-  auto issue = [&](long it) {
+  auto issue = [&](long it, int ex) {
     const int s = (int)(it % pl.nst);
     const long unit = u0 + it / nu;
-    const int slot = (int)(it % nu);
-    const int ex = __ldcg(a.w.union_ids + slot);
     const uint8_t* src = a.st.wd + ((long)ex * d + unit * kDownRd) * (long)(f / 2);
     mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
     bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
   };
+  // the routing results are complete when this grid starts: prefetch the first stages and
+  // build the CTA's tables (union slots, weights, pair indices, down-row scales) before the
+  // wait for the gate/up grid
   if (producer)
-    for (; issued < nstage && issued < pl.nst; ++issued) issue(issued);
+    for (; issued < nstage && issued < pl.nst; ++issued)
+      issue(issued, __ldcg(a.w.union_ids + (int)(issued % nu)));
+  const int row0 = (int)u0 * kDownRd, nrow = (int)(u1 - u0) * kDownRd;
+  for (int i = threadIdx.x; i <= nu; i += blockDim.x) {
+    t_ex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
+    t_off[i] = __ldcg(a.w.offsets + i);
+  }
+  for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
+    t_w[i] = __ldcg(a.w.w + i);
+    t_inv[i] = __ldcg(a.w.inv + i);
+  }
+  for (int i = threadIdx.x; i < nu * nrow; i += blockDim.x) {
+    const int slot = i / nrow, r = i - slot * nrow;
+    const int ex = __ldcg(a.w.union_ids + slot);
+    t_sd[slot * pl.max_rows + r] = a.st.sc[(long)ex * (2 * f + d) + 2 * f + row0 + r];
+  }
   // gate/up grid complete: h codes visible from here on
   griddep_wait();
 
@@ -368,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
         if (n > 0 && !mbar_wait_bounded(&empty[it % pl.nst], (uint32_t)((n - 1) & 1), &abort_flag,
                                         a.w.status))
           break;
-        issue(it);
+        issue(it, t_ex[it % nu]);
         issued = it + 1;
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
@@ -377,8 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
     for (long it = 0; it < nstage; ++it) {
       const long unit = u0 + it / nu;
       const int slot = (int)(it % nu);
-      const int ex = __ldcg(a.w.union_ids + slot);
-      const int p0 = __ldcg(a.w.offsets + slot), np = __ldcg(a.w.offsets + slot + 1) - p0;
+      const int p0 = t_off[slot], np = t_off[slot + 1] - p0;
       const int s = (int)(it % pl.nst);
       mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
       const int lr = warp * kDownRowsPerWarp;  // local row within the unit
@@ -399,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
 
-      const float* sdx = a.st.sc + (long)ex * (2 * f + d) + 2 * f;
-      const float sd0 = sdx[r0], sd1 = sdx[r0 + 1];
+      const float* sdx = t_sd + slot * pl.max_rows + (r0 - row0);
+      const float sd0 = sdx[0], sd1 = sdx[1];
       for (int q = 0; q < np; ++q) {
         const int p = p0 + q;
         uint32_t hr[GF][8];
@@ -454,8 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
           for (int j = 0; j < kDownRowsPerWarp; ++j) {
             const float* er = es + (lr + j) * P;
             float y = a.s.n_shared ? er[T * K + t] : 0.0f;
-            for (int k = 0; k < K; ++k)
-              y = __fmaf_rn(__ldcg(a.w.w + t * K + k), er[__ldcg(a.w.inv + t * K + k)], y);
+            for (int k = 0; k < K; ++k) y = __fmaf_rn(t_w[t * K + k], er[t_inv[t * K + k]], y);
             if (a.s.has_norm) y = __fadd_rn(a.x[(long)t * d + r0 + j], y);
             a.y[(long)t * d + r0 + j] = y;
           }
@@ -504,13 +564,12 @@ cudaError_t configure_expert_kernels() {
 cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
                                  const ExpertDebug& dbg, int num_sms, bool pdl,
                                  cudaStream_t stream) {
-  GateupArgs args{s, st, w, dbg, gateup_plan(s.d, s.f, s.T)};
-  const int G = (s.d / kQB + 31) / 32;
   // the unit count depends on the union size, known only on the device: size the grid for
   // the largest possible union (CTAs without work exit)
-  const long max_slots = (long)(s.T * s.K < s.E ? s.T * s.K : s.E) + s.n_shared;
-  long grid = max_slots * (s.f / 32);
+  long grid = max_union_slots(s.T, s.K, s.E, s.n_shared) * (s.f / 32);
   if (grid > num_sms) grid = num_sms;
+  GateupArgs args{s, st, w, dbg, gateup_plan(s.d, s.f, s.T, s.K, s.E, s.n_shared, (int)grid)};
+  const int G = (s.d / kQB + 31) / 32;
   void (*k)(const GateupArgs) = nullptr;
   switch (G) {
     case 1: k = gateup_decode_kernel<1>; break;
@@ -529,10 +588,10 @@ cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
 cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream) {
-  DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.n_shared), x, y};
-  const int GF = (s.f / kQB + 31) / 32;
   long grid = s.d / kDownRd;
   if (grid > num_sms) grid = num_sms;
+  DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.E, s.n_shared, (int)grid), x, y};
+  const int GF = (s.f / kQB + 31) / 32;
   void (*k)(const DownArgs) = nullptr;
   switch (GF) {
     case 1: k = down_decode_kernel<1>; break;

@@ -1,0 +1,531 @@
+// Expert kernels of the batched (prefill) path on the 5th-generation tensor cores.
+//
+// For a batch the union experts see many tokens each (up to a few hundred), so the expert
+// projections are genuinely dense grouped GEMMs: per union slot, [rows of W] x [K] x [pairs of
+// the slot's bucket].  GB300's int8 tensor rate is low, so the int8 x int4 products run as
+// kind::f16 with bf16 operands holding the exact integers (|code| <= 127, products <= 1016, a
+// 32-term block sum < 2^24: every partial is exact in the f32 accumulator).  Each K-block of 32
+// (one activation scale) is its own MMA accumulation in TMEM, so the epilogue sees the exact
+// int32 block dot and applies the canonical fp32 order of the decode path: an fma chain over
+// the blocks of each of 32 contiguous groups (registers) and the pairwise tree over the groups
+// (a 5-level stack kept in TMEM columns).  Results are therefore bit-identical to the decode
+// kernels and the CPU oracle ("colibrì 架构概述" §5 gate/up/SiLU/down; README batch union).
+//
+// CTA: 15 warps, one tile (128 weight rows x 64 pairs) at a time, persistent over tiles:
+//   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream, deep ring)
+//   warp 1      bulk-tensor copies of the bf16 activation block of each K-step
+//   warps 2-5   int4 -> bf16 conversion of the weight block into the MMA's shared layout
+//   warp 6      TMEM owner and single MMA issuer (2 x K16 MMAs per K-block, double-buffered D)
+//   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "coli_device.cuh"
+#include "coli_internal.h"
+#include "coli_tc.cuh"
+
+namespace coli {
+
+constexpr int kPfM = 128;
+constexpr int kPfN = kPrefillTileN;
+constexpr int kPfStages = 4;      // bf16 A / B ring (one 32-element K-block each)
+constexpr int kPfRawStages = 6;   // raw int4 weight ring (one lane group of blocks each)
+constexpr int kPfWarps = 15;
+constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kPfAStage = kPfM * 32 * 2;  // 8 KB
+constexpr int kPfBStage = kPfN * 32 * 2;  // 4 KB
+constexpr uint32_t kTmemCols = 512;       // acc[2] x 64 + stack[5] x 64 = 448 used
+
+struct PfArgs {
+  Shape s;
+  Store st;
+  Work w;
+  PrefillWork pw;
+  ExpertDebug dbg;
+  int down;   // 0: gate/up + SwiGLU, 1: down
+  int raw_stage_bytes;
+  int dx_bytes;
+};
+
+struct PfSmem {
+  uint8_t* raw;
+  uint8_t* a;
+  uint8_t* b;
+  float* dxs;  // [nb][64]
+  float* us;   // [64][64] u values, column-major (gate/up only)
+  uint64_t* raw_full;
+  uint64_t* raw_empty;
+  uint64_t* a_full;
+  uint64_t* b_full;
+  uint64_t* ab_empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint32_t* tmem_slot;
+  int* tp;    // [nu+1] tile prefix per union slot
+  int* tex;   // [nu]   expert id per union slot
+  int* toff;  // [nu+1] first pair per union slot
+};
+
+__device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
+  PfSmem m;
+  uint8_t* p = smem;
+  m.raw = p;
+  p += kPfRawStages * a.raw_stage_bytes;
+  m.a = p;
+  p += kPfStages * kPfAStage;
+  m.b = p;
+  p += kPfStages * kPfBStage;
+  m.dxs = reinterpret_cast<float*>(p);
+  p += a.dx_bytes;
+  m.us = reinterpret_cast<float*>(p);
+  p += a.down ? 0 : kPfN * 64 * 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p);
+  m.raw_full = bars;
+  m.raw_empty = bars + kPfRawStages;
+  m.a_full = m.raw_empty + kPfRawStages;
+  m.b_full = m.a_full + kPfStages;
+  m.ab_empty = m.b_full + kPfStages;
+  m.acc_full = m.ab_empty + kPfStages;
+  m.acc_empty = m.acc_full + 2;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + 2);
+  m.tp = reinterpret_cast<int*>(m.tmem_slot + 4);
+  m.tex = m.tp + a.s.E + 2;
+  m.toff = m.tex + a.s.E + 2;
+  return m;
+}
+
+int prefill_smem_bytes(int d, int f, int E, int down) {
+  const int K = down ? f : d;
+  const int nb = K / kQB, G = (nb + 31) / 32;
+  const int raw = kPfM * G * 16;
+  const int dx = nb * kPfN * 4;
+  const int bars = (2 * kPfRawStages + 3 * kPfStages + 4) * 8 + 16;
+  const int tabs = 3 * (E + 2) * 4;
+  return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfN * 64 * 4) +
+         bars + tabs;
+}
+
+// tile t -> (union slot, M-tile, N-tile); slots own n_mt * ntiles(slot) consecutive tiles,
+// N fastest so consecutive tiles share their weight rows (L2 reuse).  prefix: shared memory.
+__device__ __forceinline__ void pf_tile(const int* prefix, int nu, int n_mt, int t, int& u,
+                                        int& mt, int& nt) {
+  int lo = 0, hi = nu - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n_mt * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  u = lo;
+  const int base = n_mt * prefix[u];
+  const int ntu = prefix[u + 1] - prefix[u];
+  const int r = t - base;
+  mt = r / ntu;
+  nt = r - mt * ntu;
+}
+
+// int4 chunk (store layout: word k = elements 8k..8k+7, byte m low nibble 8k+m, high 8k+m+4,
+// each code + 8) -> 4 x 16 bytes of bf16 (k-core kc = elements 8kc..8kc+7 in order)
+__device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;
+    // 0x43vv is bf16(128 + v); subtracting 136 leaves v - 8 = the signed code exactly
+    uint32_t q[4] = {__byte_perm(lo, 0x43434343u, 0x4140), __byte_perm(lo, 0x43434343u, 0x4342),
+                     __byte_perm(hi, 0x43434343u, 0x4140), __byte_perm(hi, 0x43434343u, 0x4342)};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&q[j]);
+      v = __hsub2(v, off);
+      q[j] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    out[k] = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                       const PfArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ int abort_flag;
+  const PfSmem m = pf_carve(smem, a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.s.d, f = a.s.f;
+  const bool down = a.down != 0;
+  const int K = down ? f : d;
+  const int nb = K / kQB, G = (nb + 31) / 32, ngrp = nb / G;
+  const int n_mt = down ? d / kPfM : f / (kPfM / 2);
+  const int raw_bytes = kPfM * G * 16;
+  const int nu = __ldcg(a.w.n_union);
+  const int total = n_mt * __ldcg(a.pw.tile_prefix + nu);
+  int* status = a.w.status;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPfRawStages; ++i) {
+      mbar_init(&m.raw_full[i], 1);
+      mbar_init(&m.raw_empty[i], 4);
+    }
+    for (int i = 0; i < kPfStages; ++i) {
+      mbar_init(&m.a_full[i], 4);
+      mbar_init(&m.b_full[i], 1);
+      mbar_init(&m.ab_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&m.acc_full[i], 1);
+      mbar_init(&m.acc_empty[i], 8);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i <= nu; i += blockDim.x) {
+    m.tp[i] = __ldcg(a.pw.tile_prefix + i);
+    m.toff[i] = __ldcg(a.w.offsets + i);
+    m.tex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
+  }
+  if (warp == 6) tmem_alloc(m.tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *m.tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- raw int4 weight groups (128 rows x G chunks) by tensor copies
+    if (lane == 0) {
+      long kg = 0;
+      for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+        int u, mt, nt;
+        pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
+        const int ex = m.tex[u];
+        for (int gi = 0; gi < ngrp; ++gi, ++kg) {
+          const int rs = (int)(kg % kPfRawStages);
+          const long n = kg / kPfRawStages;
+          if (n > 0 && !mbar_wait_bounded(&m.raw_empty[rs], (uint32_t)((n - 1) & 1), &abort_flag, status))
+            break;
+          uint8_t* dst = m.raw + (long)rs * a.raw_stage_bytes;
+          mbar_expect_tx(&m.raw_full[rs], (uint32_t)raw_bytes);
+          if (down) {
+            tma_load_2d(dst, &map_w, gi * G * 16, ex * d + mt * kPfM, &m.raw_full[rs]);
+          } else {
+            const int y = ex * f + mt * (kPfM / 2);
+            tma_load_2d(dst, &map_w, gi * G * 16, y, &m.raw_full[rs]);
+            tma_load_2d(dst + (kPfM / 2) * G * 16, &map_w, d / 2 + gi * G * 16, y, &m.raw_full[rs]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- bf16 activation block (64 pairs x 32) of every K-step
+    if (lane == 0) {
+      long kb = 0;
+      for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+        int u, mt, nt;
+        pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
+        const int row0 = m.toff[u] + nt * kPfN;
+        for (int b = 0; b < nb; ++b, ++kb) {
+          const int s = (int)(kb % kPfStages);
+          const long n = kb / kPfStages;
+          if (n > 0 && !mbar_wait_bounded(&m.ab_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
+            break;
+          uint8_t* dst = m.b + (long)s * kPfBStage;
+          mbar_expect_tx(&m.b_full[s], (uint32_t)kPfBStage);
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc)
+            tma_load_2d(dst + kc * (kPfN * 16), &map_x, b * 32 + kc * 8, row0, &m.b_full[s]);
+        }
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- int4 -> bf16 conversion: thread r owns weight row r of the tile
+    const int r = threadIdx.x - 64;
+    long kb = 0, kg = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      for (int gi = 0; gi < ngrp; ++gi, ++kg) {
+        const int rs = (int)(kg % kPfRawStages);
+        mbar_wait_bounded(&m.raw_full[rs], (uint32_t)((kg / kPfRawStages) & 1), &abort_flag, status);
+        const uint8_t* rrow = m.raw + (long)rs * a.raw_stage_bytes + r * G * 16;
+        for (int i = 0; i < G; ++i, ++kb) {
+          const int s = (int)(kb % kPfStages);
+          const long n = kb / kPfStages;
+          if (n > 0) mbar_wait_bounded(&m.ab_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
+          const uint4 c = *reinterpret_cast<const uint4*>(rrow + (store_chunk(gi, i, G) - gi * G) * 16);
+          uint4 o[4];
+          int4_chunk_to_bf16(c, o);
+          uint8_t* ast = m.a + (long)s * kPfAStage;
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc)
+            *reinterpret_cast<uint4*>(ast + (kc * 16 + (r >> 3)) * 128 + (r & 7) * 16) = o[kc];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&m.a_full[s]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.raw_empty[rs]);
+      }
+    }
+  } else if (warp == 6) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kPfM, kPfN);
+      long kb = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int b = 0; b < nb; ++b, ++kb) {
+          const int s = (int)(kb % kPfStages);
+          const int ab = (int)(kb & 1);
+          const uint32_t ph = (uint32_t)((kb / kPfStages) & 1);
+          bool ok = mbar_wait_bounded(&m.a_full[s], ph, &abort_flag, status);
+          ok = mbar_wait_bounded(&m.b_full[s], ph, &abort_flag, status) && ok;
+          if (kb >= 2)
+            ok = mbar_wait_bounded(&m.acc_empty[ab], (uint32_t)(((kb >> 1) - 1) & 1), &abort_flag, status) && ok;
+          if (!ok) continue;
+          tc_fence_after();
+          const uint8_t* as = m.a + (long)s * kPfAStage;
+          const uint8_t* bs = m.b + (long)s * kPfBStage;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t da = smem_desc(as + ks * 2 * (kPfM / 8) * 128, (kPfM / 8) * 128, 128);
+            const uint64_t db = smem_desc(bs + ks * 2 * (kPfN / 8) * 128, (kPfN / 8) * 128, 128);
+            tc_mma_bf16(tmem + ab * kPfN, da, db, idesc, ks > 0);
+          }
+          tc_commit(&m.ab_empty[s]);
+          tc_commit(&m.acc_full[ab]);
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half*32..
+    const int q = warp & 3;
+    const int half = (warp - 7) >> 2;
+    const int row = q * 32 + lane;
+    const int etid = threadIdx.x - 7 * 32;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    long kb = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int u, mt, nt;
+      pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
+      const int ex = m.tex[u];
+      const int pb = m.toff[u] + nt * kPfN;  // first pair of the tile
+      const int pe = m.toff[u + 1];          // end of the slot's pairs
+      // this tile's activation block scales, [block][column]
+      named_bar_sync(2, 8 * 32);
+      const float* dsrc = down ? a.w.dh : a.pw.dxp;
+      for (int idx = etid; idx < nb * kPfN; idx += 8 * 32) {
+        const int b = idx / kPfN, col = idx - b * kPfN;
+        const int p = pb + col;
+        m.dxs[idx] = p < pe ? __ldcg(dsrc + (long)p * nb + b) : 0.0f;
+      }
+      named_bar_sync(2, 8 * 32);
+
+      float chain[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+      float v[32];
+      for (int b = 0; b < nb; ++b, ++kb) {
+        const int ab = (int)(kb & 1);
+        mbar_wait_bounded(&m.acc_full[ab], (uint32_t)((kb >> 1) & 1), &abort_flag, status);
+        tc_fence_after();
+        float acc[32];
+        tmem_ld32(tl + ab * kPfN + half * 32, acc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.acc_empty[ab]);
+        const float* dxb = m.dxs + b * kPfN + half * 32;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) chain[c] = __fmaf_rn(dxb[c], acc[c], chain[c]);
+        int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
+        if (Adump != nullptr) {
+          const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
+          int32_t* dump = (!down && row >= 64) ? a.dbg.Au : Adump;
+          const int nrow = down ? d : f;
+          for (int c = 0; c < 32; ++c) {
+            const int p = pb + half * 32 + c;
+            if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[c];
+          }
+        }
+        if ((b % G) == G - 1) {
+          // group leaf gi complete: push it on the pairwise-tree stack (levels in TMEM)
+          const int gi = b / G;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = chain[c];
+          int l = 0;
+          for (; (gi >> l) & 1; ++l) {
+            float sl[32];
+            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, sl);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __fadd_rn(sl[c], v[c]);
+          }
+          if (l < 5) tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+        }
+      }
+      // empty groups ngrp..31 are +0 leaves of the tree
+      for (int gi = ngrp; gi < 32; ++gi) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = 0.0f;
+        int l = 0;
+        for (; (gi >> l) & 1; ++l) {
+          float sl[32];
+          tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, sl);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __fadd_rn(sl[c], v[c]);
+        }
+        if (l < 5) tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, v);
+      }
+      // v = the canonical sum of every (row, pair) of this thread
+      const float* scx = a.st.sc + (long)ex * (2 * f + d);
+      if (down) {
+        const int r = mt * kPfM + row;
+        const float sd = scx[2 * f + r];
+        for (int c = 0; c < 32; ++c) {
+          const int p = pb + half * 32 + c;
+          if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, v[c]);
+        }
+      } else {
+        const int r = mt * (kPfM / 2) + (row & 63);
+        const bool is_up = row >= 64;
+        const float sr = is_up ? scx[f + r] : scx[r];
+        float o[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = __fmul_rn(sr, v[c]);
+        if (a.dbg.g != nullptr) {
+          float* dst = is_up ? a.dbg.u : a.dbg.g;
+          for (int c = 0; c < 32; ++c) {
+            const int p = pb + half * 32 + c;
+            if (p < pe) dst[(long)p * f + r] = o[c];
+          }
+        }
+        if (is_up) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) m.us[(half * 32 + c) * 64 + (row - 64)] = o[c];
+        }
+        named_bar_sync(2, 8 * 32);
+        if (!is_up) {
+          // h = SiLU(g) * u; the warp's 32 rows are one int8 block of h for each pair
+          const int nhb = f >> 5, hbk = r >> 5;
+          for (int c = 0; c < 32; ++c) {
+            const int p = pb + half * 32 + c;
+            const float hv = canon_silu_mul(o[c], m.us[(half * 32 + c) * 64 + row]);
+            const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
+            const int code = q8_code(hv, dd);
+            const int sq = warp_isum(code);
+            if (p < pe) {
+              a.w.hf[(long)p * f + r] = hv;
+              a.w.qh[(long)p * f + r] = (int8_t)code;
+              a.pw.hb[(long)p * f + r] = __float2bfloat16_rn((float)code);
+              if (lane == 0) {
+                a.w.dh[(long)p * nhb + hbk] = dd;
+                a.w.sh[(long)p * nhb + hbk] = sq;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 6) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ combine ----------------
+// y[t, r] = e(shared, t)[r], then fma(w_{t,k}, e(t,k)[r], y) for k = 0..K-1, (+ x[t, r])
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ x, float* __restrict__ y,
+                                                      const Shape s, const Work w, const float* __restrict__ e) {
+  const int t = blockIdx.y;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= s.d) return;
+  const int K = s.K, T = s.T;
+  float acc = s.n_shared ? e[(long)(T * K + t) * s.d + r] : 0.0f;
+  for (int k = 0; k < K; ++k)
+    acc = __fmaf_rn(__ldcg(w.w + t * K + k), e[(long)__ldcg(w.inv + t * K + k) * s.d + r], acc);
+  if (s.has_norm) acc = __fadd_rn(x[(long)t * s.d + r], acc);
+  y[(long)t * s.d + r] = acc;
+}
+
+// ------------------------------------------------------------------ host side --------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// the driver's tensor-map encoder, looked up through the runtime (no link against libcuda)
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows][cols] array (elem_bytes 1 or 2), box {box_cols, box_rows}
+static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                     uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t configure_prefill_kernels(int d, int f, int E) {
+  const int need = prefill_smem_bytes(d, f, E, 0) > prefill_smem_bytes(d, f, E, 1)
+                       ? prefill_smem_bytes(d, f, E, 0)
+                       : prefill_smem_bytes(d, f, E, 1);
+  if (need > kSmemLimit) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+}
+
+bool prefill_make_maps(PrefillMaps* maps, const Store& st, const PrefillWork& pw, int d, int f, int slots,
+                       int prow) {
+  const int Gd = (d / kQB + 31) / 32, Gf = (f / kQB + 31) / 32;
+  bool ok = make_map(&maps->wgu, st.wgu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d,
+                     (uint64_t)slots * f, (uint32_t)(Gd * 16), (uint32_t)(kPfM / 2));
+  ok = ok && make_map(&maps->wd, st.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(f / 2),
+                      (uint64_t)slots * d, (uint32_t)(Gf * 16), (uint32_t)kPfM);
+  ok = ok && make_map(&maps->xb, pw.xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)prow,
+                      8u, (uint32_t)kPfN);
+  ok = ok && make_map(&maps->hb, pw.hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)f, (uint64_t)prow,
+                      8u, (uint32_t)kPfN);
+  return ok;
+}
+
+cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, const Store& st, const Work& w,
+                                   const PrefillWork& pw, const PrefillMaps& maps, const ExpertDebug& dbg,
+                                   int num_sms, cudaStream_t stream) {
+  for (int down = 0; down < 2; ++down) {
+    PfArgs args;
+    args.s = s;
+    args.st = st;
+    args.w = w;
+    args.pw = pw;
+    args.dbg = dbg;
+    args.down = down;
+    const int K = down ? s.f : s.d;
+    const int nb = K / kQB, G = (nb + 31) / 32;
+    args.raw_stage_bytes = kPfM * G * 16;
+    args.dx_bytes = nb * kPfN * 4;
+    const int smem = prefill_smem_bytes(s.d, s.f, s.E, down);
+    expert_gemm_kernel<<<num_sms, kPfThreads, smem, stream>>>(down ? maps.wd : maps.wgu,
+                                                              down ? maps.hb : maps.xb, args);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  combine_kernel<<<dim3((s.d + 255) / 256, s.T), 256, 0, stream>>>(x, y, s, w, pw.e);
+  return cudaGetLastError();
+}
+
+}  // namespace coli

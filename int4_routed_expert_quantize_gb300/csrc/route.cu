@@ -5,6 +5,7 @@
 //   Q8_0-style int8 activations) and the README's batch union (each distinct expert of a
 //   batch is read once).
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "coli_device.cuh"
@@ -18,18 +19,24 @@ constexpr int kMaxE = 1024;
 
 // top-K of one token by (score + bias) descending, ties to the lower expert id, then weights
 // renormalised over the selected scores (sum taken in rank order).  One warp per token.
-__device__ void topk_token(const Shape& s, const Store& st, const Work& w, int t, int lane) {
+// sc: the token's E scores; ids/wt: its K outputs (shared or global memory).
+__device__ void topk_token(const Shape& s, const Store& st, const float* sc, int* ids, float* wt,
+                           int lane) {
   const int E = s.E, K = s.K;
-  const float* sc = w.scores + (long)t * E;
   uint32_t taken = 0;  // bit m: expert lane + 32*m already selected
+  float sv[32];
+  const int nm = (E + 31) >> 5;
+  for (int m = 0; m < nm; ++m) {
+    const int e = m * 32 + lane;
+    sv[m & 31] = e < E ? (st.bias ? __fadd_rn(sc[e], st.bias[e]) : sc[e]) : 0.0f;
+  }
   for (int k = 0; k < K; ++k) {
     float bv = 0.0f;
     int bi = 0x7fffffff;
-    for (int m = 0; m * 32 + lane < E; ++m) {
-      if ((taken >> m) & 1u) continue;
+    for (int m = 0; m < nm; ++m) {
       const int e = m * 32 + lane;
-      const float sv = __ldcg(sc + e);
-      const float v = st.bias ? __fadd_rn(sv, st.bias[e]) : sv;
+      if (e >= E || ((taken >> m) & 1u)) continue;
+      const float v = sv[m & 31];
       if (bi == 0x7fffffff || v > bv) {  // e ascending: a tie keeps the lower id
         bv = v;
         bi = e;
@@ -45,27 +52,26 @@ __device__ void topk_token(const Shape& s, const Store& st, const Work& w, int t
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) w.ids[t * K + k] = bi;
+    if (lane == 0) ids[k] = bi;
   }
   __syncwarp();
   if (lane == 0) {
-    const int* ids = w.ids + t * K;
-    float S = __ldcg(sc + ids[0]);
-    for (int k = 1; k < K; ++k) S = __fadd_rn(S, __ldcg(sc + ids[k]));
-    for (int k = 0; k < K; ++k)
-      w.w[t * K + k] = __fmul_rn(__fdiv_rn(__ldcg(sc + ids[k]), S), s.routed_scale);
+    float S = sc[ids[0]];
+    for (int k = 1; k < K; ++k) S = __fadd_rn(S, sc[ids[k]]);
+    for (int k = 0; k < K; ++k) wt[k] = __fmul_rn(__fdiv_rn(sc[ids[k]], S), s.routed_scale);
   }
+  __syncwarp();
 }
 
 // Batch union by one CTA: count pairs per expert, list the distinct experts in ascending id
 // order with their first pair, then place the pairs stably (pair index t*K+k ascending inside
 // each expert) with one warp; the shared expert becomes the last slot with every token.
-__device__ void union_bucket(const Shape& s, const Work& w, int* cnt, int* cursor) {
+__device__ void union_bucket(const Shape& s, const Work& w, const int* idsv, int* cnt, int* cursor) {
   const int E = s.E, K = s.K, T = s.T, TK = T * K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < TK; i += blockDim.x) atomicAdd(&cnt[w.ids[i]], 1);
+  for (int i = threadIdx.x; i < TK; i += blockDim.x) atomicAdd(&cnt[idsv[i]], 1);
   __syncthreads();
   if (warp == 0) {
     const int per = (E + 31) / 32;
@@ -99,7 +105,7 @@ __device__ void union_bucket(const Shape& s, const Work& w, int* cnt, int* curso
     for (int base = 0; base < TK; base += 32) {
       const int i = base + lane;
       const bool valid = i < TK;
-      const int e = valid ? w.ids[i] : -1 - lane;
+      const int e = valid ? idsv[i] : -1 - lane;
       const unsigned peers = __match_any_sync(FULL, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       int pos = 0;
@@ -219,14 +225,21 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
     const float4* wr = reinterpret_cast<const float4*>(st.wr + (long)e * d);
     const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
     float p = 0.0f;
-#pragma unroll 8
-    for (int i4 = 0; i4 < nchunk; ++i4) {
-      const float4 a = __ldg(wr + i4 * 32 + lane);
-      const float4 b = xp[i4 * 32 + lane];
-      p = __fmaf_rn(a.x, b.x, p);
-      p = __fmaf_rn(a.y, b.y, p);
-      p = __fmaf_rn(a.z, b.z, p);
-      p = __fmaf_rn(a.w, b.w, p);
+    for (int i0 = 0; i0 < nchunk; i0 += 16) {
+      float4 a[16];  // 16 loads in flight, then the fma chain in element order
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        a[k] = i0 + k < nchunk ? __ldg(wr + (i0 + k) * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (i0 + k < nchunk) {
+          const float4 b = xp[(i0 + k) * 32 + lane];
+          p = __fmaf_rn(a[k].x, b.x, p);
+          p = __fmaf_rn(a[k].y, b.y, p);
+          p = __fmaf_rn(a[k].z, b.z, p);
+          p = __fmaf_rn(a[k].w, b.w, p);
+        }
+      }
     }
     p = warp_tree_sum(p);
     if (lane == 0) {
@@ -240,9 +253,20 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int t = warp; t < T; t += nwarp) topk_token(s, st, w, t, lane);
+  // the last CTA: every score into shared memory in one round, selection and union there,
+  // then the results out to the workspace
+  float* ssc = xsm;  // [T][E] (the token buffer is no longer needed)
+  __shared__ int sids[kDecodeTmax * 32];
+  __shared__ float swt[kDecodeTmax * 32];
+  for (int i = threadIdx.x; i < T * E; i += blockDim.x) ssc[i] = __ldcg(w.scores + i);
   __syncthreads();
-  union_bucket(s, w, cnt, cursor);
+  for (int t = warp; t < T; t += nwarp) topk_token(s, st, ssc + t * E, sids + t * s.K, swt + t * s.K, lane);
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * s.K; i += blockDim.x) {
+    w.ids[i] = sids[i];
+    w.w[i] = swt[i];
+  }
+  union_bucket(s, w, sids, cnt, cursor);
   if (threadIdx.x == 0) *w.counter = 0;  // ready for the next call
 }
 
@@ -253,11 +277,166 @@ cudaError_t configure_route_kernels() {
                               kRouteSmemMax);
 }
 
+// ------------------------------------------------------------------ batched routing ------
+// The same routing for batches of any size (the tensor-core expert path): one CTA per token for
+// RMSNorm and the int8 blocks, a register-blocked router (each warp: 4 experts x 4 tokens, every
+// logit still one canonical chain per lane group plus the butterfly), one CTA that selects the
+// experts and builds the union and the per-slot tile counts, and a gather of every pair's codes
+// as bf16 (exact: |q| <= 127) for the matrix engine.
+
+__global__ void __launch_bounds__(256) prep_batch_kernel(const float* __restrict__ x, const Shape s,
+                                                         const Store st, const Work w) {
+  extern __shared__ __align__(16) float xs[];  // [d] natural order
+  __shared__ float rinv;
+  const int t = blockIdx.x, d = s.d, nbd = d >> 5, Gd = d >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
+  const float* xt = x + (long)t * d;
+  for (int j = threadIdx.x * 4; j < d; j += blockDim.x * 4)
+    *reinterpret_cast<float4*>(xs + j) = *reinterpret_cast<const float4*>(xt + j);
+  __syncthreads();
+  if (s.has_norm) {
+    if (warp == 0) {
+      float p = 0.0f;
+      for (int j = lane * Gd; j < lane * Gd + Gd; ++j) p = __fmaf_rn(xs[j], xs[j], p);
+      p = warp_tree_sum(p);
+      if (lane == 0) {
+        const float ms = __fdiv_rn(p, (float)d);
+        rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, s.rms_eps)));
+      }
+    }
+    __syncthreads();
+    const float r = rinv;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) xs[j] = __fmul_rn(__fmul_rn(xs[j], r), st.gamma[j]);
+    __syncthreads();
+  }
+  float* xn = w.xn + (long)t * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) xn[j] = xs[j];
+  float4* xp = reinterpret_cast<float4*>(w.xnp + (long)t * d);
+  for (int c = threadIdx.x; c < d / 4; c += blockDim.x) {
+    const int i4 = c >> 5, g = c & 31;
+    const float* src = xs + g * Gd + 4 * i4;
+    xp[c] = make_float4(src[0], src[1], src[2], src[3]);
+  }
+  for (int b = warp; b < nbd; b += nwarp) {
+    const float v = xs[b * 32 + lane];
+    const float dd = __fdiv_rn(warp_max(fabsf(v)), 127.0f);
+    const int q = q8_code(v, dd);
+    w.qx[(long)t * d + b * 32 + lane] = (int8_t)q;
+    const int sq = warp_isum(q);
+    if (lane == 0) {
+      w.dx[(long)t * nbd + b] = dd;
+      w.sx[(long)t * nbd + b] = sq;
+    }
+  }
+}
+
+// CTA = 4 experts x 32 tokens; warp w: the 4 experts x tokens t0 + 4w .. +3
+__global__ void __launch_bounds__(256) router_batch_kernel(const Shape s, const Store st, const Work w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = s.d, E = s.E, T = s.T;
+  const int e0 = blockIdx.x * 4, t0 = blockIdx.y * 32 + warp * 4;
+  if (t0 >= T) return;
+  float acc[4][4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[k][j] = 0.0f;
+  const int nchunk = d / 128;
+  for (int i4 = 0; i4 < nchunk; ++i4) {
+    float4 wv[4], xv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      wv[k] = e0 + k < E ? __ldg(reinterpret_cast<const float4*>(st.wr + (long)(e0 + k) * d) + i4 * 32 + lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      xv[j] = t0 + j < T ? __ldcg(reinterpret_cast<const float4*>(w.xnp + (long)(t0 + j) * d) + i4 * 32 + lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float p = acc[k][j];
+        p = __fmaf_rn(wv[k].x, xv[j].x, p);
+        p = __fmaf_rn(wv[k].y, xv[j].y, p);
+        p = __fmaf_rn(wv[k].z, xv[j].z, p);
+        p = __fmaf_rn(wv[k].w, xv[j].w, p);
+        acc[k][j] = p;
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float p = warp_tree_sum(acc[k][j]);
+      if (lane == 0 && e0 + k < E && t0 + j < T) {
+        w.logits[(long)(t0 + j) * E + e0 + k] = p;
+        w.scores[(long)(t0 + j) * E + e0 + k] = canon_sigmoid(p);
+      }
+    }
+}
+
+// top-K of every token, the batch union, and per union slot the number of 64-pair tiles
+// (tile_prefix[u] = sum of the counts of slots before u)
+__global__ void __launch_bounds__(1024) select_union_kernel(const Shape s, const Store st,
+                                                            const Work w, int32_t* tile_prefix,
+                                                            int tile_n) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int cursor[kMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
+  for (int t = warp; t < s.T; t += nwarp)
+    topk_token(s, st, w.scores + (long)t * s.E, w.ids + t * s.K, w.w + t * s.K, lane);
+  __syncthreads();
+  union_bucket(s, w, w.ids, cnt, cursor);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int nu = *w.n_union;
+    int acc = 0;
+    for (int u = 0; u < nu; ++u) {
+      tile_prefix[u] = acc;
+      acc += (w.offsets[u + 1] - w.offsets[u] + tile_n - 1) / tile_n;
+    }
+    tile_prefix[nu] = acc;
+  }
+}
+
+// one CTA per pair slot of the largest batch: the pair's token codes as bf16, and its scales
+__global__ void __launch_bounds__(256) gather_pairs_kernel(const Shape s, const Work w,
+                                                           __nv_bfloat16* __restrict__ xb,
+                                                           float* __restrict__ dxp) {
+  const int p = blockIdx.x;
+  const int P = w.offsets[*w.n_union];
+  if (p >= P) return;
+  const int d = s.d, nbd = d >> 5;
+  const int t = w.pair_token[p];
+  const int8_t* q = w.qx + (long)t * d;
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(xb + (long)p * d);
+  for (int j = threadIdx.x; j < d / 2; j += blockDim.x)
+    dst[j] = __floats2bfloat162_rn((float)q[2 * j], (float)q[2 * j + 1]);
+  for (int b = threadIdx.x; b < nbd; b += blockDim.x) dxp[(long)p * nbd + b] = w.dx[(long)t * nbd + b];
+}
+
+cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, const Work& w,
+                               int32_t* tile_prefix, int tile_n, __nv_bfloat16* xb, float* dxp,
+                               cudaStream_t stream) {
+  prep_batch_kernel<<<s.T, 256, (size_t)s.d * sizeof(float), stream>>>(x, s, st, w);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  router_batch_kernel<<<dim3((s.E + 3) / 4, (s.T + 31) / 32), 256, 0, stream>>>(s, st, w);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  select_union_kernel<<<1, 1024, 0, stream>>>(s, st, w, tile_prefix, tile_n);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int Pm = s.T * s.K + (s.n_shared ? s.T : 0);
+  gather_pairs_kernel<<<Pm, 256, 0, stream>>>(s, w, xb, dxp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const Work& w,
                          cudaStream_t stream) {
   // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work
   const int grid = (s.E + kRouterEpc - 1) / kRouterEpc;
-  route_kernel<<<grid, 256, (size_t)s.T * s.d * sizeof(float), stream>>>(x, s, st, w);
+  const size_t smem = (size_t)s.T * (s.d > s.E ? s.d : s.E) * sizeof(float);
+  route_kernel<<<grid, 256, smem, stream>>>(x, s, st, w);
   return cudaGetLastError();
 }
 

@@ -23,6 +23,9 @@ struct coli_moe {
   Store st;
   Work w;
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
+  bool prefill = false;     // batches above kDecodeTmax use the tensor-core path
+  PrefillWork pw;
+  PrefillMaps maps;
   bool router_loaded = false;
   std::vector<uint8_t> loaded;
   int n_loaded = 0;
@@ -86,6 +89,8 @@ Shape shape_of(const coli_moe* h, int T) {
                c.has_norm};
 }
 
+int copy_dump(coli_moe* h, int T, const coli_moe_dump* dump, cudaStream_t stream);
+
 std::once_flag g_cfg_once;
 cudaError_t g_cfg_err = cudaSuccess;
 
@@ -114,7 +119,39 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
   if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], stream);
   if (e != cudaSuccess) return COLI_ECUDA;
+  return dump ? copy_dump(h, T, dump, stream) : COLI_OK;
+}
+
+int run_prefill(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump* dump,
+                cudaStream_t stream) {
+  const Shape s = shape_of(h, T);
+  ExpertDebug dbg;
   if (dump) {
+    dbg.g = dump->g;
+    dbg.u = dump->u;
+    dbg.Ag = dump->Ag;
+    dbg.Au = dump->Au;
+    dbg.Ad = dump->Ad;
+    if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
+    if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
+  }
+  cudaError_t e = launch_route_batch(x, s, h->st, h->w, h->pw.tile_prefix, kPrefillTileN, h->pw.xb,
+                                     h->pw.dxp, stream);
+  if (e == cudaSuccess)
+    e = launch_prefill_experts(x, y, s, h->st, h->w, h->pw, h->maps, dbg, h->num_sms, stream);
+  if (e != cudaSuccess) return COLI_ECUDA;
+  if (dump) {
+    const long P = (long)T * h->cfg.top_k + (h->cfg.n_shared ? T : 0);
+    if (dump->e && cudaMemcpyAsync(dump->e, h->pw.e, sizeof(float) * P * h->cfg.d,
+                                   cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return COLI_ECUDA;
+    return copy_dump(h, T, dump, stream);
+  }
+  return COLI_OK;
+}
+
+int copy_dump(coli_moe* h, int T, const coli_moe_dump* dump, cudaStream_t stream) {
+  {
     const coli_moe_config& c = h->cfg;
     const long P = (long)T * c.top_k + (c.n_shared ? T : 0);
     struct Cp {
@@ -155,11 +192,12 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
   if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
   if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
-  if (dump && T > kDecodeTmax) return COLI_EUNSUPPORTED;
+  if (dump && T > kDecodeTmax && !h->prefill) return COLI_EUNSUPPORTED;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
   int rc = check_device(h);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
+  if (T > kDecodeTmax && h->prefill) return run_prefill(h, x, T, y, dump, st);
   // the smem-staged kernels take up to kDecodeTmax tokens; larger batches run in chunks,
   // which gives the same result per token (each token's output depends on itself only)
   for (int c0 = 0; c0 < T; c0 += kDecodeTmax) {
@@ -182,7 +220,7 @@ const char* coli_moe_strerror(int status) {
     case COLI_ESTATE: return "call out of order (weights not loaded, or wrong device)";
     case COLI_ECUDA: return "CUDA runtime error";
     case COLI_ETIMEOUT: return "a bounded device wait timed out";
-    case COLI_EUNSUPPORTED: return "unsupported shape";
+    case COLI_EUNSUPPORTED: return "unsupported shape or request";
     default: return "unknown status";
   }
 }
@@ -203,7 +241,8 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     return COLI_EINVAL;
   if (!shape_ok(c.d) || !shape_ok(c.f)) return COLI_EUNSUPPORTED;
   const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
-  if (gateup_plan(c.d, c.f, Tc).nst < 2 || down_plan(c.d, c.f, Tc, c.top_k, c.n_shared).nst < 2)
+  if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, 1).nst < 2 ||
+      down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, 1).nst < 2)
     return COLI_EUNSUPPORTED;
 
   int dev = 0;
@@ -252,13 +291,28 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.pair_token, sizeof(int32_t) * Pm)
   ALLOC(h->w.pair_rank, sizeof(int32_t) * Pm)
   ALLOC(h->w.inv, sizeof(int32_t) * Tm * K)
-  ALLOC(h->w.hf, sizeof(float) * Pm * f)
-  ALLOC(h->w.qh, Pm * f)
-  ALLOC(h->w.dh, sizeof(float) * Pm * (f / 32))
+  ALLOC(h->w.hf, sizeof(float) * (Pm + kPrefillTileN) * f)
+  ALLOC(h->w.qh, (Pm + kPrefillTileN) * f)
+  ALLOC(h->w.dh, sizeof(float) * (Pm + kPrefillTileN) * (f / 32))
   ALLOC(h->w.sh, sizeof(int32_t) * Pm * (f / 32))
   ALLOC(h->w.counter, sizeof(int32_t) * 4)
   ALLOC(h->w.status, sizeof(int32_t) * 4)
   ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
+  if (rc == COLI_OK && Tm > kDecodeTmax && configure_prefill_kernels((int)d, (int)f, (int)E) == cudaSuccess) {
+    const long prow = Pm + kPrefillTileN;
+    ALLOC(h->pw.xb, sizeof(__nv_bfloat16) * prow * d)
+    ALLOC(h->pw.dxp, sizeof(float) * prow * (d / 32))
+    ALLOC(h->pw.hb, sizeof(__nv_bfloat16) * prow * f)
+    ALLOC(h->pw.e, sizeof(float) * Pm * d)
+    ALLOC(h->pw.tile_prefix, sizeof(int32_t) * (E + 2))
+    if (rc == COLI_OK) {
+      h->prefill = prefill_make_maps(&h->maps, h->st, h->pw, (int)d, (int)f, (int)S, (int)prow);
+      if (cudaMemset(h->pw.xb, 0, sizeof(__nv_bfloat16) * prow * d) != cudaSuccess ||
+          cudaMemset(h->pw.hb, 0, sizeof(__nv_bfloat16) * prow * f) != cudaSuccess ||
+          cudaMemset(h->pw.dxp, 0, sizeof(float) * prow * (d / 32)) != cudaSuccess)
+        rc = COLI_ECUDA;
+    }
+  }
 #undef ALLOC
   if (rc == COLI_OK && (cudaMemset(h->w.counter, 0, 16) != cudaSuccess ||
                         cudaMemset(h->w.status, 0, 16) != cudaSuccess ||
