@@ -155,10 +155,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait for phase `parity` of `bar`.  Gives up after kWaitLimitNs, records
 // COLI_ETIMEOUT in the device status word and raises the CTA's abort flag; once the flag is
 // up every later wait returns false at once, so no thread of the CTA can block forever.
-static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort_flag, int* status) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort_flag, int* status) {
   if (*abort_flag) return false;
-  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -171,6 +170,13 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
       }
     }
   }
+}
+
+// fast path inline (phase already complete), the bounded loop out of line
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

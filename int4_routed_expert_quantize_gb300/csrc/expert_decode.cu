@@ -23,7 +23,7 @@ static inline int align16(int x) { return (x + 15) & ~15; }
 
 // per-CTA unit table of the gate/up kernel: slot, expert, first pair, pair count, the pairs'
 // tokens (T at most) and the 32 gate + 32 up row scales
-constexpr int kGuTabInts = 4 + kDecodeTmax;
+constexpr int kGuTabInts = 5 + kDecodeTmax;  // slot, expert, first pair, pairs, hb, tokens
 constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
 
 static long max_union_slots(int T, int K, int E, int n_shared) {
@@ -125,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   const int G_ = gridDim.x, c = blockIdx.x;
 
   // shared-expert units of this CTA: [a0, a1) of the nhb units of store slot E
-  const long UA = a.s.n_shared ? nhb : 0;
-  const long a0 = UA * c / G_, a1 = UA * (c + 1) / G_;
-  const long na = a1 - a0;
+  const int UA = a.s.n_shared ? nhb : 0;
+  const int a0 = (int)((long)UA * c / G_), a1 = (int)((long)UA * (c + 1) / G_);
+  const int na = a1 - a0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < pl.nst; ++i) {
@@ -140,11 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   __syncthreads();
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
-  long issued = 0;
+  int issued = 0;
   if (producer) {
     for (; issued < na * SPU && issued < pl.nst; ++issued) {
-      const long unit = a0 + issued / SPU;
-      const int sub = (int)(issued % SPU);
+      const int unit = a0 + issued / SPU;
+      const int sub = issued % SPU;
       const uint8_t* src = a.st.wgu + ((long)a.s.E * f + unit * 32 + sub * kGuRps) * (long)d;
       mbar_expect_tx(&full[issued], (uint32_t)pl.stage_bytes);
       bulk_g2s(ring + issued * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[issued], pol);
@@ -157,21 +157,22 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   // routed units of this CTA: the total U = UA + UB is split evenly (each CTA's shared units
   // count towards its share) when there are at least as many routed units as CTAs
   const int nu = __ldcg(a.w.n_union);
-  const long UB = (long)(nu - (a.s.n_shared ? 1 : 0)) * nhb;
-  long b0, b1;
+  const int UB = (nu - (a.s.n_shared ? 1 : 0)) * nhb;
+  int b0, b1;
   if (UB >= G_) {
     const long U = UA + UB;
-    b0 = U * c / G_ - a0;
-    b1 = U * (c + 1) / G_ - a1;
+    b0 = (int)(U * c / G_) - a0;
+    b1 = (int)(U * (c + 1) / G_) - a1;
   } else {
-    b0 = UB * c / G_;
-    b1 = UB * (c + 1) / G_;
+    b0 = (int)((long)UB * c / G_);
+    b1 = (int)((long)UB * (c + 1) / G_);
   }
-  const long nunit = na + (b1 - b0);
-  const long nstage = nunit * SPU;
+  const int nunit = na + (b1 - b0);
+  const int nstage = nunit * SPU;
 
   // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of a
   // chunk live in separate planes so a warp's 16-byte loads are consecutive
+#pragma unroll 4
   for (int idx = threadIdx.x; idx < T * nbd; idx += blockDim.x) {
     const int t = idx / nbd, b = idx - t * nbd;
     const int g = b / G, i = b - g * G;
@@ -184,20 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   }
 
   // local unit index -> (union slot, 32-row block)
-  auto unit_of = [&](long lu, int& slot, int& hb) {
+  auto unit_of = [&](int lu, int& slot, int& hb) {
     if (lu < na) {
       slot = nu - 1;
-      hb = (int)(a0 + lu);
+      hb = a0 + lu;
     } else {
-      const long r = b0 + (lu - na);
-      slot = (int)(r / nhb);
-      hb = (int)(r - (long)slot * nhb);
+      const int r = b0 + (lu - na);
+      slot = r / nhb;
+      hb = r - slot * nhb;
     }
-  };
-  auto unit_hb = [&](long lu) {
-    int slot, hb;
-    unit_of(lu, slot, hb);
-    return hb;
   };
   // unit table: every value a stage needs, loaded once (one round of memory latency)
   for (int lu = warp; lu < nunit && lu < pl.max_units; lu += kNW + 1) {
@@ -212,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       tu[1] = ex;
       tu[2] = p0;
       tu[3] = np;
+      tu[4] = hb;
     }
-    if (lane < np && lane < kDecodeTmax) tu[4 + lane] = __ldcg(a.w.pair_token + p0 + lane);
+    if (lane < np && lane < kDecodeTmax) tu[5 + lane] = __ldcg(a.w.pair_token + p0 + lane);
     const float* scx = a.st.sc + (long)ex * (2 * f + d);
     float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
     tsc[lane] = scx[hb * 32 + lane];
@@ -224,18 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   if (warp == kNW) {
     // ---------------- producer: one lane streams the remaining stages
     if (producer) {
-      for (long it = issued; it < nstage; ++it) {
-        const int s = (int)(it % pl.nst);
-        const long n = it / pl.nst;
-        if (n > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((n - 1) & 1), &abort_flag, a.w.status))
-          break;
-        int slot, hb;
-        unit_of(it / SPU, slot, hb);
-        const int ex = tab[(it / SPU) * (kGuTabInts + 64) + 1];
-        const uint8_t* src = a.st.wgu + ((long)ex * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
+      int s = issued % pl.nst;
+      uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
+      for (int it = issued; it < nstage; ++it) {
+        if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
+        const int* tu = tab + (it / SPU) * (kGuTabInts + 64);
+        const uint8_t* src = a.st.wgu + ((long)tu[1] * f + tu[4] * 32 + (it % SPU) * kGuRps) * (long)d;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
         issued = it + 1;
+        if (++s == pl.nst) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
@@ -245,14 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     float dr[G];
     int nr[G];
     int cached_tok = -1;
-    for (long it = 0; it < nstage; ++it) {
-      const long lu = it / SPU;
-      const int sub = (int)(it % SPU);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nstage; ++it) {
+      const int lu = it / SPU;
+      const int sub = it % SPU;
       const int* tu = tab + lu * (kGuTabInts + 64);
-      const int hb = unit_hb(lu);
+      const int hb = tu[4];
       const int p0 = tu[2], np = tu[3];
-      const int s = (int)(it % pl.nst);
-      mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
+      mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
       const int rr = sub * kGuRps + warp;
       const int row = hb * 32 + rr;
       const uint8_t* grow = ring + (long)s * pl.stage_bytes + (long)warp * d;
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       const float sg = tsc[rr], su = tsc[32 + rr];
       for (int q = 0; q < np; ++q) {
         const int p = p0 + q;
-        const int t = tu[4 + q];
+        const int t = tu[5 + q];
         if (t != cached_tok) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -313,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with its row pair
+      if (++s == pl.nst) {
+        s = 0;
+        ph ^= 1u;
+      }
       if (sub == SPU - 1) {
         // the unit's 32 rows of h are complete: quantise one int8 block per token
         named_bar_sync(1, kNW * 32);
@@ -364,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   float* t_sd = reinterpret_cast<float*>(t_inv + T * K);            // [slot][max_rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const long units = d / kDownRd;
-  const long u0 = units * blockIdx.x / gridDim.x;
-  const long u1 = units * (blockIdx.x + 1) / gridDim.x;
-  const long nstage = (u1 - u0) * nu;
+  const int units = d / kDownRd;
+  const int u0 = (int)((long)units * blockIdx.x / gridDim.x);
+  const int u1 = (int)((long)units * (blockIdx.x + 1) / gridDim.x);
+  const int nstage = (u1 - u0) * nu;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < pl.nst; ++i) {
@@ -380,11 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   __syncthreads();
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
-  long issued = 0;
-  auto issue = [&](long it, int ex) {
-    const int s = (int)(it % pl.nst);
-    const long unit = u0 + it / nu;
-    const uint8_t* src = a.st.wd + ((long)ex * d + unit * kDownRd) * (long)(f / 2);
+  int issued = 0;
+  auto issue = [&](int s, int unit, int ex) {
+    const uint8_t* src = a.st.wd + ((long)ex * d + (long)unit * kDownRd) * (long)(f / 2);
     mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
     bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
   };
@@ -393,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   // wait for the gate/up grid
   if (producer)
     for (; issued < nstage && issued < pl.nst; ++issued)
-      issue(issued, __ldcg(a.w.union_ids + (int)(issued % nu)));
-  const int row0 = (int)u0 * kDownRd, nrow = (int)(u1 - u0) * kDownRd;
+      issue(issued, u0 + issued / nu, __ldcg(a.w.union_ids + issued % nu));
+  const int row0 = u0 * kDownRd, nrow = (u1 - u0) * kDownRd;
   for (int i = threadIdx.x; i <= nu; i += blockDim.x) {
     t_ex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
     t_off[i] = __ldcg(a.w.offsets + i);
@@ -411,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   // gate/up grid complete: h codes visible from here on
   griddep_wait();
 
+#pragma unroll 4
   for (int idx = threadIdx.x; idx < P * nbf; idx += blockDim.x) {
     const int p = idx / nbf, b = idx - p * nbf;
     const int g = b / GF, i = b - g * GF;
@@ -425,25 +427,31 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
 
   if (warp == kNW) {
     if (producer) {
-      for (long it = issued; it < nstage; ++it) {
-        const long n = it / pl.nst;
-        if (n > 0 && !mbar_wait_bounded(&empty[it % pl.nst], (uint32_t)((n - 1) & 1), &abort_flag,
-                                        a.w.status))
-          break;
-        issue(it, t_ex[it % nu]);
+      int s = issued % pl.nst, unit = u0 + issued / nu, slot = issued % nu;
+      uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
+      for (int it = issued; it < nstage; ++it) {
+        if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
+        issue(s, unit, t_ex[slot]);
         issued = it + 1;
+        if (++s == pl.nst) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++slot == nu) {
+          slot = 0;
+          ++unit;
+        }
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
   } else {
-    for (long it = 0; it < nstage; ++it) {
-      const long unit = u0 + it / nu;
-      const int slot = (int)(it % nu);
+    int s = 0, unit = u0, slot = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nstage; ++it) {
       const int p0 = t_off[slot], np = t_off[slot + 1] - p0;
-      const int s = (int)(it % pl.nst);
-      mbar_wait_bounded(&full[s], (uint32_t)((it / pl.nst) & 1), &abort_flag, a.w.status);
+      mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
       const int lr = warp * kDownRowsPerWarp;  // local row within the unit
-      const int r0 = (int)unit * kDownRd + lr;
+      const int r0 = unit * kDownRd + lr;
       const uint8_t* srow = ring + (long)s * pl.stage_bytes + (long)lr * (f / 2);
       uint4 w0[GF], w1[GF];
 #pragma unroll
@@ -459,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == pl.nst) {
+        s = 0;
+        ph ^= 1u;
+      }
 
       const float* sdx = t_sd + slot * pl.max_rows + (r0 - row0);
       const float sd0 = sdx[0], sd1 = sdx[1];
@@ -521,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
           }
         }
         __syncwarp();
+      }
+      if (++slot == nu) {
+        slot = 0;
+        ++unit;
       }
     }
   }

@@ -267,9 +267,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 6) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kPfM, kPfN);
       long kb = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int u, mt, nt;
+        pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
+        // MMA width: the tile's valid pairs rounded up to 16 (padding columns are discarded)
+        const int nv = min(kPfN, m.toff[u + 1] - (m.toff[u] + nt * kPfN));
+        const int nmma = (nv + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(kPfM, nmma);
         for (int b = 0; b < nb; ++b, ++kb) {
           const int s = (int)(kb % kPfStages);
           const int ab = (int)(kb & 1);
@@ -307,32 +312,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int ex = m.tex[u];
       const int pb = m.toff[u] + nt * kPfN;  // first pair of the tile
       const int pe = m.toff[u + 1];          // end of the slot's pairs
+      const int nv = min(kPfN, pe - pb);       // valid pairs of the tile
+      const bool active = half * 32 < nv;       // this warp has columns to finish
       // this tile's activation block scales, [block][column]
       named_bar_sync(2, 8 * 32);
       const float* dsrc = down ? a.w.dh : a.pw.dxp;
+#pragma unroll 4
       for (int idx = etid; idx < nb * kPfN; idx += 8 * 32) {
         const int b = idx / kPfN, col = idx - b * kPfN;
-        const int p = pb + col;
-        m.dxs[idx] = p < pe ? __ldcg(dsrc + (long)p * nb + b) : 0.0f;
+        m.dxs[idx] = col < nv ? __ldcg(dsrc + (long)(pb + col) * nb + b) : 0.0f;
       }
       named_bar_sync(2, 8 * 32);
 
       float chain[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
-      float v[32];
+      int gi = 0, gb = 0;  // current group and block within it
       for (int b = 0; b < nb; ++b, ++kb) {
         const int ab = (int)(kb & 1);
         mbar_wait_bounded(&m.acc_full[ab], (uint32_t)((kb >> 1) & 1), &abort_flag, status);
         tc_fence_after();
         float acc[32];
-        tmem_ld32(tl + ab * kPfN + half * 32, acc);
+        if (active) tmem_ld32(tl + ab * kPfN + half * 32, acc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.acc_empty[ab]);
-        const float* dxb = m.dxs + b * kPfN + half * 32;
+        if (!active) continue;
+        const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfN + half * 32);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) chain[c] = __fmaf_rn(dxb[c], acc[c], chain[c]);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dv = dxb[c4];
+          chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[4 * c4 + 0], chain[4 * c4 + 0]);
+          chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[4 * c4 + 1], chain[4 * c4 + 1]);
+          chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[4 * c4 + 2], chain[4 * c4 + 2]);
+          chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[4 * c4 + 3], chain[4 * c4 + 3]);
+        }
         int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
         if (Adump != nullptr) {
           const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
@@ -343,65 +357,71 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[c];
           }
         }
-        if ((b % G) == G - 1) {
-          // group leaf gi complete: push it on the pairwise-tree stack (levels in TMEM)
-          const int gi = b / G;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = chain[c];
+        if (++gb == G) {
+          // group leaf gi complete: merge it into the pairwise-tree stack (levels in TMEM);
+          // after the last leaf `chain` holds the whole sum
+          gb = 0;
           int l = 0;
           for (; (gi >> l) & 1; ++l) {
-            float sl[32];
-            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, sl);
+            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, acc);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __fadd_rn(sl[c], v[c]);
+            for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
           }
-          if (l < 5) tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, v);
+          if (l < 5) {
+            tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, chain);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+            for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+          }
+          ++gi;
         }
       }
-      // empty groups ngrp..31 are +0 leaves of the tree
-      for (int gi = ngrp; gi < 32; ++gi) {
+      if (active) {
+        // empty groups ngrp..31 are +0 leaves of the tree
+        for (int gz = ngrp; gz < 32; ++gz) {
+          float acc[32];
+          int l = 0;
+          for (; (gz >> l) & 1; ++l) {
+            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, acc);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = 0.0f;
-        int l = 0;
-        for (; (gi >> l) & 1; ++l) {
-          float sl[32];
-          tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, sl);
+            for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
+          }
+          if (l < 5) {
+            tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, chain);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = __fadd_rn(sl[c], v[c]);
+            for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+          }
         }
-        if (l < 5) tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, v);
       }
-      // v = the canonical sum of every (row, pair) of this thread
+      // chain = the canonical sum of every (row, pair) of this thread
       const float* scx = a.st.sc + (long)ex * (2 * f + d);
       if (down) {
+        if (!active) continue;
         const int r = mt * kPfM + row;
         const float sd = scx[2 * f + r];
         for (int c = 0; c < 32; ++c) {
           const int p = pb + half * 32 + c;
-          if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, v[c]);
+          if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, chain[c]);
         }
       } else {
         const int r = mt * (kPfM / 2) + (row & 63);
         const bool is_up = row >= 64;
         const float sr = is_up ? scx[f + r] : scx[r];
-        float o[32];
+        float* o = chain;  // the row-scaled projection, in place
 #pragma unroll
-        for (int c = 0; c < 32; ++c) o[c] = __fmul_rn(sr, v[c]);
-        if (a.dbg.g != nullptr) {
+        for (int c = 0; c < 32; ++c) o[c] = __fmul_rn(sr, chain[c]);
+        if (a.dbg.g != nullptr && active) {
           float* dst = is_up ? a.dbg.u : a.dbg.g;
           for (int c = 0; c < 32; ++c) {
             const int p = pb + half * 32 + c;
             if (p < pe) dst[(long)p * f + r] = o[c];
           }
         }
-        if (is_up) {
+        if (is_up && active) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) m.us[(half * 32 + c) * 64 + (row - 64)] = o[c];
         }
         named_bar_sync(2, 8 * 32);
-        if (!is_up) {
+        if (!is_up && active) {
           // h = SiLU(g) * u; the warp's 32 rows are one int8 block of h for each pair
           const int nhb = f >> 5, hbk = r >> 5;
           for (int c = 0; c < 32; ++c) {

@@ -24,14 +24,17 @@ __device__ void topk_token(const Shape& s, const Store& st, const float* sc, int
                            int lane) {
   const int E = s.E, K = s.K;
   uint32_t taken = 0;  // bit m: expert lane + 32*m already selected
-  float sv[32];
+  float sv[32], sr[32];
   const int nm = (E + 31) >> 5;
   for (int m = 0; m < nm; ++m) {
     const int e = m * 32 + lane;
-    sv[m & 31] = e < E ? (st.bias ? __fadd_rn(sc[e], st.bias[e]) : sc[e]) : 0.0f;
+    sr[m & 31] = e < E ? sc[e] : 0.0f;
+    sv[m & 31] = e < E ? (st.bias ? __fadd_rn(sr[m & 31], st.bias[e]) : sr[m & 31]) : 0.0f;
   }
+  float S = 0.0f;      // lane 0: sum of the selected scores in rank order
+  float pick[32];      // lane 0: the selected scores
   for (int k = 0; k < K; ++k) {
-    float bv = 0.0f;
+    float bv = 0.0f, bs = 0.0f;
     int bi = 0x7fffffff;
     for (int m = 0; m < nm; ++m) {
       const int e = m * 32 + lane;
@@ -39,27 +42,30 @@ __device__ void topk_token(const Shape& s, const Store& st, const float* sc, int
       const float v = sv[m & 31];
       if (bi == 0x7fffffff || v > bv) {  // e ascending: a tie keeps the lower id
         bv = v;
+        bs = sr[m & 31];
         bi = e;
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_xor_sync(FULL, bv, off);
+      const float os = __shfl_xor_sync(FULL, bs, off);
       const int oi = __shfl_xor_sync(FULL, bi, off);
       if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
         bv = ov;
+        bs = os;
         bi = oi;
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) ids[k] = bi;
+    if (lane == 0) {
+      ids[k] = bi;
+      pick[k & 31] = bs;
+      S = k == 0 ? bs : __fadd_rn(S, bs);
+    }
   }
-  __syncwarp();
-  if (lane == 0) {
-    float S = sc[ids[0]];
-    for (int k = 1; k < K; ++k) S = __fadd_rn(S, sc[ids[k]]);
-    for (int k = 0; k < K; ++k) wt[k] = __fmul_rn(__fdiv_rn(sc[ids[k]], S), s.routed_scale);
-  }
+  if (lane == 0)
+    for (int k = 0; k < K; ++k) wt[k] = __fmul_rn(__fdiv_rn(pick[k & 31], S), s.routed_scale);
   __syncwarp();
 }
 
@@ -161,6 +167,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
 
   // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
   // i4*32 + g (coalesced float4 loads; conflict-free reads by lane)
+#pragma unroll 8
   for (int c = threadIdx.x; c < T * (d / 4); c += blockDim.x) {
     const int t = c / (d / 4), pos = c - t * (d / 4);
     const int i4 = pos >> 5, g = pos & 31;

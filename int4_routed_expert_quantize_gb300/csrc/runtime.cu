@@ -240,15 +240,22 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
       !(c.rms_eps >= 0.0f) || !std::isfinite(c.rms_eps) || c.d <= 0 || c.f <= 0)
     return COLI_EINVAL;
   if (!shape_ok(c.d) || !shape_ok(c.f)) return COLI_EUNSUPPORTED;
-  const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
-  if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, 1).nst < 2 ||
-      down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, 1).nst < 2)
-    return COLI_EUNSUPPORTED;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     return COLI_ECUDA;
+  }
+  {
+    // the decode kernels' shared-memory plans for the grids they will launch with
+    const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
+    const long slots = (long)(Tc * c.top_k < c.n_experts ? Tc * c.top_k : c.n_experts) + c.n_shared;
+    const long gu_grid = slots * (c.f / 32) < sms ? slots * (c.f / 32) : sms;
+    const long dn_grid = c.d / kDownRd < sms ? c.d / kDownRd : sms;
+    if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid).nst < 2 ||
+        down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst < 2)
+      return COLI_EUNSUPPORTED;
   }
   std::call_once(g_cfg_once, [] {
     g_cfg_err = configure_expert_kernels();
