@@ -80,7 +80,7 @@ struct PrefillWork {
 };
 
 struct PrefillMaps {
-  CUtensorMap wgu, wd, xb, hb;
+  CUtensorMap wgu, wd, xb, hb, wr, xnp;
 };
 
 struct Shape {
@@ -111,13 +111,15 @@ cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const S
                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream);
 cudaError_t configure_route_kernels();
+cudaError_t configure_route_batch_kernels(int E);
 cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, const Work& w,
+                               const CUtensorMap& map_wr, const CUtensorMap& map_x,
                                int32_t* tile_prefix, int tile_n, __nv_bfloat16* xb, float* dxp,
                                cudaStream_t stream);
 cudaError_t configure_prefill_kernels(int d, int f, int E);
 int prefill_smem_bytes(int d, int f, int E, int down);
-bool prefill_make_maps(PrefillMaps* maps, const Store& st, const PrefillWork& pw, int d, int f,
-                       int slots, int prow);
+bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const PrefillWork& pw,
+                       int d, int f, int E, int slots, int prow, int tmax);
 cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, const Store& st,
                                    const Work& w, const PrefillWork& pw, const PrefillMaps& maps,
                                    const ExpertDebug& dbg, int num_sms, cudaStream_t stream);

@@ -509,8 +509,8 @@ cudaError_t configure_prefill_kernels(int d, int f, int E) {
   return cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
-bool prefill_make_maps(PrefillMaps* maps, const Store& st, const PrefillWork& pw, int d, int f, int slots,
-                       int prow) {
+bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const PrefillWork& pw, int d,
+                       int f, int E, int slots, int prow, int tmax) {
   const int Gd = (d / kQB + 31) / 32, Gf = (f / kQB + 31) / 32;
   bool ok = make_map(&maps->wgu, st.wgu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)d,
                      (uint64_t)slots * f, (uint32_t)(Gd * 16), (uint32_t)(kPfM / 2));
@@ -520,6 +520,11 @@ bool prefill_make_maps(PrefillMaps* maps, const Store& st, const PrefillWork& pw
                       8u, (uint32_t)kPfN);
   ok = ok && make_map(&maps->hb, pw.hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)f, (uint64_t)prow,
                       8u, (uint32_t)kPfN);
+  // router rows and normalised tokens (both in the router's chunk order), 256-float boxes
+  ok = ok && make_map(&maps->wr, st.wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)d, (uint64_t)E,
+                      256u, 16u);
+  ok = ok && make_map(&maps->xnp, w.xnp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)d, (uint64_t)tmax,
+                      256u, 32u);
   return ok;
 }
 

@@ -10,6 +10,7 @@
 
 #include "coli_device.cuh"
 #include "coli_internal.h"
+#include "coli_tc.cuh"
 
 namespace coli {
 
@@ -337,64 +338,191 @@ __global__ void __launch_bounds__(256) prep_batch_kernel(const float* __restrict
   }
 }
 
-// CTA = 4 experts x 32 tokens; warp w: the 4 experts x tokens t0 + 4w .. +3
-__global__ void __launch_bounds__(256) router_batch_kernel(const Shape s, const Store st, const Work w) {
+// Router for batches: CTA tile = 16 experts x 32 tokens, K in chunks of 2 steps (256 floats of
+// every row, the same lane-group chunk order as the decode router) brought into shared memory
+// by 2-D tensor copies, double-buffered.  Warp w: experts 4*(w%4)..+3 x tokens 8*(w/4)..+7,
+// 32 canonical chains per lane, one butterfly per logit at the end.
+constexpr int kRbE = 16, kRbT = 32, kRbChunk = 256;
+constexpr int kRbStage = (kRbE + kRbT) * kRbChunk * 4;  // 48 KB
+
+__global__ void __launch_bounds__(512) router_batch_kernel(const __grid_constant__ CUtensorMap map_wr,
+                                                           const __grid_constant__ CUtensorMap map_x,
+                                                           const Shape s, const Work w) {
+  extern __shared__ __align__(128) uint8_t rsm[];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = s.d, E = s.E, T = s.T;
-  const int e0 = blockIdx.x * 4, t0 = blockIdx.y * 32 + warp * 4;
-  if (t0 >= T) return;
-  float acc[4][4];
+  const int e0 = blockIdx.x * kRbE, t0 = blockIdx.y * kRbT;
+  const int nchunk = d / kRbChunk;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int c) {
+    uint8_t* st = rsm + (c & 1) * kRbStage;
+    mbar_expect_tx(&bar[c & 1], (uint32_t)kRbStage);
+    tma_load_2d(st, &map_wr, c * kRbChunk, e0, &bar[c & 1]);
+    tma_load_2d(st + kRbE * kRbChunk * 4, &map_x, c * kRbChunk, t0, &bar[c & 1]);
+  };
+  if (threadIdx.x == 0) {
+    issue(0);
+    if (nchunk > 1) issue(1);
+  }
+  const int ew = (warp & 3) * 4, tw = (warp >> 2) * 8;
+  float acc[4][8];
 #pragma unroll
   for (int k = 0; k < 4; ++k)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[k][j] = 0.0f;
-  const int nchunk = d / 128;
-  for (int i4 = 0; i4 < nchunk; ++i4) {
-    float4 wv[4], xv[4];
+    for (int j = 0; j < 8; ++j) acc[k][j] = 0.0f;
+  for (int c = 0; c < nchunk; ++c) {
+    mbar_wait_bounded(&bar[c & 1], (uint32_t)((c >> 1) & 1), &abort_flag, w.status);
+    const float* wst = reinterpret_cast<const float*>(rsm + (c & 1) * kRbStage);
+    const float* xst = wst + kRbE * kRbChunk;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      wv[k] = e0 + k < E ? __ldg(reinterpret_cast<const float4*>(st.wr + (long)(e0 + k) * d) + i4 * 32 + lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int st = 0; st < 2; ++st) {
+      float4 wv[4], xv[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      xv[j] = t0 + j < T ? __ldcg(reinterpret_cast<const float4*>(w.xnp + (long)(t0 + j) * d) + i4 * 32 + lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 4; ++k)
+        wv[k] = reinterpret_cast<const float4*>(wst + (ew + k) * kRbChunk + st * 128)[lane];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+      for (int j = 0; j < 8; ++j)
+        xv[j] = reinterpret_cast<const float4*>(xst + (tw + j) * kRbChunk + st * 128)[lane];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float p = acc[k][j];
-        p = __fmaf_rn(wv[k].x, xv[j].x, p);
-        p = __fmaf_rn(wv[k].y, xv[j].y, p);
-        p = __fmaf_rn(wv[k].z, xv[j].z, p);
-        p = __fmaf_rn(wv[k].w, xv[j].w, p);
-        acc[k][j] = p;
-      }
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float p = acc[k][j];
+          p = __fmaf_rn(wv[k].x, xv[j].x, p);
+          p = __fmaf_rn(wv[k].y, xv[j].y, p);
+          p = __fmaf_rn(wv[k].z, xv[j].z, p);
+          p = __fmaf_rn(wv[k].w, xv[j].w, p);
+          acc[k][j] = p;
+        }
+    }
+    __syncthreads();  // every warp is done with this stage
+    if (threadIdx.x == 0 && c + 2 < nchunk) issue(c + 2);
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       const float p = warp_tree_sum(acc[k][j]);
-      if (lane == 0 && e0 + k < E && t0 + j < T) {
-        w.logits[(long)(t0 + j) * E + e0 + k] = p;
-        w.scores[(long)(t0 + j) * E + e0 + k] = canon_sigmoid(p);
+      const int e = e0 + ew + k, t = t0 + tw + j;
+      if (lane == 0 && e < E && t < T) {
+        w.logits[(long)t * E + e] = p;
+        w.scores[(long)t * E + e] = canon_sigmoid(p);
       }
     }
 }
 
-// top-K of every token, the batch union, and per union slot the number of 64-pair tiles
-// (tile_prefix[u] = sum of the counts of slots before u)
-__global__ void __launch_bounds__(1024) select_union_kernel(const Shape s, const Store st,
-                                                            const Work w, int32_t* tile_prefix,
-                                                            int tile_n) {
+// top-K of every token: one warp per token
+__global__ void __launch_bounds__(256) topk_batch_kernel(const Shape s, const Store st, const Work w) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= s.T) return;
+  topk_token(s, st, w.scores + (long)t * s.E, w.ids + t * s.K, w.w + t * s.K, lane);
+}
+
+// The batch union with all 32 warps: counts per expert and the union slots (as union_bucket
+// builds them), then each warp places a contiguous chunk of the pairs; a warp's first position
+// for expert e is the slot start plus the pairs of e in earlier chunks (a scan over the warps'
+// counts), which gives the same stable order.  Then the per-slot tile counts.
+__global__ void __launch_bounds__(1024) union_batch_kernel(const Shape s, const Work w,
+                                                           int32_t* tile_prefix, int tile_n) {
+  extern __shared__ int wcnt[];  // [32][E]
   __shared__ int cnt[kMaxE];
-  __shared__ int cursor[kMaxE];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
-  for (int t = warp; t < s.T; t += nwarp)
-    topk_token(s, st, w.scores + (long)t * s.E, w.ids + t * s.K, w.w + t * s.K, lane);
+  __shared__ int start[kMaxE];
+  const int E = s.E, K = s.K, T = s.T, TK = T * K;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  union_bucket(s, w, w.ids, cnt, cursor);
+  const int chunk = (TK + 31) / 32;
+  const int c0 = warp * chunk, c1 = min(TK, c0 + chunk);
+  for (int base = c0; base < c1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < c1;
+    const int e = valid ? w.ids[i] : -1 - lane;
+    const unsigned peers = __match_any_sync(FULL, e);
+    if (valid && (__ffs(peers) - 1) == lane) {
+      wcnt[warp * E + e] += __popc(peers);
+      atomicAdd(&cnt[e], __popc(peers));
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int a0 = lane * per, a1 = min(E, a0 + per);
+    int nz = 0, sum = 0;
+    for (int e = a0; e < a1; ++e) {
+      nz += cnt[e] > 0;
+      sum += cnt[e];
+    }
+    int nz_ex = nz, sum_ex = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(FULL, nz_ex, off), b = __shfl_up_sync(FULL, sum_ex, off);
+      if (lane >= off) {
+        nz_ex += a;
+        sum_ex += b;
+      }
+    }
+    const int n_routed = __shfl_sync(FULL, nz_ex, 31);
+    int slot = nz_ex - nz, off = sum_ex - sum;
+    for (int e = a0; e < a1; ++e) {
+      start[e] = off;
+      if (cnt[e] > 0) {
+        w.union_ids[slot] = e;
+        w.offsets[slot] = off;
+        ++slot;
+        off += cnt[e];
+      }
+    }
+    if (lane == 0) {
+      int nu = n_routed;
+      if (s.n_shared) {
+        w.union_ids[nu] = E;
+        w.offsets[nu] = TK;
+        ++nu;
+      }
+      w.offsets[nu] = TK + (s.n_shared ? T : 0);
+      *w.n_union = nu;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = start[e];
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = wcnt[ww * E + e];
+      wcnt[ww * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = c0; base < c1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < c1;
+    const int e = valid ? w.ids[i] : -1 - lane;
+    const unsigned peers = __match_any_sync(FULL, e);
+    if (valid) {
+      const int pos = wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      w.pair_token[pos] = i / K;
+      w.pair_rank[pos] = i % K;
+      w.inv[i] = pos;
+    }
+    __syncwarp();
+    if (valid && (__ffs(peers) - 1) == lane) wcnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  if (s.n_shared)
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      w.pair_token[TK + t] = t;
+      w.pair_rank[TK + t] = -1;
+    }
   __syncthreads();
   if (threadIdx.x == 0) {
     const int nu = *w.n_union;
@@ -423,15 +551,28 @@ __global__ void __launch_bounds__(256) gather_pairs_kernel(const Shape s, const 
   for (int b = threadIdx.x; b < nbd; b += blockDim.x) dxp[(long)p * nbd + b] = w.dx[(long)t * nbd + b];
 }
 
+cudaError_t configure_route_batch_kernels(int E) {
+  cudaError_t e = cudaFuncSetAttribute(router_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       2 * kRbStage);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(union_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             32 * E * 4);
+  return e;
+}
+
 cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, const Work& w,
+                               const CUtensorMap& map_wr, const CUtensorMap& map_x,
                                int32_t* tile_prefix, int tile_n, __nv_bfloat16* xb, float* dxp,
                                cudaStream_t stream) {
   prep_batch_kernel<<<s.T, 256, (size_t)s.d * sizeof(float), stream>>>(x, s, st, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  router_batch_kernel<<<dim3((s.E + 3) / 4, (s.T + 31) / 32), 256, 0, stream>>>(s, st, w);
+  router_batch_kernel<<<dim3((s.E + kRbE - 1) / kRbE, (s.T + kRbT - 1) / kRbT), 512, 2 * kRbStage,
+                        stream>>>(map_wr, map_x, s, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  select_union_kernel<<<1, 1024, 0, stream>>>(s, st, w, tile_prefix, tile_n);
+  topk_batch_kernel<<<(s.T + 7) / 8, 256, 0, stream>>>(s, st, w);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  union_batch_kernel<<<1, 1024, (size_t)32 * s.E * 4, stream>>>(s, w, tile_prefix, tile_n);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int Pm = s.T * s.K + (s.n_shared ? s.T : 0);
   gather_pairs_kernel<<<Pm, 256, 0, stream>>>(s, w, xb, dxp);

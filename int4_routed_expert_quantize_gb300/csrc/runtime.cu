@@ -135,8 +135,8 @@ int run_prefill(coli_moe* h, const float* x, int T, float* y, const coli_moe_dum
     if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
     if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
   }
-  cudaError_t e = launch_route_batch(x, s, h->st, h->w, h->pw.tile_prefix, kPrefillTileN, h->pw.xb,
-                                     h->pw.dxp, stream);
+  cudaError_t e = launch_route_batch(x, s, h->st, h->w, h->maps.wr, h->maps.xnp, h->pw.tile_prefix,
+                                     kPrefillTileN, h->pw.xb, h->pw.dxp, stream);
   if (e == cudaSuccess)
     e = launch_prefill_experts(x, y, s, h->st, h->w, h->pw, h->maps, dbg, h->num_sms, stream);
   if (e != cudaSuccess) return COLI_ECUDA;
@@ -305,7 +305,9 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.counter, sizeof(int32_t) * 4)
   ALLOC(h->w.status, sizeof(int32_t) * 4)
   ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
-  if (rc == COLI_OK && Tm > kDecodeTmax && configure_prefill_kernels((int)d, (int)f, (int)E) == cudaSuccess) {
+  if (rc == COLI_OK && Tm > kDecodeTmax && d % 256 == 0 &&
+      configure_prefill_kernels((int)d, (int)f, (int)E) == cudaSuccess &&
+      configure_route_batch_kernels((int)E) == cudaSuccess) {
     const long prow = Pm + kPrefillTileN;
     ALLOC(h->pw.xb, sizeof(__nv_bfloat16) * prow * d)
     ALLOC(h->pw.dxp, sizeof(float) * prow * (d / 32))
@@ -313,7 +315,8 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     ALLOC(h->pw.e, sizeof(float) * Pm * d)
     ALLOC(h->pw.tile_prefix, sizeof(int32_t) * (E + 2))
     if (rc == COLI_OK) {
-      h->prefill = prefill_make_maps(&h->maps, h->st, h->pw, (int)d, (int)f, (int)S, (int)prow);
+      h->prefill = prefill_make_maps(&h->maps, h->st, h->w, h->pw, (int)d, (int)f, (int)E, (int)S,
+                                     (int)prow, (int)Tm);
       if (cudaMemset(h->pw.xb, 0, sizeof(__nv_bfloat16) * prow * d) != cudaSuccess ||
           cudaMemset(h->pw.hb, 0, sizeof(__nv_bfloat16) * prow * f) != cudaSuccess ||
           cudaMemset(h->pw.dxp, 0, sizeof(float) * prow * (d / 32)) != cudaSuccess)
