@@ -160,6 +160,23 @@ int coli_quantize_i4_rows(const float* w_dev, int64_t rows, int cols, uint8_t* p
 int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_dev,
                          void* stream);
 
+/* Routing without allocating anything: the layer's router alone (fp32 logits, sigmoid, top-K by
+ * score + optional selection bias with ties to the lower id, weights renormalised over the
+ * selected scores) -- bit-identical to the ids and weights coli_moe_forward uses for the same
+ * inputs (without RMSNorm).  The source pages have no counterpart: this is an interface for
+ * callers that cannot allocate device memory, such as code running while a stream is captured
+ * into a CUDA graph (allocation calls are not allowed there) or a process whose device memory
+ * is owned by another allocator.  It needs no handle: x_dev [T,d], W_r_dev [E,d] (row major),
+ * bias_dev [E] or NULL, outputs ids_dev [T,K] and w_dev [T,K], all device pointers owned by the
+ * caller; x_dev and W_r_dev 16-byte aligned.  Limits: T <= 4, T*E <= 4096, E <= 1024,
+ * K <= min(E, 32), d a multiple of 128 up to 8192 (EINVAL beyond them).  Its scratch (16 KB)
+ * is a fixed array in the library's device memory, present on every device that loads the
+ * library until the process exits; the first call on a device looks up that array's address
+ * (make it before any stream capture); calls that overlap on the GPU race on the array. */
+int coli_route_noalloc(const float* x_dev, int T, const float* W_r_dev, const float* bias_dev,
+                       int E, int d, int K, float routed_scale, int32_t* ids_dev, float* w_dev,
+                       void* stream);
+
 const char* coli_moe_strerror(int status);
 
 #ifdef __cplusplus

@@ -70,6 +70,7 @@ def lib():
         L.coli_moe_expert_record_bytes.restype = _i64
         L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
         L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
+        L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
         L.coli_moe_strerror.argtypes = [_i]
         L.coli_moe_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -205,6 +206,18 @@ def quantize_i4_rows(w, packed=None, scales=None, stream=None):
     _check(lib().coli_quantize_i4_rows(_ptr(w), rows, cols, _ptr(packed), _ptr(scales), _stream(stream)),
            "coli_quantize_i4_rows")
     return packed, scales
+
+
+def route_noalloc(x, W_r, K, bias=None, routed_scale=1.0, stream=None):
+    """top-K ids and weights of the tokens x [T,d] (device) under router W_r [E,d] (device),
+    through the entry point that allocates nothing"""
+    T, d = x.shape
+    E = W_r.shape[0]
+    ids = torch.empty((T, K), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=x.device)
+    _check(lib().coli_route_noalloc(_ptr(x), T, _ptr(W_r), _ptr(bias), E, d, K, routed_scale,
+                                    _ptr(ids), _ptr(w), _stream(stream)), "coli_route_noalloc")
+    return ids, w
 
 
 def quantize_act_q8(x, stream=None):
