@@ -185,6 +185,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // one bulk copy global -> shared (the TMA engine's non-tensor form), completing on `bar`.
 // src, dst 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,

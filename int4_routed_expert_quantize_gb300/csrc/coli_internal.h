@@ -16,8 +16,8 @@ constexpr int kDecodeTmax = 4;                  // tokens per call on the smem-s
 constexpr int kNW = 8;                          // consumer warps per CTA of the expert kernels
 constexpr int kThreads = (kNW + 1) * 32;        // + one producer warp
 constexpr int kGuRps = 8;                       // gate/up row pairs per pipeline stage
-constexpr int kDownRowsPerWarp = 2;             // output rows per warp per down stage
-constexpr int kDownRd = kNW * kDownRowsPerWarp; // output rows per down stage
+constexpr int kDownRowsPerWarp = 8;             // output rows per warp per down stage
+constexpr int kDownChunk = kNW * kDownRowsPerWarp;  // at most this many rows per down stage
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
 constexpr int kGateupSmem = 160 * 1024;         // gate/up ring budget: leaves room on the SM for
@@ -142,5 +142,6 @@ struct DownPlan {
 };
 GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
+int down_grid(int d, int num_sms);  // CTAs of the down kernel
 
 }  // namespace coli

@@ -25,6 +25,7 @@ static inline int align16(int x) { return (x + 15) & ~15; }
 // tokens (T at most) and the 32 gate + 32 up row scales
 constexpr int kGuTabInts = 5 + kDecodeTmax;  // slot, expert, first pair, pairs, hb, tokens
 constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
+constexpr int kGuMaxSlots = kDecodeTmax * 32 + 1;  // union slots: T*K routed (K <= 32) + shared
 
 static long max_union_slots(int T, int K, int E, int n_shared) {
   return (long)(T * K < E ? T * K : E) + (n_shared ? 1 : 0);
@@ -53,13 +54,13 @@ DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   DownPlan p;
   const int P = T * K + (n_shared ? T : 0);
   const int nbf = f / kQB;
-  p.stage_bytes = kDownRd * (f / 2);
+  p.max_rows = (d + grid - 1) / grid;  // rows of the largest CTA range
+  const int chunk = p.max_rows < kDownChunk ? p.max_rows : kDownChunk;
+  p.stage_bytes = chunk * (f / 2);
   p.hq_bytes = align16(P * f);
   p.aux_bytes = align16(P * nbf * 8);
-  p.es_bytes = align16(kDownRd * P * 4);
+  p.es_bytes = align16(chunk * P * 4);
   p.max_slots = (int)max_union_slots(T, K, E, n_shared);
-  const long units = d / kDownRd;
-  p.max_rows = (int)((units + grid - 1) / grid) * kDownRd;
   p.tab_bytes = align16((2 * (p.max_slots + 1) + 2 * T * K) * 4 + p.max_slots * p.max_rows * 4);
   const int fixed = 2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes + p.tab_bytes;
   int nst = (kSmemLimit - fixed) / p.stage_bytes;
@@ -105,10 +106,11 @@ __device__ __noinline__ void drain_fills(uint64_t* full, int nst, long issued) {
 // in every CTA that has some: those are known before routing, so they are prefetched before
 // the kernel waits for the routing grid.  Warp w reduces row pair w of every stage; when a
 // unit's 32 rows are done the CTA re-quantises them (one warp per token).
-template <int G>
+template <int G, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const GateupArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
+  __shared__ int pex[kGuMaxSlots];  // expert of each union slot (producer warp)
   const int d = a.s.d, f = a.s.f, T = a.s.T;
   const int nbd = d >> 5, A = nbd / G, nhb = f >> 5;
   const GateupPlan& pl = a.pl;
@@ -154,9 +156,15 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   griddep_wait();
   griddep_launch_dependents();
 
+  // The producer warp reads the union slots' experts in the same round of memory latency as
+  // nu (entries past nu are read but never used) and starts streaming at once; the consumer
+  // warps build the tables meanwhile.
+  const int nu = __ldcg(a.w.n_union);
+  if (warp == kNW)
+    for (int i = lane; i < kGuMaxSlots && i <= a.s.E; i += 32) pex[i] = __ldcg(a.w.union_ids + i);
+
   // routed units of this CTA: the total U = UA + UB is split evenly (each CTA's shared units
   // count towards its share) when there are at least as many routed units as CTAs
-  const int nu = __ldcg(a.w.n_union);
   const int UB = (nu - (a.s.n_shared ? 1 : 0)) * nhb;
   int b0, b1;
   if (UB >= G_) {
@@ -170,20 +178,6 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   const int nunit = na + (b1 - b0);
   const int nstage = nunit * SPU;
 
-  // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of a
-  // chunk live in separate planes so a warp's 16-byte loads are consecutive
-#pragma unroll 4
-  for (int idx = threadIdx.x; idx < T * nbd; idx += blockDim.x) {
-    const int t = idx / nbd, b = idx - t * nbd;
-    const int g = b / G, i = b - g * G;
-    const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
-    uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
-    *reinterpret_cast<uint4*>(base) = __ldcg(src);
-    *reinterpret_cast<uint4*>(base + nbd * 16) = __ldcg(src + 1);
-    dxs[idx] = __ldcg(a.w.dx + (long)t * nbd + b);
-    nsx[idx] = -8 * __ldcg(a.w.sx + (long)t * nbd + b);
-  }
-
   // local unit index -> (union slot, 32-row block)
   auto unit_of = [&](int lu, int& slot, int& hb) {
     if (lu < na) {
@@ -195,38 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       hb = r - slot * nhb;
     }
   };
-  // unit table: every value a stage needs, loaded once (one round of memory latency)
-  for (int lu = warp; lu < nunit && lu < pl.max_units; lu += kNW + 1) {
-    int slot, hb;
-    unit_of(lu, slot, hb);
-    int* tu = tab + lu * (kGuTabInts + 64);
-    const int ex = __ldcg(a.w.union_ids + slot);
-    const int p0 = __ldcg(a.w.offsets + slot);
-    const int np = __ldcg(a.w.offsets + slot + 1) - p0;
-    if (lane == 0) {
-      tu[0] = slot;
-      tu[1] = ex;
-      tu[2] = p0;
-      tu[3] = np;
-      tu[4] = hb;
-    }
-    if (lane < np && lane < kDecodeTmax) tu[5 + lane] = __ldcg(a.w.pair_token + p0 + lane);
-    const float* scx = a.st.sc + (long)ex * (2 * f + d);
-    float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
-    tsc[lane] = scx[hb * 32 + lane];
-    tsc[32 + lane] = scx[f + hb * 32 + lane];
-  }
-  __syncthreads();
 
   if (warp == kNW) {
     // ---------------- producer: one lane streams the remaining stages
+    __syncwarp();
     if (producer) {
       int s = issued % pl.nst;
       uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
       for (int it = issued; it < nstage; ++it) {
         if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
-        const int* tu = tab + (it / SPU) * (kGuTabInts + 64);
-        const uint8_t* src = a.st.wgu + ((long)tu[1] * f + tu[4] * 32 + (it % SPU) * kGuRps) * (long)d;
+        int slot, hb;
+        unit_of(it / SPU, slot, hb);
+        const uint8_t* src = a.st.wgu + ((long)pex[slot] * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
         issued = it + 1;
@@ -238,6 +212,42 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
   } else {
+    // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of
+    // a chunk live in separate planes so a warp's 16-byte loads are consecutive
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < T * nbd; idx += kNW * 32) {
+      const int t = idx / nbd, b = idx - t * nbd;
+      const int g = b / G, i = b - g * G;
+      const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
+      uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
+      *reinterpret_cast<uint4*>(base) = __ldcg(src);
+      *reinterpret_cast<uint4*>(base + nbd * 16) = __ldcg(src + 1);
+      dxs[idx] = __ldcg(a.w.dx + (long)t * nbd + b);
+      nsx[idx] = -8 * __ldcg(a.w.sx + (long)t * nbd + b);
+    }
+    // unit table: every value a stage needs, loaded once (one round of memory latency)
+    for (int lu = warp; lu < nunit && lu < pl.max_units; lu += kNW) {
+      int slot, hb;
+      unit_of(lu, slot, hb);
+      int* tu = tab + lu * (kGuTabInts + 64);
+      const int ex = __ldcg(a.w.union_ids + slot);
+      const int p0 = __ldcg(a.w.offsets + slot);
+      const int np = __ldcg(a.w.offsets + slot + 1) - p0;
+      if (lane == 0) {
+        tu[0] = slot;
+        tu[1] = ex;
+        tu[2] = p0;
+        tu[3] = np;
+        tu[4] = hb;
+      }
+      if (lane < np && lane < kDecodeTmax) tu[5 + lane] = __ldcg(a.w.pair_token + p0 + lane);
+      const float* scx = a.st.sc + (long)ex * (2 * f + d);
+      float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
+      tsc[lane] = scx[hb * 32 + lane];
+      tsc[32 + lane] = scx[f + hb * 32 + lane];
+    }
+    named_bar_sync(1, kNW * 32);
+
     // ---------------- consumers: warp `warp` takes row pair `warp` of every stage
     uint32_t xr[G][8];
     float dr[G];
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
           const int au = block_dot(wu, xr[i], nr[i]);
           pg = __fmaf_rn(dr[i], __int2float_rn(ag), pg);
           pu = __fmaf_rn(dr[i], __int2float_rn(au), pu);
-          if (a.dbg.Ag != nullptr && lane < A) {
+          if (DBG && a.dbg.Ag != nullptr && lane < A) {
             const long o = ((long)p * f + row) * nbd + lane * G + i;
             a.dbg.Ag[o] = ag;
             a.dbg.Au[o] = au;
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         const float g = __fmul_rn(sg, pg), u = __fmul_rn(su, pu);
         if (lane == 0) {
           hs[((lu & 1) * 32 + rr) * T + q] = canon_silu_mul(g, u);
-          if (a.dbg.g != nullptr) {
+          if (DBG && a.dbg.g != nullptr) {
             a.dbg.g[(long)p * f + row] = g;
             a.dbg.u[(long)p * f + row] = u;
           }
@@ -339,17 +349,52 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
 }
 
 // ------------------------------------------------------------------ down + combine --------
-// Work unit = 16 output rows of y; a stage is those rows of one union expert's down matrix.
-// The union is known when this grid starts (the router finished before the gate/up grid let
-// it launch), so the first stages are prefetched before waiting for the h codes.  Warp w owns
-// rows 2w, 2w+1 of the unit; once every union expert has been seen it combines them for every
-// token in the fixed order: shared expert first, then ranks 0..K-1.
-template <int GF>
+// CTA c owns the output rows [d*c/grid, d*(c+1)/grid) -- about d/grid rows, so every CTA streams
+// the same number of bytes -- cut into chunks of at most kDownChunk rows.  A stage is one chunk
+// of one union expert's down matrix (one contiguous bulk copy).  The union is known when this
+// grid starts (the router finished before the gate/up grid let it launch), so the first stages
+// and the tables are loaded before waiting for the h codes.  Warp w owns rows w, w+8, ... of
+// the chunk: every lane folds its group's block dots for up to 8 rows, and one transposed
+// butterfly adds the 32 group partials of all 8 rows (the same pairwise tree per row as the
+// single-row butterfly).  Once a chunk has seen every union expert the warp combines its rows
+// for every token in the fixed order: shared expert first, then ranks 0..K-1.
+
+// Sum over the warp of 8 values per lane, one per row: the exchange at distance o keeps half
+// of the rows on each side, so after distances 1, 2, 4 lane l holds one row's partial, and
+// distances 8, 16 finish it.  Every row's total is the pairwise tree over lanes in lane order,
+// bit-identical to warp_tree_sum.  Returns the total of row 4*(l&1) + 2*((l>>1)&1) + ((l>>2)&1)
+// (the same in lanes l, l+8, l+16, l+24).
+__device__ __forceinline__ float warp_tree_sum8(const float (&v)[8], int lane) {
+  const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+  float u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b0 ? v[i + 4] : v[i], send = b0 ? v[i] : v[i + 4];
+    u[i] = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 1));
+  }
+  float z[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b1 ? u[i + 2] : u[i], send = b1 ? u[i] : u[i + 2];
+    z[i] = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 2));
+  }
+  const float keep = b2 ? z[1] : z[0], send = b2 ? z[0] : z[1];
+  float r = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 4));
+  r = __fadd_rn(r, __shfl_xor_sync(FULL, r, 8));
+  r = __fadd_rn(r, __shfl_xor_sync(FULL, r, 16));
+  return r;
+}
+
+__host__ __device__ inline int down_rows_begin(int d, int c, int grid) {
+  return (int)((long)d * c / grid);
+}
+
+template <int GF, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
-  const int nbf = f >> 5, A = nbf / GF;
+  const int nbf = f >> 5, A = nbf / GF, rb = f >> 1;
   const DownPlan& pl = a.pl;
   const int nu = __ldcg(a.w.n_union);
   const int P = __ldcg(a.w.offsets + nu);
@@ -359,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][2 halves][chunks][16]
   float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf]
   int* hn = reinterpret_cast<int*>(hd + P * nbf);                  // [P][nbf]  -8*sum(codes)
-  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [kDownRd][P]
+  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [chunk row][P]
   int* t_ex = reinterpret_cast<int*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
   int* t_off = t_ex + pl.max_slots + 1;
   float* t_w = reinterpret_cast<float*>(t_off + pl.max_slots + 1);  // [T*K]
@@ -367,10 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   float* t_sd = reinterpret_cast<float*>(t_inv + T * K);            // [slot][max_rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int units = d / kDownRd;
-  const int u0 = (int)((long)units * blockIdx.x / gridDim.x);
-  const int u1 = (int)((long)units * (blockIdx.x + 1) / gridDim.x);
-  const int nstage = (u1 - u0) * nu;
+  const int row0 = down_rows_begin(d, blockIdx.x, gridDim.x);
+  const int nrow = down_rows_begin(d, blockIdx.x + 1, gridDim.x) - row0;
+  const int nch = (nrow + kDownChunk - 1) / kDownChunk;
+  const int nstage = nch * nu;
+  auto chunk = [&](int ci, int& c0, int& cn) {
+    c0 = nrow * ci / nch;
+    cn = nrow * (ci + 1) / nch - c0;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < pl.nst; ++i) {
@@ -384,18 +433,19 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
   int issued = 0;
-  auto issue = [&](int s, int unit, int ex) {
-    const uint8_t* src = a.st.wd + ((long)ex * d + (long)unit * kDownRd) * (long)(f / 2);
-    mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
-    bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
+  auto issue = [&](int s, int ci, int ex) {
+    int c0, cn;
+    chunk(ci, c0, cn);
+    const uint8_t* src = a.st.wd + ((long)ex * d + row0 + c0) * (long)rb;
+    mbar_expect_tx(&full[s], (uint32_t)(cn * rb));
+    bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)(cn * rb), &full[s], pol);
   };
   // the routing results are complete when this grid starts: prefetch the first stages and
   // build the CTA's tables (union slots, weights, pair indices, down-row scales) before the
   // wait for the gate/up grid
   if (producer)
     for (; issued < nstage && issued < pl.nst; ++issued)
-      issue(issued, u0 + issued / nu, __ldcg(a.w.union_ids + issued % nu));
-  const int row0 = u0 * kDownRd, nrow = (u1 - u0) * kDownRd;
+      issue(issued, issued / nu, __ldcg(a.w.union_ids + issued % nu));
   for (int i = threadIdx.x; i <= nu; i += blockDim.x) {
     t_ex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
     t_off[i] = __ldcg(a.w.offsets + i);
@@ -427,11 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
 
   if (warp == kNW) {
     if (producer) {
-      int s = issued % pl.nst, unit = u0 + issued / nu, slot = issued % nu;
+      int s = issued % pl.nst, ci = issued / nu, slot = issued % nu;
       uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
       for (int it = issued; it < nstage; ++it) {
         if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
-        issue(s, unit, t_ex[slot]);
+        issue(s, ci, t_ex[slot]);
         issued = it + 1;
         if (++s == pl.nst) {
           s = 0;
@@ -439,41 +489,23 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
         }
         if (++slot == nu) {
           slot = 0;
-          ++unit;
+          ++ci;
         }
       }
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
   } else {
-    int s = 0, unit = u0, slot = 0;
+    int s = 0, ci = 0, slot = 0, c0 = 0, cn = 0;
     uint32_t ph = 0;
+    chunk(0, c0, cn);
+    // rows of this warp in the current chunk: w, w+8, ... below cn
+    int nj = cn > warp ? (cn - warp + kNW - 1) / kNW : 0;
+    const int jl = 4 * (lane & 1) + 2 * ((lane >> 1) & 1) + ((lane >> 2) & 1);  // row of the sum
     for (int it = 0; it < nstage; ++it) {
       const int p0 = t_off[slot], np = t_off[slot + 1] - p0;
       mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
-      const int lr = warp * kDownRowsPerWarp;  // local row within the unit
-      const int r0 = unit * kDownRd + lr;
-      const uint8_t* srow = ring + (long)s * pl.stage_bytes + (long)lr * (f / 2);
-      uint4 w0[GF], w1[GF];
-#pragma unroll
-      for (int i = 0; i < GF; ++i) {
-        if (lane < A) {
-          const int off = store_chunk(lane, i, GF) * 16;
-          w0[i] = *reinterpret_cast<const uint4*>(srow + off);
-          w1[i] = *reinterpret_cast<const uint4*>(srow + f / 2 + off);
-        } else {
-          w0[i] = make_uint4(0, 0, 0, 0);
-          w1[i] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (++s == pl.nst) {
-        s = 0;
-        ph ^= 1u;
-      }
-
-      const float* sdx = t_sd + slot * pl.max_rows + (r0 - row0);
-      const float sd0 = sdx[0], sd1 = sdx[1];
+      const uint8_t* sbase = ring + (long)s * pl.stage_bytes + (long)warp * rb;
+      const float* sdx = t_sd + slot * pl.max_rows + c0 + warp;
       for (int q = 0; q < np; ++q) {
         const int p = p0 + q;
         uint32_t hr[GF][8];
@@ -496,47 +528,58 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
             hnr[i] = 0;
           }
         }
-        float s0 = 0.0f, s1 = 0.0f;
+        float acc[kDownRowsPerWarp];
 #pragma unroll
-        for (int i = 0; i < GF; ++i) {
-          const int a0 = block_dot(w0[i], hr[i], hnr[i]);
-          const int a1 = block_dot(w1[i], hr[i], hnr[i]);
-          s0 = __fmaf_rn(hdr[i], __int2float_rn(a0), s0);
-          s1 = __fmaf_rn(hdr[i], __int2float_rn(a1), s1);
-          if (a.dbg.Ad != nullptr && lane < A) {
-            a.dbg.Ad[((long)p * d + r0) * nbf + lane * GF + i] = a0;
-            a.dbg.Ad[((long)p * d + r0 + 1) * nbf + lane * GF + i] = a1;
+        for (int j = 0; j < kDownRowsPerWarp; ++j) {
+          acc[j] = 0.0f;
+          if (j < nj) {
+            const uint8_t* srow = sbase + (long)j * kNW * rb;
+#pragma unroll
+            for (int i = 0; i < GF; ++i) {
+              uint4 wv = make_uint4(0, 0, 0, 0);
+              if (lane < A) wv = *reinterpret_cast<const uint4*>(srow + store_chunk(lane, i, GF) * 16);
+              const int ai = block_dot(wv, hr[i], hnr[i]);
+              acc[j] = __fmaf_rn(hdr[i], __int2float_rn(ai), acc[j]);
+              if (DBG && a.dbg.Ad != nullptr && lane < A)
+                a.dbg.Ad[((long)p * d + row0 + c0 + j * kNW + warp) * nbf + lane * GF + i] = ai;
+            }
           }
         }
-        s0 = warp_tree_sum(s0);
-        s1 = warp_tree_sum(s1);
-        const float e0 = __fmul_rn(sd0, s0), e1 = __fmul_rn(sd1, s1);
-        if (lane == 0) {
-          es[lr * P + p] = e0;
-          es[(lr + 1) * P + p] = e1;
-          if (a.dbg.e != nullptr) {
-            a.dbg.e[(long)p * d + r0] = e0;
-            a.dbg.e[(long)p * d + r0 + 1] = e1;
-          }
+        const float v = warp_tree_sum8(acc, lane);
+        if (lane < kDownRowsPerWarp && jl < nj) {
+          const float e = __fmul_rn(sdx[jl * kNW], v);
+          es[(jl * kNW + warp) * P + p] = e;
+          if (DBG && a.dbg.e != nullptr) a.dbg.e[(long)p * d + row0 + c0 + jl * kNW + warp] = e;
         }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == pl.nst) {
+        s = 0;
+        ph ^= 1u;
       }
       if (slot == nu - 1) {
-        __syncwarp();
-        for (int t = lane; t < T; t += 32) {
-#pragma unroll
-          for (int j = 0; j < kDownRowsPerWarp; ++j) {
-            const float* er = es + (lr + j) * P;
-            float y = a.s.n_shared ? er[T * K + t] : 0.0f;
-            for (int k = 0; k < K; ++k) y = __fmaf_rn(t_w[t * K + k], er[t_inv[t * K + k]], y);
-            if (a.s.has_norm) y = __fadd_rn(a.x[(long)t * d + r0 + j], y);
-            a.y[(long)t * d + r0 + j] = y;
+        // every union expert of this chunk is in: combine this warp's rows, one (row, token)
+        // per lane
+        const int j = lane & 7, t = lane >> 3;
+        for (int tt = t; tt < T; tt += 4) {
+          if (j < nj) {
+            const float* er = es + (j * kNW + warp) * P;
+            float y = a.s.n_shared ? er[T * K + tt] : 0.0f;
+            for (int k = 0; k < K; ++k) y = __fmaf_rn(t_w[tt * K + k], er[t_inv[tt * K + k]], y);
+            const long o = (long)tt * d + row0 + c0 + j * kNW + warp;
+            if (a.s.has_norm) y = __fadd_rn(a.x[o], y);
+            a.y[o] = y;
           }
         }
         __syncwarp();
-      }
-      if (++slot == nu) {
         slot = 0;
-        ++unit;
+        if (++ci < nch) {
+          chunk(ci, c0, cn);
+          nj = cn > warp ? (cn - warp + kNW - 1) / kNW : 0;
+        }
+      } else {
+        ++slot;
       }
     }
   }
@@ -560,22 +603,40 @@ static cudaError_t launch_ex(void (*kern)(const Args), const Args& args, int gri
   return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
+int down_grid(int d, int num_sms) { return d < num_sms ? d : num_sms; }
+
 cudaError_t configure_expert_kernels() {
   cudaError_t e = cudaSuccess;
 #define COLI_SET(KERN)                                                                      \
   if (e == cudaSuccess)                                                                     \
     e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  COLI_SET(gateup_decode_kernel<1>) COLI_SET(gateup_decode_kernel<2>)
-  COLI_SET(gateup_decode_kernel<3>) COLI_SET(gateup_decode_kernel<4>)
-  COLI_SET(gateup_decode_kernel<5>) COLI_SET(gateup_decode_kernel<6>)
-  COLI_SET(gateup_decode_kernel<7>) COLI_SET(gateup_decode_kernel<8>)
-  COLI_SET(down_decode_kernel<1>) COLI_SET(down_decode_kernel<2>)
-  COLI_SET(down_decode_kernel<3>) COLI_SET(down_decode_kernel<4>)
-  COLI_SET(down_decode_kernel<5>) COLI_SET(down_decode_kernel<6>)
-  COLI_SET(down_decode_kernel<7>) COLI_SET(down_decode_kernel<8>)
+#define COLI_SET2(TMPL, N) COLI_SET((TMPL<N, false>)) COLI_SET((TMPL<N, true>))
+  COLI_SET2(gateup_decode_kernel, 1) COLI_SET2(gateup_decode_kernel, 2)
+  COLI_SET2(gateup_decode_kernel, 3) COLI_SET2(gateup_decode_kernel, 4)
+  COLI_SET2(gateup_decode_kernel, 5) COLI_SET2(gateup_decode_kernel, 6)
+  COLI_SET2(gateup_decode_kernel, 7) COLI_SET2(gateup_decode_kernel, 8)
+  COLI_SET2(down_decode_kernel, 1) COLI_SET2(down_decode_kernel, 2)
+  COLI_SET2(down_decode_kernel, 3) COLI_SET2(down_decode_kernel, 4)
+  COLI_SET2(down_decode_kernel, 5) COLI_SET2(down_decode_kernel, 6)
+  COLI_SET2(down_decode_kernel, 7) COLI_SET2(down_decode_kernel, 8)
+#undef COLI_SET2
 #undef COLI_SET
   return e;
 }
+
+// kernel instance for N blocks per lane group, with or without the debug stores
+#define COLI_PICK(TMPL, N, DBG, OUT)                                \
+  switch (N) {                                                     \
+    case 1: OUT = DBG ? TMPL<1, true> : TMPL<1, false>; break;     \
+    case 2: OUT = DBG ? TMPL<2, true> : TMPL<2, false>; break;     \
+    case 3: OUT = DBG ? TMPL<3, true> : TMPL<3, false>; break;     \
+    case 4: OUT = DBG ? TMPL<4, true> : TMPL<4, false>; break;     \
+    case 5: OUT = DBG ? TMPL<5, true> : TMPL<5, false>; break;     \
+    case 6: OUT = DBG ? TMPL<6, true> : TMPL<6, false>; break;     \
+    case 7: OUT = DBG ? TMPL<7, true> : TMPL<7, false>; break;     \
+    case 8: OUT = DBG ? TMPL<8, true> : TMPL<8, false>; break;     \
+    default: return cudaErrorInvalidValue;                         \
+  }
 
 cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
                                  const ExpertDebug& dbg, int num_sms, bool pdl,
@@ -586,40 +647,21 @@ cudaError_t launch_gateup_decode(const Shape& s, const Store& st, const Work& w,
   if (grid > num_sms) grid = num_sms;
   GateupArgs args{s, st, w, dbg, gateup_plan(s.d, s.f, s.T, s.K, s.E, s.n_shared, (int)grid)};
   const int G = (s.d / kQB + 31) / 32;
+  const bool dbg_on = dbg.g || dbg.Ag;
   void (*k)(const GateupArgs) = nullptr;
-  switch (G) {
-    case 1: k = gateup_decode_kernel<1>; break;
-    case 2: k = gateup_decode_kernel<2>; break;
-    case 3: k = gateup_decode_kernel<3>; break;
-    case 4: k = gateup_decode_kernel<4>; break;
-    case 5: k = gateup_decode_kernel<5>; break;
-    case 6: k = gateup_decode_kernel<6>; break;
-    case 7: k = gateup_decode_kernel<7>; break;
-    case 8: k = gateup_decode_kernel<8>; break;
-    default: return cudaErrorInvalidValue;
-  }
+  COLI_PICK(gateup_decode_kernel, G, dbg_on, k)
   return launch_ex(k, args, (int)grid, args.pl.total, pdl, stream);
 }
 
 cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const Store& st,
                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream) {
-  long grid = s.d / kDownRd;
-  if (grid > num_sms) grid = num_sms;
-  DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.E, s.n_shared, (int)grid), x, y};
+  const int grid = down_grid(s.d, num_sms);
+  DownArgs args{s, st, w, dbg, down_plan(s.d, s.f, s.T, s.K, s.E, s.n_shared, grid), x, y};
   const int GF = (s.f / kQB + 31) / 32;
+  const bool dbg_on = dbg.e || dbg.Ad;
   void (*k)(const DownArgs) = nullptr;
-  switch (GF) {
-    case 1: k = down_decode_kernel<1>; break;
-    case 2: k = down_decode_kernel<2>; break;
-    case 3: k = down_decode_kernel<3>; break;
-    case 4: k = down_decode_kernel<4>; break;
-    case 5: k = down_decode_kernel<5>; break;
-    case 6: k = down_decode_kernel<6>; break;
-    case 7: k = down_decode_kernel<7>; break;
-    case 8: k = down_decode_kernel<8>; break;
-    default: return cudaErrorInvalidValue;
-  }
+  COLI_PICK(down_decode_kernel, GF, dbg_on, k)
   return launch_ex(k, args, (int)grid, args.pl.total, pdl, stream);
 }
 

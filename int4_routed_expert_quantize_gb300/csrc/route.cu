@@ -144,26 +144,147 @@ __device__ void union_bucket(const Shape& s, const Work& w, const int* idsv, int
   }
 }
 
-// One launch does the whole routing half.  Every CTA: bulk-prefetches its kRouterEpc router
-// rows into L2, lets the gate/up grid start its weight prefetch, normalises the tokens
-// (RMSNorm, one warp per token) into shared memory in the router's chunk order, writes its share
-// of the int8 activation blocks (one warp per block of 32), then computes the logits of its
-// experts for every token (one warp per (expert, token): lane g runs the fma chain over its d/32
-// contiguous elements, the warp butterfly adds the 32 partials).  The last CTA to finish
-// (ticket counter, no waiting) selects the experts and builds the union.
+// Order-preserving key of a float score: a larger float gives a larger unsigned key, equal
+// floats equal keys.  0 is below every finite score's key and marks an empty or taken entry.
+// (The scores here are sigmoids plus an optional bias: finite, never -0.)
+__device__ __forceinline__ uint32_t score_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// top-K of one token with warp reductions: lane l holds the keys of experts l, l+32, ...
+// (NM per lane, E <= 32*NM).  Each round takes the largest key, ties to the lower expert id
+// (each lane's own scan keeps its lowest id on a tie; the warp takes the lowest id among the
+// lanes holding the maximum).  sc, bias: the token's E scores and the bias, in shared memory.
+// Lane 0 writes the K ids; lane k < K writes weight k (selected scores renormalised, the sum
+// taken in rank order).
+template <int NM>
+__device__ __forceinline__ void topk_warp(const float* sc, const float* bias, int E, int K,
+                                          float routed_scale, int* ids, float* wt, int lane) {
+  uint32_t key[NM];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const int e = m * 32 + lane;
+    key[m] = e < E ? score_key(bias ? __fadd_rn(sc[e], bias[e]) : sc[e]) : 0u;
+  }
+  int my = 0;  // lane k < K: the k-th selected id
+  for (int k = 0; k < K; ++k) {
+    uint32_t bk = 0u;
+    int bm = 0;
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const bool gt = key[m] > bk;
+      bm = gt ? m : bm;
+      bk = gt ? key[m] : bk;
+    }
+    const uint32_t top = __reduce_max_sync(FULL, bk);
+    const uint32_t win = __reduce_min_sync(FULL, bk == top ? (uint32_t)(bm * 32 + lane) : 0xFFFFFFFFu);
+    const int wm = (int)(win & 31u) == lane ? (int)(win >> 5) : -1;
+#pragma unroll
+    for (int m = 0; m < NM; ++m) key[m] = m == wm ? 0u : key[m];
+    if (lane == 0) ids[k] = (int)win;
+    if (lane == k) my = (int)win;
+  }
+  // weights: the selected scores summed in rank order (values gathered by shuffle), then every
+  // lane divides its own
+  const float sk = lane < K ? sc[my] : 0.0f;
+  float S = __shfl_sync(FULL, sk, 0);
+  for (int k = 1; k < K; ++k) S = __fadd_rn(S, __shfl_sync(FULL, sk, k));
+  if (lane < K) wt[lane] = __fmul_rn(__fdiv_rn(sk, S), routed_scale);
+  __syncwarp();
+}
+
+// Batch union of at most 32 (token, rank) pairs by one warp: sorting the keys id*32 + pair
+// index (bitonic network over the lanes) lists the pairs grouped by expert in ascending id
+// order and, inside each expert, by pair index -- the stable bucket order; the slots start
+// where the id changes.  The shared expert becomes the last slot with every token.
+__device__ void union_warp(const Shape& s, const Work& w, const int* idsv, int lane) {
+  const int TK = s.T * s.K, T = s.T, K = s.K;
+  uint32_t v = lane < TK ? ((uint32_t)idsv[lane] << 5) | (uint32_t)lane : 0xFFFFFFFFu;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(FULL, v, j);
+      const bool ascending = (lane & k) == 0, lower = (lane & j) == 0;
+      v = (lower == ascending) ? min(v, o) : max(v, o);
+    }
+  }
+  const bool valid = lane < TK;
+  const int e = (int)(v >> 5), i = (int)(v & 31u);
+  const int prev = __shfl_up_sync(FULL, e, 1);
+  const bool head = valid && (lane == 0 || e != prev);
+  const uint32_t heads = __ballot_sync(FULL, head);
+  const int n_routed = __popc(heads);
+  if (head) {
+    const int slot = __popc(heads & ((1u << lane) - 1u));
+    w.union_ids[slot] = e;
+    w.offsets[slot] = lane;
+  }
+  if (valid) {
+    w.pair_token[lane] = i / K;
+    w.pair_rank[lane] = i % K;
+    w.inv[i] = lane;
+  }
+  if (lane == 0) {
+    int nu = n_routed;
+    if (s.n_shared) {
+      w.union_ids[nu] = s.E;
+      w.offsets[nu] = TK;
+      ++nu;
+    }
+    w.offsets[nu] = TK + (s.n_shared ? T : 0);
+    *w.n_union = nu;
+  }
+  if (s.n_shared && lane < T) {
+    w.pair_token[TK + lane] = lane;
+    w.pair_rank[TK + lane] = -1;
+  }
+}
+
+// After a timed-out wait, wait once more (bounded, ignoring the abort flag) for the bulk copy,
+// so that no copy still writes shared memory when the CTA exits.
+__device__ __noinline__ void route_drain(uint64_t* bar) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, 0u))
+    if (global_ns() - t0 > kWaitLimitNs / 8) break;
+}
+
+// One launch does the whole routing half.  Every CTA: one bulk copy brings its kRouterEpc
+// router rows into shared memory while all threads stage the tokens there (in the router's
+// chunk order) and the gate/up grid is let start its weight prefetch; then the optional
+// RMSNorm (one warp per token), the logits of its experts for every token (one warp per
+// (expert, token): lane g runs the fma chain over its d/32 contiguous elements, the butterfly
+// adds the 32 partials) and, on the other warps at the same time, this CTA's share of the int8
+// activation blocks (one warp per block of 32).  The last CTA to finish (ticket counter, no
+// waiting) selects the experts and builds the union in shared memory and registers.
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x, const Shape s,
                                                     const Store st, const Work w) {
-  extern __shared__ __align__(16) float xsm[];  // [T][d] normalised tokens, router chunk order
+  extern __shared__ __align__(128) float route_sm[];
+  __shared__ __align__(8) uint64_t wbar;
   __shared__ float rinv[kDecodeTmax];
   __shared__ int cnt[kMaxE];
   __shared__ int cursor[kMaxE];
+  __shared__ int sids[kDecodeTmax * 32];
+  __shared__ float swt[kDecodeTmax * 32];
   __shared__ int is_last;
+  __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
   const int d = s.d, E = s.E, T = s.T, Gd = d >> 5, nbd = d >> 5;
   const int e0 = blockIdx.x * kRouterEpc;
   const int ne = min(kRouterEpc, E - e0);
-  if (threadIdx.x == 0)
-    for (int r = 0; r < ne; ++r) bulk_prefetch_l2(st.wr + (long)(e0 + r) * d, (uint32_t)d * 4u);
+  float* wrs = route_sm;                   // [kRouterEpc][d] router rows as stored
+  float* xsm = route_sm + kRouterEpc * d;  // [T][max(d,E)] tokens, later the scores
+  float* sbias = xsm + T * max(d, E);      // [E]
+  if (threadIdx.x == 0) {
+    mbar_init(&wbar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_expect_tx(&wbar, (uint32_t)(ne * d * 4));
+    const uint64_t pol = l2_evict_last_policy();
+    for (int r = 0; r < ne; ++r)
+      bulk_g2s(wrs + r * d, st.wr + (long)(e0 + r) * d, (uint32_t)d * 4u, &wbar, pol);
+  }
   griddep_launch_dependents();
 
   // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
@@ -210,8 +331,13 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
     __syncthreads();
   }
 
-  // this CTA's share of the activation blocks: x_n (natural order), int8 codes, scale, code sum
-  for (int b = blockIdx.x * nwarp + warp; b < T * nbd; b += gridDim.x * nwarp) {
+  // this CTA's share of the activation blocks: x_n (natural order), int8 codes, scale, code sum.
+  // The warps that compute no logits take them (while the logits run); without such warps
+  // every warp takes its share first.
+  const int ndot = ne * T;
+  const int nq = ndot < nwarp ? nwarp - ndot : nwarp;
+  const int qw = ndot < nwarp ? warp - ndot : warp;
+  for (int b = qw >= 0 ? blockIdx.x * nq + qw : T * nbd; b < T * nbd; b += gridDim.x * nq) {
     const int t = b / nbd, bb = b - t * nbd;
     const int j = bb * 32 + lane;
     const int g = j / Gd, m = j - g * Gd;
@@ -227,32 +353,33 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
     }
   }
 
-  const int nchunk = d / 128;  // 4-float chunks per lane
-  for (int pi = warp; pi < ne * T; pi += nwarp) {
-    const int e = e0 + pi / T, t = pi % T;
-    const float4* wr = reinterpret_cast<const float4*>(st.wr + (long)e * d);
+  // logits: router rows and tokens both in shared memory, chunk i4*32 + g for lane g
+  bool waited = false;
+  for (int pi = warp; pi < ndot; pi += nwarp) {
+    if (!waited) {
+      waited = true;
+      if (!mbar_wait_bounded(&wbar, 0u, &abort_flag, w.status)) {
+        route_drain(&wbar);
+        break;
+      }
+    }
+    const int r = pi / T, t = pi - r * T;
+    const float4* wp = reinterpret_cast<const float4*>(wrs + (long)r * d);
     const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
     float p = 0.0f;
-    for (int i0 = 0; i0 < nchunk; i0 += 16) {
-      float4 a[16];  // 16 loads in flight, then the fma chain in element order
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        a[k] = i0 + k < nchunk ? __ldg(wr + (i0 + k) * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (i0 + k < nchunk) {
-          const float4 b = xp[(i0 + k) * 32 + lane];
-          p = __fmaf_rn(a[k].x, b.x, p);
-          p = __fmaf_rn(a[k].y, b.y, p);
-          p = __fmaf_rn(a[k].z, b.z, p);
-          p = __fmaf_rn(a[k].w, b.w, p);
-        }
-      }
+#pragma unroll 4
+    for (int i4 = 0; i4 < d / 128; ++i4) {
+      const float4 a4 = wp[i4 * 32 + lane];
+      const float4 b4 = xp[i4 * 32 + lane];
+      p = __fmaf_rn(a4.x, b4.x, p);
+      p = __fmaf_rn(a4.y, b4.y, p);
+      p = __fmaf_rn(a4.z, b4.z, p);
+      p = __fmaf_rn(a4.w, b4.w, p);
     }
     p = warp_tree_sum(p);
     if (lane == 0) {
-      w.logits[(long)t * E + e] = p;
-      w.scores[(long)t * E + e] = canon_sigmoid(p);
+      w.logits[(long)t * E + e0 + r] = p;
+      w.scores[(long)t * E + e0 + r] = canon_sigmoid(p);
     }
   }
   __threadfence();
@@ -261,28 +388,40 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // the last CTA: every score into shared memory in one round, selection and union there,
-  // then the results out to the workspace
+  // the last CTA: every score (and the bias) into shared memory in one round, selection and
+  // union there, then the results out to the workspace
   float* ssc = xsm;  // [T][E] (the token buffer is no longer needed)
-  __shared__ int sids[kDecodeTmax * 32];
-  __shared__ float swt[kDecodeTmax * 32];
   for (int i = threadIdx.x; i < T * E; i += blockDim.x) ssc[i] = __ldcg(w.scores + i);
+  if (st.bias)
+    for (int i = threadIdx.x; i < E; i += blockDim.x) sbias[i] = st.bias[i];
   __syncthreads();
-  for (int t = warp; t < T; t += nwarp) topk_token(s, st, ssc + t * E, sids + t * s.K, swt + t * s.K, lane);
+  const float* bs = st.bias ? sbias : nullptr;
+  for (int t = warp; t < T; t += nwarp) {
+    if (E <= 256)
+      topk_warp<8>(ssc + t * E, bs, E, s.K, s.routed_scale, sids + t * s.K, swt + t * s.K, lane);
+    else
+      topk_warp<32>(ssc + t * E, bs, E, s.K, s.routed_scale, sids + t * s.K, swt + t * s.K, lane);
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < T * s.K; i += blockDim.x) {
     w.ids[i] = sids[i];
     w.w[i] = swt[i];
   }
-  union_bucket(s, w, sids, cnt, cursor);
+  if (T * s.K <= 32) {
+    if (warp == 0) union_warp(s, w, sids, lane);
+  } else {
+    union_bucket(s, w, sids, cnt, cursor);
+  }
   if (threadIdx.x == 0) *w.counter = 0;  // ready for the next call
 }
 
-constexpr int kRouteSmemMax = kDecodeTmax * 8192 * 4;
+static size_t route_smem_bytes(int d, int E, int T) {
+  return ((size_t)kRouterEpc * d + (size_t)T * (d > E ? d : E) + E) * sizeof(float);
+}
 
 cudaError_t configure_route_kernels() {
   return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kRouteSmemMax);
+                              (int)route_smem_bytes(8192, kMaxE, kDecodeTmax));
 }
 
 // ------------------------------------------------------------------ batched routing ------
@@ -583,8 +722,7 @@ cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const 
                          cudaStream_t stream) {
   // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work
   const int grid = (s.E + kRouterEpc - 1) / kRouterEpc;
-  const size_t smem = (size_t)s.T * (s.d > s.E ? s.d : s.E) * sizeof(float);
-  route_kernel<<<grid, 256, smem, stream>>>(x, s, st, w);
+  route_kernel<<<grid, 256, route_smem_bytes(s.d, s.E, s.T), stream>>>(x, s, st, w);
   return cudaGetLastError();
 }
 

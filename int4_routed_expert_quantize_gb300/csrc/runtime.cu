@@ -252,7 +252,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
     const long slots = (long)(Tc * c.top_k < c.n_experts ? Tc * c.top_k : c.n_experts) + c.n_shared;
     const long gu_grid = slots * (c.f / 32) < sms ? slots * (c.f / 32) : sms;
-    const long dn_grid = c.d / kDownRd < sms ? c.d / kDownRd : sms;
+    const int dn_grid = down_grid(c.d, sms);
     if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid).nst < 2 ||
         down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst < 2)
       return COLI_EUNSUPPORTED;
