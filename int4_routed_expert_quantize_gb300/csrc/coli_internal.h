@@ -20,8 +20,6 @@ constexpr int kDownRowsPerWarp = 8;             // output rows per warp per down
 constexpr int kDownChunk = kNW * kDownRowsPerWarp;  // at most this many rows per down stage
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
-constexpr int kGateupSmem = 160 * 1024;         // gate/up ring budget: leaves room on the SM for
-                                                // a routing CTA while its prefetch runs
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
 constexpr int kPrefillTileN = 64;               // pairs per tensor-core tile
 
@@ -66,7 +64,8 @@ struct Work {
   int8_t* qh = nullptr;      // [Pm,f]
   float* dh = nullptr;       // [Pm,f/32]
   int32_t* sh = nullptr;     // [Pm,f/32]
-  int32_t* counter = nullptr;  // last-CTA ticket of the router (returns to 0 after each use)
+  int32_t* sel_flag = nullptr;  // 1 once the gate/up grid of the current call published its
+                                // expert selection (the router grid clears it)
   int32_t* status = nullptr;   // COLI_OK or COLI_ETIMEOUT
 };
 
@@ -135,10 +134,11 @@ cudaError_t configure_expert_kernels();
 
 // shared-memory plans (host and device agree on the carve-up)
 struct GateupPlan {
-  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, tab_bytes, max_units, total;
+  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, tab_bytes, sel_bytes, max_units, total;
 };
 struct DownPlan {
-  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, tab_bytes, max_rows, max_slots, total;
+  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, tab_bytes, sel_bytes, max_rows, max_slots,
+      total;
 };
 GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);

@@ -16,6 +16,7 @@
 
 #include "coli_device.cuh"
 #include "coli_internal.h"
+#include "coli_select.cuh"
 
 namespace coli {
 
@@ -25,7 +26,6 @@ static inline int align16(int x) { return (x + 15) & ~15; }
 // tokens (T at most) and the 32 gate + 32 up row scales
 constexpr int kGuTabInts = 5 + kDecodeTmax;  // slot, expert, first pair, pairs, hb, tokens
 constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
-constexpr int kGuMaxSlots = kDecodeTmax * 32 + 1;  // union slots: T*K routed (K <= 32) + shared
 
 static long max_union_slots(int T, int K, int E, int n_shared) {
   return (long)(T * K < E ? T * K : E) + (n_shared ? 1 : 0);
@@ -41,15 +41,17 @@ GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid
   const long units = max_union_slots(T, K, E, n_shared) * (f / 32);
   p.max_units = (int)((units + grid - 1) / grid) + 2;
   p.tab_bytes = align16(p.max_units * kGuTabBytes);
-  const int fixed = 2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes + p.tab_bytes;
-  int nst = ((kGateupSmem > fixed + 2 * p.stage_bytes ? kGateupSmem : kSmemLimit) - fixed) / p.stage_bytes;
+  p.sel_bytes = align16(sel_bytes(T, E));
+  const int fixed =
+      2 * kMaxStages * 8 + p.xs_bytes + p.aux_bytes + p.hs_bytes + p.tab_bytes + p.sel_bytes;
+  int nst = (kSmemLimit - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
   return p;
 }
 
-// per-CTA tables of the down kernel: union slots (expert, first pair), routing weights and pair
-// indices, and the down-row scales of this CTA's rows for every slot
+// per-CTA tables of the down kernel: the selection (coli_select.cuh) and the down-row scales of
+// this CTA's rows for every union slot
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   DownPlan p;
   const int P = T * K + (n_shared ? T : 0);
@@ -61,8 +63,10 @@ DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   p.aux_bytes = align16(P * nbf * 8);
   p.es_bytes = align16(chunk * P * 4);
   p.max_slots = (int)max_union_slots(T, K, E, n_shared);
-  p.tab_bytes = align16((2 * (p.max_slots + 1) + 2 * T * K) * 4 + p.max_slots * p.max_rows * 4);
-  const int fixed = 2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes + p.tab_bytes;
+  p.tab_bytes = align16(p.max_slots * p.max_rows * 4);
+  p.sel_bytes = align16(sel_bytes(T, E));
+  const int fixed =
+      2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes + p.tab_bytes + p.sel_bytes;
   int nst = (kSmemLimit - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
@@ -110,7 +114,6 @@ template <int G, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const GateupArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
-  __shared__ int pex[kGuMaxSlots];  // expert of each union slot (producer warp)
   const int d = a.s.d, f = a.s.f, T = a.s.T;
   const int nbd = d >> 5, A = nbd / G, nhb = f >> 5;
   const GateupPlan& pl = a.pl;
@@ -122,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   int* nsx = reinterpret_cast<int*>(dxs + T * nbd);                // [T][nbd]  -8*sum(codes)
   float* hs = reinterpret_cast<float*>(xs + pl.xs_bytes + pl.aux_bytes);  // [2][32][T]
   int* tab = reinterpret_cast<int*>(xs + pl.xs_bytes + pl.aux_bytes + pl.hs_bytes);
+  Sel sel = sel_carve(xs + pl.xs_bytes + pl.aux_bytes + pl.hs_bytes + pl.tab_bytes, T, a.s.E);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int SPU = 32 / kGuRps;
   const int G_ = gridDim.x, c = blockIdx.x;
@@ -152,16 +156,67 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       bulk_g2s(ring + issued * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[issued], pol);
     }
   }
+  // the selection bias does not depend on the routing grid
+  if (a.st.bias)
+    for (int i = threadIdx.x; i < a.s.E; i += blockDim.x) sel.bias[i] = a.st.bias[i];
   // the routing grid is complete and its results visible from here on
   griddep_wait();
   griddep_launch_dependents();
 
-  // The producer warp reads the union slots' experts in the same round of memory latency as
-  // nu (entries past nu are read but never used) and starts streaming at once; the consumer
-  // warps build the tables meanwhile.
-  const int nu = __ldcg(a.w.n_union);
-  if (warp == kNW)
-    for (int i = lane; i < kGuMaxSlots && i <= a.s.E; i += 32) pex[i] = __ldcg(a.w.union_ids + i);
+  // Every CTA selects the experts itself from the router's scores: the score loads are issued
+  // first (plain loads: the bulk-copy queue still holds the shared expert's prefetch), the
+  // token codes are staged meanwhile, then top-K and union run in shared memory.  CTA 0 also
+  // publishes the selection for the down grid and the debug dumps.
+  const int TE = T * a.s.E;
+  float sreg[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < TE) sreg[k] = __ldcg(a.w.scores + i);
+  }
+  // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of a
+  // chunk live in separate planes so a warp's 16-byte loads are consecutive.  Each thread
+  // issues the loads of 4 blocks before storing any.
+  for (int i0 = threadIdx.x; i0 < T * nbd; i0 += 4 * blockDim.x) {
+    uint4 q0[4], q1[4];
+    float dv[4];
+    int sv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = i0 + k * blockDim.x;
+      if (idx < T * nbd) {
+        const int t = idx / nbd, b = idx - t * nbd;
+        const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
+        q0[k] = __ldcg(src);
+        q1[k] = __ldcg(src + 1);
+        dv[k] = __ldcg(a.w.dx + (long)t * nbd + b);
+        sv[k] = __ldcg(a.w.sx + (long)t * nbd + b);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = i0 + k * blockDim.x;
+      if (idx < T * nbd) {
+        const int t = idx / nbd, b = idx - t * nbd;
+        const int g = b / G, i = b - g * G;
+        uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
+        *reinterpret_cast<uint4*>(base) = q0[k];
+        *reinterpret_cast<uint4*>(base + nbd * 16) = q1[k];
+        dxs[idx] = dv[k];
+        nsx[idx] = -8 * sv[k];
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < TE) sel.sc[i] = sreg[k];
+  }
+  for (int i = threadIdx.x + 4 * blockDim.x; i < TE; i += blockDim.x) sel.sc[i] = __ldcg(a.w.scores + i);
+  __syncthreads();
+  select_union(a.s, sel, a.st.bias != nullptr);
+  if (blockIdx.x == 0) sel_publish(a.s, sel, a.w);
+  const int nu = *sel.nu;
 
   // routed units of this CTA: the total U = UA + UB is split evenly (each CTA's shared units
   // count towards its share) when there are at least as many routed units as CTAs
@@ -192,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
 
   if (warp == kNW) {
     // ---------------- producer: one lane streams the remaining stages
-    __syncwarp();
     if (producer) {
       int s = issued % pl.nst;
       uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
@@ -200,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
         int slot, hb;
         unit_of(it / SPU, slot, hb);
-        const uint8_t* src = a.st.wgu + ((long)pex[slot] * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
+        const uint8_t* src =
+            a.st.wgu + ((long)sel.u_ids[slot] * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
         issued = it + 1;
@@ -212,27 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
   } else {
-    // every token's codes, with block b = g*G + i at chunk i*A + g; the two 16-byte halves of
-    // a chunk live in separate planes so a warp's 16-byte loads are consecutive
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < T * nbd; idx += kNW * 32) {
-      const int t = idx / nbd, b = idx - t * nbd;
-      const int g = b / G, i = b - g * G;
-      const uint4* src = reinterpret_cast<const uint4*>(a.w.qx + (long)t * d + b * 32);
-      uint8_t* base = xs + (long)t * d + (i * A + g) * 16;
-      *reinterpret_cast<uint4*>(base) = __ldcg(src);
-      *reinterpret_cast<uint4*>(base + nbd * 16) = __ldcg(src + 1);
-      dxs[idx] = __ldcg(a.w.dx + (long)t * nbd + b);
-      nsx[idx] = -8 * __ldcg(a.w.sx + (long)t * nbd + b);
-    }
     // unit table: every value a stage needs, loaded once (one round of memory latency)
     for (int lu = warp; lu < nunit && lu < pl.max_units; lu += kNW) {
       int slot, hb;
       unit_of(lu, slot, hb);
       int* tu = tab + lu * (kGuTabInts + 64);
-      const int ex = __ldcg(a.w.union_ids + slot);
-      const int p0 = __ldcg(a.w.offsets + slot);
-      const int np = __ldcg(a.w.offsets + slot + 1) - p0;
+      const int ex = sel.u_ids[slot];
+      const int p0 = sel.u_off[slot];
+      const int np = sel.u_off[slot + 1] - p0;
       if (lane == 0) {
         tu[0] = slot;
         tu[1] = ex;
@@ -240,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         tu[3] = np;
         tu[4] = hb;
       }
-      if (lane < np && lane < kDecodeTmax) tu[5 + lane] = __ldcg(a.w.pair_token + p0 + lane);
+      if (lane < np && lane < kDecodeTmax) tu[5 + lane] = sel.p_tok[p0 + lane];
       const float* scx = a.st.sc + (long)ex * (2 * f + d);
       float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
       tsc[lane] = scx[hb * 32 + lane];
@@ -393,29 +435,29 @@ template <int GF, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t selbar;
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
   const int nbf = f >> 5, A = nbf / GF, rb = f >> 1;
   const DownPlan& pl = a.pl;
-  const int nu = __ldcg(a.w.n_union);
-  const int P = __ldcg(a.w.offsets + nu);
+  const int Pm = T * K + (a.s.n_shared ? T : 0);  // pairs at most (the layout's stride)
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
   uint64_t* empty = full + kMaxStages;
   uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][2 halves][chunks][16]
   float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf]
-  int* hn = reinterpret_cast<int*>(hd + P * nbf);                  // [P][nbf]  -8*sum(codes)
-  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [chunk row][P]
-  int* t_ex = reinterpret_cast<int*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
-  int* t_off = t_ex + pl.max_slots + 1;
-  float* t_w = reinterpret_cast<float*>(t_off + pl.max_slots + 1);  // [T*K]
-  int* t_inv = reinterpret_cast<int*>(t_w + T * K);                 // [T*K]
-  float* t_sd = reinterpret_cast<float*>(t_inv + T * K);            // [slot][max_rows]
+  int* hn = reinterpret_cast<int*>(hd + Pm * nbf);                 // [P][nbf]  -8*sum(codes)
+  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [chunk row][Pm]
+  float* t_sd = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
+  Sel sel = sel_carve(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes + pl.tab_bytes, T, a.s.E);
+  const int* t_ex = sel.u_ids;   // [slot] expert
+  const int* t_off = sel.u_off;  // [slot] first pair
+  const float* t_w = sel.wt;     // [T*K] routing weights
+  const int* t_inv = sel.inv;    // [T*K] pair of (token, rank)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int row0 = down_rows_begin(d, blockIdx.x, gridDim.x);
   const int nrow = down_rows_begin(d, blockIdx.x + 1, gridDim.x) - row0;
   const int nch = (nrow + kDownChunk - 1) / kDownChunk;
-  const int nstage = nch * nu;
   auto chunk = [&](int ci, int& c0, int& cn) {
     c0 = nrow * ci / nch;
     cn = nrow * (ci + 1) / nch - c0;
@@ -426,10 +468,41 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kNW);
     }
+    mbar_init(&selbar, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
+  // The router finished before the gate/up grid let this grid start.  If the gate/up grid has
+  // published its selection already (one look at its flag, no waiting), load it; otherwise
+  // select the experts from the router's scores here (the same selection every CTA of both
+  // expert kernels makes).
+  __shared__ int published;
+  if (threadIdx.x == 0) published = sel_published(a.w);
+  __syncthreads();
+  const int TE = T * a.s.E;
+  if (published) {
+    sel_load_published(a.s, sel, a.w);
+  } else if ((a.s.E % 4) == 0) {
+    if (threadIdx.x == 0) {
+      const uint64_t keep = l2_evict_last_policy();
+      mbar_expect_tx(&selbar, (uint32_t)((TE + (a.st.bias ? a.s.E : 0)) * 4));
+      bulk_g2s(sel.sc, a.w.scores, (uint32_t)TE * 4u, &selbar, keep);
+      if (a.st.bias) bulk_g2s(sel.bias, a.st.bias, (uint32_t)a.s.E * 4u, &selbar, keep);
+    }
+    mbar_wait_bounded(&selbar, 0u, &abort_flag, a.w.status);
+  } else {
+    for (int i = threadIdx.x; i < TE; i += blockDim.x) sel.sc[i] = __ldcg(a.w.scores + i);
+    if (a.st.bias)
+      for (int i = threadIdx.x; i < a.s.E; i += blockDim.x) sel.bias[i] = a.st.bias[i];
+  }
+  if (!published) {
+    __syncthreads();
+    select_union(a.s, sel, a.st.bias != nullptr);
+  }
+  const int nu = *sel.nu;
+  const int P = t_off[nu];
+  const int nstage = nch * nu;
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
   int issued = 0;
@@ -440,38 +513,48 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
     mbar_expect_tx(&full[s], (uint32_t)(cn * rb));
     bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)(cn * rb), &full[s], pol);
   };
-  // the routing results are complete when this grid starts: prefetch the first stages and
-  // build the CTA's tables (union slots, weights, pair indices, down-row scales) before the
-  // wait for the gate/up grid
+  // prefetch the first stages and load this CTA's down-row scales before the wait for the
+  // gate/up grid
   if (producer)
-    for (; issued < nstage && issued < pl.nst; ++issued)
-      issue(issued, issued / nu, __ldcg(a.w.union_ids + issued % nu));
-  for (int i = threadIdx.x; i <= nu; i += blockDim.x) {
-    t_ex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
-    t_off[i] = __ldcg(a.w.offsets + i);
-  }
-  for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
-    t_w[i] = __ldcg(a.w.w + i);
-    t_inv[i] = __ldcg(a.w.inv + i);
-  }
+    for (; issued < nstage && issued < pl.nst; ++issued) issue(issued, issued / nu, t_ex[issued % nu]);
   for (int i = threadIdx.x; i < nu * nrow; i += blockDim.x) {
     const int slot = i / nrow, r = i - slot * nrow;
-    const int ex = __ldcg(a.w.union_ids + slot);
-    t_sd[slot * pl.max_rows + r] = a.st.sc[(long)ex * (2 * f + d) + 2 * f + row0 + r];
+    t_sd[slot * pl.max_rows + r] = a.st.sc[(long)t_ex[slot] * (2 * f + d) + 2 * f + row0 + r];
   }
   // gate/up grid complete: h codes visible from here on
   griddep_wait();
 
-#pragma unroll 4
-  for (int idx = threadIdx.x; idx < P * nbf; idx += blockDim.x) {
-    const int p = idx / nbf, b = idx - p * nbf;
-    const int g = b / GF, i = b - g * GF;
-    const uint4* src = reinterpret_cast<const uint4*>(a.w.qh + (long)p * f + b * 32);
-    uint8_t* base = hq + (long)p * f + (i * A + g) * 16;
-    *reinterpret_cast<uint4*>(base) = __ldcg(src);
-    *reinterpret_cast<uint4*>(base + nbf * 16) = __ldcg(src + 1);
-    hd[idx] = __ldcg(a.w.dh + (long)p * nbf + b);
-    hn[idx] = -8 * __ldcg(a.w.sh + (long)p * nbf + b);
+  // every pair's h codes (block b = g*GF + i at chunk i*A + g, two 16-byte planes), scales and
+  // code sums; each thread issues the loads of 4 blocks before storing any
+  for (int i0 = threadIdx.x; i0 < P * nbf; i0 += 4 * blockDim.x) {
+    uint4 q0[4], q1[4];
+    float dv[4];
+    int sv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = i0 + k * blockDim.x;
+      if (idx < P * nbf) {
+        const int p = idx / nbf, b = idx - p * nbf;
+        const uint4* src = reinterpret_cast<const uint4*>(a.w.qh + (long)p * f + b * 32);
+        q0[k] = __ldcg(src);
+        q1[k] = __ldcg(src + 1);
+        dv[k] = __ldcg(a.w.dh + (long)p * nbf + b);
+        sv[k] = __ldcg(a.w.sh + (long)p * nbf + b);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = i0 + k * blockDim.x;
+      if (idx < P * nbf) {
+        const int p = idx / nbf, b = idx - p * nbf;
+        const int g = b / GF, i = b - g * GF;
+        uint8_t* base = hq + (long)p * f + (i * A + g) * 16;
+        *reinterpret_cast<uint4*>(base) = q0[k];
+        *reinterpret_cast<uint4*>(base + nbf * 16) = q1[k];
+        hd[idx] = dv[k];
+        hn[idx] = -8 * sv[k];
+      }
+    }
   }
   __syncthreads();
 

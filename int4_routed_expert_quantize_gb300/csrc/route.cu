@@ -10,6 +10,7 @@
 
 #include "coli_device.cuh"
 #include "coli_internal.h"
+#include "coli_select.cuh"
 #include "coli_tc.cuh"
 
 namespace coli {
@@ -17,230 +18,6 @@ namespace coli {
 // ------------------------------------------------------------------ router ---------------
 constexpr int kRouterEpc = 2;  // experts per CTA
 constexpr int kMaxE = 1024;
-
-// top-K of one token by (score + bias) descending, ties to the lower expert id, then weights
-// renormalised over the selected scores (sum taken in rank order).  One warp per token.
-// sc: the token's E scores; ids/wt: its K outputs (shared or global memory).
-__device__ void topk_token(const Shape& s, const Store& st, const float* sc, int* ids, float* wt,
-                           int lane) {
-  const int E = s.E, K = s.K;
-  uint32_t taken = 0;  // bit m: expert lane + 32*m already selected
-  float sv[32], sr[32];
-  const int nm = (E + 31) >> 5;
-  for (int m = 0; m < nm; ++m) {
-    const int e = m * 32 + lane;
-    sr[m & 31] = e < E ? sc[e] : 0.0f;
-    sv[m & 31] = e < E ? (st.bias ? __fadd_rn(sr[m & 31], st.bias[e]) : sr[m & 31]) : 0.0f;
-  }
-  float S = 0.0f;      // lane 0: sum of the selected scores in rank order
-  float pick[32];      // lane 0: the selected scores
-  for (int k = 0; k < K; ++k) {
-    float bv = 0.0f, bs = 0.0f;
-    int bi = 0x7fffffff;
-    for (int m = 0; m < nm; ++m) {
-      const int e = m * 32 + lane;
-      if (e >= E || ((taken >> m) & 1u)) continue;
-      const float v = sv[m & 31];
-      if (bi == 0x7fffffff || v > bv) {  // e ascending: a tie keeps the lower id
-        bv = v;
-        bs = sr[m & 31];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(FULL, bv, off);
-      const float os = __shfl_xor_sync(FULL, bs, off);
-      const int oi = __shfl_xor_sync(FULL, bi, off);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bs = os;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      ids[k] = bi;
-      pick[k & 31] = bs;
-      S = k == 0 ? bs : __fadd_rn(S, bs);
-    }
-  }
-  if (lane == 0)
-    for (int k = 0; k < K; ++k) wt[k] = __fmul_rn(__fdiv_rn(pick[k & 31], S), s.routed_scale);
-  __syncwarp();
-}
-
-// Batch union by one CTA: count pairs per expert, list the distinct experts in ascending id
-// order with their first pair, then place the pairs stably (pair index t*K+k ascending inside
-// each expert) with one warp; the shared expert becomes the last slot with every token.
-__device__ void union_bucket(const Shape& s, const Work& w, const int* idsv, int* cnt, int* cursor) {
-  const int E = s.E, K = s.K, T = s.T, TK = T * K;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < TK; i += blockDim.x) atomicAdd(&cnt[idsv[i]], 1);
-  __syncthreads();
-  if (warp == 0) {
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per, e1 = min(E, e0 + per);
-    int nz = 0, sum = 0;
-    for (int e = e0; e < e1; ++e) {
-      nz += cnt[e] > 0;
-      sum += cnt[e];
-    }
-    int nz_ex = nz, sum_ex = sum;  // inclusive scans, made exclusive below
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(FULL, nz_ex, off), b = __shfl_up_sync(FULL, sum_ex, off);
-      if (lane >= off) {
-        nz_ex += a;
-        sum_ex += b;
-      }
-    }
-    const int n_routed = __shfl_sync(FULL, nz_ex, 31);
-    int slot = nz_ex - nz, off = sum_ex - sum;
-    for (int e = e0; e < e1; ++e) {
-      if (cnt[e] > 0) {
-        w.union_ids[slot] = e;
-        w.offsets[slot] = off;
-        cursor[e] = off;
-        ++slot;
-        off += cnt[e];
-      }
-    }
-    __syncwarp();
-    for (int base = 0; base < TK; base += 32) {
-      const int i = base + lane;
-      const bool valid = i < TK;
-      const int e = valid ? idsv[i] : -1 - lane;
-      const unsigned peers = __match_any_sync(FULL, e);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      int pos = 0;
-      if (valid) {
-        pos = cursor[e] + rank;
-        w.pair_token[pos] = i / K;
-        w.pair_rank[pos] = i % K;
-        w.inv[i] = pos;
-      }
-      __syncwarp();
-      if (valid && (__ffs(peers) - 1) == lane) cursor[e] += __popc(peers);
-      __syncwarp();
-    }
-    if (lane == 0) {
-      int nu = n_routed;
-      if (s.n_shared) {
-        w.union_ids[nu] = E;
-        w.offsets[nu] = TK;
-        ++nu;
-      }
-      w.offsets[nu] = TK + (s.n_shared ? T : 0);
-      *w.n_union = nu;
-    }
-    if (s.n_shared)
-      for (int t = lane; t < T; t += 32) {
-        w.pair_token[TK + t] = t;
-        w.pair_rank[TK + t] = -1;
-      }
-  }
-}
-
-// Order-preserving key of a float score: a larger float gives a larger unsigned key, equal
-// floats equal keys.  0 is below every finite score's key and marks an empty or taken entry.
-// (The scores here are sigmoids plus an optional bias: finite, never -0.)
-__device__ __forceinline__ uint32_t score_key(float v) {
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// top-K of one token with warp reductions: lane l holds the keys of experts l, l+32, ...
-// (NM per lane, E <= 32*NM).  Each round takes the largest key, ties to the lower expert id
-// (each lane's own scan keeps its lowest id on a tie; the warp takes the lowest id among the
-// lanes holding the maximum).  sc, bias: the token's E scores and the bias, in shared memory.
-// Lane 0 writes the K ids; lane k < K writes weight k (selected scores renormalised, the sum
-// taken in rank order).
-template <int NM>
-__device__ __forceinline__ void topk_warp(const float* sc, const float* bias, int E, int K,
-                                          float routed_scale, int* ids, float* wt, int lane) {
-  uint32_t key[NM];
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-    const int e = m * 32 + lane;
-    key[m] = e < E ? score_key(bias ? __fadd_rn(sc[e], bias[e]) : sc[e]) : 0u;
-  }
-  int my = 0;  // lane k < K: the k-th selected id
-  for (int k = 0; k < K; ++k) {
-    uint32_t bk = 0u;
-    int bm = 0;
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const bool gt = key[m] > bk;
-      bm = gt ? m : bm;
-      bk = gt ? key[m] : bk;
-    }
-    const uint32_t top = __reduce_max_sync(FULL, bk);
-    const uint32_t win = __reduce_min_sync(FULL, bk == top ? (uint32_t)(bm * 32 + lane) : 0xFFFFFFFFu);
-    const int wm = (int)(win & 31u) == lane ? (int)(win >> 5) : -1;
-#pragma unroll
-    for (int m = 0; m < NM; ++m) key[m] = m == wm ? 0u : key[m];
-    if (lane == 0) ids[k] = (int)win;
-    if (lane == k) my = (int)win;
-  }
-  // weights: the selected scores summed in rank order (values gathered by shuffle), then every
-  // lane divides its own
-  const float sk = lane < K ? sc[my] : 0.0f;
-  float S = __shfl_sync(FULL, sk, 0);
-  for (int k = 1; k < K; ++k) S = __fadd_rn(S, __shfl_sync(FULL, sk, k));
-  if (lane < K) wt[lane] = __fmul_rn(__fdiv_rn(sk, S), routed_scale);
-  __syncwarp();
-}
-
-// Batch union of at most 32 (token, rank) pairs by one warp: sorting the keys id*32 + pair
-// index (bitonic network over the lanes) lists the pairs grouped by expert in ascending id
-// order and, inside each expert, by pair index -- the stable bucket order; the slots start
-// where the id changes.  The shared expert becomes the last slot with every token.
-__device__ void union_warp(const Shape& s, const Work& w, const int* idsv, int lane) {
-  const int TK = s.T * s.K, T = s.T, K = s.K;
-  uint32_t v = lane < TK ? ((uint32_t)idsv[lane] << 5) | (uint32_t)lane : 0xFFFFFFFFu;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(FULL, v, j);
-      const bool ascending = (lane & k) == 0, lower = (lane & j) == 0;
-      v = (lower == ascending) ? min(v, o) : max(v, o);
-    }
-  }
-  const bool valid = lane < TK;
-  const int e = (int)(v >> 5), i = (int)(v & 31u);
-  const int prev = __shfl_up_sync(FULL, e, 1);
-  const bool head = valid && (lane == 0 || e != prev);
-  const uint32_t heads = __ballot_sync(FULL, head);
-  const int n_routed = __popc(heads);
-  if (head) {
-    const int slot = __popc(heads & ((1u << lane) - 1u));
-    w.union_ids[slot] = e;
-    w.offsets[slot] = lane;
-  }
-  if (valid) {
-    w.pair_token[lane] = i / K;
-    w.pair_rank[lane] = i % K;
-    w.inv[i] = lane;
-  }
-  if (lane == 0) {
-    int nu = n_routed;
-    if (s.n_shared) {
-      w.union_ids[nu] = s.E;
-      w.offsets[nu] = TK;
-      ++nu;
-    }
-    w.offsets[nu] = TK + (s.n_shared ? T : 0);
-    *w.n_union = nu;
-  }
-  if (s.n_shared && lane < T) {
-    w.pair_token[TK + lane] = lane;
-    w.pair_rank[TK + lane] = -1;
-  }
-}
 
 // After a timed-out wait, wait once more (bounded, ignoring the abort flag) for the bulk copy,
 // so that no copy still writes shared memory when the CTA exits.
@@ -250,33 +27,28 @@ __device__ __noinline__ void route_drain(uint64_t* bar) {
     if (global_ns() - t0 > kWaitLimitNs / 8) break;
 }
 
-// One launch does the whole routing half.  Every CTA: one bulk copy brings its kRouterEpc
-// router rows into shared memory while all threads stage the tokens there (in the router's
-// chunk order) and the gate/up grid is let start its weight prefetch; then the optional
-// RMSNorm (one warp per token), the logits of its experts for every token (one warp per
-// (expert, token): lane g runs the fma chain over its d/32 contiguous elements, the butterfly
-// adds the 32 partials) and, on the other warps at the same time, this CTA's share of the int8
-// activation blocks (one warp per block of 32).  The last CTA to finish (ticket counter, no
-// waiting) selects the experts and builds the union in shared memory and registers.
+// One launch does the routing half up to the scores.  Every CTA: one bulk copy brings its
+// kRouterEpc router rows into shared memory while all threads stage the tokens there (in the
+// router's chunk order) and the gate/up grid is let start its weight prefetch; then the optional
+// RMSNorm (one warp per token), the logits and sigmoid scores of its experts for every token
+// (one warp per (expert, token): lane g runs the fma chain over its d/32 contiguous elements,
+// the butterfly adds the 32 partials) and, on the other warps at the same time, this CTA's share
+// of the int8 activation blocks (one warp per block of 32).  The expert kernels select the
+// experts from the scores themselves (coli_select.cuh), so no CTA here waits for another.
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x, const Shape s,
                                                     const Store st, const Work w) {
   extern __shared__ __align__(128) float route_sm[];
   __shared__ __align__(8) uint64_t wbar;
   __shared__ float rinv[kDecodeTmax];
-  __shared__ int cnt[kMaxE];
-  __shared__ int cursor[kMaxE];
-  __shared__ int sids[kDecodeTmax * 32];
-  __shared__ float swt[kDecodeTmax * 32];
-  __shared__ int is_last;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
   const int d = s.d, E = s.E, T = s.T, Gd = d >> 5, nbd = d >> 5;
   const int e0 = blockIdx.x * kRouterEpc;
   const int ne = min(kRouterEpc, E - e0);
   float* wrs = route_sm;                   // [kRouterEpc][d] router rows as stored
-  float* xsm = route_sm + kRouterEpc * d;  // [T][max(d,E)] tokens, later the scores
-  float* sbias = xsm + T * max(d, E);      // [E]
+  float* xsm = route_sm + kRouterEpc * d;  // [T][d] tokens
   if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) *w.sel_flag = 0;  // this call's selection is not published yet
     mbar_init(&wbar, 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -288,13 +60,25 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
   griddep_launch_dependents();
 
   // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
-  // i4*32 + g (coalesced float4 loads; conflict-free reads by lane)
-#pragma unroll 8
-  for (int c = threadIdx.x; c < T * (d / 4); c += blockDim.x) {
-    const int t = c / (d / 4), pos = c - t * (d / 4);
-    const int i4 = pos >> 5, g = pos & 31;
-    reinterpret_cast<float4*>(xsm + (long)t * d)[pos] =
-        *reinterpret_cast<const float4*>(x + (long)t * d + g * Gd + 4 * i4);
+  // i4*32 + g (conflict-free reads by lane).  Work item w of a token is (i4 = 8*(w>>8) + (w&7),
+  // g = (w>>3)&31), so a warp reads four 128-byte runs of x and its shared-memory stores fall in
+  // 4 bank groups; each thread issues its loads in batches of 8 before storing any.
+  const int n_i4 = d / 128, per_t = 256 * ((n_i4 + 7) / 8), nw = T * per_t;
+  for (int c0 = threadIdx.x; c0 < nw; c0 += 8 * blockDim.x) {
+    float4 v[8];
+    int dst[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = c0 + k * blockDim.x;
+      const int t = c / per_t, w = c - t * per_t;
+      const int i4 = ((w >> 8) << 3) + (w & 7), g = (w >> 3) & 31;
+      dst[k] = c < nw && i4 < n_i4 ? t * (d / 4) + i4 * 32 + g : -1;
+      if (dst[k] >= 0)
+        v[k] = __ldg(reinterpret_cast<const float4*>(x + (long)t * d + g * Gd + 4 * i4));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (dst[k] >= 0) reinterpret_cast<float4*>(xsm)[dst[k]] = v[k];
   }
   __syncthreads();
   if (s.has_norm) {
@@ -316,17 +100,30 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
       }
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < T * (d / 4); c += blockDim.x) {
-      const int t = c / (d / 4), pos = c - t * (d / 4);
-      const int i4 = pos >> 5, g = pos & 31;
-      const float r = rinv[t];
-      const float4 gm = *reinterpret_cast<const float4*>(st.gamma + g * Gd + 4 * i4);
-      float4 v = reinterpret_cast<float4*>(xsm + (long)t * d)[pos];
-      v.x = __fmul_rn(__fmul_rn(v.x, r), gm.x);
-      v.y = __fmul_rn(__fmul_rn(v.y, r), gm.y);
-      v.z = __fmul_rn(__fmul_rn(v.z, r), gm.z);
-      v.w = __fmul_rn(__fmul_rn(v.w, r), gm.w);
-      reinterpret_cast<float4*>(xsm + (long)t * d)[pos] = v;
+    const int n4 = T * (d / 4);
+    for (int c0 = threadIdx.x; c0 < n4; c0 += 8 * blockDim.x) {
+      float4 gm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = c0 + k * blockDim.x;
+        if (c < n4) {
+          const int pos = c % (d / 4);
+          gm[k] = __ldg(reinterpret_cast<const float4*>(st.gamma + (pos & 31) * Gd + 4 * (pos >> 5)));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = c0 + k * blockDim.x;
+        if (c < n4) {
+          const float r = rinv[c / (d / 4)];
+          float4 v = reinterpret_cast<float4*>(xsm)[c];
+          v.x = __fmul_rn(__fmul_rn(v.x, r), gm[k].x);
+          v.y = __fmul_rn(__fmul_rn(v.y, r), gm[k].y);
+          v.z = __fmul_rn(__fmul_rn(v.z, r), gm[k].z);
+          v.w = __fmul_rn(__fmul_rn(v.w, r), gm[k].w);
+          reinterpret_cast<float4*>(xsm)[c] = v;
+        }
+      }
     }
     __syncthreads();
   }
@@ -382,46 +179,15 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
       w.scores[(long)t * E + e0 + r] = canon_sigmoid(p);
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(w.counter, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // the last CTA: every score (and the bias) into shared memory in one round, selection and
-  // union there, then the results out to the workspace
-  float* ssc = xsm;  // [T][E] (the token buffer is no longer needed)
-  for (int i = threadIdx.x; i < T * E; i += blockDim.x) ssc[i] = __ldcg(w.scores + i);
-  if (st.bias)
-    for (int i = threadIdx.x; i < E; i += blockDim.x) sbias[i] = st.bias[i];
-  __syncthreads();
-  const float* bs = st.bias ? sbias : nullptr;
-  for (int t = warp; t < T; t += nwarp) {
-    if (E <= 256)
-      topk_warp<8>(ssc + t * E, bs, E, s.K, s.routed_scale, sids + t * s.K, swt + t * s.K, lane);
-    else
-      topk_warp<32>(ssc + t * E, bs, E, s.K, s.routed_scale, sids + t * s.K, swt + t * s.K, lane);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < T * s.K; i += blockDim.x) {
-    w.ids[i] = sids[i];
-    w.w[i] = swt[i];
-  }
-  if (T * s.K <= 32) {
-    if (warp == 0) union_warp(s, w, sids, lane);
-  } else {
-    union_bucket(s, w, sids, cnt, cursor);
-  }
-  if (threadIdx.x == 0) *w.counter = 0;  // ready for the next call
 }
 
-static size_t route_smem_bytes(int d, int E, int T) {
-  return ((size_t)kRouterEpc * d + (size_t)T * (d > E ? d : E) + E) * sizeof(float);
+static size_t route_smem_bytes(int d, int T) {
+  return ((size_t)kRouterEpc * d + (size_t)T * d) * sizeof(float);
 }
 
 cudaError_t configure_route_kernels() {
   return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)route_smem_bytes(8192, kMaxE, kDecodeTmax));
+                              (int)route_smem_bytes(8192, kDecodeTmax));
 }
 
 // ------------------------------------------------------------------ batched routing ------
@@ -562,7 +328,12 @@ __global__ void __launch_bounds__(512) router_batch_kernel(const __grid_constant
 __global__ void __launch_bounds__(256) topk_batch_kernel(const Shape s, const Store st, const Work w) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= s.T) return;
-  topk_token(s, st, w.scores + (long)t * s.E, w.ids + t * s.K, w.w + t * s.K, lane);
+  if (s.E <= 256)
+    topk_warp<8>(w.scores + (long)t * s.E, st.bias, s.E, s.K, s.routed_scale, w.ids + t * s.K,
+                 w.w + t * s.K, lane);
+  else
+    topk_warp<32>(w.scores + (long)t * s.E, st.bias, s.E, s.K, s.routed_scale, w.ids + t * s.K,
+                  w.w + t * s.K, lane);
 }
 
 // The batch union with all 32 warps: counts per expert and the union slots (as union_bucket
@@ -722,7 +493,7 @@ cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const 
                          cudaStream_t stream) {
   // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work
   const int grid = (s.E + kRouterEpc - 1) / kRouterEpc;
-  route_kernel<<<grid, 256, route_smem_bytes(s.d, s.E, s.T), stream>>>(x, s, st, w);
+  route_kernel<<<grid, 256, route_smem_bytes(s.d, s.T), stream>>>(x, s, st, w);
   return cudaGetLastError();
 }
 

@@ -302,7 +302,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.qh, (Pm + kPrefillTileN) * f)
   ALLOC(h->w.dh, sizeof(float) * (Pm + kPrefillTileN) * (f / 32))
   ALLOC(h->w.sh, sizeof(int32_t) * Pm * (f / 32))
-  ALLOC(h->w.counter, sizeof(int32_t) * 4)
+  ALLOC(h->w.sel_flag, sizeof(int32_t) * 4)
   ALLOC(h->w.status, sizeof(int32_t) * 4)
   ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
   if (rc == COLI_OK && Tm > kDecodeTmax && d % 256 == 0 &&
@@ -324,7 +324,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     }
   }
 #undef ALLOC
-  if (rc == COLI_OK && (cudaMemset(h->w.counter, 0, 16) != cudaSuccess ||
+  if (rc == COLI_OK && (cudaMemset(h->w.sel_flag, 0, 16) != cudaSuccess ||
                         cudaMemset(h->w.status, 0, 16) != cudaSuccess ||
                         cudaDeviceSynchronize() != cudaSuccess))
     rc = COLI_ECUDA;
@@ -504,8 +504,8 @@ int coli_moe_status(coli_moe* h, void* stream) {
       cudaStreamSynchronize(st) != cudaSuccess)
     return COLI_ECUDA;
   if (v != COLI_OK) {
-    // an aborted call may leave the router's ticket counter mid-count: clear it with the status
-    if (cudaMemset(h->w.status, 0, 16) != cudaSuccess || cudaMemset(h->w.counter, 0, 16) != cudaSuccess ||
+    // clear the status and the selection flag together
+    if (cudaMemset(h->w.status, 0, 16) != cudaSuccess || cudaMemset(h->w.sel_flag, 0, 16) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return COLI_ECUDA;
     return v;

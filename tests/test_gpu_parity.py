@@ -194,6 +194,46 @@ def test_forced_all_experts_and_no_shared():
     assert base.K == 4
 
 
+def test_wide_selection_odd_expert_count():
+    """E > 256 (the round-based top-K) with E not a multiple of 4 (scores loaded without the
+    bulk copy), K = 6, T = 4 tokens, a zipf selection bias: every stage bit-exact"""
+    wl = W.Workload("tiny_wide", d=256, f=128, E=301, K=6, n_shared=1, T=4, bias="zipf")
+    L = synthetic.build_layer(wl, max_tokens=4)
+    OL = O.Layer(wl)
+    for T, token0 in ((1, 2), (4, 40)):
+        _compare_layer(L, OL, W.x_host(wl, T, token0), want_A=False)
+    L.close()
+
+
+def test_selection_ties_go_to_the_lower_id():
+    """Router rows copied so that two experts score exactly alike: once at the boundary of the
+    top-K (an unselected lower id takes the last place) and once at the top (the two keep id
+    order); both sides must make the same choices, and the ties must really occur"""
+    wl = W.WORKLOADS["tiny_t1"]
+    L = synthetic.build_layer(wl, max_tokens=4)
+    OL = O.Layer(wl)
+    x = W.x_host(wl, 2, 11)
+    _, ids, _ = O.route_only(wl, x, OL.Wr, OL.bias, OL.gamma)
+    last = int(ids[0][wl.K - 1])
+    lower = [e for e in range(last) if e not in ids[0]]
+    assert lower, "token 0 needs an unselected expert below its last pick"
+    u = lower[0]
+    top = int(ids[1][0])
+    v = max(e for e in range(wl.E) if e not in ids[1] and e != u and e not in ids[0])
+    Wr = OL.Wr.copy()
+    Wr[u] = Wr[last]
+    Wr[v] = Wr[top]
+    OL.Wr = Wr
+    L.load_router(torch.from_numpy(Wr).cuda(), OL.bias, OL.gamma)
+    torch.cuda.synchronize()
+    _, ids2, _ = O.route_only(wl, x, OL.Wr, OL.bias, OL.gamma)
+    assert u in ids2[0] and last not in ids2[0]
+    r_top, r_v = list(ids2[1]).index(top), list(ids2[1]).index(v)
+    assert abs(r_top - r_v) == 1 and (r_top < r_v) == (top < v)
+    _compare_layer(L, OL, x, want_A=False)
+    L.close()
+
+
 def test_norm_layer_in_place():
     wl = W.Workload("tiny_norm", d=512, f=256, E=32, K=4, n_shared=1, T=3, has_norm=True)
     L = synthetic.build_layer(wl, max_tokens=4)
