@@ -89,31 +89,124 @@ __device__ __forceinline__ void topk_warp(const float* sc, const float* bias, in
     key[m] = e < E ? score_key(bias ? __fadd_rn(sc[e], bias[e]) : sc[e]) : 0u;
   }
   int my = 0;
+  float mine = 0.0f, S = 0.0f;
   for (int k = 0; k < K; ++k) {
-    uint32_t bk = 0u;
-    int bm = 0;
+    // this lane's best key by a tree (pairs, then pairs of pairs, ...): a tie keeps the lower m
+    uint32_t bk[NM];
+    int bm[NM];
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
-      const bool gt = key[m] > bk;
-      bm = gt ? m : bm;
-      bk = gt ? key[m] : bk;
+      bk[m] = key[m];
+      bm[m] = m;
     }
-    const uint32_t top = __reduce_max_sync(FULL, bk);
-    uint32_t win = __reduce_min_sync(FULL, bk == top ? (uint32_t)(bm * 32 + lane) : 0xFFFFFFFFu);
+#pragma unroll
+    for (int w = 1; w < NM; w <<= 1) {
+#pragma unroll
+      for (int m = 0; m + w < NM; m += 2 * w) {
+        const bool gt = bk[m + w] > bk[m];
+        bk[m] = gt ? bk[m + w] : bk[m];
+        bm[m] = gt ? bm[m + w] : bm[m];
+      }
+    }
+    const uint32_t top = __reduce_max_sync(FULL, bk[0]);
+    uint32_t win = __reduce_min_sync(FULL, bk[0] == top ? (uint32_t)(bm[0] * 32 + lane) : 0xFFFFFFFFu);
     win = win < (uint32_t)E ? win : 0u;  // only scores that are not numbers could leave none
     const int wm = (int)(win & 31u) == lane ? (int)(win >> 5) : -1;
 #pragma unroll
     for (int m = 0; m < NM; ++m) key[m] = m == wm ? 0u : key[m];
-    if (lane == k) my = (int)win;
+    // the selected scores summed in rank order as they are found
+    const float v = sc[win];
+    S = k == 0 ? v : __fadd_rn(S, v);
+    my = lane == k ? (int)win : my;
+    mine = lane == k ? v : mine;
   }
-  const float sk = lane < K ? sc[my] : 0.0f;
-  float S = __shfl_sync(FULL, sk, 0);
-  for (int k = 1; k < K; ++k) S = __fadd_rn(S, __shfl_sync(FULL, sk, k));
   if (lane < K) {
     ids[lane] = my;
-    wt[lane] = __fmul_rn(__fdiv_rn(sk, S), routed_scale);
+    wt[lane] = __fmul_rn(__fdiv_rn(mine, S), routed_scale);
   }
   __syncwarp();
+}
+
+// The common decode case (E <= 256, K <= 8, one token) in one warp with no CTA barrier inside
+// and no divergent branch: each of the K rounds takes every lane's best key by a depth-3 tree
+// (ties keep the lower expert), the warp maximum and the lowest expert among the lanes holding
+// it (two warp reductions), and clears the winner's key; the rank-order sum of the selected
+// scores builds up during the rounds.  With one token the union is the K distinct experts in
+// ascending order, one pair each, then the shared expert: every lane knows all K winners, so
+// lane j places pair j directly.
+__device__ __forceinline__ void select_t1_fast(const Shape& s, Sel& m, const float* bias,
+                                               int lane) {
+  const int E = s.E, K = s.K;
+  const float* sc = m.sc;
+  uint32_t key[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = j * 32 + lane;
+    key[j] = e < E ? score_key(bias ? __fadd_rn(sc[e], bias[e]) : sc[e]) : 0u;
+  }
+  int wid[8];
+  float S = 0.0f, mine = 0.0f;
+  int my = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    wid[k] = 0x7fffffff;
+    if (k < K) {
+      uint32_t k4[4];
+      int m4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool gt = key[2 * i + 1] > key[2 * i];
+        k4[i] = gt ? key[2 * i + 1] : key[2 * i];
+        m4[i] = gt ? 2 * i + 1 : 2 * i;
+      }
+      uint32_t k2[2];
+      int m2[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const bool gt = k4[2 * i + 1] > k4[2 * i];
+        k2[i] = gt ? k4[2 * i + 1] : k4[2 * i];
+        m2[i] = gt ? m4[2 * i + 1] : m4[2 * i];
+      }
+      const bool gt = k2[1] > k2[0];
+      const uint32_t bk = gt ? k2[1] : k2[0];
+      const int bm = gt ? m2[1] : m2[0];
+      const uint32_t top = __reduce_max_sync(FULL, bk);
+      uint32_t win = __reduce_min_sync(FULL, bk == top ? (uint32_t)(bm * 32 + lane) : 0xFFFFFFFFu);
+      win = win < (uint32_t)E ? win : 0u;  // only scores that are not numbers could leave none
+      const int wm = (int)(win & 31u) == lane ? (int)(win >> 5) : -1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) key[j] = j == wm ? 0u : key[j];
+      const float v = sc[win];
+      S = k == 0 ? v : __fadd_rn(S, v);
+      wid[k] = (int)win;
+      my = lane == k ? (int)win : my;
+      mine = lane == k ? v : mine;
+    }
+  }
+  int slot = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) slot += wid[k] < my ? 1 : 0;
+  if (lane < K) {
+    m.ids[lane] = my;
+    m.wt[lane] = __fmul_rn(__fdiv_rn(mine, S), s.routed_scale);
+    m.u_ids[slot] = my;
+    m.u_off[slot] = slot;
+    m.p_tok[slot] = 0;
+    m.p_rank[slot] = lane;
+    m.inv[lane] = slot;
+  }
+  if (lane == 0) {
+    int nu = K;
+    if (s.n_shared) {
+      m.u_ids[nu] = E;
+      m.u_off[nu] = K;
+      m.p_tok[K] = 0;
+      m.p_rank[K] = -1;
+      ++nu;
+    }
+    m.u_off[nu] = K + (s.n_shared ? 1 : 0);
+    *m.nu = nu;
+  }
 }
 
 // Batch union of at most 32 (token, rank) pairs by one warp: sorting the keys id*32 + pair
@@ -172,6 +265,11 @@ __device__ inline void select_union(const Shape& s, Sel& m, bool has_bias) {
   const int T = s.T, K = s.K, E = s.E, TK = T * K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* bias = has_bias ? m.bias : nullptr;
+  if (T == 1 && E <= 256 && K <= 8) {
+    if (warp == 0) select_t1_fast(s, m, bias, lane);
+    __syncthreads();
+    return;
+  }
   if (warp < T) {
     if (E <= 256)
       topk_warp<8>(m.sc + warp * E, bias, E, K, s.routed_scale, m.ids + warp * K, m.wt + warp * K, lane);
