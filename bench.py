@@ -97,11 +97,18 @@ def recorded_traffic(kernel, workload):
         return None
     if not rec:
         return None
+    return rec["bytes_per_launch"] if source_digest(rec["sources"]) == rec["sources_sha256_16"] else None
+
+
+def source_digest(names):
+    """digest of the kernel's source files (csrc/), so a recorded traffic figure is used only
+    while the code it was measured on is unchanged"""
     import hashlib
-    src = os.path.join(ROOT, "int4_routed_expert_quantize_gb300", "csrc", rec["source"])
-    with open(src, "rb") as fh:
-        digest = hashlib.sha256(fh.read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if digest == rec["source_sha256_16"] else None
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "int4_routed_expert_quantize_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ distributed ------------
