@@ -60,7 +60,7 @@ DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   const int chunk = p.max_rows < kDownChunk ? p.max_rows : kDownChunk;
   p.stage_bytes = chunk * (f / 2);
   p.hq_bytes = align16(P * f);
-  p.aux_bytes = align16(P * nbf * 8);
+  p.aux_bytes = 2 * align16(P * nbf * 4);
   p.es_bytes = align16(chunk * P * 4);
   p.max_slots = (int)max_union_slots(T, K, E, n_shared);
   p.tab_bytes = align16(p.max_slots * p.max_rows * 4);
@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
   __shared__ __align__(8) uint64_t selbar;
+  __shared__ __align__(8) uint64_t inbar;  // the h codes, scales and code sums are in
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
   const int nbf = f >> 5, A = nbf / GF, rb = f >> 1;
   const DownPlan& pl = a.pl;
@@ -443,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
   uint64_t* empty = full + kMaxStages;
-  uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][2 halves][chunks][16]
-  float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf]
-  int* hn = reinterpret_cast<int*>(hd + Pm * nbf);                 // [P][nbf]  -8*sum(codes)
+  uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][f] h codes
+  float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf] block scales
+  int* hsum = reinterpret_cast<int*>(hq + pl.hq_bytes + pl.aux_bytes / 2);  // [P][nbf] code sums
   float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [chunk row][Pm]
   float* t_sd = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
   Sel sel = sel_carve(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes + pl.tab_bytes, T, a.s.E);
@@ -469,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       mbar_init(&empty[i], kNW);
     }
     mbar_init(&selbar, 1);
+    mbar_init(&inbar, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -521,60 +523,26 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   // which streams weights that do not depend on it.
   const int nthr = kNW * 32;
   auto stage_inputs = [&]() {
-    // gate/up grid complete: h codes visible from here on
+    // gate/up grid complete: h codes visible from here on.  Every pair's codes, block scales
+    // and code sums arrive as they lie in the workspace: three bulk copies, one round of memory
+    // latency (plain loads when a size is not a multiple of 16 bytes).
     griddep_wait();
-    // this CTA's down-row scales: their loads go out with the h codes' below (one round of memory
-    // latency for both), their stores after
-    float sdv[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * nthr;
-      if (i < nu * nrow) {
-        const int slot = i / nrow, r = i - slot * nrow;
-        sdv[k] = a.st.sc[(long)t_ex[slot] * (2 * f + d) + 2 * f + row0 + r];
+    const uint32_t qbytes = (uint32_t)(P * f), sbytes = (uint32_t)(P * nbf * 4);
+    if ((sbytes & 15u) == 0) {
+      if (threadIdx.x == 0) {
+        mbar_expect_tx(&inbar, qbytes + 2 * sbytes);
+        bulk_g2s(hq, a.w.qh, qbytes, &inbar, pol);
+        bulk_g2s(hd, a.w.dh, sbytes, &inbar, pol);
+        bulk_g2s(hsum, a.w.sh, sbytes, &inbar, pol);
       }
-    }
-
-    // every pair's h codes (block b = g*GF + i at chunk i*A + g, two 16-byte planes), scales and
-    // code sums; each thread issues the loads of 4 blocks before storing any
-    for (int i0 = threadIdx.x; i0 < P * nbf; i0 += 4 * nthr) {
-      uint4 q0[4], q1[4];
-      float dv[4];
-      int sv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int idx = i0 + k * nthr;
-        if (idx < P * nbf) {
-          const int p = idx / nbf, b = idx - p * nbf;
-          const uint4* src = reinterpret_cast<const uint4*>(a.w.qh + (long)p * f + b * 32);
-          q0[k] = __ldcg(src);
-          q1[k] = __ldcg(src + 1);
-          dv[k] = __ldcg(a.w.dh + (long)p * nbf + b);
-          sv[k] = __ldcg(a.w.sh + (long)p * nbf + b);
-        }
+      mbar_wait_bounded(&inbar, 0u, &abort_flag, a.w.status);
+    } else {
+      for (int i = threadIdx.x; i < P * f / 16; i += nthr)
+        reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(a.w.qh) + i);
+      for (int i = threadIdx.x; i < P * nbf; i += nthr) {
+        hd[i] = __ldcg(a.w.dh + i);
+        hsum[i] = __ldcg(a.w.sh + i);
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int idx = i0 + k * nthr;
-        if (idx < P * nbf) {
-          const int p = idx / nbf, b = idx - p * nbf;
-          const int g = b / GF, i = b - g * GF;
-          uint8_t* base = hq + (long)p * f + (i * A + g) * 16;
-          *reinterpret_cast<uint4*>(base) = q0[k];
-          *reinterpret_cast<uint4*>(base + nbf * 16) = q1[k];
-          hd[idx] = dv[k];
-          hn[idx] = -8 * sv[k];
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * nthr;
-      if (i < nu * nrow) t_sd[(i / nrow) * pl.max_rows + i % nrow] = sdv[k];
-    }
-    for (int i = threadIdx.x + 4 * nthr; i < nu * nrow; i += nthr) {
-      const int slot = i / nrow, r = i - slot * nrow;
-      t_sd[slot * pl.max_rows + r] = a.st.sc[(long)t_ex[slot] * (2 * f + d) + 2 * f + row0 + r];
     }
     named_bar_sync(1, nthr);
   };
@@ -600,6 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       if (abort_flag) drain_fills(full, pl.nst, issued);
     }
   } else {
+    // this CTA's down-row scales for every union slot (they do not depend on the gate/up grid)
+    for (int i = threadIdx.x; i < nu * nrow; i += nthr) {
+      const int sl = i / nrow, r = i - sl * nrow;
+      t_sd[sl * pl.max_rows + r] = a.st.sc[(long)t_ex[sl] * (2 * f + d) + 2 * f + row0 + r];
+    }
     int s = 0, ci = 0, slot = 0, c0 = 0, cn = 0;
     uint32_t ph = 0;
     chunk(0, c0, cn);
@@ -626,13 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
 #pragma unroll
         for (int i = 0; i < GF; ++i) {
           if (lane < A) {
-            const uint8_t* base = hq + (long)p * f + (i * A + lane) * 16;
+            const uint8_t* base = hq + (long)p * f + (lane * GF + i) * 32;
             const uint4 v0 = *reinterpret_cast<const uint4*>(base);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(base + nbf * 16);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(base + 16);
             hr[i][0] = v0.x; hr[i][1] = v0.y; hr[i][2] = v0.z; hr[i][3] = v0.w;
             hr[i][4] = v1.x; hr[i][5] = v1.y; hr[i][6] = v1.z; hr[i][7] = v1.w;
             hdr[i] = hd[p * nbf + lane * GF + i];
-            hnr[i] = hn[p * nbf + lane * GF + i];
+            hnr[i] = -8 * hsum[p * nbf + lane * GF + i];
           } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) hr[i][k] = 0u;
