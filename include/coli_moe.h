@@ -128,8 +128,10 @@ int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
 
 /* coli_moe_forward that also records `events[0..3]` (cudaEvent_t handles created by the
  * caller) on `stream`: before the routing kernel, after it, after the gate/up kernel and after
- * the down kernel -- so the caller can time each launch.  The events serialise the launches
- * (no programmatic overlap between them).  T <= 4.  EINVAL: n_events < 4 or T out of range. */
+ * the down kernel -- so the caller can time each launch.  When the forward runs the expert half
+ * as one fused kernel (coli_moe_launches returns 2) events 1..2 bracket that kernel and events
+ * 2..3 nothing.  The events serialise the launches (no programmatic overlap between them).
+ * T <= 4.  EINVAL: n_events < 4 or T out of range. */
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream);
 
@@ -145,6 +147,12 @@ int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, 
 /* Device status word of the handle: COLI_OK, or COLI_ETIMEOUT if a bounded device-side wait
  * of an earlier forward gave up (the word is then cleared).  Synchronises `stream`. */
 int coli_moe_status(coli_moe* h, void* stream);
+
+/* Number of kernel launches one coli_moe_forward of T tokens makes on this handle: 2 for one
+ * token when the expert half runs as one fused kernel (router, then gate/up + down), 3 per
+ * chunk of at most 4 tokens on the decode path, 8 on the batched tensor-core path.  Negative
+ * status on error (EINVAL: T < 1 or T > max_tokens). */
+int coli_moe_launches(const coli_moe* h, int T);
 
 /* Bytes of one expert record in the canonical format (3*d*f/2 + 4*(2f+d)). */
 int64_t coli_moe_expert_record_bytes(int d, int f);

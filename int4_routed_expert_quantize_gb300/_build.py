@@ -9,8 +9,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "libcoli_moe.so")
-SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "expert_prefill.cu", "runtime.cu",
-           "noalloc.cu"]
+SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "expert_fused.cu", "expert_prefill.cu",
+           "runtime.cu", "noalloc.cu"]
 
 
 def nvcc_flags(arch="sm_103a"):

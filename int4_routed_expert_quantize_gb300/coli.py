@@ -68,6 +68,7 @@ def lib():
         L.coli_moe_status.argtypes = [_vp, _vp]
         L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
         L.coli_moe_expert_record_bytes.restype = _i64
+        L.coli_moe_launches.argtypes = [_vp, _i]
         L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
         L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
         L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
@@ -188,6 +189,13 @@ class MoeLayer:
 
     def status(self, stream=None):
         return int(lib().coli_moe_status(self.h, _stream(stream)))
+
+    def launches(self, T):
+        """kernel launches one forward of T tokens makes"""
+        n = int(lib().coli_moe_launches(self.h, T))
+        if n < 0:
+            raise ColiError(n, "coli_moe_launches")
+        return n
 
 
 def stack_forward(layers, x, stream=None):

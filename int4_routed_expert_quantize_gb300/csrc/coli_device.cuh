@@ -218,4 +218,43 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ------------------------------------------------------------------ shared by the expert kernels
+// Sum over the warp of 8 values per lane, one per row: the exchange at distance o keeps half
+// of the rows on each side, so after distances 1, 2, 4 lane l holds one row's partial, and
+// distances 8, 16 finish it.  Every row's total is the pairwise tree over lanes in lane order,
+// bit-identical to warp_tree_sum.  Returns the total of row 4*(l&1) + 2*((l>>1)&1) + ((l>>2)&1)
+// (the same in lanes l, l+8, l+16, l+24).
+__device__ __forceinline__ float warp_tree_sum8(const float (&v)[8], int lane) {
+  const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+  float u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b0 ? v[i + 4] : v[i], send = b0 ? v[i] : v[i + 4];
+    u[i] = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 1));
+  }
+  float z[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b1 ? u[i + 2] : u[i], send = b1 ? u[i] : u[i + 2];
+    z[i] = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 2));
+  }
+  const float keep = b2 ? z[1] : z[0], send = b2 ? z[0] : z[1];
+  float r = __fadd_rn(keep, __shfl_xor_sync(FULL, send, 4));
+  r = __fadd_rn(r, __shfl_xor_sync(FULL, r, 8));
+  r = __fadd_rn(r, __shfl_xor_sync(FULL, r, 16));
+  return r;
+}
+
+// After an abort, wait (bounded, ignoring the abort flag) for the last fills the producer
+// issued, so no bulk copy is still writing shared memory when the CTA exits.
+static __device__ __noinline__ void drain_fills(uint64_t* full, int nst, long issued) {
+  const long first = issued > nst ? issued - nst : 0;
+  for (long it = first; it < issued; ++it) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(&full[it % nst], (uint32_t)((it / nst) & 1))) {
+      if (global_ns() - t0 > kWaitLimitNs / 8) break;
+    }
+  }
+}
+
 }  // namespace coli

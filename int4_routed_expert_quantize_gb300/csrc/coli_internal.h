@@ -64,8 +64,9 @@ struct Work {
   int8_t* qh = nullptr;      // [Pm,f]
   float* dh = nullptr;       // [Pm,f/32]
   int32_t* sh = nullptr;     // [Pm,f/32]
-  int32_t* sel_flag = nullptr;  // 1 once the gate/up grid of the current call published its
-                                // expert selection (the router grid clears it)
+  int32_t* sel_flag = nullptr;  // [0] 1 once the gate/up grid of the current call published its
+                                // expert selection; [1] the fused kernel's barrier counter
+                                // (the router grid clears both)
   int32_t* status = nullptr;   // COLI_OK or COLI_ETIMEOUT
 };
 
@@ -140,6 +141,19 @@ struct DownPlan {
   int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, tab_bytes, sel_bytes, max_rows, max_slots,
       total;
 };
+// shared-memory plan of the fused one-token expert kernel (gate/up ring, a region used first by
+// the gate/up phase and then by the down phase, the selection)
+struct FusedPlan {
+  int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, tab_bytes, max_units;
+  int hq_bytes, haux_bytes, es_bytes, tsd_bytes, max_rows, chunk, max_slots;
+  int region, sel_bytes, total;
+};
+FusedPlan fused_plan(int d, int f, int K, int E, int n_shared, int grid);
+bool fused_supported(int d, int f, int K, int E, int n_shared, int num_sms);
+cudaError_t configure_fused_kernels();
+cudaError_t launch_expert_fused(const float* x, float* y, const Shape& s, const Store& st,
+                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
+                                cudaStream_t stream);
 GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 int down_grid(int d, int num_sms);  // CTAs of the down kernel

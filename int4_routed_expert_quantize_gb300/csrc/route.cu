@@ -48,7 +48,10 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
   float* wrs = route_sm;                   // [kRouterEpc][d] router rows as stored
   float* xsm = route_sm + kRouterEpc * d;  // [T][d] tokens
   if (threadIdx.x == 0) {
-    if (blockIdx.x == 0) *w.sel_flag = 0;  // this call's selection is not published yet
+    if (blockIdx.x == 0) {  // this call's selection is not published yet; no CTA at the barrier
+      w.sel_flag[0] = 0;
+      w.sel_flag[1] = 0;
+    }
     mbar_init(&wbar, 1);
     abort_flag = 0;
     fence_barrier_init();

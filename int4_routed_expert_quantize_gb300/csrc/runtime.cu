@@ -24,6 +24,7 @@ struct coli_moe {
   Work w;
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
   bool prefill = false;     // batches above kDecodeTmax use the tensor-core path
+  bool fused = false;       // one-token forwards use the fused expert kernel
   PrefillWork pw;
   PrefillMaps maps;
   bool router_loaded = false;
@@ -108,15 +109,22 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
     if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
     if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
   }
-  // route (ordinary launch) -> gate/up -> down; the expert kernels are programmatic dependents
-  // that prefetch weights before waiting, unless events are recorded between the launches
+  // route (ordinary launch) -> gate/up -> down, or for one token route -> the fused expert
+  // kernel; the expert kernels are programmatic dependents that prefetch weights before
+  // waiting, unless events are recorded between the launches (with the fused kernel the
+  // events bracket route | fused | nothing)
   const bool pdl = (ev == nullptr);
   cudaError_t e = ev ? cudaEventRecord(ev[0], stream) : cudaSuccess;
   if (e == cudaSuccess) e = launch_route(x, s, h->st, h->w, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], stream);
-  if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, pdl, stream);
-  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
-  if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
+  if (T == 1 && h->fused) {
+    if (e == cudaSuccess) e = launch_expert_fused(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
+  } else {
+    if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, pdl, stream);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
+    if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
+  }
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], stream);
   if (e != cudaSuccess) return COLI_ECUDA;
   return dump ? copy_dump(h, T, dump, stream) : COLI_OK;
@@ -225,6 +233,13 @@ const char* coli_moe_strerror(int status) {
   }
 }
 
+int coli_moe_launches(const coli_moe* h, int T) {
+  if (!h || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
+  if (T == 1 && h->fused) return 2;
+  if (T > kDecodeTmax && h->prefill) return 8;
+  return 3 * ((T + kDecodeTmax - 1) / kDecodeTmax);
+}
+
 int64_t coli_moe_expert_record_bytes(int d, int f) {
   return rec_bytes(d, f) + 4LL * (2LL * f + d);
 }
@@ -260,6 +275,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   std::call_once(g_cfg_once, [] {
     g_cfg_err = configure_expert_kernels();
     if (g_cfg_err == cudaSuccess) g_cfg_err = configure_route_kernels();
+    if (g_cfg_err == cudaSuccess) g_cfg_err = configure_fused_kernels();
   });
   if (g_cfg_err != cudaSuccess) return COLI_ECUDA;
 
@@ -273,6 +289,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   }
   h->slots = c.n_experts + c.n_shared;
   h->loaded.assign(h->slots, 0);
+  h->fused = fused_supported(c.d, c.f, c.top_k, c.n_experts, c.n_shared, h->num_sms);
   const long S = h->slots, d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
   const long Pm = Tm * K + (c.n_shared ? Tm : 0);
   int rc = COLI_OK;
