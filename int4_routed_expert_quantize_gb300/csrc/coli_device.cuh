@@ -202,6 +202,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// asynchronous copies global -> shared through the load path (not the bulk-copy engine, whose
+// queue may hold weight stages): 4 bytes through L1, or 16 bytes from L2 (data other SMs wrote
+// during this kernel); the thread's copies are complete after cp_async_wait_all()
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_l2(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 // programmatic dependent launch: wait for the preceding grid (no-op without the attribute) /
 // allow the next grid in the stream to start its prologue
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

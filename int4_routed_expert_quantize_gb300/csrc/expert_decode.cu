@@ -402,7 +402,6 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
   const int nbf = f >> 5, A = nbf / GF, rb = f >> 1;
   const DownPlan& pl = a.pl;
-  const int Pm = T * K + (a.s.n_shared ? T : 0);  // pairs at most (the layout's stride)
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
   uint64_t* empty = full + kMaxStages;

@@ -11,8 +11,8 @@
 //  * the down phase reuses the CTA's selection (no second selection, no second launch);
 //  * the down phase's buffers overlay the gate/up phase's token and table buffers.
 // The barrier is a counter in the workspace (cleared by the router grid each call) that every
-// CTA increments and then polls with a bounded wait; the kernel is launched cooperatively, so
-// all of its CTAs are resident together.
+// CTA increments and then polls with a bounded wait; grid <= SM count with one CTA per SM, so
+// all of its CTAs are resident together once the router grid ahead of it has retired.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,10 +48,10 @@ FusedPlan fused_plan(int d, int f, int K, int E, int n_shared, int grid) {
   p.haux_bytes = 2 * align16f(P * nbf * 4);
   p.es_bytes = align16f(p.chunk * P * 4);
   p.tsd_bytes = align16f(p.max_slots * p.max_rows * 4);
-  const int dn_region = p.hq_bytes + p.haux_bytes + p.es_bytes + p.tsd_bytes;
+  const int dn_region = p.hq_bytes + p.haux_bytes + p.es_bytes;
   p.region = gu_region > dn_region ? gu_region : dn_region;
   p.sel_bytes = align16f(sel_bytes(T, E));
-  const int fixed = 2 * kMaxStages * 8 + p.region + p.sel_bytes;
+  const int fixed = 2 * kMaxStages * 8 + p.region + p.tsd_bytes + p.sel_bytes;
   int nst = (kSmemLimit - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   // a down stage (one chunk of rows) must fit a ring slot
@@ -70,7 +70,7 @@ struct FusedArgs {
   float* y;
 };
 
-template <int G, int GF, bool DBG>
+template <int G, int GF, int RPW, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
@@ -90,13 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
   float* hs = reinterpret_cast<float*>(xs + pl.xs_bytes + pl.aux_bytes);  // [2][32]
   int* tab = reinterpret_cast<int*>(xs + pl.xs_bytes + pl.aux_bytes + pl.hs_bytes);
   // down phase, over the same bytes: h codes [P][f], block scales and code sums [P][nbf], the
-  // expert outputs of a chunk [chunk row][P], the down-row scales [slot][max_rows]
+  // expert outputs of a chunk [chunk row][P]; after them the down-row scales [slot][max_rows]
   uint8_t* hq = region;
   float* hd = reinterpret_cast<float*>(region + pl.hq_bytes);
   int* hsum = reinterpret_cast<int*>(region + pl.hq_bytes + pl.haux_bytes / 2);
   float* es = reinterpret_cast<float*>(region + pl.hq_bytes + pl.haux_bytes);
-  float* t_sd = reinterpret_cast<float*>(region + pl.hq_bytes + pl.haux_bytes + pl.es_bytes);
-  Sel sel = sel_carve(region + pl.region, 1, a.s.E);
+  float* t_sd = reinterpret_cast<float*>(region + pl.region);
+  Sel sel = sel_carve(region + pl.region + pl.tsd_bytes, 1, a.s.E);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int SPU = 32 / kGuRps;
   const int G_ = gridDim.x, c = blockIdx.x;
@@ -271,6 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
       tsc[lane] = scx[hb * 32 + lane];
       tsc[32 + lane] = scx[f + hb * 32 + lane];
     }
+    // this CTA's down-row scales of every union expert: asynchronous copies that land while the
+    // gate/up stages run (each thread waits for its own before the grid barrier)
+    for (int i = threadIdx.x; i < nu * nrow; i += kNW * 32) {
+      const int sl = i / nrow, r = i - sl * nrow;
+      cp_async4(t_sd + sl * pl.max_rows + r, a.st.sc + (long)sel.u_ids[sl] * (2 * f + d) + 2 * f + row0 + r);
+    }
     named_bar_sync(1, kNW * 32);
 
     // ---------------- consumers, gate/up phase: warp `warp` takes row pair `warp` of every
@@ -363,67 +369,72 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
     }
 
     // ---------------- grid barrier: every CTA's h blocks are written.  Each thread fences its
-    // own stores, the consumers meet, one thread counts the CTA in and polls (bounded) until all
-    // CTAs are counted; the router grid cleared the counter for this call.
+    // own stores, the consumers meet, one thread counts the CTA in; it polls (bounded) until all
+    // CTAs are counted at the first real down stage below.  The router grid cleared the counter
+    // for this call.
+    cp_async_wait_all();
     __threadfence();
     named_bar_sync(1, kNW * 32);
-    if (threadIdx.x == 0 && !abort_flag) {
-      int* counter = a.w.sel_flag + 1;
-      atomicAdd(counter, 1);
-      const uint64_t t0 = global_ns();
-      for (uint32_t k = 1;; ++k) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
-        if (v >= (int)gridDim.x) break;
-        if ((k & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
-          abort_flag = 1;
-          atomicExch(a.w.status, COLI_ETIMEOUT);
-          break;
-        }
-      }
-      // the h codes are read below by bulk copies (the async proxy)
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
-    named_bar_sync(1, kNW * 32);
+    int* counter = a.w.sel_flag + 1;
+    if (threadIdx.x == 0 && !abort_flag) atomicAdd(counter, 1);
 
-    // ---------------- down phase.  The gate/up buffers are free: this CTA's down-row scales,
-    // then every pair's h codes, block scales and code sums as they lie in the workspace (three
-    // bulk copies, or plain loads when a size is not a multiple of 16 bytes)
+    // ---------------- down phase.  Warp w owns rows w, w+8, ... of each chunk: each lane folds
+    // its group's block dots for up to RPW rows (rows past the warp's last one repeat it and are
+    // dropped, so every load is unconditional), one transposed butterfly adds the group partials
+    // of all rows; once a chunk has seen every union expert the warp combines its rows in the
+    // fixed order (shared expert first, then ranks 0..K-1).
+    // Iteration nst_gu - 1 is a dry run of the stage code on whatever the ring slot and the
+    // buffers hold (no wait, no result, no arrival): it brings the loop's instructions into the
+    // SM's caches while the CTA waits for the others at the barrier.
     const int nthr = kNW * 32;
-    for (int i = threadIdx.x; i < nu * nrow; i += nthr) {
-      const int sl = i / nrow, r = i - sl * nrow;
-      t_sd[sl * pl.max_rows + r] = a.st.sc[(long)sel.u_ids[sl] * (2 * f + d) + 2 * f + row0 + r];
-    }
-    const uint32_t qbytes = (uint32_t)(P * f), sbytes = (uint32_t)(P * nbf * 4);
-    if ((sbytes & 15u) == 0) {
-      if (threadIdx.x == 0 && !abort_flag) {
-        mbar_expect_tx(&inbar, qbytes + 2 * sbytes);
-        bulk_g2s(hq, a.w.qh, qbytes, &inbar, pol);
-        bulk_g2s(hd, a.w.dh, sbytes, &inbar, pol);
-        bulk_g2s(hsum, a.w.sh, sbytes, &inbar, pol);
-      }
-      mbar_wait_bounded(&inbar, 0u, &abort_flag, a.w.status);
-    } else {
-      for (int i = threadIdx.x; i < P * f / 16; i += nthr)
-        reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(a.w.qh) + i);
-      for (int i = threadIdx.x; i < P * nbf; i += nthr) {
-        hd[i] = __ldcg(a.w.dh + i);
-        hsum[i] = __ldcg(a.w.sh + i);
-      }
-    }
-    named_bar_sync(1, nthr);
-
-    // warp w owns rows w, w+8, ... of each chunk: each lane folds its group's block dots for up
-    // to 8 rows, one transposed butterfly adds the group partials of all 8 rows; once a chunk
-    // has seen every union expert the warp combines its rows in the fixed order (shared expert
-    // first, then ranks 0..K-1)
     int ci = 0, slot = 0, c0 = 0, cn = 0;
     chunk(0, c0, cn);
     int nj = cn > warp ? (cn - warp + kNW - 1) / kNW : 0;
     const int jl = 4 * (lane & 1) + 2 * ((lane >> 1) & 1) + ((lane >> 2) & 1);  // row of the sum
-    for (int it = nst_gu; it < nst_all; ++it) {
-      const int p0 = sel.u_off[slot], np = sel.u_off[slot + 1] - p0;
-      mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
+#pragma unroll 1
+    for (int it = nst_gu - 1; it < nst_all; ++it) {
+      const bool dry = it < nst_gu;
+      if (it == nst_gu) {
+        // all CTAs counted (bounded wait); then the gate/up buffers are free: every pair's h
+        // codes, block scales and code sums as they lie in the workspace (three bulk copies, or
+        // plain loads when a size is not a multiple of 16 bytes)
+        if (threadIdx.x == 0 && !abort_flag) {
+          const uint64_t t0 = global_ns();
+          for (uint32_t k = 1;; ++k) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+            if (v >= (int)gridDim.x) break;
+            if ((k & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+              abort_flag = 1;
+              atomicExch(a.w.status, COLI_ETIMEOUT);
+              break;
+            }
+          }
+          // the h codes are read below by bulk copies (the async proxy)
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        named_bar_sync(1, nthr);
+        const uint32_t qbytes = (uint32_t)(P * f), sbytes = (uint32_t)(P * nbf * 4);
+        if ((sbytes & 15u) == 0) {
+          if (threadIdx.x == 0 && !abort_flag) {
+            mbar_expect_tx(&inbar, qbytes + 2 * sbytes);
+            bulk_g2s(hq, a.w.qh, qbytes, &inbar, pol);
+            bulk_g2s(hd, a.w.dh, sbytes, &inbar, pol);
+            bulk_g2s(hsum, a.w.sh, sbytes, &inbar, pol);
+          }
+          mbar_wait_bounded(&inbar, 0u, &abort_flag, a.w.status);
+        } else {
+          for (int i = threadIdx.x; i < P * f / 16; i += nthr)
+            reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(a.w.qh) + i);
+          for (int i = threadIdx.x; i < P * nbf; i += nthr) {
+            hd[i] = __ldcg(a.w.dh + i);
+            hsum[i] = __ldcg(a.w.sh + i);
+          }
+        }
+        named_bar_sync(1, nthr);
+      }
+      const int p0 = sel.u_off[slot], np = dry ? 1 : sel.u_off[slot + 1] - p0;
+      if (!dry) mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
       const uint8_t* sbase = ring + (long)s * pl.stage_bytes + (long)warp * rb;
       const float* sdx = t_sd + slot * pl.max_rows + c0 + warp;
       for (int q = 0; q < np; ++q) {
@@ -450,29 +461,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
         }
         float acc[kDownRowsPerWarp];
 #pragma unroll
-        for (int j = 0; j < kDownRowsPerWarp; ++j) {
-          acc[j] = 0.0f;
-          if (j < nj) {
-            const uint8_t* srow = sbase + (long)j * kNW * rb;
+        for (int j = 0; j < kDownRowsPerWarp; ++j) acc[j] = 0.0f;
+        if (nj > 0) {
+#pragma unroll
+          for (int j = 0; j < RPW; ++j) {
+            const int jj = j < nj ? j : nj - 1;
+            const uint8_t* srow = sbase + (long)jj * kNW * rb;
 #pragma unroll
             for (int i = 0; i < GF; ++i) {
               uint4 wv = make_uint4(0, 0, 0, 0);
               if (lane < AF) wv = *reinterpret_cast<const uint4*>(srow + store_chunk(lane, i, GF) * 16);
               const int ai = block_dot(wv, hr[i], hnr[i]);
               acc[j] = __fmaf_rn(hdr[i], __int2float_rn(ai), acc[j]);
-              if (DBG && a.dbg.Ad != nullptr && lane < AF)
+              if (DBG && !dry && a.dbg.Ad != nullptr && lane < AF && j < nj)
                 a.dbg.Ad[((long)p * d + row0 + c0 + j * kNW + warp) * nbf + lane * GF + i] = ai;
             }
           }
         }
         const float v = warp_tree_sum8(acc, lane);
-        if (lane < kDownRowsPerWarp && jl < nj) {
+        if (!dry && lane < kDownRowsPerWarp && jl < nj) {
           const float e = __fmul_rn(sdx[jl * kNW], v);
           es[(jl * kNW + warp) * P + p] = e;
           if (DBG && a.dbg.e != nullptr) a.dbg.e[(long)p * d + row0 + c0 + jl * kNW + warp] = e;
         }
       }
       __syncwarp();
+      if (dry) continue;
       if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == pl.nst) {
         s = 0;
@@ -504,20 +518,33 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
 }
 
 // ------------------------------------------------------------------ host side --------------
-// Instances built: G blocks per lane group on the gate/up side (d/32/32 rounded up) and GF on
-// the down side (f/32/32): the GLM-shaped layer (d = 6144, f = 2048) and layers with one block
-// per group on both sides.  Other shapes use the two-kernel path.
+// Instances built: G blocks per lane group on the gate/up side (d/32/32 rounded up), GF on the
+// down side (f/32/32), and RPW down rows per warp and chunk (at least ceil(chunk rows / 8)): the
+// GLM-shaped layer (d = 6144, f = 2048: 41 rows per CTA on 152 SMs) and layers with one block
+// per group on both sides, each with an 8-row fallback.  Other shapes use the two-kernel path.
 typedef void (*FusedKernel)(const FusedArgs);
 
-static FusedKernel fused_kernel_for(int G, int GF, bool dbg) {
-  if (G == 6 && GF == 2) return dbg ? expert_fused_kernel<6, 2, true> : expert_fused_kernel<6, 2, false>;
-  if (G == 1 && GF == 1) return dbg ? expert_fused_kernel<1, 1, true> : expert_fused_kernel<1, 1, false>;
+template <int G, int GF, int RPW>
+static FusedKernel pick(bool dbg) {
+  return dbg ? expert_fused_kernel<G, GF, RPW, true> : expert_fused_kernel<G, GF, RPW, false>;
+}
+
+static FusedKernel fused_kernel_for(int G, int GF, int rpw, bool dbg) {
+  if (G == 6 && GF == 2) return rpw <= 6 ? pick<6, 2, 6>(dbg) : pick<6, 2, 8>(dbg);
+  if (G == 1 && GF == 1) return rpw <= 2 ? pick<1, 1, 2>(dbg) : pick<1, 1, 8>(dbg);
   return nullptr;
 }
 
+// rows per warp of the largest down chunk
+static int fused_rpw(const FusedPlan& p) {
+  const int chunk = p.max_rows < kDownChunk ? p.max_rows : kDownChunk;
+  return (chunk + kNW - 1) / kNW;
+}
+
 cudaError_t configure_fused_kernels() {
-  const FusedKernel ks[] = {expert_fused_kernel<6, 2, true>, expert_fused_kernel<6, 2, false>,
-                            expert_fused_kernel<1, 1, true>, expert_fused_kernel<1, 1, false>};
+  const FusedKernel ks[] = {pick<6, 2, 6>(true), pick<6, 2, 6>(false), pick<6, 2, 8>(true),
+                            pick<6, 2, 8>(false), pick<1, 1, 2>(true), pick<1, 1, 2>(false),
+                            pick<1, 1, 8>(true),  pick<1, 1, 8>(false)};
   for (FusedKernel k : ks) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -529,33 +556,34 @@ int fused_grid(int d, int num_sms) { return d < num_sms ? d : num_sms; }
 
 bool fused_supported(int d, int f, int K, int E, int n_shared, int num_sms) {
   const int G = (d / kQB + 31) / 32, GF = (f / kQB + 31) / 32;
-  if (!fused_kernel_for(G, GF, false)) return false;
+  if (!fused_kernel_for(G, GF, kDownRowsPerWarp, false)) return false;
   return fused_plan(d, f, K, E, n_shared, fused_grid(d, num_sms)).nst >= 2;
 }
 
-// One launch of the fused expert kernel for one token: cooperative (its CTAs wait on each other
-// at the barrier, so all must be resident) and, unless events are recorded between launches, a
-// programmatic dependent of the router grid.
+// One launch of the fused expert kernel for one token, a programmatic dependent of the router
+// grid unless events are recorded between launches.  Its CTAs wait on each other at the barrier,
+// so all of them must be resident together: grid <= SM count and one CTA per SM (its shared
+// memory allows no second one).  The router grid ahead of it waits on nothing, so the CTAs that
+// cannot start while it holds their SMs start as soon as it retires.  (A cooperative launch
+// would guarantee the same but starts no CTA before the router grid has finished.)
 cudaError_t launch_expert_fused(const float* x, float* y, const Shape& s, const Store& st,
                                 const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                 cudaStream_t stream) {
   const int grid = fused_grid(s.d, num_sms);
   FusedArgs args{s, st, w, dbg, fused_plan(s.d, s.f, s.K, s.E, s.n_shared, grid), x, y};
   const int G = (s.d / kQB + 31) / 32, GF = (s.f / kQB + 31) / 32;
-  const FusedKernel k = fused_kernel_for(G, GF, dbg.g || dbg.Ag || dbg.e || dbg.Ad);
+  const FusedKernel k = fused_kernel_for(G, GF, fused_rpw(args.pl), dbg.g || dbg.Ag || dbg.e || dbg.Ad);
   if (!k || s.T != 1) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)args.pl.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k, args);
 }
 
