@@ -61,6 +61,9 @@ WORKLOADS = {
                                layers=16, has_norm=True),
     "glm_prefill_t512": Workload("glm_prefill_t512", d=6144, f=2048, E=256, K=8, n_shared=1,
                                  T=512, bias="zipf"),
+    # the GLM layer's shapes with 32 routed experts: the same kernels and per-step bytes
+    # (9 experts, 170 MB, more than L2) with 0.6 GB resident, for counter captures
+    "glm_e32_decode_t1": Workload("glm_e32_decode_t1", d=6144, f=2048, E=32, K=8, n_shared=1, T=1),
 }
 
 

@@ -316,16 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
       const float* tsc = reinterpret_cast<const float*>(tu + kFuTabInts);
       const float sg = tsc[rr], su = tsc[32 + rr];
       float pg = 0.0f, pu = 0.0f;
+      // the row pair's weights into registers first, then the dots
+      uint4 wg[G], wu[G];
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        uint4 wg = make_uint4(0, 0, 0, 0), wu = make_uint4(0, 0, 0, 0);
+        wg[i] = make_uint4(0, 0, 0, 0);
+        wu[i] = make_uint4(0, 0, 0, 0);
         if (lane < A) {
           const int off = store_chunk(lane, i, G) * 16;
-          wg = *reinterpret_cast<const uint4*>(grow + off);
-          wu = *reinterpret_cast<const uint4*>(grow + d / 2 + off);
+          wg[i] = *reinterpret_cast<const uint4*>(grow + off);
+          wu[i] = *reinterpret_cast<const uint4*>(grow + d / 2 + off);
         }
-        const int ag = block_dot(wg, xr[i], nr[i]);
-        const int au = block_dot(wu, xr[i], nr[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int ag = block_dot(wg[i], xr[i], nr[i]);
+        const int au = block_dot(wu[i], xr[i], nr[i]);
         pg = __fmaf_rn(dr[i], __int2float_rn(ag), pg);
         pu = __fmaf_rn(dr[i], __int2float_rn(au), pu);
         if (DBG && a.dbg.Ag != nullptr && lane < A) {
@@ -463,15 +469,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
 #pragma unroll
         for (int j = 0; j < kDownRowsPerWarp; ++j) acc[j] = 0.0f;
         if (nj > 0) {
+          // every row's weights into registers first, then the dots
+          uint4 wv[RPW][GF];
 #pragma unroll
           for (int j = 0; j < RPW; ++j) {
             const int jj = j < nj ? j : nj - 1;
             const uint8_t* srow = sbase + (long)jj * kNW * rb;
 #pragma unroll
+            for (int i = 0; i < GF; ++i)
+              wv[j][i] = lane < AF ? *reinterpret_cast<const uint4*>(srow + store_chunk(lane, i, GF) * 16)
+                                   : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int j = 0; j < RPW; ++j) {
+#pragma unroll
             for (int i = 0; i < GF; ++i) {
-              uint4 wv = make_uint4(0, 0, 0, 0);
-              if (lane < AF) wv = *reinterpret_cast<const uint4*>(srow + store_chunk(lane, i, GF) * 16);
-              const int ai = block_dot(wv, hr[i], hnr[i]);
+              const int ai = block_dot(wv[j][i], hr[i], hnr[i]);
               acc[j] = __fmaf_rn(hdr[i], __int2float_rn(ai), acc[j]);
               if (DBG && !dry && a.dbg.Ad != nullptr && lane < AF && j < nj)
                 a.dbg.Ad[((long)p * d + row0 + c0 + j * kNW + warp) * nbf + lane * GF + i] = ai;
