@@ -99,6 +99,28 @@ __device__ __forceinline__ int block_dot(const uint4 w, const uint32_t (&x)[8], 
   return a1 + (a16 >> 4) + neg8sx;
 }
 
+// block_dot with the weight words already split into their low-nibble and high-nibble halves
+// (lo[k] = w.k & 0x0F0F0F0F, hi[k] = w.k & 0xF0F0F0F0), for a block dotted with several tokens
+__device__ __forceinline__ void split_nibbles(const uint4 w, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+  lo[0] = w.x & 0x0F0F0F0Fu; hi[0] = w.x & 0xF0F0F0F0u;
+  lo[1] = w.y & 0x0F0F0F0Fu; hi[1] = w.y & 0xF0F0F0F0u;
+  lo[2] = w.z & 0x0F0F0F0Fu; hi[2] = w.z & 0xF0F0F0F0u;
+  lo[3] = w.w & 0x0F0F0F0Fu; hi[3] = w.w & 0xF0F0F0F0u;
+}
+__device__ __forceinline__ int block_dot_split(const uint32_t (&lo)[4], const uint32_t (&hi)[4],
+                                               const uint32_t (&x)[8], int neg8sx) {
+  int a1 = 0, a16 = 0;
+  a1 = dp4a_us(lo[0], x[0], a1);
+  a16 = dp4a_us(hi[0], x[1], a16);
+  a1 = dp4a_us(lo[1], x[2], a1);
+  a16 = dp4a_us(hi[1], x[3], a16);
+  a1 = dp4a_us(lo[2], x[4], a1);
+  a16 = dp4a_us(hi[2], x[5], a16);
+  a1 = dp4a_us(lo[3], x[6], a1);
+  a16 = dp4a_us(hi[3], x[7], a16);
+  return a1 + (a16 >> 4) + neg8sx;
+}
+
 // Position, within a stored row, of block b = g*G + i (G blocks per lane group): the groups are
 // contiguous and a group's blocks are rotated by one for groups 4..7 mod 8, so that the
 // 16-byte loads of 8 consecutive lanes fall in distinct shared-memory banks.

@@ -26,6 +26,13 @@ static inline int align16(int x) { return (x + 15) & ~15; }
 // tokens (T at most) and the 32 gate + 32 up row scales
 constexpr int kGuTabInts = 5 + kDecodeTmax;  // slot, expert, first pair, pairs, hb, tokens
 constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
+// Relative cost of one gate/up unit whose union slot serves np tokens: its bytes take the same
+// time whatever np (kGuCostBytes), its dots grow with np (kGuCostPair each); the larger bounds
+// the unit.  The routed units are split over the CTAs by this cost, not by count.
+constexpr int kGuCostBytes = 4, kGuCostPair = 3;
+__host__ __device__ constexpr int gu_unit_cost(int np) {
+  return kGuCostPair * np > kGuCostBytes ? kGuCostPair * np : kGuCostBytes;
+}
 
 static long max_union_slots(int T, int K, int E, int n_shared) {
   return (long)(T * K < E ? T * K : E) + (n_shared ? 1 : 0);
@@ -38,8 +45,10 @@ GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid
   p.xs_bytes = align16(T * d);
   p.aux_bytes = align16(T * nbd * 8);
   p.hs_bytes = align16(2 * 32 * T * 4);
+  // the cost split gives a CTA at most its share of the costliest layout in the cheapest units
   const long units = max_union_slots(T, K, E, n_shared) * (f / 32);
-  p.max_units = (int)((units + grid - 1) / grid) + 2;
+  const long wmax = gu_unit_cost(T), wmin = gu_unit_cost(1);
+  p.max_units = (int)((units * wmax + wmin * grid - 1) / (wmin * grid)) + 4;
   p.tab_bytes = align16(p.max_units * kGuTabBytes);
   p.sel_bytes = align16(sel_bytes(T, E));
   const int fixed =
@@ -98,6 +107,83 @@ struct DownArgs {
 // in every CTA that has some: those are known before routing, so they are prefetched before
 // the kernel waits for the routing grid.  Warp w reduces row pair w of every stage; when a
 // unit's 32 rows are done the CTA re-quantises them (one warp per token).
+// One gate/up row pair of one stage dotted with NP tokens' codes (the union slot's bucket):
+// each of the warp's G blocks is loaded and split into nibble halves once for all tokens.
+struct GuRow {
+  const uint8_t* grow;  // the row pair in the stage: gate row, then up row (d/2 bytes each)
+  const uint8_t* xs;    // the tokens' codes in lane-group order
+  const float* dxs;
+  const int* nsx;
+  int d, nbd, A, lane;
+  float sg, su;  // the row's gate and up scales
+  int row, f, p0;
+  float* hrow;   // h of this row for the slot's tokens (stride 1)
+  ExpertDebug dbg;
+};
+
+template <int G, int NP, bool DBG>
+__device__ __forceinline__ void gu_multi(const GuRow& r, const int (&toks)[kDecodeTmax]) {
+  float pg[NP], pu[NP];
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    pg[q] = 0.0f;
+    pu[q] = 0.0f;
+  }
+  const bool on = r.lane < r.A;
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    uint4 wg = make_uint4(0, 0, 0, 0), wu = make_uint4(0, 0, 0, 0);
+    if (on) {
+      const int off = store_chunk(r.lane, i, G) * 16;
+      wg = *reinterpret_cast<const uint4*>(r.grow + off);
+      wu = *reinterpret_cast<const uint4*>(r.grow + r.d / 2 + off);
+    }
+    uint32_t gl[4], gh[4], ul[4], uh[4];
+    split_nibbles(wg, gl, gh);
+    split_nibbles(wu, ul, uh);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      const int t = toks[q];
+      uint32_t xq[8];
+      float dq = 0.0f;
+      int nq = 0;
+      if (on) {
+        const uint8_t* base = r.xs + (long)t * r.d + (i * r.A + r.lane) * 16;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(base);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(base + r.nbd * 16);
+        xq[0] = v0.x; xq[1] = v0.y; xq[2] = v0.z; xq[3] = v0.w;
+        xq[4] = v1.x; xq[5] = v1.y; xq[6] = v1.z; xq[7] = v1.w;
+        dq = r.dxs[t * r.nbd + r.lane * G + i];
+        nq = r.nsx[t * r.nbd + r.lane * G + i];
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xq[k] = 0u;
+      }
+      const int ag = block_dot_split(gl, gh, xq, nq);
+      const int au = block_dot_split(ul, uh, xq, nq);
+      pg[q] = __fmaf_rn(dq, __int2float_rn(ag), pg[q]);
+      pu[q] = __fmaf_rn(dq, __int2float_rn(au), pu[q]);
+      if (DBG && r.dbg.Ag != nullptr && on) {
+        const long o = ((long)(r.p0 + q) * r.f + r.row) * r.nbd + r.lane * G + i;
+        r.dbg.Ag[o] = ag;
+        r.dbg.Au[o] = au;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const float tg = warp_tree_sum(pg[q]), tuu = warp_tree_sum(pu[q]);
+    const float g = __fmul_rn(r.sg, tg), u = __fmul_rn(r.su, tuu);
+    if (r.lane == 0) {
+      r.hrow[q] = canon_silu_mul(g, u);
+      if (DBG && r.dbg.g != nullptr) {
+        r.dbg.g[(long)(r.p0 + q) * r.f + r.row] = g;
+        r.dbg.u[(long)(r.p0 + q) * r.f + r.row] = u;
+      }
+    }
+  }
+}
+
 template <int G, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const GateupArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -206,18 +292,35 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
   if (blockIdx.x == 0) sel_publish(a.s, sel, a.w);
   const int nu = *sel.nu;
 
-  // routed units of this CTA: the total U = UA + UB is split evenly (each CTA's shared units
-  // count towards its share) when there are at least as many routed units as CTAs
-  const int UB = (nu - (a.s.n_shared ? 1 : 0)) * nhb;
-  int b0, b1;
-  if (UB >= G_) {
-    const long U = UA + UB;
-    b0 = (int)(U * c / G_) - a0;
-    b1 = (int)(U * (c + 1) / G_) - a1;
-  } else {
-    b0 = (int)((long)UB * c / G_);
-    b1 = (int)((long)UB * (c + 1) / G_);
-  }
+  // routed units of this CTA: the routed units (slot-major, union order) are split by cost
+  // (gu_unit_cost of the slot's pairs).  CTA c's share ends where the cost prefix of all units,
+  // shared ones included, reaches c+1 G-ths of the total; when one CTA's shared units could
+  // outweigh an average share (so the ranges might not increase with c) the routed units alone
+  // are split by cost.
+  const int nr = nu - (a.s.n_shared ? 1 : 0), UB = nr * nhb;
+  const long wsh = a.s.n_shared ? gu_unit_cost(sel.u_off[nu] - sel.u_off[nu - 1]) : 0;
+  long cr = 0;  // cost of all routed units
+  for (int sl = 0; sl < nr; ++sl) cr += (long)nhb * gu_unit_cost(sel.u_off[sl + 1] - sel.u_off[sl]);
+  const long call = cr + (long)UA * wsh;
+  const long na_max = (UA + G_ - 1) / G_;
+  const bool with_shared = call >= (long)G_ * (na_max * wsh + 1);
+  // first routed unit whose cost prefix reaches cost target t
+  auto first_at = [&](long t) -> int {
+    if (t <= 0) return 0;
+    long acc = 0;
+    for (int sl = 0; sl < nr; ++sl) {
+      const long w = gu_unit_cost(sel.u_off[sl + 1] - sel.u_off[sl]);
+      if (acc + w * nhb >= t) return sl * nhb + (int)((t - acc + w - 1) / w);
+      acc += w * nhb;
+    }
+    return UB;
+  };
+  auto target = [&](int cc) -> long {
+    if (!with_shared) return cr * cc / G_;
+    const long as = (long)UA * cc / G_;  // shared units of CTAs before cc
+    return call * cc / G_ - as * wsh;
+  };
+  const int b0 = first_at(target(c)), b1 = first_at(target(c + 1));
   const int nunit = na + (b1 - b0);
   const int nstage = nunit * SPU;
 
@@ -297,9 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
       const uint8_t* grow = ring + (long)s * pl.stage_bytes + (long)warp * d;
       const float* tsc = reinterpret_cast<const float*>(tu + kGuTabInts);
       const float sg = tsc[rr], su = tsc[32 + rr];
-      for (int q = 0; q < np; ++q) {
-        const int p = p0 + q;
-        const int t = tu[5 + q];
+      if (np == 1) {
+        // one token: its codes stay in registers while consecutive units serve the same token
+        const int p = p0;
+        const int t = tu[5];
         if (t != cached_tok) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -318,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
               nr[i] = 0;
             }
           }
-          cached_tok = (np == 1) ? t : -1;
+          cached_tok = t;
         }
         float pg = 0.0f, pu = 0.0f;
 #pragma unroll
@@ -343,12 +447,29 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         pu = warp_tree_sum(pu);
         const float g = __fmul_rn(sg, pg), u = __fmul_rn(su, pu);
         if (lane == 0) {
-          hs[((lu & 1) * 32 + rr) * T + q] = canon_silu_mul(g, u);
+          hs[((lu & 1) * 32 + rr) * T] = canon_silu_mul(g, u);
           if (DBG && a.dbg.g != nullptr) {
             a.dbg.g[(long)p * f + row] = g;
             a.dbg.u[(long)p * f + row] = u;
           }
         }
+      } else {
+        // several tokens: each block's weights are loaded and split into nibble halves once,
+        // then dotted with every token's codes of that block; each token keeps its own fma
+        // chain over the blocks in order (the token count is a template argument, so the
+        // tokens' chains interleave with no branch between them)
+        cached_tok = -1;
+        int toks[kDecodeTmax];
+#pragma unroll
+        for (int q = 0; q < kDecodeTmax; ++q) toks[q] = q < np ? tu[5 + q] : 0;
+        const GuRow r{grow, xs, dxs, nsx, d, nbd, A, lane, sg, su, row, f, p0,
+                      hs + ((lu & 1) * 32 + rr) * T, DBG ? a.dbg : ExpertDebug{}};
+        if (np == 2)
+          gu_multi<G, 2, DBG>(r, toks);
+        else if (np == 3)
+          gu_multi<G, 3, DBG>(r, toks);
+        else
+          gu_multi<G, 4, DBG>(r, toks);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with its row pair
@@ -391,6 +512,81 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
 
 __host__ __device__ inline int down_rows_begin(int d, int c, int grid) {
   return (int)((long)d * c / grid);
+}
+
+// The down rows of one stage (warp `warp`'s rows of the chunk) dotted with the h codes of NP
+// consecutive pairs p, p+1, ...: each row block's weights are loaded and split once for all.
+struct DnRows {
+  const uint8_t* sbase;  // the warp's first row in the stage
+  const uint8_t* hq;     // [P][f] h codes
+  const float* hd;       // [P][nbf] block scales
+  const int* hsum;       // [P][nbf] code sums
+  const float* sdx;      // the warp's first down-row scale of the chunk (stride kNW)
+  float* es;             // [chunk row][P] expert outputs
+  int f, nbf, A, lane, warp, nj, jl, P, d, row0c;  // row0c: first output row of the chunk
+  bool dry;
+  ExpertDebug dbg;
+};
+
+template <int GF, int NP, bool DBG>
+__device__ __forceinline__ void dn_rows(const DnRows& r, int p) {
+  const bool on = r.lane < r.A;
+  const int rb = r.f >> 1;
+  uint32_t hr[NP][GF][8];
+  float hdr[NP][GF];
+  int hnr[NP][GF];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+#pragma unroll
+    for (int i = 0; i < GF; ++i) {
+      if (on) {
+        const uint8_t* base = r.hq + (long)(p + k) * r.f + (r.lane * GF + i) * 32;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(base);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(base + 16);
+        hr[k][i][0] = v0.x; hr[k][i][1] = v0.y; hr[k][i][2] = v0.z; hr[k][i][3] = v0.w;
+        hr[k][i][4] = v1.x; hr[k][i][5] = v1.y; hr[k][i][6] = v1.z; hr[k][i][7] = v1.w;
+        hdr[k][i] = r.hd[(p + k) * r.nbf + r.lane * GF + i];
+        hnr[k][i] = -8 * r.hsum[(p + k) * r.nbf + r.lane * GF + i];
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) hr[k][i][t] = 0u;
+        hdr[k][i] = 0.0f;
+        hnr[k][i] = 0;
+      }
+    }
+  }
+  float acc[NP][kDownRowsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kDownRowsPerWarp; ++j) {
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[k][j] = 0.0f;
+    if (j < r.nj) {
+      const uint8_t* srow = r.sbase + (long)j * kNW * rb;
+#pragma unroll
+      for (int i = 0; i < GF; ++i) {
+        uint4 wv = make_uint4(0, 0, 0, 0);
+        if (on) wv = *reinterpret_cast<const uint4*>(srow + store_chunk(r.lane, i, GF) * 16);
+        uint32_t lo[4], hi[4];
+        split_nibbles(wv, lo, hi);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          const int ai = block_dot_split(lo, hi, hr[k][i], hnr[k][i]);
+          acc[k][j] = __fmaf_rn(hdr[k][i], __int2float_rn(ai), acc[k][j]);
+          if (DBG && !r.dry && r.dbg.Ad != nullptr && on)
+            r.dbg.Ad[((long)(p + k) * r.d + r.row0c + j * kNW + r.warp) * r.nbf + r.lane * GF + i] = ai;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const float v = warp_tree_sum8(acc[k], r.lane);
+    if (!r.dry && r.lane < kDownRowsPerWarp && r.jl < r.nj) {
+      const float e = __fmul_rn(r.sdx[r.jl * kNW], v);
+      r.es[(r.jl * kNW + r.warp) * r.P + p + k] = e;
+      if (DBG && r.dbg.e != nullptr) r.dbg.e[(long)(p + k) * r.d + r.row0c + r.jl * kNW + r.warp] = e;
+    }
+  }
 }
 
 template <int GF, bool DBG>
@@ -552,50 +748,18 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       if (!dry) mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
       const uint8_t* sbase = ring + (long)s * pl.stage_bytes + (long)warp * rb;
       const float* sdx = t_sd + slot * pl.max_rows + c0 + warp;
-      for (int q = 0; q < np; ++q) {
-        const int p = p0 + q;
-        uint32_t hr[GF][8];
-        float hdr[GF];
-        int hnr[GF];
-#pragma unroll
-        for (int i = 0; i < GF; ++i) {
-          if (lane < A) {
-            const uint8_t* base = hq + (long)p * f + (lane * GF + i) * 32;
-            const uint4 v0 = *reinterpret_cast<const uint4*>(base);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(base + 16);
-            hr[i][0] = v0.x; hr[i][1] = v0.y; hr[i][2] = v0.z; hr[i][3] = v0.w;
-            hr[i][4] = v1.x; hr[i][5] = v1.y; hr[i][6] = v1.z; hr[i][7] = v1.w;
-            hdr[i] = hd[p * nbf + lane * GF + i];
-            hnr[i] = -8 * hsum[p * nbf + lane * GF + i];
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) hr[i][k] = 0u;
-            hdr[i] = 0.0f;
-            hnr[i] = 0;
-          }
-        }
-        float acc[kDownRowsPerWarp];
-#pragma unroll
-        for (int j = 0; j < kDownRowsPerWarp; ++j) {
-          acc[j] = 0.0f;
-          if (j < nj) {
-            const uint8_t* srow = sbase + (long)j * kNW * rb;
-#pragma unroll
-            for (int i = 0; i < GF; ++i) {
-              uint4 wv = make_uint4(0, 0, 0, 0);
-              if (lane < A) wv = *reinterpret_cast<const uint4*>(srow + store_chunk(lane, i, GF) * 16);
-              const int ai = block_dot(wv, hr[i], hnr[i]);
-              acc[j] = __fmaf_rn(hdr[i], __int2float_rn(ai), acc[j]);
-              if (DBG && !dry && a.dbg.Ad != nullptr && lane < A)
-                a.dbg.Ad[((long)p * d + row0 + c0 + j * kNW + warp) * nbf + lane * GF + i] = ai;
-            }
-          }
-        }
-        const float v = warp_tree_sum8(acc, lane);
-        if (!dry && lane < kDownRowsPerWarp && jl < nj) {
-          const float e = __fmul_rn(sdx[jl * kNW], v);
-          es[(jl * kNW + warp) * P + p] = e;
-          if (DBG && a.dbg.e != nullptr) a.dbg.e[(long)p * d + row0 + c0 + jl * kNW + warp] = e;
+      // pairs two at a time (the pair count is a template argument, so both pairs' chains
+      // interleave with no branch between them); each row block's weights are loaded and split
+      // into nibble halves once for both
+      const DnRows r{sbase, hq, hd, hsum, sdx, es, f, nbf, A, lane, warp, nj, jl, P, d, row0 + c0,
+                     dry, DBG ? a.dbg : ExpertDebug{}};
+      for (int q = 0; q < np;) {
+        if (np - q >= 2) {
+          dn_rows<GF, 2, DBG>(r, p0 + q);
+          q += 2;
+        } else {
+          dn_rows<GF, 1, DBG>(r, p0 + q);
+          q += 1;
         }
       }
       __syncwarp();
