@@ -15,7 +15,7 @@
 //   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream, deep ring)
 //   warp 1      bulk-tensor copies of the bf16 activation block of each K-step
 //   warps 2-5   int4 -> bf16 conversion of the weight block into the MMA's shared layout
-//   warp 6      TMEM owner and single MMA issuer (2 x K16 MMAs per K-block, double-buffered D)
+//   warp 6      TMEM owner and single MMA issuer (2 x K16 MMAs per K-block, 3 accumulator buffers)
 //   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,7 +36,8 @@ constexpr int kPfWarps = 15;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfAStage = kPfM * 32 * 2;  // 8 KB
 constexpr int kPfBStage = kPfN * 32 * 2;  // 4 KB
-constexpr uint32_t kTmemCols = 512;       // acc[2] x 64 + stack[5] x 64 = 448 used
+constexpr int kPfAcc = 3;                 // accumulator buffers: K-blocks in flight between MMA and epilogue
+constexpr uint32_t kTmemCols = 512;       // acc[3] x 64 + stack[5] x 64 = 512 used
 
 struct PfArgs {
   Shape s;
@@ -88,8 +89,8 @@ __device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
   m.b_full = m.a_full + kPfStages;
   m.ab_empty = m.b_full + kPfStages;
   m.acc_full = m.ab_empty + kPfStages;
-  m.acc_empty = m.acc_full + 2;
-  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + 2);
+  m.acc_empty = m.acc_full + kPfAcc;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfAcc);
   m.tp = reinterpret_cast<int*>(m.tmem_slot + 4);
   m.tex = m.tp + a.s.E + 2;
   m.toff = m.tex + a.s.E + 2;
@@ -101,7 +102,7 @@ int prefill_smem_bytes(int d, int f, int E, int down) {
   const int nb = K / kQB, G = (nb + 31) / 32;
   const int raw = kPfM * G * 16;
   const int dx = nb * kPfN * 4;
-  const int bars = (2 * kPfRawStages + 3 * kPfStages + 4) * 8 + 16;
+  const int bars = (2 * kPfRawStages + 3 * kPfStages + 2 * kPfAcc) * 8 + 16;
   const int tabs = 3 * (E + 2) * 4;
   return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfN * 64 * 4) +
          bars + tabs;
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&m.b_full[i], 1);
       mbar_init(&m.ab_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPfAcc; ++i) {
       mbar_init(&m.acc_full[i], 1);
       mbar_init(&m.acc_empty[i], 8);
     }
@@ -268,6 +269,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       long kb = 0;
+      int ab = 0;          // accumulator buffer of K-block kb
+      uint32_t aph = 0;    // parity of its current use
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
         int u, mt, nt;
         pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
@@ -277,12 +280,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(kPfM, nmma);
         for (int b = 0; b < nb; ++b, ++kb) {
           const int s = (int)(kb % kPfStages);
-          const int ab = (int)(kb & 1);
           const uint32_t ph = (uint32_t)((kb / kPfStages) & 1);
           bool ok = mbar_wait_bounded(&m.a_full[s], ph, &abort_flag, status);
           ok = mbar_wait_bounded(&m.b_full[s], ph, &abort_flag, status) && ok;
-          if (kb >= 2)
-            ok = mbar_wait_bounded(&m.acc_empty[ab], (uint32_t)(((kb >> 1) - 1) & 1), &abort_flag, status) && ok;
+          if (kb >= kPfAcc) ok = mbar_wait_bounded(&m.acc_empty[ab], aph ^ 1u, &abort_flag, status) && ok;
+          const int abuf = ab;
+          if (++ab == kPfAcc) {
+            ab = 0;
+            aph ^= 1u;
+          }
           if (!ok) continue;
           tc_fence_after();
           const uint8_t* as = m.a + (long)s * kPfAStage;
@@ -291,10 +297,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int ks = 0; ks < 2; ++ks) {
             const uint64_t da = smem_desc(as + ks * 2 * (kPfM / 8) * 128, (kPfM / 8) * 128, 128);
             const uint64_t db = smem_desc(bs + ks * 2 * (kPfN / 8) * 128, (kPfN / 8) * 128, 128);
-            tc_mma_bf16(tmem + ab * kPfN, da, db, idesc, ks > 0);
+            tc_mma_bf16(tmem + abuf * kPfN, da, db, idesc, ks > 0);
           }
           tc_commit(&m.ab_empty[s]);
-          tc_commit(&m.acc_full[ab]);
+          tc_commit(&m.acc_full[abuf]);
         }
       }
     }
@@ -305,7 +311,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int row = q * 32 + lane;
     const int etid = threadIdx.x - 7 * 32;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    long kb = 0;
+    int ab = 0;          // accumulator buffer of the next K-block
+    uint32_t aph = 0;    // parity of its current use
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int u, mt, nt;
       pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
@@ -328,15 +335,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
       int gi = 0, gb = 0;  // current group and block within it
-      for (int b = 0; b < nb; ++b, ++kb) {
-        const int ab = (int)(kb & 1);
-        mbar_wait_bounded(&m.acc_full[ab], (uint32_t)((kb >> 1) & 1), &abort_flag, status);
+      for (int b = 0; b < nb; ++b) {
+        mbar_wait_bounded(&m.acc_full[ab], aph, &abort_flag, status);
         tc_fence_after();
         float acc[32];
         if (active) tmem_ld32(tl + ab * kPfN + half * 32, acc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.acc_empty[ab]);
+        if (++ab == kPfAcc) {
+          ab = 0;
+          aph ^= 1u;
+        }
         if (!active) continue;
         const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfN + half * 32);
 #pragma unroll
@@ -363,12 +373,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           gb = 0;
           int l = 0;
           for (; (gi >> l) & 1; ++l) {
-            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, acc);
+            tmem_ld32(tl + kPfAcc * kPfN + l * kPfN + half * 32, acc);
 #pragma unroll
             for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
           }
           if (l < 5) {
-            tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, chain);
+            tmem_st32(tl + kPfAcc * kPfN + l * kPfN + half * 32, chain);
 #pragma unroll
             for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
           }
@@ -381,12 +391,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           float acc[32];
           int l = 0;
           for (; (gz >> l) & 1; ++l) {
-            tmem_ld32(tl + 2 * kPfN + l * kPfN + half * 32, acc);
+            tmem_ld32(tl + kPfAcc * kPfN + l * kPfN + half * 32, acc);
 #pragma unroll
             for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
           }
           if (l < 5) {
-            tmem_st32(tl + 2 * kPfN + l * kPfN + half * 32, chain);
+            tmem_st32(tl + kPfAcc * kPfN + l * kPfN + half * 32, chain);
 #pragma unroll
             for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
           }
