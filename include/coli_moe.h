@@ -148,6 +148,16 @@ int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, 
  * of an earlier forward gave up (the word is then cleared).  Synchronises `stream`. */
 int coli_moe_status(coli_moe* h, void* stream);
 
+/* Failure-path test knob.  fault = COLI_FAULT_SKIP_ARRIVAL makes the next one-token forward on
+ * this handle that runs the fused expert kernel (coli_moe_launches(h, 1) == 2) leave CTA 0 out
+ * of that kernel's grid barrier: every CTA's bounded wait at the barrier then runs out (about
+ * 2 s), the call's output is undefined and coli_moe_status reports COLI_ETIMEOUT; nothing
+ * hangs and the handle stays usable.  The knob applies to one such forward and then clears
+ * itself; fault = 0 clears it.  Not for production use (and not to be captured in a CUDA
+ * graph: the knob is read when the forward is launched).  EINVAL: unknown fault code. */
+#define COLI_FAULT_SKIP_ARRIVAL 1
+int coli_moe_inject_fault(coli_moe* h, int fault);
+
 /* Number of kernel launches one coli_moe_forward of T tokens makes on this handle: 2 for one
  * token when the expert half runs as one fused kernel (router, then gate/up + down), 3 per
  * chunk of at most 4 tokens on the decode path, 8 on the batched tensor-core path.  Negative

@@ -17,6 +17,8 @@ _i, _f, _vp, _i64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int6
 STATUS = {0: "COLI_OK", -1: "COLI_EINVAL", -2: "COLI_ENOMEM", -3: "COLI_ESTATE", -4: "COLI_ECUDA",
           -5: "COLI_ETIMEOUT", -6: "COLI_EUNSUPPORTED"}
 HEADER = os.path.join(_build.INCLUDE, "coli_moe.h")
+ETIMEOUT = -5
+FAULT_SKIP_ARRIVAL = 1  # coli_moe_inject_fault: the next fused forward leaves CTA 0 out of its barrier
 
 
 class ColiError(RuntimeError):
@@ -69,6 +71,7 @@ def lib():
         L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
         L.coli_moe_expert_record_bytes.restype = _i64
         L.coli_moe_launches.argtypes = [_vp, _i]
+        L.coli_moe_inject_fault.argtypes = [_vp, _i]
         L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
         L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
         L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
@@ -189,6 +192,11 @@ class MoeLayer:
 
     def status(self, stream=None):
         return int(lib().coli_moe_status(self.h, _stream(stream)))
+
+    def inject_fault(self, fault):
+        """failure-path test knob (coli_moe_inject_fault): 1 = the next fused one-token forward
+        leaves CTA 0 out of the grid barrier, so its bounded waits run out"""
+        _check(lib().coli_moe_inject_fault(self.h, fault), "coli_moe_inject_fault")
 
     def launches(self, T):
         """kernel launches one forward of T tokens makes"""

@@ -153,7 +153,7 @@ bool fused_supported(int d, int f, int K, int E, int n_shared, int num_sms);
 cudaError_t configure_fused_kernels();
 cudaError_t launch_expert_fused(const float* x, float* y, const Shape& s, const Store& st,
                                 const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
-                                cudaStream_t stream);
+                                bool skip_arrival, cudaStream_t stream);
 GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
 int down_grid(int d, int num_sms);  // CTAs of the down kernel

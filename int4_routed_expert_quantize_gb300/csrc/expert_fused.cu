@@ -68,6 +68,7 @@ struct FusedArgs {
   FusedPlan pl;
   const float* x;
   float* y;
+  int skip_arrival;  // failure-path test: CTA 0 stays out of the grid barrier
 };
 
 template <int G, int GF, int RPW, bool DBG>
@@ -382,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
     __threadfence();
     named_bar_sync(1, kNW * 32);
     int* counter = a.w.sel_flag + 1;
-    if (threadIdx.x == 0 && !abort_flag) atomicAdd(counter, 1);
+    if (threadIdx.x == 0 && !abort_flag && !(a.skip_arrival && blockIdx.x == 0))
+      atomicAdd(counter, 1);
 
     // ---------------- down phase.  Warp w owns rows w, w+8, ... of each chunk: each lane folds
     // its group's block dots for up to RPW rows (rows past the warp's last one repeat it and are
@@ -581,9 +583,10 @@ bool fused_supported(int d, int f, int K, int E, int n_shared, int num_sms) {
 // would guarantee the same but starts no CTA before the router grid has finished.)
 cudaError_t launch_expert_fused(const float* x, float* y, const Shape& s, const Store& st,
                                 const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
-                                cudaStream_t stream) {
+                                bool skip_arrival, cudaStream_t stream) {
   const int grid = fused_grid(s.d, num_sms);
-  FusedArgs args{s, st, w, dbg, fused_plan(s.d, s.f, s.K, s.E, s.n_shared, grid), x, y};
+  FusedArgs args{s, st, w, dbg, fused_plan(s.d, s.f, s.K, s.E, s.n_shared, grid), x, y,
+                 skip_arrival ? 1 : 0};
   const int G = (s.d / kQB + 31) / 32, GF = (s.f / kQB + 31) / 32;
   const FusedKernel k = fused_kernel_for(G, GF, fused_rpw(args.pl), dbg.g || dbg.Ag || dbg.e || dbg.Ad);
   if (!k || s.T != 1) return cudaErrorInvalidValue;

@@ -25,6 +25,7 @@ struct coli_moe {
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
   bool prefill = false;     // batches above kDecodeTmax use the tensor-core path
   bool fused = false;       // one-token forwards use the fused expert kernel
+  int fault = 0;            // one-shot failure-path knob (coli_moe_inject_fault)
   PrefillWork pw;
   PrefillMaps maps;
   bool router_loaded = false;
@@ -118,7 +119,10 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
   if (e == cudaSuccess) e = launch_route(x, s, h->st, h->w, stream);
   if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], stream);
   if (T == 1 && h->fused) {
-    if (e == cudaSuccess) e = launch_expert_fused(x, y, s, h->st, h->w, dbg, h->num_sms, pdl, stream);
+    if (e == cudaSuccess)
+      e = launch_expert_fused(x, y, s, h->st, h->w, dbg, h->num_sms, pdl,
+                              h->fault == COLI_FAULT_SKIP_ARRIVAL, stream);
+    h->fault = 0;
     if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
   } else {
     if (e == cudaSuccess) e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, pdl, stream);
@@ -231,6 +235,12 @@ const char* coli_moe_strerror(int status) {
     case COLI_EUNSUPPORTED: return "unsupported shape or request";
     default: return "unknown status";
   }
+}
+
+int coli_moe_inject_fault(coli_moe* h, int fault) {
+  if (!h || (fault != 0 && fault != COLI_FAULT_SKIP_ARRIVAL)) return COLI_EINVAL;
+  h->fault = fault;
+  return COLI_OK;
 }
 
 int coli_moe_launches(const coli_moe* h, int T) {
