@@ -148,6 +148,12 @@ int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, 
  * of an earlier forward gave up (the word is then cleared).  Synchronises `stream`. */
 int coli_moe_status(coli_moe* h, void* stream);
 
+/* Batches of at least min_tokens tokens (min_tokens > 4) take the batched tensor-core path
+ * (when the handle has it: max_tokens > 4); smaller batches run the decode kernels in chunks of
+ * at most 4 tokens.  Both give the same result for every token.  The default, 256, is where the
+ * two cost the same on the GLM-shaped layer.  EINVAL: min_tokens <= 4. */
+int coli_moe_set_prefill_min(coli_moe* h, int min_tokens);
+
 /* Failure-path test knob.  fault = COLI_FAULT_SKIP_ARRIVAL makes the next one-token forward on
  * this handle that runs the fused expert kernel (coli_moe_launches(h, 1) == 2) leave CTA 0 out
  * of that kernel's grid barrier: every CTA's bounded wait at the barrier then runs out (about
@@ -160,7 +166,8 @@ int coli_moe_inject_fault(coli_moe* h, int fault);
 
 /* Number of kernel launches one coli_moe_forward of T tokens makes on this handle: 2 for one
  * token when the expert half runs as one fused kernel (router, then gate/up + down), 3 per
- * chunk of at most 4 tokens on the decode path, 8 on the batched tensor-core path.  Negative
+ * chunk of at most 4 tokens on the decode path, 8 on the batched tensor-core path (batches of at
+ * least the coli_moe_set_prefill_min size, 256 by default).  Negative
  * status on error (EINVAL: T < 1 or T > max_tokens). */
 int coli_moe_launches(const coli_moe* h, int T);
 

@@ -72,6 +72,7 @@ def lib():
         L.coli_moe_expert_record_bytes.restype = _i64
         L.coli_moe_launches.argtypes = [_vp, _i]
         L.coli_moe_inject_fault.argtypes = [_vp, _i]
+        L.coli_moe_set_prefill_min.argtypes = [_vp, _i]
         L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
         L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
         L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
@@ -192,6 +193,11 @@ class MoeLayer:
 
     def status(self, stream=None):
         return int(lib().coli_moe_status(self.h, _stream(stream)))
+
+    def set_prefill_min(self, min_tokens):
+        """batches of at least min_tokens (> 4) take the tensor-core path, smaller ones the
+        decode kernels in chunks of 4 (coli_moe_set_prefill_min)"""
+        _check(lib().coli_moe_set_prefill_min(self.h, min_tokens), "coli_moe_set_prefill_min")
 
     def inject_fault(self, fault):
         """failure-path test knob (coli_moe_inject_fault): 1 = the next fused one-token forward

@@ -23,7 +23,8 @@ struct coli_moe {
   Store st;
   Work w;
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
-  bool prefill = false;     // batches above kDecodeTmax use the tensor-core path
+  bool prefill = false;     // the tensor-core path is set up (max_tokens > kDecodeTmax)
+  int prefill_min = kPrefillMinTokens;  // batches of at least this many tokens take it
   bool fused = false;       // one-token forwards use the fused expert kernel
   int fault = 0;            // one-shot failure-path knob (coli_moe_inject_fault)
   PrefillWork pw;
@@ -204,12 +205,13 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
   if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
   if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
-  if (dump && T > kDecodeTmax && !h->prefill) return COLI_EUNSUPPORTED;
+  const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
+  if (dump && T > kDecodeTmax && !batched) return COLI_EUNSUPPORTED;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
   int rc = check_device(h);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  if (T > kDecodeTmax && h->prefill) return run_prefill(h, x, T, y, dump, st);
+  if (batched) return run_prefill(h, x, T, y, dump, st);
   // the smem-staged kernels take up to kDecodeTmax tokens; larger batches run in chunks,
   // which gives the same result per token (each token's output depends on itself only)
   for (int c0 = 0; c0 < T; c0 += kDecodeTmax) {
@@ -237,6 +239,12 @@ const char* coli_moe_strerror(int status) {
   }
 }
 
+int coli_moe_set_prefill_min(coli_moe* h, int min_tokens) {
+  if (!h || min_tokens <= kDecodeTmax) return COLI_EINVAL;
+  h->prefill_min = min_tokens;
+  return COLI_OK;
+}
+
 int coli_moe_inject_fault(coli_moe* h, int fault) {
   if (!h || (fault != 0 && fault != COLI_FAULT_SKIP_ARRIVAL)) return COLI_EINVAL;
   h->fault = fault;
@@ -246,7 +254,7 @@ int coli_moe_inject_fault(coli_moe* h, int fault) {
 int coli_moe_launches(const coli_moe* h, int T) {
   if (!h || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
   if (T == 1 && h->fused) return 2;
-  if (T > kDecodeTmax && h->prefill) return 8;
+  if (T > kDecodeTmax && h->prefill && T >= h->prefill_min) return 8;
   return 3 * ((T + kDecodeTmax - 1) / kDecodeTmax);
 }
 

@@ -71,6 +71,7 @@ def test_null_arguments(built):
     assert L.coli_quantize_i4_rows(None, 4, 7, None, None, None) == -1
     assert L.coli_moe_status(None, None) == -1
     assert L.coli_moe_inject_fault(None, 1) == -1
+    assert L.coli_moe_set_prefill_min(None, 64) == -1
     assert L.coli_moe_launches(None, 1) == -1
     L.coli_moe_destroy(None)
 

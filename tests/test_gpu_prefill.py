@@ -50,6 +50,7 @@ def _full_compare(L, OL, x, want_A):
 def tiny32():
     wl = W.Workload("tiny_batch", d=512, f=256, E=32, K=4, n_shared=1, T=32)
     L = synthetic.build_layer(wl, max_tokens=32)
+    L.set_prefill_min(5)  # these tests exercise the tensor-core path at small batches
     yield wl, L, O.Layer(wl)
     L.close()
 
@@ -73,6 +74,7 @@ def test_tiny_tensor_core_matches_decode_path(tiny32):
 def glm64():
     wl = W.Workload("glm_batch", d=6144, f=2048, E=256, K=8, n_shared=1, T=64)
     L = synthetic.build_layer(wl, max_tokens=64)
+    L.set_prefill_min(5)  # these tests exercise the tensor-core path at small batches
     yield wl, L, O.Layer(wl)
     L.close()
 
@@ -89,6 +91,23 @@ def test_glm_tensor_core_matches_decode_path(glm64):
     for t in (0, 31, 63):
         y1 = to_np(L.forward(x[t:t + 1].contiguous()))
         assert np.array_equal(yb[t], y1[0])
+    assert L.status() == 0
+
+
+def test_glm_batch_paths_agree(glm64):
+    # the same 64-token batch through the tensor-core path and through chunked decode (the
+    # default below the crossover): bit-identical outputs
+    wl, L, OL = glm64
+    x = synthetic.x_tokens(wl, 64, token0=2000)
+    yt = to_np(L.forward(x))
+    assert L.launches(64) == 8
+    L.set_prefill_min(65)
+    try:
+        assert L.launches(64) == 3 * 16
+        yd = to_np(L.forward(x))
+    finally:
+        L.set_prefill_min(5)
+    assert np.array_equal(yt, yd)
     assert L.status() == 0
 
 
