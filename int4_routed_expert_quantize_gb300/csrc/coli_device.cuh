@@ -224,14 +224,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// asynchronous copies global -> shared through the load path (not the bulk-copy engine, whose
-// queue may hold weight stages): 4 bytes through L1, or 16 bytes from L2 (data other SMs wrote
-// during this kernel); the thread's copies are complete after cp_async_wait_all()
+// asynchronous 4-byte copy global -> shared through the load path (not the bulk-copy engine,
+// whose queue may hold weight stages); the thread's copies are complete after
+// cp_async_wait_all()
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16_l2(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
@@ -242,11 +239,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// bring [src, src+bytes) into L2 (bulk prefetch; src 16-byte aligned, bytes a multiple of 16)
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
