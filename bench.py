@@ -445,12 +445,12 @@ def run_coli(args):
         xh = pool[:64].cpu().pin_memory()
         yh = torch.empty((T, wl.d), dtype=torch.float32).pin_memory()
         n_e2e = min(args.steps, 2000)
-        for i in range(20):
-            layers[0].forward_host(xh[i % 64], yh)
+        for i in range(min(20, max(3, args.warmup))):
+            layers[0].forward_host(xh[i % len(xh)], yh)
         barrier(world)
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            layers[0].forward_host(xh[i % 64], yh)
+            layers[0].forward_host(xh[i % len(xh)], yh)
         el = reduce_max(time.perf_counter() - t0, world)
         out["e2e"] = {"value": world * n_e2e * T / el, "unit": "tokens/s",
                       "h2d_bytes_per_step": T * wl.d * 4, "d2h_bytes_per_step": T * wl.d * 4,
@@ -461,7 +461,7 @@ def run_coli(args):
         barrier(world)
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            xs.copy_(xh[i % 64], non_blocking=True)
+            xs.copy_(xh[i % len(xh)], non_blocking=True)
             coli.stack_forward(layers, xs)
             yh = xs.to("cpu")
         el = reduce_max(time.perf_counter() - t0, world)
