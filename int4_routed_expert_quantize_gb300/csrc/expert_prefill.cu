@@ -13,7 +13,8 @@
 //
 // CTA: 15 warps, one tile (128 weight rows x 64 pairs) at a time, persistent over tiles:
 //   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream, deep ring)
-//   warp 1      bulk-tensor copies of the bf16 activation block of each K-step
+//   warp 1      bulk-tensor copies of the bf16 activation block of each K-step (completing on
+//               the same barrier as the converted weights, so the MMA issuer waits once)
 //   warps 2-5   int4 -> bf16 conversion of the weight block into the MMA's shared layout
 //   warp 6      TMEM owner and single MMA issuer (2 x K16 MMAs per K-block, 3 accumulator buffers)
 //   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
@@ -58,8 +59,7 @@ struct PfSmem {
   float* us;   // [64][64] u values, column-major (gate/up only)
   uint64_t* raw_full;
   uint64_t* raw_empty;
-  uint64_t* a_full;
-  uint64_t* b_full;
+  uint64_t* a_full;    // the K-block's converted weights and activation block are in
   uint64_t* ab_empty;
   uint64_t* acc_full;
   uint64_t* acc_empty;
@@ -86,8 +86,7 @@ __device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
   m.raw_full = bars;
   m.raw_empty = bars + kPfRawStages;
   m.a_full = m.raw_empty + kPfRawStages;
-  m.b_full = m.a_full + kPfStages;
-  m.ab_empty = m.b_full + kPfStages;
+  m.ab_empty = m.a_full + kPfStages;
   m.acc_full = m.ab_empty + kPfStages;
   m.acc_empty = m.acc_full + kPfAcc;
   m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfAcc);
@@ -102,7 +101,7 @@ int prefill_smem_bytes(int d, int f, int E, int down) {
   const int nb = K / kQB, G = (nb + 31) / 32;
   const int raw = kPfM * G * 16;
   const int dx = nb * kPfN * 4;
-  const int bars = (2 * kPfRawStages + 3 * kPfStages + 2 * kPfAcc) * 8 + 16;
+  const int bars = (2 * kPfRawStages + 2 * kPfStages + 2 * kPfAcc) * 8 + 16;
   const int tabs = 3 * (E + 2) * 4;
   return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfN * 64 * 4) +
          bars + tabs;
@@ -169,8 +168,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&m.raw_empty[i], 4);
     }
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&m.a_full[i], 4);
-      mbar_init(&m.b_full[i], 1);
+      mbar_init(&m.a_full[i], 5);  // 4 converter warps + the activation loader (expect_tx)
       mbar_init(&m.ab_empty[i], 1);
     }
     for (int i = 0; i < kPfAcc; ++i) {
@@ -230,10 +228,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (n > 0 && !mbar_wait_bounded(&m.ab_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
             break;
           uint8_t* dst = m.b + (long)s * kPfBStage;
-          mbar_expect_tx(&m.b_full[s], (uint32_t)kPfBStage);
+          mbar_expect_tx(&m.a_full[s], (uint32_t)kPfBStage);
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc)
-            tma_load_2d(dst + kc * (kPfN * 16), &map_x, b * 32 + kc * 8, row0, &m.b_full[s]);
+            tma_load_2d(dst + kc * (kPfN * 16), &map_x, b * 32 + kc * 8, row0, &m.a_full[s]);
         }
       }
     }
@@ -281,8 +279,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int b = 0; b < nb; ++b, ++kb) {
           const int s = (int)(kb % kPfStages);
           const uint32_t ph = (uint32_t)((kb / kPfStages) & 1);
+          // both operands of the K-block: the converted weights and the activation block
           bool ok = mbar_wait_bounded(&m.a_full[s], ph, &abort_flag, status);
-          ok = mbar_wait_bounded(&m.b_full[s], ph, &abort_flag, status) && ok;
           if (kb >= kPfAcc) ok = mbar_wait_bounded(&m.acc_empty[ab], aph ^ 1u, &abort_flag, status) && ok;
           const int abuf = ab;
           if (++ab == kPfAcc) {
