@@ -225,18 +225,22 @@ def cpu_baseline(wl, seconds):
     # generate the experts of the candidate sample outside the timing
     _, ids, _ = O.route_only(wl, x[: 16 * wl.T], OL.Wr, OL.bias, OL.gamma)
     OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
+    # the 16 batches' experts are generated once; the timed loop cycles over those batches until
+    # the time budget is spent (each token streams all its experts' bytes, far more than the
+    # host's caches hold, so repeating a batch does not make it cheaper)
     t0 = time.perf_counter()
     done = 0
     while True:
-        OL.forward(x[done * wl.T:(done + 1) * wl.T], want_dump=False, want_y64=False)
+        j = done % 16
+        OL.forward(x[j * wl.T:(j + 1) * wl.T], want_dump=False, want_y64=False)
         done += 1
         el = time.perf_counter() - t0
-        if (el >= seconds and done >= ntok) or done >= 16:
+        if el >= seconds and done >= ntok:
             break
     return {"value": done * wl.T / el, "unit": "tokens/s", "cores": O.lib().orc_num_threads(),
             "kind": "oracle",
-            "sample": f"{done} batches of T={wl.T} token(s) of {wl.name} through the full layer "
-                      f"(experts pre-generated), {el:.1f} s"}
+            "sample": f"{done} batches of T={wl.T} token(s) of {wl.name} (16 distinct batches, "
+                      f"cycled) through the full layer (experts pre-generated), {el:.1f} s"}
 
 
 def run_reference(args):
