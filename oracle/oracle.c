@@ -209,6 +209,62 @@ void orc_i4_matvec(const uint8_t* W, const float* s, int rows, int cols, const i
 }
 
 /* ------------------------------------------------------------------------------------------
+ * int8 rows.  P1 §3.1: "int8 (dense and MTP-head precision)", one value per byte
+ * (quantize_rows), and the IDOT fast path's integer dot of int8 weights with int8 activation
+ * codes (dot_i8i8).  Reading (the pages say no more): one f32 scale per row, symmetric
+ * s = max|w| / 127, code = round(w / s) half away from zero clamped to [-127, 127], as for the
+ * int4 rows and the activation blocks; an all-zero row has s = 0 and codes 0.
+ * ---------------------------------------------------------------------------------------- */
+void orc_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q, float* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* wr = w + r * cols;
+    float amax = 0.0f;
+    for (int j = 0; j < cols; ++j) {
+      float a = fabsf(wr[j]);
+      if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    const int lim = ORC_MUTANT == 13 ? 126 : 127;
+    for (int j = 0; j < cols; ++j) {
+      int v = 0;
+      if (s != 0.0f) {
+        v = (int)roundf(wr[j] / s);
+        if (v > lim) v = lim;
+        if (v < -lim) v = -lim;
+      }
+      q[r * cols + j] = (int8_t)v;
+    }
+    scales[r] = s;
+  }
+}
+
+/* Integer dot of block b (32 elements) of an int8 row with int8 activation codes; exact in
+ * int32: |sum| <= 32 * 127 * 127. */
+int32_t orc_i8_block_dot(const int8_t* wrow, const int8_t* qx, int b) {
+  int32_t acc = 0;
+  const int end = (b + 1) * QB - (ORC_MUTANT == 14 ? 1 : 0);
+  for (int j = b * QB; j < end; ++j) acc += (int32_t)wrow[j] * (int32_t)qx[j];
+  return acc;
+}
+
+/* out[r] = s[r] * canon_blocksum(dx, A[r, :]) with A[r,b] = i8_block_dot(row r, b): the int8
+ * counterpart of orc_i4_matvec (same canonical fp32 epilogue). */
+void orc_i8_matvec(const int8_t* W, const float* s, int rows, int cols, const int8_t* qx,
+                   const float* dx, float* out, int32_t* A) {
+  const int nb = cols / QB;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    int32_t* Ar = (int32_t*)malloc(sizeof(int32_t) * (size_t)nb);
+    const int8_t* wrow = W + (int64_t)r * cols;
+    for (int b = 0; b < nb; ++b) Ar[b] = orc_i8_block_dot(wrow, qx, b);
+    out[r] = s[r] * orc_canon_blocksum(dx, Ar, nb);
+    if (A) memcpy(A + (int64_t)r * nb, Ar, sizeof(int32_t) * (size_t)nb);
+    free(Ar);
+  }
+}
+
+/* ------------------------------------------------------------------------------------------
  * Router.  P1 §5 (moe step: sigmoid routing, pick the top-8 experts) and P3 (DeepSeek-V3-style
  * sigmoid router).  Readings: the optional per-expert bias changes only which experts are
  * selected (DeepSeek-V3 semantics); weights come from the unbiased scores, renormalised over

@@ -96,6 +96,14 @@ float orc_canon_blocksum(const float* d, const int32_t* A, int nb);
 /* ---- integer dot of one 32-element block (P1 §4 dot_i4i8) ---- */
 int32_t orc_block_dot(const uint8_t* wrow, const int8_t* qx, int b);
 
+/* int8 rows (P1 §3.1 "int8", quantize_rows / dot_i8i8): one f32 scale per row, s = max|w|/127,
+ * codes round(w/s) half away from zero in [-127, 127]; block dots exact in int32; the matvec
+ * applies the same canonical fp32 epilogue as the int4 one. */
+void orc_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q, float* scales);
+int32_t orc_i8_block_dot(const int8_t* wrow, const int8_t* qx, int b);
+void orc_i8_matvec(const int8_t* W, const float* s, int rows, int cols, const int8_t* qx,
+                   const float* dx, float* out, int32_t* A);
+
 /* ---- int4 x int8 matrix-vector product with dequant-on-use (P1 §3.1, matmul_i4 + IDOT) ---- */
 void orc_i4_matvec(const uint8_t* W, const float* s, int rows, int cols, const int8_t* qx,
                    const float* dx, float* out, int32_t* A);

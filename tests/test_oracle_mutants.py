@@ -26,6 +26,10 @@ MUTANTS = {
     10: ("RMSNorm without eps", ["test_rmsnorm_closed_form"]),
     11: ("bucket records the wrong rank", ["test_union_bucket_brute_force"]),
     12: ("block dot pairs block b with block nb-1-b", ["test_matvec_accumulators_brute_force"]),
+    13: ("int8 row codes clamped to 126", ["test_int8_row_quant_bounds", "test_int8_row_quant_golden",
+                                            "test_int8_codes_round_trip_exhaustively"]),
+    14: ("int8 block dot drops the block's last element", ["test_i8_block_dot_brute_force",
+                                                           "test_i8_matvec_accumulators_brute_force"]),
 }
 
 

@@ -187,6 +187,78 @@ def test_matvec_accumulators_brute_force():
     assert np.all(np.abs(out.astype(np.float64) - exact) <= bound)
 
 
+# ------------------------------------------------------------------ int8 rows ----------
+
+def test_int8_row_quant_golden():
+    g = golden("int8_row_quant.json")
+    w = np.array([g["w"]], dtype=np.float32)
+    q, s = O.quantize_i8_rows(w)
+    assert s[0] == np.float32(np.float32(1.27) / np.float32(127))
+    assert q[0].tolist() == g["codes"]
+
+
+def test_int8_row_quant_bounds():
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal((64, 256)) * rng.uniform(0.001, 3, (64, 1))).astype(np.float32)
+    w[5] = 0.0
+    q8, s = O.quantize_i8_rows(w)
+    q = q8.astype(np.float64)
+    amax = np.abs(w).max(axis=1)
+    assert np.array_equal(s, (amax / np.float32(127)).astype(np.float32))
+    assert s[5] == 0 and np.all(q[5] == 0)
+    assert q.min() >= -127 and q.max() <= 127
+    live = s > 0
+    err = np.abs(w[live].astype(np.float64) - s[live, None].astype(np.float64) * q[live])
+    assert np.all(err <= s[live, None] * (0.5 + 1e-5))
+    # the largest magnitude of every live row lands on +-127 with its sign
+    arg = np.abs(w).argmax(axis=1)
+    ext = q[np.arange(64), arg]
+    assert np.all(np.abs(ext[live]) == 127)
+    assert np.all(np.sign(ext[live]) == np.sign(w[np.arange(64), arg][live]))
+
+
+def test_int8_codes_round_trip_exhaustively():
+    # a row holding every code -127..127 times a power-of-two step is reproduced exactly
+    codes = np.arange(-127, 128, dtype=np.float32)
+    w = (codes * np.float32(2.0 ** -7)).reshape(1, -1)
+    w = np.concatenate([w, np.zeros((1, 1), np.float32)], axis=1)  # 256 columns
+    q, s = O.quantize_i8_rows(w)
+    assert s[0] == np.float32(2.0 ** -7)
+    assert np.array_equal(q[0, :255].astype(np.int64), codes.astype(np.int64))
+
+
+def test_i8_block_dot_brute_force():
+    rng = np.random.default_rng(12)
+    cols = 256
+    W = rng.integers(-127, 128, (16, cols), dtype=np.int8)
+    W[0] = -127
+    qx = rng.integers(-127, 128, cols, dtype=np.int8)
+    qx[:32] = -127
+    for r in range(16):
+        for b in range(cols // 32):
+            ref = int(np.sum(W[r, 32 * b:32 * b + 32].astype(np.int64) * qx[32 * b:32 * b + 32].astype(np.int64)))
+            assert O.lib().orc_i8_block_dot(W[r].ctypes.data, qx.ctypes.data, b) == ref
+    assert O.lib().orc_i8_block_dot(W[0].ctypes.data, qx.ctypes.data, 0) == 32 * 127 * 127
+
+
+def test_i8_matvec_accumulators_brute_force():
+    rng = np.random.default_rng(13)
+    rows, cols = 40, 512
+    W = rng.integers(-127, 128, (rows, cols), dtype=np.int8)
+    s = rng.uniform(0.0001, 0.001, rows).astype(np.float32)
+    x = rng.standard_normal(cols).astype(np.float32)
+    qx, dx = O.quantize_q8(x)
+    out, A = O.i8_matvec(W, s, cols, qx, dx, want_A=True)
+    ref = (W.astype(np.int64).reshape(rows, -1, 32) * qx.astype(np.int64).reshape(1, -1, 32)).sum(axis=2)
+    assert np.array_equal(A, ref)
+    # fp64 value from the same integers, within the canonical sum's rounding bound
+    exact = s.astype(np.float64) * (ref * dx.astype(np.float64)).sum(axis=1)
+    mag = np.abs(s.astype(np.float64)) * (np.abs(ref) * dx.astype(np.float64)).sum(axis=1)
+    nb = cols // 32
+    bound = (math.ceil(nb / 32) + 5 + 2) * EPS32 * mag
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= bound)
+
+
 # ------------------------------------------------------------------ canonical fp32 -----
 
 def ulp32(v):
