@@ -8,11 +8,14 @@
 //  * the producer lane keeps streaming: after its CTA's last gate/up stage it issues the CTA's
 //    down stages into the same ring, so they arrive while the last gate/up stages are consumed
 //    and while the CTA waits at the barrier;
-//  * the down phase reuses the CTA's selection (no second selection, no second launch);
+//  * the down phase reuses the CTA's selection (no second selection, no second launch), and
+//    the CTA's down-row scales are copied asynchronously right after the selection;
 //  * the down phase's buffers overlay the gate/up phase's token and table buffers.
 // The barrier is a counter in the workspace (cleared by the router grid each call) that every
-// CTA increments and then polls with a bounded wait; grid <= SM count with one CTA per SM, so
-// all of its CTAs are resident together once the router grid ahead of it has retired.
+// CTA increments; while it waits for the others a CTA runs one dry down stage (bringing that
+// loop's instructions into its caches), then polls with a bounded wait.  grid <= SM count with
+// one CTA per SM, so all of its CTAs are resident together once the router grid ahead of it
+// has retired.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
