@@ -265,6 +265,81 @@ void orc_i8_matvec(const int8_t* W, const float* s, int rows, int cols, const in
 }
 
 /* ------------------------------------------------------------------------------------------
+ * int2 rows.  P1 §3.1 "int2 packed (experimental)": four 2-bit values per byte (pack_int2),
+ * used by matmul_i2 with dequant-on-use.  Readings (the pages say no more):
+ *   - one f32 scale per row and symmetric codes, as for int4: s = max|w| / 1 (the largest
+ *     symmetric 2-bit code is 1, as 7 is for 4 bits), code = round(w / s) half away from zero
+ *     clamped to [-1, 1]; an all-zero row has s = 0 and codes 0;
+ *   - two's-complement 2-bit fields; the pattern 10 (-2) is never written but decodes;
+ *   - element 4i+k in bits 2k..2k+1 of byte i (lowest bits first, as the int4 low nibble);
+ *   - the matvec takes the int4 rows' IDOT route: int8 activation codes in blocks of 32,
+ *     exact int32 block dots, the same canonical fp32 epilogue.
+ * ---------------------------------------------------------------------------------------- */
+int orc_i2_get(const uint8_t* row, int j) {
+  const int k = ORC_MUTANT == 15 ? 3 - (j & 3) : (j & 3);
+  const int code = (row[j >> 2] >> (2 * k)) & 3;
+  return (code >= 2 && ORC_MUTANT != 16) ? code - 4 : code;
+}
+
+void orc_pack_i2_row(const int8_t* q, int cols, uint8_t* packed_row) {
+  for (int i = 0; i < cols / 4; ++i) {
+    int byte = 0;
+    for (int k = 0; k < 4; ++k) byte |= (q[4 * i + k] & 3) << (2 * k);
+    packed_row[i] = (uint8_t)byte;
+  }
+}
+
+void orc_quantize_i2_rows(const float* w, int64_t rows, int cols, uint8_t* packed, float* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* wr = w + r * cols;
+    float amax = 0.0f;
+    for (int j = 0; j < cols; ++j) {
+      float a = fabsf(wr[j]);
+      if (a > amax) amax = a;
+    }
+    const float s = amax / (ORC_MUTANT == 17 ? 2.0f : 1.0f);
+    int8_t* q = (int8_t*)malloc((size_t)cols);
+    for (int j = 0; j < cols; ++j) {
+      int v = 0;
+      if (s != 0.0f) {
+        v = (int)roundf(wr[j] / s);
+        if (v > 1) v = 1;
+        if (v < -1) v = -1;
+      }
+      q[j] = (int8_t)v;
+    }
+    orc_pack_i2_row(q, cols, packed + r * (cols / 4));
+    free(q);
+    scales[r] = s;
+  }
+}
+
+/* Integer dot of block b (32 elements) of an int2 row with int8 activation codes; exact in
+ * int32: |sum| <= 32 * 2 * 127. */
+int32_t orc_i2_block_dot(const uint8_t* wrow, const int8_t* qx, int b) {
+  int32_t acc = 0;
+  for (int j = b * QB; j < (b + 1) * QB; ++j) acc += orc_i2_get(wrow, j) * (int32_t)qx[j];
+  return acc;
+}
+
+/* out[r] = s[r] * canon_blocksum(dx, A[r, :]) with A[r,b] = i2_block_dot(row r, b): the int2
+ * counterpart of orc_i4_matvec; the rows stay packed (dequant-on-use). */
+void orc_i2_matvec(const uint8_t* W, const float* s, int rows, int cols, const int8_t* qx,
+                   const float* dx, float* out, int32_t* A) {
+  const int nb = cols / QB;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    int32_t* Ar = (int32_t*)malloc(sizeof(int32_t) * (size_t)nb);
+    const uint8_t* wrow = W + (int64_t)r * (cols / 4);
+    for (int b = 0; b < nb; ++b) Ar[b] = orc_i2_block_dot(wrow, qx, b);
+    out[r] = s[r] * orc_canon_blocksum(dx, Ar, nb);
+    if (A) memcpy(A + (int64_t)r * nb, Ar, sizeof(int32_t) * (size_t)nb);
+    free(Ar);
+  }
+}
+
+/* ------------------------------------------------------------------------------------------
  * Router.  P1 §5 (moe step: sigmoid routing, pick the top-8 experts) and P3 (DeepSeek-V3-style
  * sigmoid router).  Readings: the optional per-expert bias changes only which experts are
  * selected (DeepSeek-V3 semantics); weights come from the unbiased scores, renormalised over

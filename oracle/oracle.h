@@ -104,6 +104,17 @@ int32_t orc_i8_block_dot(const int8_t* wrow, const int8_t* qx, int b);
 void orc_i8_matvec(const int8_t* W, const float* s, int rows, int cols, const int8_t* qx,
                    const float* dx, float* out, int32_t* A);
 
+/* int2 rows (P1 §3.1 "int2 packed", pack_int2 / matmul_i2): four 2-bit two's-complement codes
+ * per byte, element 4i+k in bits 2k..2k+1 of byte i; one f32 scale per row, s = max|w|,
+ * codes round(w/s) half away from zero in [-1, 1] (-2 decodes but is never written); block
+ * dots with int8 activation codes exact in int32; the matvec's fp32 epilogue is the int4 one. */
+int orc_i2_get(const uint8_t* row, int j);
+void orc_pack_i2_row(const int8_t* q, int cols, uint8_t* packed_row);
+void orc_quantize_i2_rows(const float* w, int64_t rows, int cols, uint8_t* packed, float* scales);
+int32_t orc_i2_block_dot(const uint8_t* wrow, const int8_t* qx, int b);
+void orc_i2_matvec(const uint8_t* W, const float* s, int rows, int cols, const int8_t* qx,
+                   const float* dx, float* out, int32_t* A);
+
 /* ---- int4 x int8 matrix-vector product with dequant-on-use (P1 §3.1, matmul_i4 + IDOT) ---- */
 void orc_i4_matvec(const uint8_t* W, const float* s, int rows, int cols, const int8_t* qx,
                    const float* dx, float* out, int32_t* A);

@@ -71,6 +71,13 @@ def lib():
         L.orc_i8_block_dot.argtypes = [_vp, _vp, _i]
         L.orc_i8_block_dot.restype = ctypes.c_int32
         L.orc_i8_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp]
+        L.orc_i2_get.argtypes = [_vp, _i]
+        L.orc_i2_get.restype = _i
+        L.orc_pack_i2_row.argtypes = [_vp, _i, _vp]
+        L.orc_quantize_i2_rows.argtypes = [_vp, _i64, _i, _vp, _vp]
+        L.orc_i2_block_dot.argtypes = [_vp, _vp, _i]
+        L.orc_i2_block_dot.restype = ctypes.c_int32
+        L.orc_i2_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp]
         L.orc_topk.argtypes = [_vp, _i, _i, _vp]
         L.orc_route_token.argtypes = [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp]
         L.orc_rmsnorm.argtypes = [_vp, _vp, _i, _f, _vp]
@@ -115,6 +122,16 @@ def quantize_i8_rows(w):
     scales = np.empty(rows, dtype=np.float32)
     lib().orc_quantize_i8_rows(w.ctypes.data, rows, cols, q.ctypes.data, scales.ctypes.data)
     return q, scales
+
+
+def quantize_i2_rows(w):
+    """int2 rows (four codes per byte) and one f32 scale per row"""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    packed = np.empty((rows, cols // 4), dtype=np.uint8)
+    scales = np.empty(rows, dtype=np.float32)
+    lib().orc_quantize_i2_rows(w.ctypes.data, rows, cols, packed.ctypes.data, scales.ctypes.data)
+    return packed, scales
 
 
 def quantize_q8(x):
@@ -165,6 +182,16 @@ def i8_matvec(W, s, cols, qx, dx, want_A=False):
     out = np.empty(rows, dtype=np.float32)
     A = np.empty((rows, cols // QB), dtype=np.int32) if want_A else None
     lib().orc_i8_matvec(W.ctypes.data, s.ctypes.data, rows, cols, qx.ctypes.data, dx.ctypes.data,
+                        out.ctypes.data, _p(A))
+    return out, A
+
+
+def i2_matvec(W, s, cols, qx, dx, want_A=False):
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    rows = W.shape[0]
+    out = np.empty(rows, dtype=np.float32)
+    A = np.empty((rows, cols // QB), dtype=np.int32) if want_A else None
+    lib().orc_i2_matvec(W.ctypes.data, s.ctypes.data, rows, cols, qx.ctypes.data, dx.ctypes.data,
                         out.ctypes.data, _p(A))
     return out, A
 

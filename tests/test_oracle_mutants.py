@@ -30,6 +30,11 @@ MUTANTS = {
                                             "test_int8_codes_round_trip_exhaustively"]),
     14: ("int8 block dot drops the block's last element", ["test_i8_block_dot_brute_force",
                                                            "test_i8_matvec_accumulators_brute_force"]),
+    15: ("int2 fields read from the high bits down", ["test_int2_decode_golden", "test_int2_pack_exhaustive",
+                                                       "test_i2_block_dot_brute_force"]),
+    16: ("int2 codes not sign-extended", ["test_int2_decode_golden", "test_int2_pack_exhaustive",
+                                          "test_i2_matvec_accumulators_brute_force"]),
+    17: ("int2 row scale max|w|/2", ["test_int2_row_quant_golden", "test_int2_row_quant_bounds"]),
 }
 
 

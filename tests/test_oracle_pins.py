@@ -259,6 +259,121 @@ def test_i8_matvec_accumulators_brute_force():
     assert np.all(np.abs(out.astype(np.float64) - exact) <= bound)
 
 
+# ------------------------------------------------------------------ int2 rows ---------
+
+def decode_i2(packed):
+    """independent int2 decode: two's-complement 2-bit fields, lowest bits = element 4i"""
+    p = packed.astype(np.int16)
+    out = np.empty(packed.shape[:-1] + (packed.shape[-1] * 4,), dtype=np.int16)
+    for k in range(4):
+        c = (p >> (2 * k)) & 3
+        out[..., k::4] = np.where(c >= 2, c - 4, c)
+    return out
+
+
+def test_int2_decode_golden():
+    for case in golden("int2_rows.json")["decode"]:
+        row = np.array([case["byte"]], dtype=np.uint8)
+        got = [O.lib().orc_i2_get(row.ctypes.data, k) for k in range(4)]
+        assert got == case["codes"], case["why"]
+
+
+def test_int2_row_quant_golden():
+    rows = golden("int2_rows.json")["rows"]
+    w = np.array([r["w"] for r in rows], dtype=np.float32)
+    packed, s = O.quantize_i2_rows(w)
+    assert s.tolist() == [float(np.float32(0.3)), 1.0, 0.0]
+    for i, r in enumerate(rows):
+        assert packed[i].tolist() == r["bytes"], r["why"]
+        got = [O.lib().orc_i2_get(packed[i].ctypes.data, j) for j in range(8)]
+        assert got == r["codes"], r["why"]
+
+
+def test_int2_pack_exhaustive():
+    """all 256 four-code tuples over [-2, 1] pack into distinct bytes and decode back"""
+    codes = np.array([(a, b, c, e) for a in range(-2, 2) for b in range(-2, 2)
+                      for c in range(-2, 2) for e in range(-2, 2)], dtype=np.int8).ravel()
+    packed = np.empty(codes.size // 4, dtype=np.uint8)
+    O.lib().orc_pack_i2_row(codes.ctypes.data, codes.size, packed.ctypes.data)
+    assert sorted(packed.tolist()) == list(range(256))
+    assert np.array_equal(decode_i2(packed), codes)
+    got = np.array([O.lib().orc_i2_get(packed.ctypes.data, j) for j in range(codes.size)])
+    assert np.array_equal(got, codes)
+
+
+def test_int2_row_quant_bounds():
+    rng = np.random.default_rng(14)
+    w = (rng.standard_normal((64, 256)) * rng.uniform(0.001, 3, (64, 1))).astype(np.float32)
+    w[9] = 0.0
+    packed, s = O.quantize_i2_rows(w)
+    q = decode_i2(packed).astype(np.float64)
+    amax = np.abs(w).max(axis=1)
+    assert np.array_equal(s, amax)
+    assert s[9] == 0 and np.all(q[9] == 0)
+    assert q.min() >= -1 and q.max() <= 1
+    live = s > 0
+    err = np.abs(w[live].astype(np.float64) - s[live, None].astype(np.float64) * q[live])
+    assert np.all(err <= s[live, None] * (0.5 + 1e-6))
+    arg = np.abs(w).argmax(axis=1)
+    ext = q[np.arange(64), arg]
+    assert np.all(ext[live] == np.sign(w[np.arange(64), arg][live]))
+
+
+def test_i2_block_dot_brute_force():
+    rng = np.random.default_rng(15)
+    cols = 256
+    W = rng.integers(0, 256, (16, cols // 4), dtype=np.uint8)  # every field pattern, -2 included
+    W[0] = 0xAA
+    qx = rng.integers(-127, 128, cols, dtype=np.int8)
+    qx[:32] = -127
+    Wd = decode_i2(W).astype(np.int64)
+    for r in range(16):
+        for b in range(cols // 32):
+            ref = int(np.sum(Wd[r, 32 * b:32 * b + 32] * qx[32 * b:32 * b + 32].astype(np.int64)))
+            assert O.lib().orc_i2_block_dot(W[r].ctypes.data, qx.ctypes.data, b) == ref
+    assert O.lib().orc_i2_block_dot(W[0].ctypes.data, qx.ctypes.data, 0) == 32 * 2 * 127
+
+
+def test_i2_matvec_accumulators_brute_force():
+    rng = np.random.default_rng(16)
+    rows, cols = 40, 512
+    W = rng.integers(0, 256, (rows, cols // 4), dtype=np.uint8)
+    s = rng.uniform(0.0001, 0.001, rows).astype(np.float32)
+    x = rng.standard_normal(cols).astype(np.float32)
+    qx, dx = O.quantize_q8(x)
+    out, A = O.i2_matvec(W, s, cols, qx, dx, want_A=True)
+    ref = (decode_i2(W).astype(np.int64).reshape(rows, -1, 32)
+           * qx.astype(np.int64).reshape(1, -1, 32)).sum(axis=2)
+    assert np.array_equal(A, ref)
+    exact = s.astype(np.float64) * (ref * dx.astype(np.float64)).sum(axis=1)
+    mag = np.abs(s.astype(np.float64)) * (np.abs(ref) * dx.astype(np.float64)).sum(axis=1)
+    nb = cols // 32
+    bound = (math.ceil(nb / 32) + 5 + 2) * EPS32 * mag
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= bound)
+
+
+def test_i2_i4_i8_rows_of_equal_codes_agree():
+    """codes in [-1, 1] stored as int2, int4 and int8 rows give the same accumulators and the
+    same fp32 outputs: the three formats differ only in how a code is stored"""
+    rng = np.random.default_rng(17)
+    rows, cols = 24, 1024
+    codes = rng.integers(-1, 2, (rows, cols), dtype=np.int8)
+    s = rng.uniform(0.001, 0.01, rows).astype(np.float32)
+    x = rng.standard_normal(cols).astype(np.float32)
+    qx, dx = O.quantize_q8(x)
+    p2 = np.empty((rows, cols // 4), dtype=np.uint8)
+    p4 = np.empty((rows, cols // 2), dtype=np.uint8)
+    for r in range(rows):
+        O.lib().orc_pack_i2_row(codes[r].ctypes.data, cols, p2[r].ctypes.data)
+        O.lib().orc_pack_i4_row(codes[r].ctypes.data, cols, p4[r].ctypes.data)
+    o2, A2 = O.i2_matvec(p2, s, cols, qx, dx, want_A=True)
+    o4, A4 = O.i4_matvec(p4, s, cols, qx, dx, want_A=True)
+    o8, A8 = O.i8_matvec(codes, s, cols, qx, dx, want_A=True)
+    assert np.array_equal(A2, A8) and np.array_equal(A4, A8)
+    assert np.array_equal(o2.view(np.uint32), o8.view(np.uint32))
+    assert np.array_equal(o4.view(np.uint32), o8.view(np.uint32))
+
+
 # ------------------------------------------------------------------ canonical fp32 -----
 
 def ulp32(v):
