@@ -50,6 +50,7 @@ extern "C" {
 #define COLI_ECUDA (-4)        /* a CUDA runtime call or kernel launch failed              */
 #define COLI_ETIMEOUT (-5)     /* a bounded device-side wait gave up (see coli_moe_status) */
 #define COLI_EUNSUPPORTED (-6) /* shape the kernels do not cover (see coli_moe_create)     */
+#define COLI_EIO (-7)          /* a file could not be opened, read or written in full       */
 
 typedef struct coli_moe coli_moe; /* opaque; owned by the library */
 

@@ -1,4 +1,5 @@
-"""Build of libcoli_moe.so: nvcc for sm_103a, one object per source compiled in parallel."""
+"""Build of libcoli_moe.so: nvcc for sm_103a (the host-only tier manager through nvcc's host
+compiler), one object per source compiled in parallel."""
 import os
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -10,7 +11,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "libcoli_moe.so")
 SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "expert_fused.cu", "expert_prefill.cu",
-           "runtime.cu", "noalloc.cu"]
+           "runtime.cu", "noalloc.cu", "tier.cpp"]
 
 
 def nvcc_flags(arch="sm_103a"):
@@ -24,7 +25,7 @@ def build(arch="sm_103a", verbose=False, extra=()):
     flags = nvcc_flags(arch) + list(extra)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = ["nvcc"] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))

@@ -5,8 +5,11 @@ PyTorch supplies device memory and streams.  If the shared library is missing th
 `lib()` raises: there is no CPU fallback.
 """
 import ctypes
+import glob
 import os
 import re
+
+import numpy as np
 
 import torch
 
@@ -15,7 +18,7 @@ from . import _build
 _i, _f, _vp, _i64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int64
 
 STATUS = {0: "COLI_OK", -1: "COLI_EINVAL", -2: "COLI_ENOMEM", -3: "COLI_ESTATE", -4: "COLI_ECUDA",
-          -5: "COLI_ETIMEOUT", -6: "COLI_EUNSUPPORTED"}
+          -5: "COLI_ETIMEOUT", -6: "COLI_EUNSUPPORTED", -7: "COLI_EIO"}
 HEADER = os.path.join(_build.INCLUDE, "coli_moe.h")
 ETIMEOUT = -5
 FAULT_SKIP_ARRIVAL = 1  # coli_moe_inject_fault: the next fused forward leaves CTA 0 out of its barrier
@@ -33,6 +36,10 @@ class Config(ctypes.Structure):
                 ("has_norm", _i)]
 
 
+class TierConfig(ctypes.Structure):
+    _fields_ = [("n_layers", _i), ("n_experts", _i), ("n_pin", _i), ("n_lru", _i)]
+
+
 DUMP_FIELDS = ["xn", "qx", "dx", "logits", "scores", "ids", "w", "n_union", "union_ids", "offsets",
                "pair_token", "pair_rank", "inv", "g", "u", "h", "qh", "dh", "e", "Ag", "Au", "Ad"]
 
@@ -45,8 +52,8 @@ _lib = None
 
 
 def header_functions():
-    """names of the functions include/coli_moe.h declares"""
-    text = open(HEADER).read()
+    """names of the functions the headers under include/ declare"""
+    text = "".join(open(h).read() for h in sorted(glob.glob(os.path.join(_build.INCLUDE, "*.h"))))
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(coli_\w+)\s*\(", text, re.M)))
 
 
@@ -76,6 +83,19 @@ def lib():
         L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
         L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
         L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
+        _ip = ctypes.POINTER(_i)
+        L.coli_tier_create.argtypes = [ctypes.POINTER(TierConfig), ctypes.POINTER(_vp)]
+        L.coli_tier_destroy.argtypes = [_vp]
+        L.coli_tier_destroy.restype = None
+        L.coli_tier_lookup.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _ip, _vp, _vp, _ip]
+        L.coli_tier_prefetch.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+        L.coli_tier_repin.argtypes = [_vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+        L.coli_tier_state.argtypes = [_vp, _i, _vp, _ip, _vp, _ip, _vp]
+        L.coli_tier_heat.argtypes = [_vp, _i, _vp]
+        L.coli_tier_set_heat.argtypes = [_vp, _i, _vp]
+        L.coli_tier_stats.argtypes = [_vp, _vp]
+        L.coli_tier_save_usage.argtypes = [_vp, ctypes.c_char_p]
+        L.coli_tier_load_usage.argtypes = [_vp, ctypes.c_char_p]
         L.coli_moe_strerror.argtypes = [_i]
         L.coli_moe_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -248,3 +268,116 @@ def quantize_act_q8(x, stream=None):
     _check(lib().coli_quantize_act_q8(_ptr(x), x.numel(), _ptr(q), _ptr(d), _stream(stream)),
            "coli_quantize_act_q8")
     return q, d
+
+
+TIER_STATS = ("pin_hits", "lru_hits", "misses", "evictions", "prefetch_fetches", "prefetch_used",
+              "prefetch_wasted", "repin_fetches")
+
+
+class Tier:
+    """Expert residency tiers of n_layers MoE layers (include/coli_tier.h): host-side decisions
+    of which expert records sit in which HBM slots; the caller moves the data."""
+
+    def __init__(self, n_layers, n_experts, n_pin, n_lru):
+        self.cfg = TierConfig(n_layers, n_experts, n_pin, n_lru)
+        h = _vp()
+        _check(lib().coli_tier_create(ctypes.byref(self.cfg), ctypes.byref(h)), "coli_tier_create")
+        self.h = h
+        self.n_layers, self.n_experts, self.n_pin, self.n_lru = n_layers, n_experts, n_pin, n_lru
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            lib().coli_tier_destroy(self.h)
+            self.h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _ids(ids):
+        return np.ascontiguousarray(ids, dtype=np.int32)
+
+    def lookup(self, layer, ids):
+        """-> dict(cls, slot, fetch_ids, fetch_slots, evict_ids, evict_slots) as int32 arrays"""
+        ids = self._ids(ids)
+        n = ids.size
+        out = {k: np.empty(n, np.int32) for k in
+               ("cls", "slot", "fetch_ids", "fetch_slots", "evict_ids", "evict_slots")}
+        nf, ne = _i(), _i()
+        _check(lib().coli_tier_lookup(self.h, layer, ids.ctypes.data, n, out["cls"].ctypes.data,
+                                      out["slot"].ctypes.data, out["fetch_ids"].ctypes.data,
+                                      out["fetch_slots"].ctypes.data, ctypes.byref(nf),
+                                      out["evict_ids"].ctypes.data, out["evict_slots"].ctypes.data,
+                                      ctypes.byref(ne)), "coli_tier_lookup")
+        for k in ("fetch_ids", "fetch_slots"):
+            out[k] = out[k][:nf.value]
+        for k in ("evict_ids", "evict_slots"):
+            out[k] = out[k][:ne.value]
+        return out
+
+    def prefetch(self, layer, ids):
+        """-> dict(fetch_ids, fetch_slots, evict_ids, evict_slots)"""
+        ids = self._ids(ids)
+        n = ids.size
+        out = {k: np.empty(n, np.int32) for k in ("fetch_ids", "fetch_slots", "evict_ids", "evict_slots")}
+        nf, ne = _i(), _i()
+        _check(lib().coli_tier_prefetch(self.h, layer, ids.ctypes.data, n,
+                                        out["fetch_ids"].ctypes.data, out["fetch_slots"].ctypes.data,
+                                        ctypes.byref(nf), out["evict_ids"].ctypes.data,
+                                        out["evict_slots"].ctypes.data, ctypes.byref(ne)),
+               "coli_tier_prefetch")
+        for k in ("fetch_ids", "fetch_slots"):
+            out[k] = out[k][:nf.value]
+        for k in ("evict_ids", "evict_slots"):
+            out[k] = out[k][:ne.value]
+        return out
+
+    def repin(self, layer):
+        """-> dict(fetch_ids, fetch_slots, drop_ids, drop_slots)"""
+        m = max(self.n_pin, 1)
+        out = {k: np.empty(m, np.int32) for k in ("fetch_ids", "fetch_slots", "drop_ids", "drop_slots")}
+        nf, nd = _i(), _i()
+        _check(lib().coli_tier_repin(self.h, layer, out["fetch_ids"].ctypes.data,
+                                     out["fetch_slots"].ctypes.data, ctypes.byref(nf),
+                                     out["drop_ids"].ctypes.data, out["drop_slots"].ctypes.data,
+                                     ctypes.byref(nd)), "coli_tier_repin")
+        for k in ("fetch_ids", "fetch_slots"):
+            out[k] = out[k][:nf.value]
+        for k in ("drop_ids", "drop_slots"):
+            out[k] = out[k][:nd.value]
+        return out
+
+    def state(self, layer):
+        """-> (pinned ascending, LRU list most recent first, slot_of[n_experts])"""
+        pinned = np.empty(max(self.n_pin, 1), np.int32)
+        lru = np.empty(self.n_lru, np.int32)
+        slot_of = np.empty(self.n_experts, np.int32)
+        npin, nlru = _i(), _i()
+        _check(lib().coli_tier_state(self.h, layer, pinned.ctypes.data, ctypes.byref(npin),
+                                     lru.ctypes.data, ctypes.byref(nlru), slot_of.ctypes.data),
+               "coli_tier_state")
+        return pinned[:npin.value], lru[:nlru.value], slot_of
+
+    def heat(self, layer):
+        h = np.empty(self.n_experts, np.int64)
+        _check(lib().coli_tier_heat(self.h, layer, h.ctypes.data), "coli_tier_heat")
+        return h
+
+    def set_heat(self, layer, heat):
+        heat = np.ascontiguousarray(heat, dtype=np.int64)
+        assert heat.size == self.n_experts
+        _check(lib().coli_tier_set_heat(self.h, layer, heat.ctypes.data), "coli_tier_set_heat")
+
+    def stats(self):
+        st = np.empty(len(TIER_STATS), np.int64)
+        _check(lib().coli_tier_stats(self.h, st.ctypes.data), "coli_tier_stats")
+        return dict(zip(TIER_STATS, (int(v) for v in st)))
+
+    def save_usage(self, path):
+        _check(lib().coli_tier_save_usage(self.h, os.fsencode(path)), "coli_tier_save_usage")
+
+    def load_usage(self, path):
+        _check(lib().coli_tier_load_usage(self.h, os.fsencode(path)), "coli_tier_load_usage")

@@ -235,6 +235,7 @@ const char* coli_moe_strerror(int status) {
     case COLI_ECUDA: return "CUDA runtime error";
     case COLI_ETIMEOUT: return "a bounded device wait timed out";
     case COLI_EUNSUPPORTED: return "unsupported shape or request";
+    case COLI_EIO: return "file input/output error";
     default: return "unknown status";
   }
 }

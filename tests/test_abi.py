@@ -1,4 +1,4 @@
-"""The C-ABI library builds, loads and exports every function include/coli_moe.h declares;
+"""The C-ABI library builds, loads and exports every function the headers under include/ declare;
 argument validation that needs no GPU.  CPU only (no kernel is launched)."""
 import ctypes
 import shutil
@@ -30,7 +30,7 @@ def test_exports_match_header(built):
 
 
 def test_strerror_and_record_bytes(built):
-    for st in (0, -1, -2, -3, -4, -5, -6):
+    for st in (0, -1, -2, -3, -4, -5, -6, -7):
         assert built.coli_moe_strerror(st)
     assert coli.expert_record_bytes(6144, 2048) == 18_915_328
 

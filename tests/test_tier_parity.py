@@ -1,0 +1,238 @@
+"""The library's tier manager (coli_tier_*) against the residency-tier oracle, op by op.
+
+Seeded random sequences of lookups, prefetches, repins and heat restores run on both sides.
+After every op these must be identical:
+- the hit classes, the loads, and the evictions and drops, in order;
+- the pinned sets and the LRU order;
+- the heat and the counters.
+
+Slots are the library's own choice, so they are checked for validity instead:
+- each resident expert holds one distinct slot in range;
+- a slot stays with its expert until that expert is evicted or dropped;
+- a load goes to a slot that was free, or that the same call freed.
+
+Host code only: no GPU is used.
+"""
+import os
+import struct
+import subprocess
+
+import numpy as np
+import pytest
+
+from gen.trace import routing_trace
+from int4_routed_expert_quantize_gb300 import _build, coli
+from oracle.tier import TierOracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    syms = ""
+    if os.path.exists(_build.SO):
+        syms = subprocess.run(["nm", "-D", "--defined-only", _build.SO], capture_output=True,
+                              text=True).stdout
+    if "coli_tier_create" not in syms:
+        _build.build()
+    coli._lib = None
+    return coli.lib()
+
+
+def snapshot(t, o):
+    """compare the full state of library tier t and oracle o; return slot_of per layer"""
+    slots = []
+    n_slots = o.n_pin + o.n_lru
+    for l in range(o.n_layers):
+        pinned, lru, slot_of = t.state(l)
+        assert pinned.tolist() == sorted(o.pinned[l])
+        assert lru.tolist() == o.lru[l]
+        assert t.heat(l).tolist() == o.heat[l]
+        res = np.flatnonzero(slot_of >= 0)
+        assert set(res.tolist()) == o.resident(l)
+        used = slot_of[res]
+        assert used.min(initial=0) >= 0 and used.max(initial=0) < n_slots
+        assert len(set(used.tolist())) == used.size
+        slots.append(slot_of.copy())
+    assert t.stats() == o.stats
+    return slots
+
+
+def check_moves(before, after, fetch_ids, fetch_slots, freed_ids, freed_slots):
+    """slot bookkeeping of one op on one layer"""
+    assert before[freed_ids].tolist() == freed_slots.tolist()
+    assert np.all(after[freed_ids[~np.isin(freed_ids, fetch_ids)]] == -1)
+    assert after[fetch_ids].tolist() == fetch_slots.tolist()
+    busy_before = set(before[before >= 0].tolist()) - set(freed_slots.tolist())
+    assert not busy_before & set(fetch_slots.tolist())
+    kept = (before >= 0) & (after >= 0)
+    kept[fetch_ids] = False
+    assert np.array_equal(before[kept], after[kept])
+
+
+CONFIGS = [  # n_layers, n_experts, n_pin, n_lru, per_call
+    (3, 64, 4, 8, 8),
+    (2, 32, 0, 8, 8),       # no pinned store
+    (2, 40, 40, 6, 6),      # pinned store as large as the layer
+    (1, 16, 2, 1, 1),       # one LRU place, one expert per call
+    (4, 256, 16, 24, 8),    # GLM-like: 256 experts, top-8
+    (2, 48, 5, 48, 12),     # LRU as large as the layer
+]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=[f"L{c[0]}E{c[1]}p{c[2]}r{c[3]}k{c[4]}" for c in CONFIGS])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tier_matches_oracle(lib, cfg, seed):
+    n_layers, E, n_pin, n_lru, k = cfg
+    actual, predicted = routing_trace(100 + seed, 60, n_layers, E, k)
+    t, o = coli.Tier(n_layers, E, n_pin, n_lru), TierOracle(n_layers, E, n_pin, n_lru)
+    rng = np.random.default_rng(seed)
+    slots = snapshot(t, o)
+    for s in range(len(actual)):
+        for l in range(n_layers):
+            op = rng.random()
+            if op < 0.5:
+                r = t.prefetch(l, predicted[s][l])
+                f, ev = o.prefetch(l, predicted[s][l])
+                assert r["fetch_ids"].tolist() == f and r["evict_ids"].tolist() == ev
+                new = snapshot(t, o)
+                check_moves(slots[l], new[l], r["fetch_ids"], r["fetch_slots"], r["evict_ids"],
+                            r["evict_slots"])
+                slots = new
+            ids = actual[s][l]
+            try:
+                o_res = o.lookup(l, ids)
+            except ValueError:  # more unpinned experts than LRU places: both reject
+                with pytest.raises(coli.ColiError):
+                    t.lookup(l, ids)
+                assert all(np.array_equal(a, b) for a, b in zip(snapshot(t, o), slots))
+                continue
+            r = t.lookup(l, ids)
+            cls, f, ev = o_res
+            assert r["cls"].tolist() == cls
+            assert r["fetch_ids"].tolist() == f and r["evict_ids"].tolist() == ev
+            new = snapshot(t, o)
+            assert r["slot"].tolist() == new[l][ids].tolist()
+            check_moves(slots[l], new[l], r["fetch_ids"], r["fetch_slots"], r["evict_ids"],
+                        r["evict_slots"])
+            slots = new
+        if rng.random() < 0.15:
+            l = int(rng.integers(n_layers))
+            if rng.random() < 0.3:  # restore a saved usage map
+                heat = rng.integers(0, 5, E)
+                t.set_heat(l, heat)
+                o.set_heat(l, heat.tolist())
+            r = t.repin(l)
+            f, dropped = o.repin(l)
+            assert r["fetch_ids"].tolist() == f and r["drop_ids"].tolist() == dropped
+            new = snapshot(t, o)
+            check_moves(slots[l], new[l], r["fetch_ids"], r["fetch_slots"], r["drop_ids"],
+                        r["drop_slots"])
+            slots = new
+    st = t.stats()
+    assert st["misses"] + st["lru_hits"] + st["pin_hits"] > 0
+
+
+def test_rejected_calls_change_nothing(lib):
+    t, o = coli.Tier(1, 32, 2, 4), TierOracle(1, 32, 2, 4)
+    t.lookup(0, [1, 2, 3])
+    o.lookup(0, [1, 2, 3])
+    before = snapshot(t, o)
+    for ids in ([3, 3], [5, 2], [-1], [32], [4, 5, 6, 7, 8]):
+        with pytest.raises(coli.ColiError) as e:
+            t.lookup(0, ids)
+        assert e.value.status == -1
+        assert snapshot(t, o)[0].tolist() == before[0].tolist()
+    with pytest.raises(coli.ColiError):
+        t.prefetch(0, [1, 2, 3, 4, 5])  # more than n_lru predictions
+    for bad_layer in (-1, 1):
+        with pytest.raises(coli.ColiError):
+            t.lookup(bad_layer, [1])
+        with pytest.raises(coli.ColiError):
+            t.repin(bad_layer)
+    with pytest.raises(coli.ColiError):
+        t.set_heat(0, np.full(32, -1))
+    snapshot(t, o)
+
+
+@pytest.mark.parametrize("cfg", [(0, 8, 0, 1), (1, 0, 0, 1), (1, 8, 9, 1), (1, 8, 0, 0),
+                                 (1, 8, 0, 9), (1, 8, -1, 1), (4097, 8, 0, 1), (1, 65537, 0, 1)])
+def test_create_rejects_bad_config(lib, cfg):
+    with pytest.raises(coli.ColiError) as e:
+        coli.Tier(*cfg)
+    assert e.value.status == -1
+
+
+def test_empty_call_is_a_no_op(lib):
+    t = coli.Tier(1, 8, 1, 2)
+    r = t.lookup(0, [])
+    assert r["cls"].size == 0 and r["fetch_ids"].size == 0
+    assert t.stats() == dict.fromkeys(coli.TIER_STATS, 0)
+
+
+def test_usage_file_layout_and_round_trip(lib, tmp_path):
+    t = coli.Tier(2, 3, 1, 2)
+    t.set_heat(0, [5, 0, 2 ** 40])
+    t.set_heat(1, [1, 2, 3])
+    path = tmp_path / "usage.bin"
+    t.save_usage(path)
+    data = path.read_bytes()
+    # written out by hand: magic, int32 n_layers = 2, int32 n_experts = 3, six int64 counts
+    expect = (b"COLIUSE1" + b"\x02\x00\x00\x00" + b"\x03\x00\x00\x00"
+              + b"\x05" + b"\x00" * 7 + b"\x00" * 8 + b"\x00" * 5 + b"\x01" + b"\x00" * 2
+              + b"\x01" + b"\x00" * 7 + b"\x02" + b"\x00" * 7 + b"\x03" + b"\x00" * 7)
+    assert data == expect
+    u = coli.Tier(2, 3, 1, 2)
+    u.load_usage(path)
+    assert u.heat(0).tolist() == [5, 0, 2 ** 40] and u.heat(1).tolist() == [1, 2, 3]
+    # start-up autopin: the hottest expert of each layer is pinned from the learned usage
+    assert u.repin(0)["fetch_ids"].tolist() == [2] and u.repin(1)["fetch_ids"].tolist() == [2]
+
+
+def test_usage_file_rejections_leave_heat_alone(lib, tmp_path):
+    t = coli.Tier(2, 3, 1, 2)
+    t.set_heat(0, [7, 8, 9])
+    good = tmp_path / "good.bin"
+    t.save_usage(good)
+    data = good.read_bytes()
+    u = coli.Tier(2, 3, 1, 2)
+    u.set_heat(1, [4, 4, 4])
+    cases = {
+        "magic.bin": (b"COLIUSE2" + data[8:], -1),
+        "shape.bin": (data[:8] + struct.pack("<ii", 2, 4) + data[16:], -1),
+        "short.bin": (data[:-3], -7),
+        "long.bin": (data + b"\x00", -1),
+        "negative.bin": (data[:16] + struct.pack("<q", -1) + data[24:], -1),
+    }
+    for name, (blob, status) in cases.items():
+        p = tmp_path / name
+        p.write_bytes(blob)
+        with pytest.raises(coli.ColiError) as e:
+            u.load_usage(p)
+        assert e.value.status == status, name
+        assert u.heat(0).tolist() == [0, 0, 0] and u.heat(1).tolist() == [4, 4, 4]
+    with pytest.raises(coli.ColiError) as e:
+        u.load_usage(tmp_path / "missing.bin")
+    assert e.value.status == -7
+    with pytest.raises(coli.ColiError) as e:
+        t.save_usage(tmp_path)  # a directory cannot be opened for writing
+    assert e.value.status == -7
+
+
+def test_glm_sized_trace_hit_rates(lib):
+    """a GLM-sized layer set (8 layers x 256 experts, top-8 per call) behaves as the oracle
+    does over a longer trace, with lookahead prefetch and a repin every 64 steps"""
+    n_layers, E, n_pin, n_lru, k = 8, 256, 32, 64, 8
+    actual, predicted = routing_trace(7, 256, n_layers, E, k)
+    t, o = coli.Tier(n_layers, E, n_pin, n_lru), TierOracle(n_layers, E, n_pin, n_lru)
+    for s in range(len(actual)):
+        for l in range(n_layers):
+            if l + 1 < n_layers:
+                t.prefetch(l + 1, predicted[s][l + 1])
+                o.prefetch(l + 1, predicted[s][l + 1])
+            r = t.lookup(l, actual[s][l])
+            assert r["cls"].tolist() == o.lookup(l, actual[s][l])[0]
+        if s % 64 == 63:
+            for l in range(n_layers):
+                assert t.repin(l)["fetch_ids"].tolist() == o.repin(l)[0]
+    assert t.stats() == o.stats
+    st = o.stats
+    assert st["pin_hits"] > 0 and st["lru_hits"] > 0 and st["prefetch_used"] > 0
