@@ -112,9 +112,11 @@ def _ptr(a):
     if a is None:
         return None
     if isinstance(a, torch.Tensor):
-        assert a.is_contiguous()
+        if not a.is_contiguous():
+            raise ValueError("the library takes contiguous tensors")
         return a.data_ptr()
-    assert a.flags["C_CONTIGUOUS"]
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("the library takes C-contiguous arrays")
     return a.ctypes.data
 
 
@@ -368,7 +370,8 @@ class Tier:
 
     def set_heat(self, layer, heat):
         heat = np.ascontiguousarray(heat, dtype=np.int64)
-        assert heat.size == self.n_experts
+        if heat.size != self.n_experts:
+            raise ValueError(f"heat needs {self.n_experts} counts, got {heat.size}")
         _check(lib().coli_tier_set_heat(self.h, layer, heat.ctypes.data), "coli_tier_set_heat")
 
     def stats(self):
