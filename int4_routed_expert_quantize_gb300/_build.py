@@ -11,7 +11,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "libcoli_moe.so")
 SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "expert_fused.cu", "expert_prefill.cu",
-           "runtime.cu", "noalloc.cu", "tier.cpp"]
+           "runtime.cu", "noalloc.cu", "tier.cpp", "status.cpp"]
+HOST_SOURCES = ["tier.cpp", "status.cpp"]  # the parts that need no CUDA
 
 
 def nvcc_flags(arch="sm_103a"):
@@ -37,3 +38,14 @@ def build(arch="sm_103a", verbose=False, extra=()):
     subprocess.check_call(["nvcc", "-shared", "-cudart", "static", "-Xlinker",
                            "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", SO] + objs)
     return SO
+
+
+def build_host(out, sanitize=False):
+    """Build the host-only parts (tier manager, status strings) with g++ into `out`; with
+    `sanitize`, under AddressSanitizer and UndefinedBehaviorSanitizer (for tests)."""
+    flags = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-I", INCLUDE, "-I", CSRC]
+    if sanitize:
+        flags += ["-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined",
+                  "-fno-sanitize-recover=undefined"]
+    subprocess.check_call(flags + [os.path.join(CSRC, f) for f in HOST_SOURCES] + ["-o", out])
+    return out

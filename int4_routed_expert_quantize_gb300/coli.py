@@ -57,6 +57,48 @@ def header_functions():
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(coli_\w+)\s*\(", text, re.M)))
 
 
+def _bind_host(L):
+    """argument types of the host-only entry points (tier manager, status strings)"""
+    _ip = ctypes.POINTER(_i)
+    L.coli_tier_create.argtypes = [ctypes.POINTER(TierConfig), ctypes.POINTER(_vp)]
+    L.coli_tier_destroy.argtypes = [_vp]
+    L.coli_tier_destroy.restype = None
+    L.coli_tier_lookup.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _ip, _vp, _vp, _ip]
+    L.coli_tier_prefetch.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+    L.coli_tier_repin.argtypes = [_vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+    L.coli_tier_state.argtypes = [_vp, _i, _vp, _ip, _vp, _ip, _vp]
+    L.coli_tier_heat.argtypes = [_vp, _i, _vp]
+    L.coli_tier_set_heat.argtypes = [_vp, _i, _vp]
+    L.coli_tier_stats.argtypes = [_vp, _vp]
+    L.coli_tier_save_usage.argtypes = [_vp, ctypes.c_char_p]
+    L.coli_tier_load_usage.argtypes = [_vp, ctypes.c_char_p]
+    L.coli_moe_strerror.argtypes = [_i]
+    L.coli_moe_strerror.restype = ctypes.c_char_p
+
+
+def _bind_layer(L):
+    """argument types of the layer's entry points"""
+    L.coli_moe_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(_vp)]
+    L.coli_moe_destroy.argtypes = [_vp]
+    L.coli_moe_destroy.restype = None
+    L.coli_moe_load_router.argtypes = [_vp, _vp, _vp, _vp, _vp]
+    L.coli_moe_load_experts.argtypes = [_vp, _i, _i, _vp, _vp, _vp]
+    L.coli_moe_forward.argtypes = [_vp, _vp, _i, _vp, _vp]
+    L.coli_moe_forward_debug.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(Dump), _vp]
+    L.coli_moe_forward_host.argtypes = [_vp, _vp, _i, _vp, _vp]
+    L.coli_moe_forward_profiled.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(_vp), _i, _vp]
+    L.coli_moe_stack_forward.argtypes = [ctypes.POINTER(_vp), _i, _vp, _i, _vp]
+    L.coli_moe_status.argtypes = [_vp, _vp]
+    L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
+    L.coli_moe_expert_record_bytes.restype = _i64
+    L.coli_moe_launches.argtypes = [_vp, _i]
+    L.coli_moe_inject_fault.argtypes = [_vp, _i]
+    L.coli_moe_set_prefill_min.argtypes = [_vp, _i]
+    L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
+    L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
+    L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -64,42 +106,20 @@ def lib():
             raise RuntimeError(f"{_build.SO} is missing: build the CUDA extension first "
                                "(python -c 'import __graft_entry__ as g; g.build()')")
         L = ctypes.CDLL(_build.SO)
-        L.coli_moe_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(_vp)]
-        L.coli_moe_destroy.argtypes = [_vp]
-        L.coli_moe_destroy.restype = None
-        L.coli_moe_load_router.argtypes = [_vp, _vp, _vp, _vp, _vp]
-        L.coli_moe_load_experts.argtypes = [_vp, _i, _i, _vp, _vp, _vp]
-        L.coli_moe_forward.argtypes = [_vp, _vp, _i, _vp, _vp]
-        L.coli_moe_forward_debug.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(Dump), _vp]
-        L.coli_moe_forward_host.argtypes = [_vp, _vp, _i, _vp, _vp]
-        L.coli_moe_forward_profiled.argtypes = [_vp, _vp, _i, _vp, ctypes.POINTER(_vp), _i, _vp]
-        L.coli_moe_stack_forward.argtypes = [ctypes.POINTER(_vp), _i, _vp, _i, _vp]
-        L.coli_moe_status.argtypes = [_vp, _vp]
-        L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
-        L.coli_moe_expert_record_bytes.restype = _i64
-        L.coli_moe_launches.argtypes = [_vp, _i]
-        L.coli_moe_inject_fault.argtypes = [_vp, _i]
-        L.coli_moe_set_prefill_min.argtypes = [_vp, _i]
-        L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
-        L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
-        L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
-        _ip = ctypes.POINTER(_i)
-        L.coli_tier_create.argtypes = [ctypes.POINTER(TierConfig), ctypes.POINTER(_vp)]
-        L.coli_tier_destroy.argtypes = [_vp]
-        L.coli_tier_destroy.restype = None
-        L.coli_tier_lookup.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _ip, _vp, _vp, _ip]
-        L.coli_tier_prefetch.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
-        L.coli_tier_repin.argtypes = [_vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
-        L.coli_tier_state.argtypes = [_vp, _i, _vp, _ip, _vp, _ip, _vp]
-        L.coli_tier_heat.argtypes = [_vp, _i, _vp]
-        L.coli_tier_set_heat.argtypes = [_vp, _i, _vp]
-        L.coli_tier_stats.argtypes = [_vp, _vp]
-        L.coli_tier_save_usage.argtypes = [_vp, ctypes.c_char_p]
-        L.coli_tier_load_usage.argtypes = [_vp, ctypes.c_char_p]
-        L.coli_moe_strerror.argtypes = [_i]
-        L.coli_moe_strerror.restype = ctypes.c_char_p
+        _bind_host(L)
+        _bind_layer(L)
         _lib = L
     return _lib
+
+
+def use_host_library(path):
+    """Bind a host-only build of the tier manager (_build.build_host) in place of the full
+    library: for the tier calls alone, e.g. a sanitizer run.  The layer calls are absent."""
+    global _lib
+    L = ctypes.CDLL(path)
+    _bind_host(L)
+    _lib = L
+    return L
 
 
 def _check(rc, where):

@@ -226,20 +226,6 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
 
 extern "C" {
 
-const char* coli_moe_strerror(int status) {
-  switch (status) {
-    case COLI_OK: return "ok";
-    case COLI_EINVAL: return "invalid argument";
-    case COLI_ENOMEM: return "out of memory";
-    case COLI_ESTATE: return "call out of order (weights not loaded, or wrong device)";
-    case COLI_ECUDA: return "CUDA runtime error";
-    case COLI_ETIMEOUT: return "a bounded device wait timed out";
-    case COLI_EUNSUPPORTED: return "unsupported shape or request";
-    case COLI_EIO: return "file input/output error";
-    default: return "unknown status";
-  }
-}
-
 int coli_moe_set_prefill_min(coli_moe* h, int min_tokens) {
   if (!h || min_tokens <= kDecodeTmax) return COLI_EINVAL;
   h->prefill_min = min_tokens;

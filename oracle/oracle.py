@@ -11,7 +11,7 @@ import subprocess
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SO = os.path.join(HERE, "liboracle.so")
+SO = os.environ.get("COLI_ORACLE_SO") or os.path.join(HERE, "liboracle.so")  # a sanitized build may stand in
 QB = 32
 
 _i, _f, _vp, _i64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int64
@@ -30,11 +30,16 @@ class Dump(ctypes.Structure):
     _fields_ = [(n, _vp) for n in _DUMP_FIELDS]
 
 
-def build(openmp=True):
+def build(openmp=True, out=None, sanitize=False):
+    """Compile oracle.c into `out` (default: the library the tests load); with `sanitize`,
+    under AddressSanitizer and UndefinedBehaviorSanitizer."""
     flags = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math"]
     if openmp:
         flags.append("-fopenmp")
-    subprocess.check_call(flags + [os.path.join(HERE, "oracle.c"), "-o", SO, "-lm"])
+    if sanitize:
+        flags += ["-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined",
+                  "-fno-sanitize-recover=undefined"]
+    subprocess.check_call(flags + [os.path.join(HERE, "oracle.c"), "-o", out or SO, "-lm"])
 
 
 _lib = None

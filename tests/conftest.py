@@ -18,6 +18,9 @@ def _built_host_parts():
     """The oracle and the host generator are plain C: (re)build them once per session."""
     from gen import gen
     from oracle import oracle
+    if os.environ.get("COLI_ORACLE_SO") or os.environ.get("COLI_TIER_HOST_SO"):
+        yield  # a child run against prebuilt (sanitized) libraries: build nothing here
+        return
     gen.build(cuda=False)
     oracle.build()
     yield

@@ -27,6 +27,8 @@ from oracle.tier import TierOracle
 
 @pytest.fixture(scope="module")
 def lib():
+    if os.environ.get("COLI_TIER_HOST_SO"):  # a host-only (sanitized) build is under test
+        return coli.use_host_library(os.environ["COLI_TIER_HOST_SO"])
     syms = ""
     if os.path.exists(_build.SO):
         syms = subprocess.run(["nm", "-D", "--defined-only", _build.SO], capture_output=True,
