@@ -238,3 +238,63 @@ def test_glm_sized_trace_hit_rates(lib):
     assert t.stats() == o.stats
     st = o.stats
     assert st["pin_hits"] > 0 and st["lru_hits"] > 0 and st["prefetch_used"] > 0
+
+
+def _same(t, o, layers):
+    for l in layers:
+        pinned, lru, slot_of = t.state(l)
+        assert pinned.tolist() == sorted(o.pinned[l]) and lru.tolist() == o.lru[l]
+        assert set(np.flatnonzero(slot_of >= 0).tolist()) == o.resident(l)
+    assert t.stats() == o.stats
+
+
+def test_largest_configurations(lib):
+    # 65536 experts with as many pinned and LRU slots: ids at both ends of the range
+    E = 65536
+    t, o = coli.Tier(1, E, E, E), TierOracle(1, E, E, E)
+    for ids in ([0, 1, E - 2, E - 1], [5, 40000, E - 1], list(range(E - 64, E))):
+        r = t.lookup(0, ids)
+        assert r["cls"].tolist() == o.lookup(0, ids)[0]
+    heat = np.zeros(E, np.int64)
+    heat[[3, E - 1, 777]] = [9, 9, 2]
+    t.set_heat(0, heat)
+    o.set_heat(0, heat.tolist())
+    assert t.repin(0)["fetch_ids"].tolist() == o.repin(0)[0]
+    _same(t, o, [0])
+    # 4096 layers
+    t, o = coli.Tier(4096, 8, 1, 2), TierOracle(4096, 8, 1, 2)
+    for l in (0, 1, 4094, 4095):
+        assert t.lookup(l, [1, 7])["cls"].tolist() == o.lookup(l, [1, 7])[0]
+        t.repin(l)
+        o.repin(l)
+    _same(t, o, [0, 4095])
+
+
+def test_degenerate_cases(lib):
+    E = 16
+    # equal heat everywhere: the lowest ids are pinned
+    t, o = coli.Tier(1, E, 4, 4), TierOracle(1, E, 4, 4)
+    t.set_heat(0, np.full(E, 3))
+    o.set_heat(0, [3] * E)
+    assert t.repin(0)["fetch_ids"].tolist() == o.repin(0)[0] == [0, 1, 2, 3]
+    # predicted experts that are pinned load nothing and keep their pinned place
+    r = t.prefetch(0, [0, 1, 2, 3])
+    assert r["fetch_ids"].size == 0 and o.prefetch(0, [0, 1, 2, 3]) == ([], [])
+    _same(t, o, [0])
+    # no pinned slots: a repin pins nothing and drops nothing
+    t, o = coli.Tier(1, E, 0, 3), TierOracle(1, E, 0, 3)
+    t.lookup(0, [2, 4])
+    o.lookup(0, [2, 4])
+    r = t.repin(0)
+    assert r["fetch_ids"].size == 0 and r["drop_ids"].size == 0 and o.repin(0) == ([], [])
+    _same(t, o, [0])
+    # a repin after the heat was cleared drops every pinned expert
+    t, o = coli.Tier(1, E, 2, 2), TierOracle(1, E, 2, 2)
+    for tier in (t, o):
+        tier.set_heat(0, [1] * E if tier is o else np.ones(E))
+        tier.repin(0)
+        tier.set_heat(0, [0] * E if tier is o else np.zeros(E))
+    r = t.repin(0)
+    f, dropped = o.repin(0)
+    assert r["drop_ids"].tolist() == dropped == [0, 1] and r["fetch_ids"].size == 0 and f == []
+    _same(t, o, [0])
