@@ -97,7 +97,9 @@ class TierOracle:
         return evicted
 
     def lookup(self, layer, ids):
-        """-> (classes, fetched ids, evicted ids), all in the order they happened"""
+        """One call's experts ("colibrì 架构概述" §5, moe step: pin, then ecache, else
+        expert_load; LRU promotion after the experts ran).
+        -> (classes, fetched ids, evicted ids), all in the order they happened"""
         ids = self._check_ids(layer, ids)
         pinned, lru = self.pinned[layer], self.lru[layer]
         if sum(1 for e in ids if e not in pinned) > self.n_lru:
@@ -118,7 +120,8 @@ class TierOracle:
         return classes, fetched, self._cut_back(layer)
 
     def prefetch(self, layer, ids):
-        """-> (fetched ids, evicted ids)"""
+        """Predicted experts of a layer ("colibrì 架构概述" §5 pilot_prefetch; README
+        "絕不為同一次硬碟讀取等待兩遍", router lookahead). -> (fetched ids, evicted ids)"""
         ids = self._check_ids(layer, ids)
         if len(ids) > self.n_lru:
             raise ValueError("more predicted experts than LRU places")
@@ -133,7 +136,8 @@ class TierOracle:
         return fetched, self._cut_back(layer)
 
     def repin(self, layer):
-        """-> (fetched ids, dropped ids), each ascending"""
+        """Heat-driven repin ("colibrì 架构概述" §4 tier.h, §5 repin_pass and autopin; README
+        "統一記憶體階層"). -> (fetched ids, dropped ids), each ascending"""
         if not 0 <= layer < self.n_layers:
             raise ValueError("layer out of range")
         h = self.heat[layer]
@@ -157,6 +161,7 @@ class TierOracle:
         return fetched, dropped
 
     def set_heat(self, layer, heat):
+        """Restore a learned usage map (the .coli_usage file, "colibrì 架构概述" §5 start-up)."""
         if not 0 <= layer < self.n_layers or len(heat) != self.n_experts or min(heat) < 0:
             raise ValueError("bad usage map")
         self.heat[layer] = [int(v) for v in heat]
