@@ -298,3 +298,43 @@ def test_degenerate_cases(lib):
     f, dropped = o.repin(0)
     assert r["drop_ids"].tolist() == dropped == [0, 1] and r["fetch_ids"].size == 0 and f == []
     _same(t, o, [0])
+
+
+def test_null_arguments(lib, tmp_path):
+    """the C ABI's NULL rules: a NULL handle or input is EINVAL; every output may be NULL"""
+    import ctypes
+    L = coli.lib()
+    EINVAL = -1
+    h = ctypes.c_void_p()
+    cfg = coli.TierConfig(1, 8, 1, 2)
+    assert L.coli_tier_create(None, ctypes.byref(h)) == EINVAL
+    assert L.coli_tier_create(ctypes.byref(cfg), None) == EINVAL
+    assert L.coli_tier_create(ctypes.byref(cfg), ctypes.byref(h)) == 0
+    ids = np.array([1, 5], np.int32)
+    p = ids.ctypes.data
+    assert L.coli_tier_lookup(None, 0, p, 2, *[None] * 8) == EINVAL
+    assert L.coli_tier_lookup(h, 0, None, 2, *[None] * 8) == EINVAL
+    assert L.coli_tier_lookup(h, 0, None, 0, *[None] * 8) == 0  # an empty call needs no ids
+    assert L.coli_tier_lookup(h, 0, p, 2, *[None] * 8) == 0    # outputs are optional
+    assert L.coli_tier_prefetch(None, 0, p, 2, *[None] * 6) == EINVAL
+    assert L.coli_tier_prefetch(h, 0, p, 2, *[None] * 6) == 0
+    assert L.coli_tier_repin(None, 0, *[None] * 6) == EINVAL
+    assert L.coli_tier_repin(h, 0, *[None] * 6) == 0
+    assert L.coli_tier_state(None, 0, *[None] * 5) == EINVAL
+    assert L.coli_tier_state(h, 0, *[None] * 5) == 0
+    assert L.coli_tier_heat(h, 0, None) == EINVAL and L.coli_tier_heat(None, 0, p) == EINVAL
+    assert L.coli_tier_set_heat(h, 0, None) == EINVAL
+    assert L.coli_tier_stats(h, None) == EINVAL and L.coli_tier_stats(None, p) == EINVAL
+    path = str(tmp_path / "u.bin").encode()
+    assert L.coli_tier_save_usage(h, None) == EINVAL and L.coli_tier_save_usage(None, path) == EINVAL
+    assert L.coli_tier_load_usage(h, None) == EINVAL and L.coli_tier_load_usage(None, path) == EINVAL
+    # the calls with NULL outputs still did their work: 1 and 5 were used once each, and the
+    # repin pinned the lower of the two
+    heat = np.empty(8, np.int64)
+    assert L.coli_tier_heat(h, 0, heat.ctypes.data) == 0
+    assert heat.tolist() == [0, 1, 0, 0, 0, 1, 0, 0]
+    pinned, n_pinned = np.empty(1, np.int32), ctypes.c_int()
+    assert L.coli_tier_state(h, 0, pinned.ctypes.data, ctypes.byref(n_pinned), None, None, None) == 0
+    assert n_pinned.value == 1 and pinned[0] == 1
+    L.coli_tier_destroy(h)
+    L.coli_tier_destroy(None)  # a no-op
