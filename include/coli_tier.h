@@ -13,14 +13,17 @@
  *   - README "統一記憶體階層": a learning cache records where the workload routes and pins the
  *     hottest experts;
  *   - README "絕不為同一次硬碟讀取等待兩遍": the next layer's router predicts its experts
- *     one layer ahead.
+ *     one layer ahead;
+ *   - ai4coding.ru "colibrì: движок GLM-5.2", "Обучающийся кэш": start-up pins the hottest
+ *     experts of the usage file, and the optional live repin (--repin N) swaps cold pinned
+ *     experts for hotter ones by a decaying session heat map.
  *
  * The rules below fix the steps the pages leave open:
  *   - Per layer there is a pinned set (at most n_pin experts) and an LRU list (at most n_lru
  *     experts, most recently used first). The two are disjoint. The shared expert is always
  *     resident and is not tracked here.
  *   - A lookup classifies each expert of a call as a pinned hit, an LRU hit or a miss, and
- *     adds 1 to its heat.
+ *     adds 1 to its usage heat and its session heat.
  *   - The lookup then loads the misses and moves every unpinned expert of the call to the
  *     front of the list, in ascending id order, so the largest id ends in front. It cuts the
  *     list back to n_lru from its tail; those experts are evicted, least recent first.
@@ -30,9 +33,15 @@
  *     expert it loads.
  *   - A marked expert later counts as a used prefetch (an LRU hit on it, or a repin that pins
  *     it) or as a wasted one (it is evicted).
- *   - A repin makes the pinned set the n_pin experts of highest heat among those with heat > 0.
- *     Equal heat goes to the lower id. Experts that leave the set are dropped; an entering
- *     expert found in the LRU list keeps its slot; any other entering expert is loaded.
+ *   - Usage heat is a cumulative use count, and the usage file saves it. Session heat counts
+ *     the same uses, but coli_tier_decay halves it (rounding down). The caller's interval
+ *     between decays sets its half-life.
+ *   - Autopin pins by usage heat (start-up); repin pins by session heat (live). Both rank the
+ *     pinned experts and every expert with heat > 0: higher heat first, then pinned before
+ *     unpinned, then the lower id. The top n_pin form the new pinned set. So an expert replaces
+ *     a pinned one only if strictly hotter, and a map of zeros changes nothing.
+ *   - Experts that leave the set are dropped. An entering expert found in the LRU list keeps
+ *     its slot; any other entering expert is loaded.
  *
  * Slots are layer-local indices 0 .. n_pin+n_lru-1. Each resident expert holds exactly one
  * slot, and keeps it until it is evicted or dropped. A load takes the lowest free slot after
@@ -98,13 +107,19 @@ int coli_tier_prefetch(coli_tier* t, int layer, const int32_t* ids, int n, int32
                        int32_t* fetch_slots, int* n_fetch, int32_t* evict_ids,
                        int32_t* evict_slots, int* n_evict);
 
-/* Repins `layer` from its heat.  Outputs (any may be NULL; arrays of n_pin entries):
+/* Live repin of `layer` by its session heat (coli_tier_autopin: the same by usage heat, for
+ * start-up after coli_tier_load_usage).  Outputs (any may be NULL; arrays of n_pin entries):
  * fetch_ids/fetch_slots/*n_fetch  the entering experts that must be loaded (ascending);
  * drop_ids/drop_slots/*n_drop     the experts that left the pinned set (ascending) and the
  *                                 slots they freed.
  * EINVAL: NULL t or a bad layer. */
 int coli_tier_repin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_slots,
                     int* n_fetch, int32_t* drop_ids, int32_t* drop_slots, int* n_drop);
+int coli_tier_autopin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_slots,
+                      int* n_fetch, int32_t* drop_ids, int32_t* drop_slots, int* n_drop);
+
+/* Halves every layer's session heat (rounding down).  EINVAL: NULL t. */
+int coli_tier_decay(coli_tier* t);
 
 /* State of `layer`: pinned[n_pin] ascending and *n_pinned; lru[n_lru] most recent first and
  * *n_lru_used; slot_of[n_experts] (-1 = not resident); any output may be NULL.
@@ -112,17 +127,18 @@ int coli_tier_repin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_
 int coli_tier_state(const coli_tier* t, int layer, int32_t* pinned, int* n_pinned,
                     int32_t* lru, int* n_lru_used, int32_t* slot_of);
 
-/* Heat of `layer`: heat[n_experts], the number of lookups that used each expert (or what
- * coli_tier_set_heat / coli_tier_load_usage put there).  EINVAL: NULL argument, bad layer,
- * or (set) a negative count. */
+/* Usage heat of `layer`: heat[n_experts], the number of lookups that used each expert (or
+ * what coli_tier_set_heat / coli_tier_load_usage put there); coli_tier_session_heat gives the
+ * decayed session heat.  EINVAL: NULL argument, bad layer, or (set) a negative count. */
 int coli_tier_heat(const coli_tier* t, int layer, int64_t* heat);
+int coli_tier_session_heat(const coli_tier* t, int layer, int64_t* heat);
 int coli_tier_set_heat(coli_tier* t, int layer, const int64_t* heat);
 
 /* stats[COLI_TIER_N_STATS], the counters listed above, summed over all layers since create. */
 int coli_tier_stats(const coli_tier* t, int64_t* stats);
 
-/* The usage file: the learned heat of every layer, so a later process can pin the hottest
- * experts at start-up (coli_tier_load_usage, then coli_tier_repin per layer).  Format: the 8
+/* The usage file: the usage heat of every layer, so a later process can pin the hottest
+ * experts at start-up (coli_tier_load_usage, then coli_tier_autopin per layer).  Format: the 8
  * bytes "COLIUSE1", int32 n_layers, int32 n_experts, then int64 heat[n_layers][n_experts],
  * all little-endian.  save writes the whole file or reports an error.  load replaces every
  * layer's heat only after the whole file has been read and checked.  EINVAL: NULL argument,

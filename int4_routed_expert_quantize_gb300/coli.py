@@ -66,6 +66,9 @@ def _bind_host(L):
     L.coli_tier_lookup.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _ip, _vp, _vp, _ip]
     L.coli_tier_prefetch.argtypes = [_vp, _i, _vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
     L.coli_tier_repin.argtypes = [_vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+    L.coli_tier_autopin.argtypes = [_vp, _i, _vp, _vp, _ip, _vp, _vp, _ip]
+    L.coli_tier_decay.argtypes = [_vp]
+    L.coli_tier_session_heat.argtypes = [_vp, _i, _vp]
     L.coli_tier_state.argtypes = [_vp, _i, _vp, _ip, _vp, _ip, _vp]
     L.coli_tier_heat.argtypes = [_vp, _i, _vp]
     L.coli_tier_set_heat.argtypes = [_vp, _i, _vp]
@@ -357,20 +360,36 @@ class Tier:
             out[k] = out[k][:ne.value]
         return out
 
-    def repin(self, layer):
-        """-> dict(fetch_ids, fetch_slots, drop_ids, drop_slots)"""
+    def _pin(self, fn, layer):
         m = max(self.n_pin, 1)
         out = {k: np.empty(m, np.int32) for k in ("fetch_ids", "fetch_slots", "drop_ids", "drop_slots")}
         nf, nd = _i(), _i()
-        _check(lib().coli_tier_repin(self.h, layer, out["fetch_ids"].ctypes.data,
-                                     out["fetch_slots"].ctypes.data, ctypes.byref(nf),
-                                     out["drop_ids"].ctypes.data, out["drop_slots"].ctypes.data,
-                                     ctypes.byref(nd)), "coli_tier_repin")
+        _check(getattr(lib(), fn)(self.h, layer, out["fetch_ids"].ctypes.data,
+                                  out["fetch_slots"].ctypes.data, ctypes.byref(nf),
+                                  out["drop_ids"].ctypes.data, out["drop_slots"].ctypes.data,
+                                  ctypes.byref(nd)), fn)
         for k in ("fetch_ids", "fetch_slots"):
             out[k] = out[k][:nf.value]
         for k in ("drop_ids", "drop_slots"):
             out[k] = out[k][:nd.value]
         return out
+
+    def repin(self, layer):
+        """live repin by session heat -> dict(fetch_ids, fetch_slots, drop_ids, drop_slots)"""
+        return self._pin("coli_tier_repin", layer)
+
+    def autopin(self, layer):
+        """start-up pinning by usage heat -> dict(fetch_ids, fetch_slots, drop_ids, drop_slots)"""
+        return self._pin("coli_tier_autopin", layer)
+
+    def decay(self):
+        """halve every layer's session heat"""
+        _check(lib().coli_tier_decay(self.h), "coli_tier_decay")
+
+    def session_heat(self, layer):
+        h = np.empty(self.n_experts, np.int64)
+        _check(lib().coli_tier_session_heat(self.h, layer, h.ctypes.data), "coli_tier_session_heat")
+        return h
 
     def state(self, layer):
         """-> (pinned ascending, LRU list most recent first, slot_of[n_experts])"""

@@ -1,7 +1,7 @@
 // Expert residency tiers: the host-side decisions of which expert records sit in which HBM
 // slots of each MoE layer ("colibrì 架构概述" §4, expert cache and scheduling layer; §5, the moe
-// step's pin -> LRU -> load order, repin_pass and pilot_prefetch).  The rules are stated in
-// coli_tier.h.  Every call is O(ids + evictions) except repin and state (O(n_experts)).
+// step's pin -> LRU -> load order, autopin, repin_pass and pilot_prefetch; ai4coding.ru
+// "Обучающийся кэш", the decaying session heat map).  The rules are stated in coli_tier.h.  Every call is O(ids + evictions) except repin and state (O(n_experts)).
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -21,7 +21,8 @@ struct Layer {
   std::vector<int32_t> next;     // more recently used neighbour
   int32_t head = -1, tail = -1;  // most and least recently used
   int lru_size = 0, pin_size = 0;
-  std::vector<int64_t> heat;
+  std::vector<int64_t> heat;       // usage heat: cumulative use count
+  std::vector<int64_t> session;    // session heat: use count, halved by coli_tier_decay
   std::vector<uint8_t> marked;     // loaded by a prefetch, not used yet
   std::vector<uint64_t> free_bits; // bit s set: slot s is free
   std::vector<uint32_t> stamp;     // == the tier's call counter: the expert is in this call
@@ -165,6 +166,7 @@ int coli_tier_create(const coli_tier_config* cfg, coli_tier** out) {
       L.prev.assign(E, -1);
       L.next.assign(E, -1);
       L.heat.assign(E, 0);
+      L.session.assign(E, 0);
       L.marked.assign(E, 0);
       L.stamp.assign(E, 0u);
       L.free_bits.assign(words, ~0ull);
@@ -196,6 +198,7 @@ int coli_tier_lookup(coli_tier* t, int layer, const int32_t* ids, int n, int32_t
     const int32_t e = ids[i];
     L.stamp[e] = call;
     ++L.heat[e];
+    ++L.session[e];
     const int c = L.where[e] == kPinned ? COLI_TIER_PIN_HIT
                 : L.where[e] == kInLru  ? COLI_TIER_LRU_HIT
                                         : COLI_TIER_MISS;
@@ -253,20 +256,27 @@ int coli_tier_prefetch(coli_tier* t, int layer, const int32_t* ids, int n, int32
   return COLI_OK;
 }
 
-int coli_tier_repin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_slots,
-                    int* n_fetch, int32_t* drop_ids, int32_t* drop_slots, int* n_drop) {
-  if (!t || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
-  Layer& L = t->layers[layer];
+}  // extern "C"
+
+namespace {
+
+// New pinned set of L: the n_pin first of the pinned experts and every expert with key > 0,
+// ranked by key (higher first), then pinned before unpinned, then lower id.
+int pin_by(coli_tier* t, Layer& L, const std::vector<int64_t>& key, int32_t* fetch_ids,
+           int32_t* fetch_slots, int* n_fetch, int32_t* drop_ids, int32_t* drop_slots,
+           int* n_drop) {
   std::vector<int32_t> hot;
   try {
     for (int32_t e = 0; e < t->n_experts; ++e)
-      if (L.heat[e] > 0) hot.push_back(e);
+      if (key[e] > 0 || L.where[e] == kPinned) hot.push_back(e);
   } catch (const std::bad_alloc&) {
     return COLI_ENOMEM;
   }
   const size_t keep = std::min(hot.size(), (size_t)t->n_pin);
-  std::partial_sort(hot.begin(), hot.begin() + keep, hot.end(), [&L](int32_t a, int32_t b) {
-    return L.heat[a] != L.heat[b] ? L.heat[a] > L.heat[b] : a < b;
+  std::partial_sort(hot.begin(), hot.begin() + keep, hot.end(), [&L, &key](int32_t a, int32_t b) {
+    if (key[a] != key[b]) return key[a] > key[b];
+    const bool pa = L.where[a] == kPinned, pb = L.where[b] == kPinned;
+    return pa != pb ? pa : a < b;
   });
   hot.resize(keep);
   std::sort(hot.begin(), hot.end());
@@ -307,6 +317,31 @@ int coli_tier_repin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_
   return COLI_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int coli_tier_repin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_slots,
+                    int* n_fetch, int32_t* drop_ids, int32_t* drop_slots, int* n_drop) {
+  if (!t || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
+  Layer& L = t->layers[layer];
+  return pin_by(t, L, L.session, fetch_ids, fetch_slots, n_fetch, drop_ids, drop_slots, n_drop);
+}
+
+int coli_tier_autopin(coli_tier* t, int layer, int32_t* fetch_ids, int32_t* fetch_slots,
+                      int* n_fetch, int32_t* drop_ids, int32_t* drop_slots, int* n_drop) {
+  if (!t || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
+  Layer& L = t->layers[layer];
+  return pin_by(t, L, L.heat, fetch_ids, fetch_slots, n_fetch, drop_ids, drop_slots, n_drop);
+}
+
+int coli_tier_decay(coli_tier* t) {
+  if (!t) return COLI_EINVAL;
+  for (Layer& L : t->layers)
+    for (int64_t& v : L.session) v >>= 1;  // counts are never negative: this rounds down
+  return COLI_OK;
+}
+
 int coli_tier_state(const coli_tier* t, int layer, int32_t* pinned, int* n_pinned,
                     int32_t* lru, int* n_lru_used, int32_t* slot_of) {
   if (!t || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
@@ -332,6 +367,12 @@ int coli_tier_state(const coli_tier* t, int layer, int32_t* pinned, int* n_pinne
 int coli_tier_heat(const coli_tier* t, int layer, int64_t* heat) {
   if (!t || !heat || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
   std::memcpy(heat, t->layers[layer].heat.data(), sizeof(int64_t) * (size_t)t->n_experts);
+  return COLI_OK;
+}
+
+int coli_tier_session_heat(const coli_tier* t, int layer, int64_t* heat) {
+  if (!t || !heat || layer < 0 || layer >= t->n_layers) return COLI_EINVAL;
+  std::memcpy(heat, t->layers[layer].session.data(), sizeof(int64_t) * (size_t)t->n_experts);
   return COLI_OK;
 }
 

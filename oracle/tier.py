@@ -13,6 +13,9 @@ Where each step comes from:
   hottest experts.
 - README "絕不為同一次硬碟讀取等待兩遍": the router lookahead preloads the next layer's
   experts.
+- ai4coding.ru "colibrì: движок GLM-5.2", "Обучающийся кэш": the usage file records which
+  experts the workload reaches, and start-up pins the hottest. The optional live repin
+  (--repin N) swaps cold pinned experts for hotter ones by a decaying session heat map.
 
 Readings (the pages name the steps, not their details):
 - One tier object covers every MoE layer. Each layer has a pinned set of at most n_pin
@@ -20,7 +23,7 @@ Readings (the pages name the steps, not their details):
   expert is always resident and is not tracked.
 - lookup(layer, ids) takes the distinct routed experts of one call (the batch union), in
   ascending order. It classifies each as PIN_HIT, LRU_HIT or MISS, and adds 1 to each
-  one's heat.
+  one's usage heat and session heat.
 - The misses are loaded. Then every unpinned expert of the call moves to the front of the
   LRU list (hits and misses alike, in ascending order, so the largest id ends in front), and
   the list is cut back to n_lru entries from its tail; the cut entries are evicted, least
@@ -35,11 +38,18 @@ Readings (the pages name the steps, not their details):
 - A later lookup that hits a marked expert counts the prefetch as used, and so does a repin
   that pins it (its load is kept). An eviction of a marked expert counts it as wasted. At
   most n_lru ids per call.
-- repin(layer) makes the pinned set the n_pin hottest experts with heat > 0. Equal heat
-  goes to the lower expert id.
-- A repin drops the experts that leave the pinned set. An entering expert that sits in the
-  LRU list moves out of the list (no load); any other entering expert is loaded.
-- Heat is a cumulative use count per (layer, expert); set_heat restores a saved usage map.
+- Two heats per (layer, expert). Usage heat is a cumulative use count; set_heat restores a
+  saved usage map. Session heat counts uses too, but decay() halves it for every layer
+  (integer halving, rounding down). The pages give no decay rate: the caller's interval
+  between decays sets the half-life.
+- autopin(layer) pins by usage heat (start-up); repin(layer) pins by session heat (live).
+- Both rank the candidates by heat, higher first. The candidates are the pinned experts and
+  every expert with heat > 0. On equal heat a pinned expert goes first, then the lower id.
+  The top n_pin form the new pinned set. So an expert replaces a pinned one only if it is
+  strictly hotter, and a map of zeros changes nothing.
+- A repin or autopin drops the experts that leave the pinned set. An entering expert that
+  sits in the LRU list moves out of the list (no load); any other entering expert is
+  loaded.
 
 Pure Python over lists and sets, so the steps can be checked by eye.  Nothing here is
 shared with the library's own tier manager.
@@ -62,7 +72,8 @@ class TierOracle:
         self.n_layers, self.n_experts, self.n_pin, self.n_lru = n_layers, n_experts, n_pin, n_lru
         self.pinned = [set() for _ in range(n_layers)]
         self.lru = [[] for _ in range(n_layers)]  # most recently used first
-        self.heat = [[0] * n_experts for _ in range(n_layers)]
+        self.heat = [[0] * n_experts for _ in range(n_layers)]  # usage heat
+        self.session = [[0] * n_experts for _ in range(n_layers)]  # decayed session heat
         self.marked = [set() for _ in range(n_layers)]  # prefetched, not used yet
         self.stats = dict.fromkeys(STAT_KEYS, 0)
 
@@ -108,6 +119,7 @@ class TierOracle:
         classes = [PIN_HIT if e in pinned else LRU_HIT if e in lru else MISS for e in ids]
         for e, c in zip(ids, classes):
             self.heat[layer][e] += 1
+            self.session[layer][e] += 1
             self.stats[("pin_hits", "lru_hits", "misses")[c]] += 1
             if c == LRU_HIT and e in self.marked[layer]:
                 if MUTANT != 6:
@@ -135,17 +147,16 @@ class TierOracle:
         self._to_front(layer, [e for e in ids if e not in pinned])
         return fetched, self._cut_back(layer)
 
-    def repin(self, layer):
-        """Heat-driven repin ("colibrì 架构概述" §4 tier.h, §5 repin_pass and autopin; README
-        "統一記憶體階層"). -> (fetched ids, dropped ids), each ascending"""
+    def _pin_by(self, layer, h):
         if not 0 <= layer < self.n_layers:
             raise ValueError("layer out of range")
-        h = self.heat[layer]
-        tie = -1 if MUTANT == 2 else 1
-        hottest = sorted((e for e in range(self.n_experts) if h[e] > 0 or MUTANT == 5),
-                         key=lambda e: (-h[e], tie * e))
-        new = set(hottest[:self.n_pin])
         old = self.pinned[layer]
+        tie = -1 if MUTANT == 2 else 1
+        incumbent_first = MUTANT != 8
+        candidates = [e for e in range(self.n_experts) if h[e] > 0 or e in old or MUTANT == 5]
+        ranked = sorted(candidates,
+                        key=lambda e: (-h[e], 0 if (e in old and incumbent_first) else 1, tie * e))
+        new = set(ranked[:self.n_pin])
         fetched = []
         for e in sorted(new - old):
             if e in self.lru[layer]:
@@ -159,6 +170,25 @@ class TierOracle:
         dropped = sorted(old - new)
         self.pinned[layer] = new
         return fetched, dropped
+
+    def autopin(self, layer):
+        """Start-up pinning from the learned usage heat ("colibrì 架构概述" §5 autopin;
+        ai4coding.ru "Обучающийся кэш"; README "統一記憶體階層").
+        -> (fetched ids, dropped ids), each ascending"""
+        return self._pin_by(layer, self.heat[layer])
+
+    def repin(self, layer):
+        """Live repin by the decayed session heat ("colibrì 架构概述" §4 tier.h, §5 repin_pass;
+        ai4coding.ru "Обучающийся кэш", --repin N). -> (fetched ids, dropped ids), ascending"""
+        return self._pin_by(layer, self.session[layer])
+
+    def decay(self):
+        """Halve every session heat (rounding down): the decay of the session heat map."""
+        if MUTANT == 7:
+            return
+        for row in self.session:
+            for e in range(self.n_experts):
+                row[e] //= 2
 
     def set_heat(self, layer, heat):
         """Restore a learned usage map (the .coli_usage file, "colibrì 架构概述" §5 start-up)."""

@@ -5,7 +5,8 @@ The facts are:
 - the inclusion property of a stack algorithm;
 - the closed form of a cyclic access pattern;
 - heat from a brute-force count;
-- the pinned set from a full sort;
+- the pinned sets from full sorts (usage heat at start-up, decayed session heat live);
+- the halving closed form of the session-heat decay;
 - conservation of prefetched loads;
 - the per-call guarantees the readings state.
 
@@ -85,9 +86,10 @@ def test_calls_keep_their_own_experts_and_heat_is_a_count():
             for l in range(3):
                 t.repin(l)
     assert np.array_equal(np.array(t.heat), count)
+    assert np.array_equal(np.array(t.session), count)  # no decay yet: the same count
 
 
-def test_repin_equals_full_sort():
+def test_autopin_equals_full_sort():
     rng = np.random.default_rng(4)
     E, n_pin = 50, 7
     for trial in range(20):
@@ -100,7 +102,7 @@ def test_repin_equals_full_sort():
             t.lookup(0, [int(e)])
         t.set_heat(0, heat.tolist())
         lru_before, old = list(t.lru[0]), set(t.pinned[0])
-        fetched, dropped = t.repin(0)
+        fetched, dropped = t.autopin(0)
         order = sorted(range(E), key=lambda e: (-int(heat[e]), e))  # full stable sort
         expect = {e for e in order[:n_pin] if heat[e] > 0}
         assert t.pinned[0] == expect
@@ -109,10 +111,49 @@ def test_repin_equals_full_sort():
         assert t.lru[0] == [e for e in lru_before if e not in expect]
 
 
+def test_live_repin_equals_full_sort_with_incumbents_first():
+    """live repin ranks pinned experts and every expert with session heat > 0 by heat, then
+    incumbents first, then id: an expert displaces a pinned one only if strictly hotter"""
+    rng = np.random.default_rng(8)
+    E, n_pin = 40, 6
+    for trial in range(25):
+        t = TierOracle(1, E, n_pin, E)
+        t.set_heat(0, rng.integers(0, 3, E).tolist())
+        t.autopin(0)  # some incumbents
+        for _ in range(int(rng.integers(0, 30))):
+            t.lookup(0, sorted(rng.choice(E, int(rng.integers(1, 5)), replace=False).tolist()))
+        for _ in range(int(rng.integers(0, 3))):
+            t.decay()
+        old, sess = set(t.pinned[0]), list(t.session[0])
+        t.repin(0)
+        cand = [e for e in range(E) if sess[e] > 0 or e in old]
+        order = sorted(cand, key=lambda e: (-sess[e], e not in old, e))  # full sort
+        assert t.pinned[0] == set(order[:n_pin])
+    # a session map of zeros changes nothing
+    t = TierOracle(1, E, n_pin, E)
+    t.set_heat(0, list(range(E)))
+    t.autopin(0)
+    before = set(t.pinned[0])
+    assert t.repin(0) == ([], []) and t.pinned[0] == before
+
+
+def test_decay_halves_session_heat():
+    """u uses followed by m decays leave floor(u / 2^m) of session heat; usage heat keeps u"""
+    t = TierOracle(2, 16, 0, 16)
+    uses = {3: 1, 5: 7, 9: 13, 15: 64}
+    for e, u in uses.items():
+        for _ in range(u):
+            t.lookup(1, [e])
+    for m in range(8):
+        for e, u in uses.items():
+            assert t.session[1][e] == u >> m and t.heat[1][e] == u
+        t.decay()
+
+
 def test_pinned_experts_hit_and_leave_the_lru_alone():
     t = TierOracle(1, 32, 3, 4)
     t.set_heat(0, [5 if e in (2, 9, 30) else 0 for e in range(32)])
-    t.repin(0)
+    t.autopin(0)
     t.lookup(0, [1, 4])
     before = list(t.lru[0])
     classes, fetched, evicted = t.lookup(0, [2, 9, 30])
@@ -165,11 +206,13 @@ def test_rejected_calls_change_nothing(ids):
 
 TIER_MUTANTS = {
     1: ("evicts the most recently used expert", ["test_lru_hits_equal_stack_distance"]),
-    2: ("repin ties go to the higher id", ["test_repin_equals_full_sort"]),
+    2: ("repin ties go to the higher id", ["test_autopin_equals_full_sort"]),
     3: ("prefetch counts heat", ["test_calls_keep_their_own_experts_and_heat_is_a_count"]),
     4: ("LRU hits are not promoted", ["test_lru_hits_equal_stack_distance"]),
-    5: ("repin pins experts never used", ["test_repin_equals_full_sort"]),
+    5: ("repin pins experts never used", ["test_autopin_equals_full_sort"]),
     6: ("a used prefetch stays marked", ["test_perfect_prefetch_leaves_no_misses_and_loads_are_conserved"]),
+    7: ("decay leaves the session heat as it is", ["test_decay_halves_session_heat"]),
+    8: ("incumbents lose ties at a repin", ["test_live_repin_equals_full_sort_with_incumbents_first"]),
 }
 
 

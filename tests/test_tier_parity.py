@@ -48,6 +48,7 @@ def snapshot(t, o):
         assert pinned.tolist() == sorted(o.pinned[l])
         assert lru.tolist() == o.lru[l]
         assert t.heat(l).tolist() == o.heat[l]
+        assert t.session_heat(l).tolist() == o.session[l]
         res = np.flatnonzero(slot_of >= 0)
         assert set(res.tolist()) == o.resident(l)
         used = slot_of[res]
@@ -116,14 +117,20 @@ def test_tier_matches_oracle(lib, cfg, seed):
             check_moves(slots[l], new[l], r["fetch_ids"], r["fetch_slots"], r["evict_ids"],
                         r["evict_slots"])
             slots = new
+        if rng.random() < 0.1:
+            t.decay()
+            o.decay()
         if rng.random() < 0.15:
             l = int(rng.integers(n_layers))
-            if rng.random() < 0.3:  # restore a saved usage map
+            if rng.random() < 0.3:  # restore a saved usage map and pin from it
                 heat = rng.integers(0, 5, E)
                 t.set_heat(l, heat)
                 o.set_heat(l, heat.tolist())
-            r = t.repin(l)
-            f, dropped = o.repin(l)
+                r = t.autopin(l)
+                f, dropped = o.autopin(l)
+            else:  # live repin by the session heat
+                r = t.repin(l)
+                f, dropped = o.repin(l)
             assert r["fetch_ids"].tolist() == f and r["drop_ids"].tolist() == dropped
             new = snapshot(t, o)
             check_moves(slots[l], new[l], r["fetch_ids"], r["fetch_slots"], r["drop_ids"],
@@ -186,7 +193,9 @@ def test_usage_file_layout_and_round_trip(lib, tmp_path):
     u.load_usage(path)
     assert u.heat(0).tolist() == [5, 0, 2 ** 40] and u.heat(1).tolist() == [1, 2, 3]
     # start-up autopin: the hottest expert of each layer is pinned from the learned usage
-    assert u.repin(0)["fetch_ids"].tolist() == [2] and u.repin(1)["fetch_ids"].tolist() == [2]
+    assert u.autopin(0)["fetch_ids"].tolist() == [2] and u.autopin(1)["fetch_ids"].tolist() == [2]
+    # the session heat starts empty in the new process: a live repin changes nothing
+    assert u.repin(0)["fetch_ids"].size == 0 and u.repin(0)["drop_ids"].size == 0
 
 
 def test_usage_file_rejections_leave_heat_alone(lib, tmp_path):
@@ -232,6 +241,9 @@ def test_glm_sized_trace_hit_rates(lib):
                 o.prefetch(l + 1, predicted[s][l + 1])
             r = t.lookup(l, actual[s][l])
             assert r["cls"].tolist() == o.lookup(l, actual[s][l])[0]
+        if s % 32 == 31:
+            t.decay()
+            o.decay()
         if s % 64 == 63:
             for l in range(n_layers):
                 assert t.repin(l)["fetch_ids"].tolist() == o.repin(l)[0]
@@ -259,7 +271,8 @@ def test_largest_configurations(lib):
     heat[[3, E - 1, 777]] = [9, 9, 2]
     t.set_heat(0, heat)
     o.set_heat(0, heat.tolist())
-    assert t.repin(0)["fetch_ids"].tolist() == o.repin(0)[0]
+    assert t.autopin(0)["fetch_ids"].tolist() == o.autopin(0)[0]
+    assert t.repin(0)["drop_ids"].tolist() == o.repin(0)[1]
     _same(t, o, [0])
     # 4096 layers
     t, o = coli.Tier(4096, 8, 1, 2), TierOracle(4096, 8, 1, 2)
@@ -276,7 +289,7 @@ def test_degenerate_cases(lib):
     t, o = coli.Tier(1, E, 4, 4), TierOracle(1, E, 4, 4)
     t.set_heat(0, np.full(E, 3))
     o.set_heat(0, [3] * E)
-    assert t.repin(0)["fetch_ids"].tolist() == o.repin(0)[0] == [0, 1, 2, 3]
+    assert t.autopin(0)["fetch_ids"].tolist() == o.autopin(0)[0] == [0, 1, 2, 3]
     # predicted experts that are pinned load nothing and keep their pinned place
     r = t.prefetch(0, [0, 1, 2, 3])
     assert r["fetch_ids"].size == 0 and o.prefetch(0, [0, 1, 2, 3]) == ([], [])
@@ -288,15 +301,21 @@ def test_degenerate_cases(lib):
     r = t.repin(0)
     assert r["fetch_ids"].size == 0 and r["drop_ids"].size == 0 and o.repin(0) == ([], [])
     _same(t, o, [0])
-    # a repin after the heat was cleared drops every pinned expert
+    # a cleared map keeps the pinned experts; an expert displaces one only if strictly hotter
     t, o = coli.Tier(1, E, 2, 2), TierOracle(1, E, 2, 2)
     for tier in (t, o):
         tier.set_heat(0, [1] * E if tier is o else np.ones(E))
-        tier.repin(0)
+        tier.autopin(0)  # pins 0 and 1
         tier.set_heat(0, [0] * E if tier is o else np.zeros(E))
-    r = t.repin(0)
-    f, dropped = o.repin(0)
-    assert r["drop_ids"].tolist() == dropped == [0, 1] and r["fetch_ids"].size == 0 and f == []
+    r = t.autopin(0)
+    assert r["drop_ids"].size == 0 and o.autopin(0) == ([], [])
+    hot = [0] * E
+    hot[7], hot[9], hot[0] = 2, 1, 1  # 7 is hotter than both; 9 ties with pinned 0
+    t.set_heat(0, np.array(hot))
+    o.set_heat(0, hot)
+    r = t.autopin(0)
+    f, dropped = o.autopin(0)
+    assert r["fetch_ids"].tolist() == f == [7] and r["drop_ids"].tolist() == dropped == [1]
     _same(t, o, [0])
 
 
@@ -320,6 +339,10 @@ def test_null_arguments(lib, tmp_path):
     assert L.coli_tier_prefetch(h, 0, p, 2, *[None] * 6) == 0
     assert L.coli_tier_repin(None, 0, *[None] * 6) == EINVAL
     assert L.coli_tier_repin(h, 0, *[None] * 6) == 0
+    assert L.coli_tier_autopin(None, 0, *[None] * 6) == EINVAL
+    assert L.coli_tier_decay(None) == EINVAL
+    assert L.coli_tier_session_heat(h, 0, None) == EINVAL
+    assert L.coli_tier_session_heat(None, 0, p) == EINVAL
     assert L.coli_tier_state(None, 0, *[None] * 5) == EINVAL
     assert L.coli_tier_state(h, 0, *[None] * 5) == 0
     assert L.coli_tier_heat(h, 0, None) == EINVAL and L.coli_tier_heat(None, 0, p) == EINVAL
