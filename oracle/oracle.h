@@ -119,7 +119,7 @@ void orc_i2_matvec(const uint8_t* W, const float* s, int rows, int cols, const i
 void orc_i4_matvec(const uint8_t* W, const float* s, int rows, int cols, const int8_t* qx,
                    const float* dx, float* out, int32_t* A);
 
-/* ---- router (P1 §5 "sigmoid 路由，选 top-8 专家"; P3 DeepSeek-V3-style sigmoid router) ---- */
+/* ---- router (P1 §5, the moe step: sigmoid routing picks the top 8; P3 DeepSeek-V3-style) ---- */
 void orc_topk(const float* sel, int E, int K, int32_t* ids);
 void orc_route_token(const float* Wr, const float* bias, const float* x, int E, int d, int K,
                      float routed_scale, float* logits, float* scores, int32_t* ids, float* w);
