@@ -385,8 +385,8 @@ void orc_rmsnorm(const float* x, const float* gamma, int d, float eps, float* ou
 }
 
 /* ------------------------------------------------------------------------------------------
- * Batch union (P2 "絕不為同一次硬碟讀取等待兩遍", the batch union): the T*K (token, expert) pairs are grouped by expert so each
- * distinct expert is visited once.  Stable counting sort by expert id, then token; union
+ * Batch union (P2 "絕不為同一次硬碟讀取等待兩遍"): the T*K (token, expert) pairs are grouped
+ * by expert so each distinct expert is visited once.  Stable counting sort by expert id, then token; union
  * slots in ascending expert id; the shared expert (id E) is appended as the last slot with
  * every token.  Returns the number of union slots.
  * ---------------------------------------------------------------------------------------- */

@@ -81,7 +81,7 @@ void orc_quantize_i4_rows(const float* w, int64_t rows, int cols, uint8_t* packe
 int orc_i4_get(const uint8_t* row, int j);
 void orc_pack_i4_row(const int8_t* q, int cols, uint8_t* packed_row);
 
-/* ---- activation int8 blocks (P1 §3.1 IDOT; P3 "Q8_0-style int8 activations") ---- */
+/* ---- activation int8 blocks (P1 §3.1 IDOT; P3 "Что реализовано", Q8_0-style) ---- */
 void orc_quantize_q8(const float* x, int64_t n, int8_t* q, float* d);
 
 /* ---- canonical fp32 arithmetic ---- */
