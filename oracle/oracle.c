@@ -454,6 +454,45 @@ void orc_expert_ffn(const uint8_t* rec, const float* sc, int d, int f, const int
   free(h);
 }
 
+/* ------------------------------------------------------------------------------------------
+ * One expert whose rows are int8, int4 or int2 (P1 §3.1 "int8", "int4 packed", "int2 packed";
+ * P1 §5 gate/up/SiLU/down).  Reading: the record keeps the int4 layout [gate f x d | up f x d |
+ * down d x f] at bits/8 bytes per weight (int8: one code per byte; int2: four per byte), with
+ * the same f32 row scales [s_g | s_u | s_d]; the steps are those of orc_expert_ffn, each
+ * matvec taking the rows' own format.  bits = 4 gives orc_expert_ffn's result.
+ * ---------------------------------------------------------------------------------------- */
+static void matvec_bits(int bits, const uint8_t* W, const float* s, int rows, int cols,
+                        const int8_t* q, const float* dq, float* out) {
+  if (bits == 8) orc_i8_matvec((const int8_t*)W, s, rows, cols, q, dq, out, NULL);
+  else if (bits == 2) orc_i2_matvec(W, s, rows, cols, q, dq, out, NULL);
+  else orc_i4_matvec(W, s, rows, cols, q, dq, out, NULL);
+}
+
+int orc_expert_ffn_bits(int bits, const uint8_t* rec, const float* sc, int d, int f,
+                        const int8_t* qx, const float* dx, int8_t* qh, float* dh, float* e,
+                        float* g_out, float* u_out, float* h_out) {
+  if (bits != 8 && bits != 4 && bits != 2) return -1;
+  const int64_t mat = (int64_t)f * d * (ORC_MUTANT == 18 && bits == 8 ? 4 : bits) / 8;
+  const uint8_t* Wg = rec;
+  const uint8_t* Wu = rec + mat;
+  const uint8_t* Wd = rec + 2 * mat;
+  float* g = (float*)malloc(sizeof(float) * (size_t)f);
+  float* u = (float*)malloc(sizeof(float) * (size_t)f);
+  float* h = (float*)malloc(sizeof(float) * (size_t)f);
+  matvec_bits(bits, Wg, sc, f, d, qx, dx, g);
+  matvec_bits(bits, Wu, sc + f, f, d, qx, dx, u);
+  for (int r = 0; r < f; ++r) h[r] = orc_silu_mul(g[r], u[r]);
+  orc_quantize_q8(h, f, qh, dh);
+  matvec_bits(bits, Wd, sc + 2 * f, d, f, qh, dh, e);
+  if (g_out) memcpy(g_out, g, sizeof(float) * (size_t)f);
+  if (u_out) memcpy(u_out, u, sizeof(float) * (size_t)f);
+  if (h_out) memcpy(h_out, h, sizeof(float) * (size_t)f);
+  free(g);
+  free(u);
+  free(h);
+  return 0;
+}
+
 /* fp64 value of one int4 x int8 output row from the same integer codes */
 static double matvec_row64(const uint8_t* W, const float* s, int r, int cols, const int8_t* q,
                            const float* dq) {

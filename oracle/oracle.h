@@ -136,6 +136,12 @@ int orc_union_bucket(const int32_t* ids, int T, int K, int E, int n_shared, int3
 void orc_expert_ffn(const uint8_t* rec, const float* sc, int d, int f, const int8_t* qx,
                     const float* dx, int8_t* qh, float* dh, float* e, float* g_out,
                     float* u_out, float* h_out, int32_t* Ag, int32_t* Au, int32_t* Ad);
+/* one expert with int8 (bits 8), int4 (4) or int2 (2) rows: the int4 record layout at bits/8
+ * bytes per weight, the same steps as orc_expert_ffn (g_out, u_out, h_out may be NULL).
+ * Returns -1 for another width. */
+int orc_expert_ffn_bits(int bits, const uint8_t* rec, const float* sc, int d, int f,
+                        const int8_t* qx, const float* dx, int8_t* qh, float* dh, float* e,
+                        float* g_out, float* u_out, float* h_out);
 
 /* ---- full layer ----
  * rec[id], sc[id] for id in 0..E (E = shared); entries of experts nobody selects may be NULL.

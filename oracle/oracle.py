@@ -88,6 +88,9 @@ def lib():
         L.orc_rmsnorm.argtypes = [_vp, _vp, _i, _f, _vp]
         L.orc_union_bucket.argtypes = [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
         L.orc_union_bucket.restype = _i
+        L.orc_expert_ffn_bits.argtypes = [_i, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                                          _vp, _vp]
+        L.orc_expert_ffn_bits.restype = _i
         L.orc_expert_ffn.argtypes = [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      _vp, _vp, _vp]
         L.orc_moe_forward.argtypes = [ctypes.POINTER(Cfg), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -199,6 +202,21 @@ def i2_matvec(W, s, cols, qx, dx, want_A=False):
     lib().orc_i2_matvec(W.ctypes.data, s.ctypes.data, rows, cols, qx.ctypes.data, dx.ctypes.data,
                         out.ctypes.data, _p(A))
     return out, A
+
+
+def expert_ffn_bits(bits, rec, sc, d, f, qx, dx):
+    """one expert with int8 / int4 / int2 rows on one token -> dict(qh, dh, e, g, u, h)"""
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    sc = np.ascontiguousarray(sc, dtype=np.float32)
+    out = dict(qh=np.empty(f, dtype=np.int8), dh=np.empty(f // QB, dtype=np.float32),
+               e=np.empty(d, dtype=np.float32), g=np.empty(f, dtype=np.float32),
+               u=np.empty(f, dtype=np.float32), h=np.empty(f, dtype=np.float32))
+    rc = lib().orc_expert_ffn_bits(bits, rec.ctypes.data, sc.ctypes.data, d, f, qx.ctypes.data,
+                                   dx.ctypes.data, *(out[k].ctypes.data for k in
+                                                     ("qh", "dh", "e", "g", "u", "h")))
+    if rc != 0:
+        raise ValueError(f"no {bits}-bit rows")
+    return out
 
 
 def topk(sel, K):

@@ -572,6 +572,77 @@ def test_expert_ffn_against_fp64():
     assert np.all(np.abs(r["e"] - e64) <= 10 * EPS32 * mag)
 
 
+# ------------------------------------------------------------------ experts of other widths
+
+def _packed(codes, bits):
+    """rows of codes in the int8 (one per byte), int4 or int2 row format"""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    if bits == 8:
+        return codes.view(np.uint8).ravel().copy()
+    rows, cols = codes.shape
+    out = np.empty((rows, cols * bits // 8), dtype=np.uint8)
+    pack = O.lib().orc_pack_i4_row if bits == 4 else O.lib().orc_pack_i2_row
+    for r in range(rows):
+        pack(codes[r].ctypes.data, cols, out[r].ctypes.data)
+    return out.ravel()
+
+
+def _expert_record(cg, cu, cd, bits):
+    return np.concatenate([_packed(m, bits) for m in (cg, cu, cd)])
+
+
+def test_expert_of_equal_codes_is_the_same_in_every_width():
+    """an expert whose codes fit every width gives the same bits stored as int2, int4 or int8
+    rows (the record layout differs only in the bytes per code), and 4-bit rows give
+    orc_expert_ffn's result"""
+    rng = np.random.default_rng(18)
+    d, f = 512, 256
+    sc = rng.uniform(0.002, 0.02, 2 * f + d).astype(np.float32)
+    qx, dx = O.quantize_q8(rng.standard_normal(d).astype(np.float32))
+    keys = ("qh", "dh", "e", "g", "u", "h")
+    cg, cu, cd = (rng.integers(-1, 2, shp, dtype=np.int8) for shp in ((f, d), (f, d), (d, f)))
+    outs = [O.expert_ffn_bits(b, _expert_record(cg, cu, cd, b), sc, d, f, qx, dx) for b in (2, 4, 8)]
+    for o in outs[1:]:
+        for k in keys:
+            assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8)), k
+    cg, cu, cd = (rng.integers(-7, 8, shp, dtype=np.int8) for shp in ((f, d), (f, d), (d, f)))
+    r4 = _expert_record(cg, cu, cd, 4)
+    o4 = O.expert_ffn_bits(4, r4, sc, d, f, qx, dx)
+    o8 = O.expert_ffn_bits(8, _expert_record(cg, cu, cd, 8), sc, d, f, qx, dx)
+    ref = O.expert_ffn(r4, sc, d, f, qx, dx)
+    for k in keys:
+        assert np.array_equal(o8[k].view(np.uint8), o4[k].view(np.uint8)), k
+        assert np.array_equal(o4[k].view(np.uint8), ref[k].view(np.uint8)), k
+    with pytest.raises(ValueError):
+        O.expert_ffn_bits(3, r4, sc, d, f, qx, dx)
+
+
+def test_int8_expert_against_fp64():
+    """full-range int8 rows: every step against fp64 evaluated from brute-force integer sums"""
+    rng = np.random.default_rng(19)
+    d, f = 512, 256
+    cg, cu, cd = (rng.integers(-127, 128, shp, dtype=np.int8) for shp in ((f, d), (f, d), (d, f)))
+    sc = (rng.uniform(0.5, 2.0, 2 * f + d) / 127 * 0.02).astype(np.float32)
+    qx, dx = O.quantize_q8(rng.standard_normal(d).astype(np.float32))
+    r = O.expert_ffn_bits(8, _expert_record(cg, cu, cd, 8), sc, d, f, qx, dx)
+    q64 = qx.astype(np.int64).reshape(1, -1, 32)
+    for name, codes, s, out in (("g", cg, sc[:f], r["g"]), ("u", cu, sc[f:2 * f], r["u"])):
+        A = (codes.astype(np.int64).reshape(f, -1, 32) * q64).sum(axis=2)
+        v64 = s.astype(np.float64) * (A * dx.astype(np.float64)).sum(axis=1)
+        mag = s.astype(np.float64) * (np.abs(A) * dx.astype(np.float64)).sum(axis=1)
+        assert np.all(np.abs(out - v64) <= 10 * EPS32 * mag), name
+    h64 = r["g"].astype(np.float64) / (1 + np.exp(-r["g"].astype(np.float64))) * r["u"]
+    assert np.all(np.abs(r["h"] - h64) <= 8 * EPS32 * np.abs(h64) + 1e-30)
+    hb = r["h"].reshape(-1, 32)
+    assert np.array_equal(r["dh"], (np.abs(hb).max(axis=1) / np.float32(127)).astype(np.float32))
+    err = np.abs(hb - r["dh"][:, None] * r["qh"].reshape(-1, 32).astype(np.float32))
+    assert np.all(err <= r["dh"][:, None] * 0.5001)
+    Ad = (cd.astype(np.int64).reshape(d, -1, 32) * r["qh"].astype(np.int64).reshape(1, -1, 32)).sum(axis=2)
+    e64 = sc[2 * f:].astype(np.float64) * (Ad * r["dh"].astype(np.float64)).sum(axis=1)
+    mag = sc[2 * f:].astype(np.float64) * (np.abs(Ad) * r["dh"].astype(np.float64)).sum(axis=1)
+    assert np.all(np.abs(r["e"] - e64) <= 10 * EPS32 * mag)
+
+
 # ------------------------------------------------------------------ layer identities ---
 
 def _layer_inputs(wl, layer=0):
