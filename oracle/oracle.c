@@ -493,12 +493,18 @@ int orc_expert_ffn_bits(int bits, const uint8_t* rec, const float* sc, int d, in
   return 0;
 }
 
-/* fp64 value of one int4 x int8 output row from the same integer codes */
-static double matvec_row64(const uint8_t* W, const float* s, int r, int cols, const int8_t* q,
-                           const float* dq) {
-  const uint8_t* wrow = W + (int64_t)r * (cols / 2);
+/* fp64 value of one output row of int8, int4 or int2 rows x int8 codes, from the same
+ * integer codes */
+static double matvec_row64(int bits, const uint8_t* W, const float* s, int r, int cols,
+                           const int8_t* q, const float* dq) {
+  const uint8_t* wrow = W + (int64_t)r * cols * bits / 8;
   double acc = 0.0;
-  for (int b = 0; b < cols / QB; ++b) acc += (double)dq[b] * (double)orc_block_dot(wrow, q, b);
+  for (int b = 0; b < cols / QB; ++b) {
+    const int32_t A = bits == 8   ? orc_i8_block_dot((const int8_t*)wrow, q, b)
+                      : bits == 2 ? orc_i2_block_dot(wrow, q, b)
+                                  : orc_block_dot(wrow, q, b);
+    acc += (double)dq[b] * (double)A;
+  }
   return (double)s[r] * acc;
 }
 
@@ -511,9 +517,11 @@ static double matvec_row64(const uint8_t* W, const float* s, int r, int cols, co
 int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, const float* bias,
                     const float* gamma, const uint8_t* const* rec, const float* const* sc, float* y,
                     double* y64, const orc_dump* dump) {
-  const int d = c->d, f = c->f, E = c->n_experts, K = c->top_k;
+  const int d = c->d, f = c->f, E = c->n_experts, K = c->top_k, bits = c->wbits;
   if (T <= 0) return 0;
   if (d % 64 || f % 64 || K < 1 || K > E || c->qblock != QB) return -1;
+  if (bits != 4 && bits != 8 && bits != 2) return -1;
+  const int64_t down_at = 2 * ((int64_t)f * d * (ORC_MUTANT == 19 ? 4 : bits) / 8); /* down rows */
   const int P = T * K + (c->n_shared ? T : 0);
   float* xn = (float*)malloc(sizeof(float) * (size_t)T * d);
   int8_t* qx = (int8_t*)malloc((size_t)T * d);
@@ -548,6 +556,15 @@ int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, co
     if (!rec[ex] || !sc[ex]) { rc = -1; goto done; }
     for (int p = offsets[s]; p < offsets[s + 1]; ++p) {
       int t = pair_token[p];
+      if (bits != 4) { /* int8 / int2 experts (no per-block accumulator dump) */
+        orc_expert_ffn_bits(bits, rec[ex], sc[ex], d, f, qx + (int64_t)t * d,
+                            dx + (int64_t)t * (d / QB), qh + (int64_t)p * f,
+                            dh + (int64_t)p * (f / QB), e + (int64_t)p * d,
+                            dump && dump->g ? dump->g + (int64_t)p * f : NULL,
+                            dump && dump->u ? dump->u + (int64_t)p * f : NULL,
+                            dump && dump->h ? dump->h + (int64_t)p * f : NULL);
+        continue;
+      }
       orc_expert_ffn(rec[ex], sc[ex], d, f, qx + (int64_t)t * d, dx + (int64_t)t * (d / QB),
                      qh + (int64_t)p * f, dh + (int64_t)p * (f / QB), e + (int64_t)p * d,
                      dump && dump->g ? dump->g + (int64_t)p * f : NULL,
@@ -570,14 +587,15 @@ int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, co
       for (int r = 0; r < d; ++r) {
         double acc = 0.0;
         if (ps >= 0) {
-          const uint8_t* Wd = rec[E] + (int64_t)f * d;
-          acc = matvec_row64(Wd, sc[E] + 2 * f, r, f, qh + (int64_t)ps * f, dh + (int64_t)ps * (f / QB));
+          const uint8_t* Wd = rec[E] + down_at;
+          acc = matvec_row64(bits, Wd, sc[E] + 2 * f, r, f, qh + (int64_t)ps * f,
+                             dh + (int64_t)ps * (f / QB));
         }
         for (int k = 0; k < K; ++k) {
           int p = inv[t * K + k], ex = ids[t * K + k];
-          const uint8_t* Wd = rec[ex] + (int64_t)f * d;
-          acc += (double)w[t * K + k] *
-                 matvec_row64(Wd, sc[ex] + 2 * f, r, f, qh + (int64_t)p * f, dh + (int64_t)p * (f / QB));
+          const uint8_t* Wd = rec[ex] + down_at;
+          acc += (double)w[t * K + k] * matvec_row64(bits, Wd, sc[ex] + 2 * f, r, f,
+                                                     qh + (int64_t)p * f, dh + (int64_t)p * (f / QB));
         }
         if (c->has_norm) acc += (double)x[(int64_t)t * d + r];
         y64[(int64_t)t * d + r] = acc;
@@ -615,6 +633,7 @@ int orc_moe_dequant64(const orc_cfg* c, const float* xn, int T, const int32_t* i
                       const float* w, const uint8_t* const* rec, const float* const* sc,
                       const float* x_resid, double* y) {
   const int d = c->d, f = c->f, E = c->n_experts, K = c->top_k;
+  if (c->wbits != 4) return -1; /* the dequantised reference is written for int4 records */
   double* g = (double*)malloc(sizeof(double) * (size_t)f);
   double* u = (double*)malloc(sizeof(double) * (size_t)f);
   double* e = (double*)malloc(sizeof(double) * (size_t)d);

@@ -48,6 +48,7 @@ typedef struct {
   int d, f, n_experts, top_k, n_shared, qblock;
   float routed_scale, rms_eps;
   int has_norm;
+  int wbits; /* expert code width: 4 (int4 records), 8 or 2 (orc_expert_ffn_bits's layout) */
 } orc_cfg;
 
 /* optional intermediates; any NULL entry is skipped.  P = T*K + n_shared*T pairs. */

@@ -19,7 +19,8 @@ _i, _f, _vp, _i64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int6
 
 class Cfg(ctypes.Structure):
     _fields_ = [("d", _i), ("f", _i), ("n_experts", _i), ("top_k", _i), ("n_shared", _i),
-                ("qblock", _i), ("routed_scale", _f), ("rms_eps", _f), ("has_norm", _i)]
+                ("qblock", _i), ("routed_scale", _f), ("rms_eps", _f), ("has_norm", _i),
+                ("wbits", _i)]
 
 
 _DUMP_FIELDS = ["xn", "qx", "dx", "logits", "scores", "ids", "w", "n_union", "union_ids", "offsets",
@@ -107,8 +108,9 @@ def _p(a):
     return None if a is None else a.ctypes.data
 
 
-def cfg_of(wl, routed_scale=1.0):
-    return Cfg(wl.d, wl.f, wl.E, wl.K, wl.n_shared, QB, routed_scale, wl.rms_eps, int(wl.has_norm))
+def cfg_of(wl, routed_scale=1.0, wbits=4):
+    return Cfg(wl.d, wl.f, wl.E, wl.K, wl.n_shared, QB, routed_scale, wl.rms_eps, int(wl.has_norm),
+               wbits)
 
 
 # ---------------- formats ----------------
@@ -297,13 +299,17 @@ def expert_record(wl, layer, expert):
 # ---------------- full layer ----------------
 
 def forward(wl, x, Wr, bias, gamma, recs, want_dump=True, want_A=False, want_y64=True,
-            routed_scale=1.0):
-    """recs: dict expert id -> (rec, sc) for at least every selected expert and the shared one."""
+            routed_scale=1.0, wbits=4):
+    """recs: dict expert id -> (rec, sc) for at least every selected expert and the shared one;
+    wbits: the records' code width (4, or 8 / 2 for int8 / int2 experts, without the per-block
+    accumulator dumps)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     T, d = x.shape
     E, K, f = wl.E, wl.K, wl.f
     P = T * K + (T if wl.n_shared else 0)
-    cfg = cfg_of(wl, routed_scale)
+    if want_A and wbits != 4:
+        raise ValueError("per-block accumulators are dumped for int4 experts only")
+    cfg = cfg_of(wl, routed_scale, wbits)
     y = np.empty((T, d), dtype=np.float32)
     y64 = np.empty((T, d), dtype=np.float64) if want_y64 else None
     recp = (ctypes.c_void_p * (E + 1))()

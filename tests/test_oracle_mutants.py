@@ -36,7 +36,10 @@ MUTANTS = {
                                           "test_i2_matvec_accumulators_brute_force"]),
     17: ("int2 row scale max|w|/2", ["test_int2_row_quant_golden", "test_int2_row_quant_bounds"]),
     18: ("int8 expert records read at the int4 offsets", ["test_expert_of_equal_codes_is_the_same_in_every_width",
-                                                          "test_int8_expert_against_fp64"]),
+                                                          "test_int8_expert_against_fp64",
+                                                          "test_layer_of_equal_codes_is_the_same_in_every_width"]),
+    19: ("fp64 layer output reads down rows at the int4 offset", [
+        "test_layer_of_equal_codes_is_the_same_in_every_width"]),
 }
 
 

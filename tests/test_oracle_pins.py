@@ -643,6 +643,35 @@ def test_int8_expert_against_fp64():
     assert np.all(np.abs(r["e"] - e64) <= 10 * EPS32 * mag)
 
 
+def test_layer_of_equal_codes_is_the_same_in_every_width():
+    """a whole layer (routing, union, experts, fixed-order combine) whose expert codes fit
+    every width gives the same bits with int2, int4 or int8 expert records; the fp64 output
+    agrees too"""
+    wl = W.WORKLOADS["tiny_t1"]
+    d, f = wl.d, wl.f
+    rng = np.random.default_rng(20)
+    L = O.Layer(wl)
+    codes = {e: [rng.integers(-1, 2, shp, dtype=np.int8) for shp in ((f, d), (f, d), (d, f))]
+             for e in range(wl.E + wl.n_shared)}
+    scs = {e: rng.uniform(0.005, 0.05, 2 * f + d).astype(np.float32) for e in codes}
+    x = W.x_host(wl, 3, 7)
+    outs = {}
+    for bits in (2, 4, 8):
+        recs = {e: (_expert_record(*codes[e], bits), scs[e]) for e in codes}
+        outs[bits] = O.forward(wl, x, L.Wr, L.bias, L.gamma, recs, wbits=bits)
+    assert int(outs[4]["n_union"][0]) > wl.K  # several experts, shared one included
+    for bits in (2, 8):
+        for k in ("y", "y64", "qh", "dh", "e", "ids", "w", "offsets"):
+            assert np.array_equal(np.ascontiguousarray(outs[bits][k]).view(np.uint8),
+                                  np.ascontiguousarray(outs[4][k]).view(np.uint8)), (bits, k)
+    assert normwise_rel64(outs[8]["y"], outs[8]["y64"]) < 1e-5
+
+
+def normwise_rel64(a, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.abs(np.asarray(a, dtype=np.float64) - ref).max() / np.abs(ref).max())
+
+
 # ------------------------------------------------------------------ layer identities ---
 
 def _layer_inputs(wl, layer=0):
