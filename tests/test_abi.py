@@ -82,3 +82,21 @@ def test_create_without_gpu_reports_cuda_error(built):
         pytest.skip("a GPU is present")
     rc, h = _create()
     assert rc == -4 and h is None
+
+
+def test_binding_constants_match_the_headers():
+    """status codes, tier classes and counters in the binding are the headers' #defines"""
+    import glob
+    import os
+    import re
+    text = "".join(open(h).read() for h in glob.glob(os.path.join(_build.INCLUDE, "*.h")))
+    defs = {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"^#define\s+(COLI_\w+)\s+\(?(-?\d+)\)?", text, re.M)}
+    for code, name in coli.STATUS.items():
+        assert defs[name] == code, name
+    assert {v for k, v in defs.items() if re.fullmatch(r"COLI_E[A-Z]+|COLI_OK", k)} == set(coli.STATUS)
+    assert coli.ETIMEOUT == defs["COLI_ETIMEOUT"]
+    assert coli.FAULT_SKIP_ARRIVAL == defs["COLI_FAULT_SKIP_ARRIVAL"]
+    assert defs["COLI_TIER_N_STATS"] == len(coli.TIER_STATS)
+    from oracle.tier import LRU_HIT, MISS, PIN_HIT
+    assert (defs["COLI_TIER_PIN_HIT"], defs["COLI_TIER_LRU_HIT"], defs["COLI_TIER_MISS"]) == (PIN_HIT, LRU_HIT, MISS)
