@@ -69,7 +69,7 @@ typedef struct {
   int n_experts; /* routed experts per layer, 1 .. 65536 (ids 0 .. n_experts-1) */
   int n_pin;     /* pinned slots per layer, 0 .. n_experts                      */
   int n_lru;     /* LRU slots per layer, 1 .. n_experts                         */
-} coli_tier_config;
+} coli_tier_config; /* and n_layers * n_experts <= 2^24 (about 30 bytes of state each) */
 
 /* Hit classes written by coli_tier_lookup. */
 #define COLI_TIER_PIN_HIT 0

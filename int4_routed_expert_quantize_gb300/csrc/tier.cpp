@@ -148,7 +148,8 @@ int coli_tier_create(const coli_tier_config* cfg, coli_tier** out) {
   *out = nullptr;
   const coli_tier_config c = *cfg;
   if (c.n_layers < 1 || c.n_layers > 4096 || c.n_experts < 1 || c.n_experts > 65536 ||
-      c.n_pin < 0 || c.n_pin > c.n_experts || c.n_lru < 1 || c.n_lru > c.n_experts)
+      c.n_pin < 0 || c.n_pin > c.n_experts || c.n_lru < 1 || c.n_lru > c.n_experts ||
+      (int64_t)c.n_layers * c.n_experts > (int64_t)1 << 24)
     return COLI_EINVAL;
   coli_tier* t = new (std::nothrow) coli_tier;
   if (!t) return COLI_ENOMEM;

@@ -163,7 +163,8 @@ def test_rejected_calls_change_nothing(lib):
 
 
 @pytest.mark.parametrize("cfg", [(0, 8, 0, 1), (1, 0, 0, 1), (1, 8, 9, 1), (1, 8, 0, 0),
-                                 (1, 8, 0, 9), (1, 8, -1, 1), (4097, 8, 0, 1), (1, 65537, 0, 1)])
+                                 (1, 8, 0, 9), (1, 8, -1, 1), (4097, 8, 0, 1), (1, 65537, 0, 1),
+                                 (257, 65536, 0, 1)])  # the last: more than 2^24 entries
 def test_create_rejects_bad_config(lib, cfg):
     with pytest.raises(coli.ColiError) as e:
         coli.Tier(*cfg)
