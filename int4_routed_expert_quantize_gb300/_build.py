@@ -21,6 +21,16 @@ def nvcc_flags(arch="sm_103a"):
             "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
 
+def is_stale():
+    """True when the library is missing or older than a source or header it is built from"""
+    if not os.path.exists(SO):
+        return True
+    built = os.path.getmtime(SO)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + \
+        [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
+    return any(os.path.getmtime(p) > built for p in deps if os.path.isfile(p))
+
+
 def build(arch="sm_103a", verbose=False, extra=()):
     os.makedirs(BUILD, exist_ok=True)
     flags = nvcc_flags(arch) + list(extra)

@@ -8,6 +8,7 @@ import ctypes
 import glob
 import os
 import re
+import sys
 
 import numpy as np
 
@@ -177,6 +178,8 @@ class MoeLayer:
             self.h = _vp()
 
     def __del__(self):
+        if sys.is_finalizing():  # the process is exiting: no native calls during teardown
+            return
         try:
             self.close()
         except Exception:
@@ -316,6 +319,8 @@ class Tier:
             self.h = _vp()
 
     def __del__(self):
+        if sys.is_finalizing():  # the process is exiting: no native calls during teardown
+            return
         try:
             self.close()
         except Exception:

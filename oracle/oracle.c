@@ -472,6 +472,7 @@ int orc_expert_ffn_bits(int bits, const uint8_t* rec, const float* sc, int d, in
                         const int8_t* qx, const float* dx, int8_t* qh, float* dh, float* e,
                         float* g_out, float* u_out, float* h_out) {
   if (bits != 8 && bits != 4 && bits != 2) return -1;
+  /* planted mistake 18 reads an int8 record at the int4 offsets (still inside the record) */
   const int64_t mat = (int64_t)f * d * (ORC_MUTANT == 18 && bits == 8 ? 4 : bits) / 8;
   const uint8_t* Wg = rec;
   const uint8_t* Wu = rec + mat;
@@ -521,7 +522,9 @@ int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, co
   if (T <= 0) return 0;
   if (d % 64 || f % 64 || K < 1 || K > E || c->qblock != QB) return -1;
   if (bits != 4 && bits != 8 && bits != 2) return -1;
-  const int64_t down_at = 2 * ((int64_t)f * d * (ORC_MUTANT == 19 ? 4 : bits) / 8); /* down rows */
+  /* the down rows of a record (the planted mistake 19 reads an int8 record at the int4
+   * offset, which stays inside the record) */
+  const int64_t down_at = 2 * ((int64_t)f * d * (ORC_MUTANT == 19 && bits == 8 ? 4 : bits) / 8);
   const int P = T * K + (c->n_shared ? T : 0);
   float* xn = (float*)malloc(sizeof(float) * (size_t)T * d);
   int8_t* qx = (int8_t*)malloc((size_t)T * d);

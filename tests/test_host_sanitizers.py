@@ -52,3 +52,40 @@ def test_tier_manager_under_sanitizers(tmp_path):
     so = str(tmp_path / "libcoli_tier_san.so")
     _build.build_host(so, sanitize=True)
     _child_pytest(_sanitizer_env(COLI_TIER_HOST_SO=so), "tests/test_tier_parity.py")
+
+
+def test_planted_mistakes_stay_memory_safe(tmp_path):
+    """every planted mistake of the C oracle only changes values: built with the sanitizers,
+    its guard pins fail by assertion, never by an invalid access or undefined operation"""
+    from concurrent.futures import ThreadPoolExecutor
+
+    from . import test_oracle_mutants as M
+    sos = {}
+
+    def build(n):
+        so = str(tmp_path / f"liboracle_m{n}_san.so")
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
+                               "-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined",
+                               "-fno-sanitize-recover=undefined", f"-DORC_MUTANT={n}",
+                               os.path.join(O.HERE, "oracle.c"), "-o", so, "-lm"])
+        sos[n] = so
+
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        list(ex.map(build, sorted(M.MUTANTS)))
+    plan = {n: (sos[n], M.MUTANTS[n][1]) for n in sorted(M.MUTANTS)}
+    code = (f"import sys\nsys.path.insert(0, {ROOT!r})\n"
+            "from oracle import oracle as O\n"
+            "from tests import test_oracle_pins as P\n"
+            f"for n, (so, guards) in {plan!r}.items():\n"
+            "    O.SO, O._lib = so, None\n"
+            "    for g in guards:\n"
+            "        try:\n"
+            "            getattr(P, g)()\n"
+            "        except AssertionError:\n"
+            "            pass\n"
+            "print('all mutants ran')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=_sanitizer_env(),
+                       capture_output=True, text=True, timeout=600)
+    tail = (r.stdout + r.stderr)[-4000:]
+    assert r.returncode == 0 and "all mutants ran" in r.stdout, tail
+    assert "ERROR: AddressSanitizer" not in tail and "runtime error:" not in tail, tail

@@ -15,7 +15,6 @@ Host code only: no GPU is used.
 """
 import os
 import struct
-import subprocess
 
 import numpy as np
 import pytest
@@ -29,11 +28,7 @@ from oracle.tier import TierOracle
 def lib():
     if os.environ.get("COLI_TIER_HOST_SO"):  # a host-only (sanitized) build is under test
         return coli.use_host_library(os.environ["COLI_TIER_HOST_SO"])
-    syms = ""
-    if os.path.exists(_build.SO):
-        syms = subprocess.run(["nm", "-D", "--defined-only", _build.SO], capture_output=True,
-                              text=True).stdout
-    if "coli_tier_create" not in syms:
+    if _build.is_stale():
         _build.build()
     coli._lib = None
     return coli.lib()
