@@ -15,11 +15,6 @@
 
 #define QB 32 /* activation block length (Q8_0-style blocks of 32) */
 
-/* ORC_MUTANT plants one known mistake (tests/test_oracle_mutants.py checks that a pin
- * catches each); the oracle the tests trust is built with ORC_MUTANT == 0. */
-#ifndef ORC_MUTANT
-#define ORC_MUTANT 0
-#endif
 
 int orc_num_threads(void) {
 #ifdef _OPENMP
@@ -37,7 +32,7 @@ int orc_num_threads(void) {
  * ---------------------------------------------------------------------------------------- */
 int orc_i4_get(const uint8_t* row, int j) {
   int byte = row[j >> 1];
-  int nib = ((j & 1) ^ (ORC_MUTANT == 1)) ? (byte >> 4) : (byte & 15);
+  int nib = (j & 1) ? (byte >> 4) : (byte & 15);
   return nib >= 8 ? nib - 16 : nib;
 }
 
@@ -90,7 +85,7 @@ void orc_quantize_q8(const float* x, int64_t n, int8_t* q, float* d) {
     for (int j = 0; j < QB; ++j) {
       int v = 0;
       if (db != 0.0f) {
-        v = (int)(ORC_MUTANT == 2 ? truncf(xb[j] / db) : roundf(xb[j] / db));
+        v = (int)roundf(xb[j] / db);
         if (v > 127) v = 127;
         if (v < -127) v = -127;
       }
@@ -128,7 +123,7 @@ float orc_exp(float x) {
   float p = 0x1.a01a02p-13f;     /* 1/7! */
   p = fmaf(p, r, 0x1.6c16c2p-10f); /* 1/6! */
   p = fmaf(p, r, 0x1.111112p-7f);  /* 1/5! */
-  if (ORC_MUTANT != 3) p = fmaf(p, r, 0x1.555556p-5f); /* 1/4! */
+  p = fmaf(p, r, 0x1.555556p-5f); /* 1/4! */
   p = fmaf(p, r, 0x1.555556p-3f);  /* 1/3! */
   p = fmaf(p, r, 0.5f);            /* 1/2! */
   p = fmaf(p, r, 1.0f);            /* 1/1! */
@@ -146,7 +141,6 @@ float orc_sigmoid(float x) { return 1.0f / (1.0f + orc_exp(-x)); }
 
 /* SwiGLU element: SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)) */
 float orc_silu_mul(float g, float u) {
-  if (ORC_MUTANT == 4) { float t = g; g = u; u = t; }
   float s = g / (1.0f + orc_exp(-g));
   return s * u;
 }
@@ -165,8 +159,7 @@ float orc_canon_dot(const float* a, const float* b, int n) {
   for (int g = 0; g < 32; ++g) {
     p[g] = 0.0f;
     for (int j = g * G; j < (g + 1) * G && j < n; ++j) {
-      int jj = ORC_MUTANT == 5 ? (j - g * G) * 32 + g : j; /* strided groups */
-      if (jj < n) p[g] = fmaf(a[jj], b[jj], p[g]);
+      p[g] = fmaf(a[j], b[j], p[g]);
     }
   }
   return orc_pairwise32(p);
@@ -201,7 +194,7 @@ void orc_i4_matvec(const uint8_t* W, const float* s, int rows, int cols, const i
   for (int r = 0; r < rows; ++r) {
     int32_t* Ar = (int32_t*)malloc(sizeof(int32_t) * (size_t)nb);
     const uint8_t* wrow = W + (int64_t)r * (cols / 2);
-    for (int b = 0; b < nb; ++b) Ar[b] = orc_block_dot(wrow, qx, ORC_MUTANT == 12 ? nb - 1 - b : b);
+    for (int b = 0; b < nb; ++b) Ar[b] = orc_block_dot(wrow, qx, b);
     out[r] = s[r] * orc_canon_blocksum(dx, Ar, nb);
     if (A) memcpy(A + (int64_t)r * nb, Ar, sizeof(int32_t) * (size_t)nb);
     free(Ar);
@@ -225,7 +218,7 @@ void orc_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q, flo
       if (a > amax) amax = a;
     }
     const float s = amax / 127.0f;
-    const int lim = ORC_MUTANT == 13 ? 126 : 127;
+    const int lim = 127;
     for (int j = 0; j < cols; ++j) {
       int v = 0;
       if (s != 0.0f) {
@@ -243,7 +236,7 @@ void orc_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q, flo
  * int32: |sum| <= 32 * 127 * 127. */
 int32_t orc_i8_block_dot(const int8_t* wrow, const int8_t* qx, int b) {
   int32_t acc = 0;
-  const int end = (b + 1) * QB - (ORC_MUTANT == 14 ? 1 : 0);
+  const int end = (b + 1) * QB;
   for (int j = b * QB; j < end; ++j) acc += (int32_t)wrow[j] * (int32_t)qx[j];
   return acc;
 }
@@ -276,9 +269,9 @@ void orc_i8_matvec(const int8_t* W, const float* s, int rows, int cols, const in
  *     exact int32 block dots, the same canonical fp32 epilogue.
  * ---------------------------------------------------------------------------------------- */
 int orc_i2_get(const uint8_t* row, int j) {
-  const int k = ORC_MUTANT == 15 ? 3 - (j & 3) : (j & 3);
+  const int k = j & 3;
   const int code = (row[j >> 2] >> (2 * k)) & 3;
-  return (code >= 2 && ORC_MUTANT != 16) ? code - 4 : code;
+  return code >= 2 ? code - 4 : code;
 }
 
 void orc_pack_i2_row(const int8_t* q, int cols, uint8_t* packed_row) {
@@ -298,7 +291,7 @@ void orc_quantize_i2_rows(const float* w, int64_t rows, int cols, uint8_t* packe
       float a = fabsf(wr[j]);
       if (a > amax) amax = a;
     }
-    const float s = amax / (ORC_MUTANT == 17 ? 2.0f : 1.0f);
+    const float s = amax / 1.0f;
     int8_t* q = (int8_t*)malloc((size_t)cols);
     for (int j = 0; j < cols; ++j) {
       int v = 0;
@@ -351,7 +344,7 @@ void orc_topk(const float* sel, int E, int K, int32_t* ids) {
     int best = -1;
     for (int e = 0; e < E; ++e) {
       if (taken[e]) continue;
-      if (best < 0 || sel[e] > sel[best] || (ORC_MUTANT == 6 && sel[e] == sel[best]))
+      if (best < 0 || sel[e] > sel[best])
         best = e; /* strict: the lower index keeps a tie */
     }
     taken[best] = 1;
@@ -371,16 +364,15 @@ void orc_route_token(const float* Wr, const float* bias, const float* x, int E, 
   orc_topk(sel, E, K, ids);
   float S = scores[ids[0]];
   for (int k = 1; k < K; ++k) S = S + scores[ids[k]];
-  if (ORC_MUTANT == 7) { S = sel[ids[0]]; for (int k = 1; k < K; ++k) S = S + sel[ids[k]]; }
   for (int k = 0; k < K; ++k)
-    w[k] = ((ORC_MUTANT == 7 ? sel[ids[k]] : scores[ids[k]]) / S) * routed_scale;
+    w[k] = (scores[ids[k]] / S) * routed_scale;
   free(sel);
 }
 
 /* RMSNorm: x * (1 / sqrt(mean(x^2) + eps)) * gamma */
 void orc_rmsnorm(const float* x, const float* gamma, int d, float eps, float* out) {
   float ms = orc_canon_dot(x, x, d) / (float)d;
-  float r = 1.0f / sqrtf(ORC_MUTANT == 10 ? ms : ms + eps);
+  float r = 1.0f / sqrtf(ms + eps);
   for (int j = 0; j < d; ++j) out[j] = (x[j] * r) * gamma[j];
 }
 
@@ -403,7 +395,7 @@ int orc_union_bucket(const int32_t* ids, int T, int K, int E, int n_shared, int3
       for (int k = 0; k < K; ++k)
         if (ids[t * K + k] == e) {
           pair_token[p] = t;
-          pair_rank[p] = ORC_MUTANT == 11 ? K - 1 - k : k;
+          pair_rank[p] = k;
           inv[t * K + k] = p;
           ++p;
         }
@@ -472,8 +464,7 @@ int orc_expert_ffn_bits(int bits, const uint8_t* rec, const float* sc, int d, in
                         const int8_t* qx, const float* dx, int8_t* qh, float* dh, float* e,
                         float* g_out, float* u_out, float* h_out) {
   if (bits != 8 && bits != 4 && bits != 2) return -1;
-  /* planted mistake 18 reads an int8 record at the int4 offsets (still inside the record) */
-  const int64_t mat = (int64_t)f * d * (ORC_MUTANT == 18 && bits == 8 ? 4 : bits) / 8;
+  const int64_t mat = (int64_t)f * d * bits / 8;
   const uint8_t* Wg = rec;
   const uint8_t* Wu = rec + mat;
   const uint8_t* Wd = rec + 2 * mat;
@@ -522,9 +513,8 @@ int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, co
   if (T <= 0) return 0;
   if (d % 64 || f % 64 || K < 1 || K > E || c->qblock != QB) return -1;
   if (bits != 4 && bits != 8 && bits != 2) return -1;
-  /* the down rows of a record (the planted mistake 19 reads an int8 record at the int4
-   * offset, which stays inside the record) */
-  const int64_t down_at = 2 * ((int64_t)f * d * (ORC_MUTANT == 19 && bits == 8 ? 4 : bits) / 8);
+  /* the down rows of a record */
+  const int64_t down_at = 2 * ((int64_t)f * d * bits / 8);
   const int P = T * K + (c->n_shared ? T : 0);
   float* xn = (float*)malloc(sizeof(float) * (size_t)T * d);
   int8_t* qx = (int8_t*)malloc((size_t)T * d);
@@ -581,9 +571,9 @@ int orc_moe_forward(const orc_cfg* c, const float* x, int T, const float* Wr, co
   for (int t = 0; t < T; ++t) {
     const int ps = c->n_shared ? T * K + t : -1;
     for (int r = 0; r < d; ++r) {
-      float acc = ps >= 0 && ORC_MUTANT != 8 ? e[(int64_t)ps * d + r] : 0.0f;
+      float acc = ps >= 0 ? e[(int64_t)ps * d + r] : 0.0f;
       for (int k = 0; k < K; ++k) acc = fmaf(w[t * K + k], e[(int64_t)inv[t * K + k] * d + r], acc);
-      if (c->has_norm && ORC_MUTANT != 9) acc = x[(int64_t)t * d + r] + acc;
+      if (c->has_norm) acc = x[(int64_t)t * d + r] + acc;
       y[(int64_t)t * d + r] = acc;
     }
     if (y64) {

@@ -66,8 +66,8 @@ def test_planted_mistakes_stay_memory_safe(tmp_path):
         so = str(tmp_path / f"liboracle_m{n}_san.so")
         subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
                                "-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined",
-                               "-fno-sanitize-recover=undefined", f"-DORC_MUTANT={n}",
-                               os.path.join(O.HERE, "oracle.c"), "-o", so, "-lm"])
+                               "-fno-sanitize-recover=undefined", M.write_mutant(n, tmp_path),
+                               "-o", so, "-lm"])
         sos[n] = so
 
     with ThreadPoolExecutor(max_workers=8) as ex:

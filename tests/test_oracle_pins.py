@@ -764,7 +764,10 @@ def test_idot_accuracy_band():
     a block of 32 to int8 adds error of RMS amax/(127*sqrt(12)); relative to the operand's RMS
     that is p_x for x (enters g and u independently) and p_h for h = SiLU(g)*u, so the layer's
     relative RMS error is about sqrt(2 p_x^2 + p_h^2), ~1% for Gaussian x (h is heavier-tailed
-    than real activations).  The measured error must sit within 0.7x..1.4x of that."""
+    than real activations).  The measured error must sit within 0.8x..1.2x of that: a path with
+    twice the error, or one that skips the re-quantisation of h (about 0.7x), fails.  The
+    measured 1.10% lies above the <= 1% band first proposed for this check, and above the
+    pages' ~0.3%: the prediction, not the band, is what Gaussian synthetic inputs give."""
     wl = W.WORKLOADS["tiny_t1"]
     L = _layer_inputs(wl)
     x = W.x_host(wl, 16)
@@ -777,8 +780,8 @@ def test_idot_accuracy_band():
         return np.abs(b).max(axis=1).mean() / (127 * math.sqrt(12)) / math.sqrt((b ** 2).mean())
 
     pred = math.sqrt(2 * block_noise(out["xn"]) ** 2 + block_noise(out["h"]) ** 2)
-    assert 0.7 * pred <= rel <= 1.4 * pred, (rel, pred)
-    assert 1e-3 <= rel <= 2e-2
+    assert 0.8 * pred <= rel <= 1.2 * pred, (rel, pred)
+    assert 5e-3 <= rel <= 1.5e-2
 
 
 def test_expert_size_matches_pages():
