@@ -2,27 +2,36 @@
 """Benchmark of the int4 routed-expert MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl coli|reference]
+                    [--configs all|none|name,name,...]
 
 A step is one pass of the whole layer (prep + router/top-K/union + gate/up SwiGLU + down/combine)
-over one batch of synthetic tokens that already sit in HBM; the token changes every step (a pool
-of 4096 seeded tokens), and L2 is flushed between steps by writing a 256 MB buffer, so expert
-weights always come from HBM.  Each step is timed with CUDA events on the stream the kernels run
-on; the per-kernel events give the roofline of the dominant kernel (gate/up).  With --gpus N under
-torchrun every rank runs its own replica on its own tokens (weak scaling, no collective on the
-data path) and the slowest rank's time is used.  Prints one JSON line.
+over one batch of synthetic tokens that already sit in HBM; the batch changes every step (a pool
+of seeded batches), and L2 is flushed between steps by writing a 256 MB buffer outside the timed
+events, so expert weights always come from HBM.  Each step is timed with CUDA events on the
+stream the kernels run on.  A second, profiled pass records events between the launches and
+gives the roofline of the dominant kernel: the fused expert kernel for one token, the gate/up
+kernel for 2-4 tokens, the two tensor-core GEMMs for a prefill batch.
+
+The JSON line's top level is the headline workload (--workload, default glm_decode_t1: one
+GLM-5.2-shaped layer, one token).  `configs` holds a shorter timed run of each of the other
+layer configurations (tiny layer, 4-token verify batch, 16-layer stack, 512-token prefill), each
+with its own roofline and clock record.
+
+With --gpus N under torchrun every rank runs its own replica on its own tokens (weak scaling, no
+collective on the data path) and the slowest rank's time is used.
 
 --impl reference times the plain CPU oracle (oracle/) on the host cores instead, on the same
-workload and metric; each of its steps is one token with the expert rows sampled so the whole
-run stays within a few minutes.
+workload and metric; each of its steps runs whole tokens of one batch through the oracle's
+layer (as many of the batch's tokens as the time budget allows).
 """
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -36,17 +45,24 @@ POOL = 4096
 FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+# the layer configurations the JSON line's `configs` object times besides the headline
+CONFIGS = ["tiny_t1", "glm_decode_t1", "glm_verify_t4", "glm_stack16_t1", "glm_prefill_t512"]
+# steps of a `configs` entry are capped so the whole default run stays within a few minutes
+CONFIG_STEP_CAP = {"glm_prefill_t512": 60, "glm_stack16_t1": 300}
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="glm_decode_t1", choices=sorted(W.WORKLOADS))
     p.add_argument("--impl", default="coli", choices=["coli", "reference"])
+    p.add_argument("--configs", default="all",
+                   help="'all', 'none', or a comma list of workloads to time besides the headline")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="target CPU time of the oracle baseline sample")
+                   help="target CPU time of the oracle baseline sample (all cores)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--pool", type=int, default=POOL, help="distinct token batches cycled")
@@ -68,12 +84,22 @@ def gateup_bytes(wl, n_union_total):
     return n_union_total * (wl.f * wl.d + 8 * wl.f)
 
 
-def hbm_peak():
+def expert_ops(wl, T):
+    """integer multiply-adds of one forward, counted as 2 ops each: every (token, expert) pair
+    and the shared expert's T rows run gate, up and down (3 d f MACs)"""
+    pairs = T * wl.K + (T if wl.n_shared else 0)
+    return 2 * pairs * 3 * wl.d * wl.f
+
+
+def peaks():
+    """(hbm GB/s, bf16 TFLOP/s burst, bf16 sustained, source)"""
     try:
         with open(PEAKS_FILE) as fh:
-            return float(json.load(fh)["hbm_gbs"]), "measured"
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained",
+                                                                            p["bf16_tflops"])), "measured"
     except Exception:
-        return FALLBACK_HBM, "fallback"
+        return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
 
 
 def recorded_traffic(kernel, workload):
@@ -98,6 +124,24 @@ def source_digest(names):
         with open(os.path.join(ROOT, "int4_routed_expert_quantize_gb300", "csrc", n), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 # ------------------------------------------------------------------ distributed ------------
@@ -182,65 +226,44 @@ def oracle_layer(wl, layer=0):
     return O.Layer(wl, layer)
 
 
-def oracle_sample_step(OL, x_tok, phi):
-    """One token through the oracle with a fraction phi of every expert's rows: full router,
-    top-K and union; gate/up on the first phi*f rows (the rest of h is zero), h re-quantised,
-    down on the first phi*d rows; combine in rank order.  phi = 1 is the whole layer."""
-    import numpy as np
-
-    from oracle import oracle as O
-    wl = OL.wl
-    if phi >= 1.0:
-        return OL.forward(x_tok, want_dump=False, want_y64=False)["y"]
-    d, f = wl.d, wl.f
-    xn, ids, w = O.route_only(wl, x_tok, OL.Wr, OL.bias, OL.gamma)
-    fr = max(32, int(round(phi * f / 32)) * 32)
-    dr = max(1, int(round(phi * d)))
-    y = np.zeros((x_tok.shape[0], dr), dtype=np.float32)
-    for t in range(x_tok.shape[0]):
-        qx, dx = O.quantize_q8(xn[t])
-        experts = ([(wl.E, 1.0)] if wl.n_shared else []) + list(zip(ids[t], w[t]))
-        for k, (ex, wk) in enumerate(experts):
-            rec, sc = OL.recs[int(ex)]
-            Wg = rec[: f * d // 2].reshape(f, d // 2)
-            Wu = rec[f * d // 2: f * d].reshape(f, d // 2)
-            Wd = rec[f * d:].reshape(d, f // 2)
-            g, _ = O.i4_matvec(np.ascontiguousarray(Wg[:fr]), np.ascontiguousarray(sc[:fr]), d, qx, dx)
-            u, _ = O.i4_matvec(np.ascontiguousarray(Wu[:fr]), np.ascontiguousarray(sc[f:f + fr]), d, qx, dx)
-            h = np.zeros(f, dtype=np.float32)
-            h[:fr] = [O.lib().orc_silu_mul(float(a), float(b)) for a, b in zip(g, u)]
-            qh, dh = O.quantize_q8(h)
-            e, _ = O.i4_matvec(np.ascontiguousarray(Wd[:dr]), np.ascontiguousarray(sc[2 * f:2 * f + dr]),
-                               f, qh, dh)
-            y[t] = e if k == 0 else (np.float32(wk) * e + y[t])
-    return y
-
-
-def cpu_baseline(wl, seconds):
-    """the oracle as it stands, whole layer per token, on a bounded sample of tokens"""
-    from oracle import oracle as O
-    OL = oracle_layer(wl)
-    ntok = 2
-    x = W.x_host(wl, 64 * wl.T)
-    # generate the experts of the candidate sample outside the timing
-    _, ids, _ = O.route_only(wl, x[: 16 * wl.T], OL.Wr, OL.bias, OL.gamma)
-    OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
-    # the 16 batches' experts are generated once; the timed loop cycles over those batches until
-    # the time budget is spent (each token streams all its experts' bytes, far more than the
-    # host's caches hold, so repeating a batch does not make it cheaper)
+def oracle_run(OL, x, seconds, min_batches=2):
+    """whole batches of x (cycled) through the oracle's layer until `seconds` have passed;
+    -> (batches, tokens, elapsed s)"""
+    T = OL.wl.T
+    nb = x.shape[0] // T
     t0 = time.perf_counter()
     done = 0
     while True:
-        j = done % 16
-        OL.forward(x[j * wl.T:(j + 1) * wl.T], want_dump=False, want_y64=False)
+        j = done % nb
+        OL.forward(x[j * T:(j + 1) * T], want_dump=False, want_y64=False)
         done += 1
         el = time.perf_counter() - t0
-        if el >= seconds and done >= ntok:
-            break
-    return {"value": done * wl.T / el, "unit": "tokens/s", "cores": O.lib().orc_num_threads(),
-            "kind": "oracle",
-            "sample": f"{done} batches of T={wl.T} token(s) of {wl.name} (16 distinct batches, "
-                      f"cycled) through the full layer (experts pre-generated), {el:.1f} s"}
+        if el >= seconds and done >= min_batches:
+            return done, done * T, el
+
+
+def cpu_baseline(wl, seconds):
+    """the oracle as it stands, whole layer per token, on a bounded sample of tokens: all host
+    cores, then one core"""
+    from oracle import oracle as O
+    OL = oracle_layer(wl)
+    x = W.x_host(wl, 16 * wl.T)
+    # generate the experts of the sample outside the timing
+    _, ids, _ = O.route_only(wl, x, OL.Wr, OL.bias, OL.gamma)
+    OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
+    lib = O.lib()
+    cores = lib.orc_num_threads()
+    nb, ntok, el = oracle_run(OL, x, seconds)
+    lib.orc_set_num_threads(1)
+    try:
+        nb1, ntok1, el1 = oracle_run(OL, x, seconds / 2, min_batches=1)
+    finally:
+        lib.orc_set_num_threads(cores)
+    return {"value": ntok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "value_1core": ntok1 / el1,
+            "sample": f"{nb} batches of T={wl.T} token(s) of {wl.name} (16 distinct batches, "
+                      f"cycled) through the full layer (experts pre-generated), {el:.1f} s on "
+                      f"{cores} threads; then {nb1} batches on 1 thread, {el1:.1f} s"}
 
 
 def run_reference(args):
@@ -249,74 +272,93 @@ def run_reference(args):
         return None
     from oracle import oracle as O
     wl = W.WORKLOADS[args.workload]
-    if wl.layers > 1:
+    layers = wl.layers
+    if layers > 1:  # one layer of the stack per token, rate divided by the layer count
         wl = W.WORKLOADS["glm_decode_t1"] if wl.d == 6144 else wl
     OL = oracle_layer(wl)
-    x = W.x_host(wl, 64 * wl.T)
+    nbatch = 8
+    x = W.x_host(wl, nbatch * wl.T)
     _, ids, _ = O.route_only(wl, x, OL.Wr, OL.bias, OL.gamma)
     OL.ensure(sorted(set(ids.ravel().tolist()) | ({wl.E} if wl.n_shared else set())))
-    # size the per-step sample: a full token if it fits the budget, else a row fraction
+    # tokens per step: the whole batch if the budget allows, else its first `m` tokens (each
+    # token through the full layer); the rate is tokens processed over time
     t0 = time.perf_counter()
-    oracle_sample_step(OL, x[: wl.T], 1.0)
-    full = time.perf_counter() - t0
-    phi = min(1.0, args.reference_budget / max(1, args.steps + args.warmup) / max(full, 1e-6))
-    phi = max(phi, 1.0 / 64)
+    OL.forward(x[:1], want_dump=False, want_y64=False)
+    per_token = time.perf_counter() - t0
+    m = int(max(1, min(wl.T, args.reference_budget / max(1, args.steps + args.warmup) / max(per_token, 1e-6))))
+
+    def step(i):
+        j = i % nbatch
+        OL.forward(x[j * wl.T: j * wl.T + m], want_dump=False, want_y64=False)
+
     for i in range(args.warmup):
-        j = i % 64
-        oracle_sample_step(OL, x[j * wl.T:(j + 1) * wl.T], phi)
+        step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        j = i % 64
-        oracle_sample_step(OL, x[j * wl.T:(j + 1) * wl.T], phi)
+        step(i)
     el = time.perf_counter() - t0
-    value = args.steps * wl.T * phi / el
+    value = args.steps * m / el / layers
     cores = O.lib().orc_num_threads()
-    sample = (f"one batch of T={wl.T} of {wl.name} per step with {phi:.4f} of every expert's rows "
-              f"(full router and union); tokens/s scaled by that fraction")
+    sample = (f"{m} of the {wl.T} token(s) of one {wl.name} batch per step, each through the full "
+              f"layer (router, union, every selected expert's rows)"
+              + (f"; rate divided by {layers} layers per token" if layers > 1 else ""))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "i4xi8->i32,f32", "data": "synthetic",
-            "config": {"workload": wl.name, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
-                       "n_shared": wl.n_shared, "T": wl.T, "layers": 1},
+            "config": {"workload": args.workload, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
+                       "n_shared": wl.n_shared, "T": wl.T, "layers": layers},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
 # ------------------------------------------------------------------ GPU arm ----------------
 
-def run_coli(args):
+class Bench:
+    """state shared by the timed runs of one process: rank, stream, flush buffer"""
+
+    def __init__(self, args):
+        import torch
+        self.args = args
+        self.world, self.rank, local = dist_info()
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            torch.cuda.set_device(0)
+        self.dev_index = torch.cuda.current_device()
+        self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.hbm, self.bf16, self.bf16_sus, self.peak_kind = peaks()
+
+    def flush_l2(self, i):
+        # write more than L2 holds: no line of the previous step's working set survives
+        self.flush.fill_(float(i & 1023))
+
+    def close(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def measure(B, wl, steps, warmup, want_e2e, pool):
+    """Timed run of one workload: `steps` forwards (graph replay unless --no-graph), each on a new
+    batch, L2 flushed before each; then a profiled pass for the per-kernel times.  -> dict"""
     import torch
 
     from int4_routed_expert_quantize_gb300 import coli, synthetic
-    world, rank, local = dist_info()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev_index = torch.cuda.current_device()
-    wl = W.WORKLOADS[args.workload]
+    args, world, rank = B.args, B.world, B.rank
     T = wl.T
     layers = [synthetic.build_layer(wl, layer=l, max_tokens=T) for l in range(wl.layers)]
     stacked = wl.layers > 1
-    npool = max(1, args.pool)
-    pool = synthetic.x_tokens(wl, npool * T, token0=rank * npool * T).view(npool, T, wl.d)
+    npool = max(1, min(pool, (1 << 28) // (T * wl.d * 4)))  # at most 256 MB of tokens
+    xpool = synthetic.x_tokens(wl, npool * T, token0=rank * npool * T).view(npool, T, wl.d)
     y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
-    xs = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")  # stack works in place
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-
-    def flush_l2(i):
-        # write more than L2 holds: no line of the previous step's working set survives
-        flush.fill_(float(i & 1023))
-    stream = torch.cuda.current_stream()
-
-    # one step's forward, optionally captured once into a CUDA graph (input copied into a static
-    # buffer before the timed events, so the graph replays the same pointers every step)
+    xs = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")  # the stack works in place
     xin = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
 
     def fwd():
         if stacked:
@@ -326,8 +368,8 @@ def run_coli(args):
 
     graph = None
     if not args.no_graph:
-        xin.copy_(pool[0])
-        xs.copy_(pool[0])
+        xin.copy_(xpool[0])
+        xs.copy_(xpool[0])
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -340,11 +382,8 @@ def run_coli(args):
         torch.cuda.synchronize()
 
     def step(i, evs):
-        flush_l2(i)
-        if stacked:
-            xs.copy_(pool[i % npool])
-        else:
-            xin.copy_(pool[i % npool])
+        B.flush_l2(i)
+        (xs if stacked else xin).copy_(xpool[i % npool])
         evs[0].record(stream)
         if graph is not None:
             graph.replay()
@@ -352,23 +391,21 @@ def run_coli(args):
             fwd()
         evs[1].record(stream)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i, [torch.cuda.Event(enable_timing=True) for _ in range(2)])
     torch.cuda.synchronize()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    clocks = ClockSampler(dev_index) if rank == 0 else None
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    clocks = ClockSampler(B.dev_index) if rank == 0 else None
     if clocks:
         clocks.start()
         time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("bench_timed")
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(args.warmup + i, events[i])
+    for i in range(steps):
+        step(warmup + i, events[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
-    torch.cuda.nvtx.range_pop()
     barrier(world)
     clk = clocks.stop() if clocks else None
     for L in layers:
@@ -376,114 +413,162 @@ def run_coli(args):
         if st != 0:
             raise RuntimeError(f"device status {st}")
     fwd_ms = [ev[0].elapsed_time(ev[1]) for ev in events]
-    mean_fwd_ms = statistics.fmean(fwd_ms)
     total_fwd_s = reduce_max(sum(fwd_ms) / 1000.0, world)
-    tokens = world * args.steps * T
-    value = tokens / total_fwd_s
-    # per-kernel durations: a second timed pass through the profiled entry point (events
-    # between the three launches; no programmatic overlap there)
-    kern = None
-    if not stacked and T <= 4:
-        n_prof = min(args.steps, 4000)
-        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_push("bench_profiled")
-        for i in range(n_prof):
-            flush_l2(i)
-            layers[0].forward_profiled(pool[i % npool], y, pev[i])
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-        kern = {"route": statistics.fmean(e[0].elapsed_time(e[1]) for e in pev),
-                "gateup": statistics.fmean(e[1].elapsed_time(e[2]) for e in pev),
-                "down": statistics.fmean(e[2].elapsed_time(e[3]) for e in pev),
-                "steps": n_prof}
-    n_launch = layers[0].launches(T)  # kernels one forward of one layer launches
-    # union size of each step (T=1: always K+1); averaged over the pool for T>1
+    value = world * steps * T / total_fwd_s
+    n_launch = sum(L.launches(T) for L in layers)
+
+    # per-kernel durations: a profiled pass (events between the launches, no programmatic
+    # overlap), every layer of the stack in turn
+    n_prof = min(steps, 400)
+    pev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers] for _ in range(n_prof)]
+    torch.cuda.synchronize()
+    for i in range(n_prof):
+        B.flush_l2(i)
+        if stacked:
+            xs.copy_(xpool[i % npool])
+            for L, ev in zip(layers, pev[i]):
+                L.forward_profiled(xs, xs, ev)
+        else:
+            layers[0].forward_profiled(xpool[i % npool], y, pev[i][0])
+    torch.cuda.synchronize()
+
+    def mean_ms(a, b):
+        return statistics.fmean(sum(e[a].elapsed_time(e[b]) for e in evl) for evl in pev)
+
+    kern = {"route": mean_ms(0, 1), "gateup": mean_ms(1, 2), "down": mean_ms(2, 3), "steps": n_prof}
+    # union size of each step (one token: always K + shared); averaged over sampled batches
     if T == 1:
         n_union = wl.K + wl.n_shared
     else:
         sizes = []
-        for i in range(min(args.steps, 256)):
-            dmp = layers[0].forward_debug(pool[i % npool])
+        for i in range(min(steps, 64 if T <= 4 else 4)):
+            dmp = layers[0].forward_debug(xpool[i % npool])
             sizes.append(int(dmp["n_union"].item()))
+            del dmp
         n_union = statistics.fmean(sizes)
     ebytes = expert_bytes(wl, n_union) * wl.layers
-    peak, peak_kind = hbm_peak()
-    mean_s = total_fwd_s / (args.steps)
+    mean_s = total_fwd_s / steps
     expert_gbs = ebytes / mean_s / 1e9
-    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_fwd_ms,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "i4xi8->i32,f32", "data": "synthetic",
+    out = {"value": value, "unit": "tokens/s", "ms_per_step": 1000.0 * mean_s,
            "config": {"workload": wl.name, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
-                      "n_shared": wl.n_shared, "T": T, "layers": wl.layers,
+                      "n_shared": wl.n_shared, "T": T, "layers": wl.layers, "bias": wl.bias,
                       "resident_expert_gb": round(wl.layers * (wl.E + wl.n_shared) * wl.expert_bytes / 1e9, 2),
                       "l2": "flushed between steps (256 MB write, outside the timed events)",
                       "tokens": f"pool of {npool} seeded batches, one per step",
                       "launch": "CUDA graph replay" if graph is not None else "direct launches"},
+           "steps": steps, "warmup": warmup,
            "expert_bytes_per_step": ebytes, "mean_union_experts": n_union,
-           "expert_gbs": expert_gbs, "expert_hbm_frac": expert_gbs / peak,
-           "wall_s": wall, "gpu_launches": n_launch * wl.layers * args.steps}
-    if kern:
-        # the dominant kernel: the fused expert kernel when the forward runs as two launches
-        # (all union expert bytes), else the gate/up kernel (its two thirds of them)
-        if n_launch == 2:
-            name, gb, t_ms = "expert_fused_kernel", expert_bytes(wl, n_union), kern["gateup"]
-            kern = {"route": kern["route"], "experts": kern["gateup"], "steps": kern["steps"]}
-        else:
-            name, gb, t_ms = "gateup_decode_kernel", gateup_bytes(wl, n_union), kern["gateup"]
-            db = n_union * (wl.d * wl.f // 2 + 4 * wl.d)
-            out["down_gbs"] = db / (kern["down"] / 1000.0) / 1e9
+           "expert_gbs": expert_gbs, "expert_hbm_frac": expert_gbs / B.hbm,
+           "wall_s": wall, "gpu_launches": n_launch * steps + n_launch * n_prof, "kernel_ms": kern}
+    hbm_src = f"{B.peak_kind} hbm_gbs (copy, burst)"
+    if T > 4:
+        # tensor-core path: the two GEMM launches (gate/up, then down + the combine)
+        t_ms = kern["gateup"] + kern["down"]
+        ach = expert_bytes(wl, n_union) / (t_ms / 1000.0) / 1e9
+        flops = expert_ops(wl, T)
+        tf = flops / (t_ms / 1000.0) / 1e12
+        out["roofline"] = {"kernel": "expert_gemm_kernel (gate/up, down) + combine_kernel",
+                           "bound": "hbm", "achieved": ach, "peak": B.hbm, "peak_source": hbm_src,
+                           "unit": "GB/s", "frac": ach / B.hbm,
+                           "algorithmic_bytes": expert_bytes(wl, n_union),
+                           "traffic": recorded_traffic("expert_gemm_kernel", wl.name),
+                           "tensor": {"achieved": tf, "peak": B.bf16, "unit": "TFLOP/s",
+                                      "frac": tf / B.bf16, "algorithmic_flops": flops,
+                                      "peak_source": f"{B.peak_kind} bf16_tflops (burst); the MMAs "
+                                                     "run kind::f16 on bf16 copies of the int8/int4 codes"},
+                           "timing": "CUDA events around the launches, profiled pass"}
+    elif n_launch == 2 * wl.layers:
+        # the fused expert kernel reads every union expert's bytes
+        t_ms = kern["gateup"] / wl.layers
+        gb = expert_bytes(wl, n_union)
         ach = gb / (t_ms / 1000.0) / 1e9
-        out["roofline"] = {"kernel": name, "bound": "hbm", "achieved": ach,
-                           "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                           "unit": "GB/s", "frac": ach / peak, "algorithmic_bytes": gb,
-                           "traffic": recorded_traffic(name, wl.name),
+        out["roofline"] = {"kernel": "expert_fused_kernel", "bound": "hbm", "achieved": ach,
+                           "peak": B.hbm, "peak_source": hbm_src, "unit": "GB/s",
+                           "frac": ach / B.hbm, "algorithmic_bytes": gb,
+                           "traffic": recorded_traffic("expert_fused_kernel", wl.name),
+                           "timing": "CUDA events around the launch, profiled pass"
+                                     + (" (mean over the layers)" if stacked else "")}
+        if wl.name == "tiny_t1":
+            out["roofline"]["bound"] = "latency"
+            out["roofline"]["note"] = "1 MB per step: launch- and latency-bound, %HBM not meaningful"
+    else:
+        gb = gateup_bytes(wl, n_union)
+        t_ms = kern["gateup"] / wl.layers
+        ach = gb / (t_ms / 1000.0) / 1e9
+        out["roofline"] = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": ach,
+                           "peak": B.hbm, "peak_source": hbm_src, "unit": "GB/s",
+                           "frac": ach / B.hbm, "algorithmic_bytes": gb,
+                           "traffic": recorded_traffic("gateup_decode_kernel", wl.name),
                            "timing": "CUDA events around the launch, profiled pass"}
-        out["kernel_ms"] = kern
-        out["gpu_launches"] += n_launch * kern["steps"]
+        db = n_union * (wl.d * wl.f // 2 + 4 * wl.d)
+        out["down_gbs"] = db / (kern["down"] / 1000.0) / 1e9
     if clk:
         out["clocks"] = clk
-    # end to end through the host-buffer entry point (pinned buffers, copies in the region)
-    if not args.no_e2e and not stacked:
-        xh = pool[:64].cpu().pin_memory()
-        yh = torch.empty((T, wl.d), dtype=torch.float32).pin_memory()
-        n_e2e = min(args.steps, 2000)
-        for i in range(min(20, max(3, args.warmup))):
-            layers[0].forward_host(xh[i % len(xh)], yh)
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(n_e2e):
-            layers[0].forward_host(xh[i % len(xh)], yh)
-        el = reduce_max(time.perf_counter() - t0, world)
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    if want_e2e:
+        xh = xpool[:64].cpu().pin_memory()
+        n_e2e = min(steps, 2000)
+        if not stacked:
+            yh = torch.empty((T, wl.d), dtype=torch.float32).pin_memory()
+            for i in range(min(20, max(3, warmup))):
+                layers[0].forward_host(xh[i % len(xh)], yh)
+            barrier(world)
+            t0 = time.perf_counter()
+            for i in range(n_e2e):
+                layers[0].forward_host(xh[i % len(xh)], yh)
+            el = reduce_max(time.perf_counter() - t0, world)
+            note = ("coli_moe_forward_host: x into the handle's pinned staging, one graph launch "
+                    "(H2D x, forward, D2H y), sync")
+        else:
+            barrier(world)
+            t0 = time.perf_counter()
+            for i in range(n_e2e):
+                xs.copy_(xh[i % len(xh)], non_blocking=True)
+                coli.stack_forward(layers, xs)
+                yh = xs.to("cpu")
+            el = reduce_max(time.perf_counter() - t0, world)
+            note = "pinned H2D x, coli_moe_stack_forward (16 layers), D2H y"
         out["e2e"] = {"value": world * n_e2e * T / el, "unit": "tokens/s",
                       "h2d_bytes_per_step": T * wl.d * 4, "d2h_bytes_per_step": T * wl.d * 4,
-                      "steps": n_e2e, "note": "coli_moe_forward_host: H2D x, forward, D2H y, sync"}
-    elif not args.no_e2e and stacked:
-        xh = pool[:64].cpu().pin_memory()
-        n_e2e = min(args.steps, 500)
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(n_e2e):
-            xs.copy_(xh[i % len(xh)], non_blocking=True)
-            coli.stack_forward(layers, xs)
-            yh = xs.to("cpu")
-        el = reduce_max(time.perf_counter() - t0, world)
-        out["e2e"] = {"value": world * n_e2e * T / el, "unit": "tokens/s",
-                      "h2d_bytes_per_step": T * wl.d * 4, "d2h_bytes_per_step": T * wl.d * 4,
-                      "steps": n_e2e}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl if not stacked else W.WORKLOADS["glm_decode_t1"],
-                                           args.cpu_seconds)
-        if stacked:
-            out["cpu_baseline"]["value"] /= wl.layers
-            out["cpu_baseline"]["sample"] += f"; divided by {wl.layers} layers per token"
+                      "steps": n_e2e, "note": note}
     for L in layers:
         L.close()
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return out if rank == 0 else None
+    del layers, xpool
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_coli(args):
+    B = Bench(args)
+    wl = W.WORKLOADS[args.workload]
+    head = measure(B, wl, args.steps, args.warmup, not args.no_e2e, args.pool)
+    out = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": B.world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "i4xi8->i32,f32", "data": "synthetic"}
+    out.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step", "steps", "warmup")})
+    if args.configs != "none":
+        names = CONFIGS if args.configs == "all" else [n for n in args.configs.split(",") if n]
+        cfgs = {}
+        for name in names:
+            if name == wl.name:
+                continue
+            cwl = W.WORKLOADS[name]
+            steps = max(1, min(args.steps, CONFIG_STEP_CAP.get(name, args.steps)))
+            warm = max(3, min(args.warmup, 10))
+            cfgs[name] = measure(B, cwl, steps, warm, False, args.pool)
+            out["gpu_launches"] += cfgs[name]["gpu_launches"]
+        out["configs"] = cfgs
+    if B.rank == 0 and B.world == 1 and not args.no_cpu_baseline:
+        base = wl if wl.layers == 1 else W.WORKLOADS["glm_decode_t1"]
+        out["cpu_baseline"] = cpu_baseline(base, args.cpu_seconds)
+        if wl.layers > 1:
+            out["cpu_baseline"]["value"] /= wl.layers
+            out["cpu_baseline"]["value_1core"] /= wl.layers
+            out["cpu_baseline"]["sample"] += f"; divided by {wl.layers} layers per token"
+    B.close()
+    return out if B.rank == 0 else None
 
 
 def main(argv=None):

@@ -55,7 +55,7 @@ extern "C" {
 typedef struct coli_moe coli_moe; /* opaque; owned by the library */
 
 typedef struct {
-  int d;            /* model width; multiple of 128, d/32 divisible by ceil(d/1024), <= 16384 */
+  int d;            /* model width; multiple of 128, d/32 divisible by ceil(d/1024), <= 8192  */
   int f;            /* expert hidden width (routed and shared); same rules as d              */
   int n_experts;    /* E routed experts, 1..1024                                              */
   int top_k;        /* K experts per token, 1..min(E, 32)                                      */
@@ -128,16 +128,23 @@ int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
                            const coli_moe_dump* dump, void* stream);
 
 /* coli_moe_forward that also records `events[0..3]` (cudaEvent_t handles created by the
- * caller) on `stream`: before the routing kernel, after it, after the gate/up kernel and after
- * the down kernel -- so the caller can time each launch.  When the forward runs the expert half
- * as one fused kernel (coli_moe_launches returns 2) events 1..2 bracket that kernel and events
- * 2..3 nothing.  The events serialise the launches (no programmatic overlap between them).
- * T <= 4.  EINVAL: n_events < 4 or T out of range. */
+ * caller) on `stream`: before the routing kernel(s), after them, after the gate/up kernel and
+ * after the down kernel -- so the caller can time each launch.  When the forward runs the expert
+ * half as one fused kernel (coli_moe_launches returns 2) events 1..2 bracket that kernel and
+ * events 2..3 nothing; on the batched tensor-core path events 0..1 bracket the five routing
+ * launches and events 2..3 the down GEMM and the combine.  The events serialise the launches (no
+ * programmatic overlap between them).  T <= 4, or a batch that takes the tensor-core path.
+ * EINVAL: n_events < 4 or T out of range. */
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream);
 
 /* Host-buffer form: copies x_host [T,d] to the device, runs forward, copies y back to
- * y_host [T,d] and synchronises `stream`.  Pinned host memory gives the fastest copies. */
+ * y_host [T,d] and synchronises `stream`; any host memory (pageable or pinned).  Batches of up to
+ * 8 tokens go through the handle's own pinned staging and one CUDA graph per token count (copy
+ * in, the forward's kernels, copy out), captured on the handle's stream on the first call with
+ * that count and launched on `stream`; larger batches copy directly.  Returns COLI_ETIMEOUT (and
+ * clears it, as coli_moe_status does) when a bounded device wait of this forward gave up; y_host
+ * is then undefined. */
 int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host, void* stream);
 
 /* Runs n_layers has_norm layers in sequence on x_dev [T,d] in place:
@@ -190,15 +197,17 @@ int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_
  * score + optional selection bias with ties to the lower id, weights renormalised over the
  * selected scores) -- bit-identical to the ids and weights coli_moe_forward uses for the same
  * inputs (without RMSNorm).  The source pages have no counterpart: this is an interface for
- * callers that cannot allocate device memory, such as code running while a stream is captured
- * into a CUDA graph (allocation calls are not allowed there) or a process whose device memory
- * is owned by another allocator.  It needs no handle: x_dev [T,d], W_r_dev [E,d] (row major),
- * bias_dev [E] or NULL, outputs ids_dev [T,K] and w_dev [T,K], all device pointers owned by the
- * caller; x_dev and W_r_dev 16-byte aligned.  Limits: T <= 4, T*E <= 4096, E <= 1024,
- * K <= min(E, 32), d a multiple of 128 up to 8192 (EINVAL beyond them).  Its scratch (16 KB)
- * is a fixed array in the library's device memory, present on every device that loads the
- * library until the process exits; the first call on a device looks up that array's address
- * (make it before any stream capture); calls that overlap on the GPU race on the array. */
+ * callers that cannot call cudaMalloc, such as a process whose device memory is owned entirely
+ * by another allocator (a serving framework that reserves the device up front and hands out
+ * pieces of its own pool), where a direct allocation would fail or break that allocator's
+ * accounting.  It needs no handle: x_dev [T,d], W_r_dev [E,d] (row major), bias_dev [E] or
+ * NULL, outputs ids_dev [T,K] and w_dev [T,K], all device pointers owned by the caller; x_dev
+ * and W_r_dev 16-byte aligned.  Limits: T <= 4, T*E <= 4096, E <= 1024, K <= min(E, 32), d a
+ * multiple of 128 up to 8192 (EINVAL beyond them).  Its scratch (16 KB) is a fixed array in the
+ * library's device memory, present on every device that loads the library until the process
+ * exits; the first call on a device looks up that array's address and keeps it, so calls after
+ * a cudaDeviceReset of that device are not supported.  Every call shares the array: calls that
+ * overlap on the GPU (for example on two streams) race on it. */
 int coli_route_noalloc(const float* x_dev, int T, const float* W_r_dev, const float* bias_dev,
                        int E, int d, int K, float routed_scale, int32_t* ids_dev, float* w_dev,
                        void* stream);

@@ -126,7 +126,8 @@ bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const 
                        int d, int f, int E, int slots, int prow, int tmax);
 cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, const Store& st,
                                    const Work& w, const PrefillWork& pw, const PrefillMaps& maps,
-                                   const ExpertDebug& dbg, int num_sms, cudaStream_t stream);
+                                   const ExpertDebug& dbg, int num_sms, cudaStream_t stream,
+                                   cudaEvent_t after_gateup = nullptr);
 cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
                                  int64_t dst_row_stride, cudaStream_t stream);
 cudaError_t launch_permute_router(const float* src, float* dst, int E, int d,

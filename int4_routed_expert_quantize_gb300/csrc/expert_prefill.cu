@@ -538,8 +538,12 @@ bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const 
 
 cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, const Store& st, const Work& w,
                                    const PrefillWork& pw, const PrefillMaps& maps, const ExpertDebug& dbg,
-                                   int num_sms, cudaStream_t stream) {
+                                   int num_sms, cudaStream_t stream, cudaEvent_t after_gateup) {
   for (int down = 0; down < 2; ++down) {
+    if (down && after_gateup) {
+      const cudaError_t e = cudaEventRecord(after_gateup, stream);
+      if (e != cudaSuccess) return e;
+    }
     PfArgs args;
     args.s = s;
     args.st = st;

@@ -1,9 +1,10 @@
 // Routing with no device allocation at all: the sigmoid top-K router of the layer (same
-// arithmetic, bit for bit) for callers that cannot call cudaMalloc -- for example code that
-// runs while a stream is being captured into a CUDA graph (where allocation calls are not
-// allowed), or a process whose device memory is owned entirely by another allocator.  The
-// caller passes inputs and outputs; the scratch the kernel needs (the per-token scores and the
-// last-CTA ticket) lives in the fixed array below.
+// arithmetic, bit for bit) for callers that cannot call cudaMalloc -- for example a process
+// whose device memory is owned entirely by another allocator (a serving framework that
+// reserves the whole device up front and hands out pieces of its own pool), where a direct
+// allocation would fail or break that allocator's accounting.  The caller passes inputs and
+// outputs; the scratch the kernel needs (the per-token scores and the last-CTA ticket) lives in
+// the fixed array below.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,6 +13,7 @@
 #include "coli_device.cuh"
 #include "coli_internal.h"
 #include "coli_moe.h"
+#include "coli_select.cuh"
 
 namespace coli {
 namespace {
@@ -72,48 +74,52 @@ __global__ void __launch_bounds__(256) route_noalloc_kernel(const float* __restr
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // the last CTA: top-K per token by score + bias (ties to the lower id), weights renormalised
-  // over the selected scores summed in rank order
+  // the last CTA: top-K per token by score + bias, ranked by the same order-preserving key as
+  // the layer's selection (a taken expert's key is 0; a tie goes to the lower id, so scores that
+  // are not numbers give the same ids too), weights renormalised over the selected scores summed
+  // in rank order
+  const int NM = E <= 256 ? 8 : 32;  // experts per lane the layer's selection scans
   for (int t = warp; t < T; t += nwarp) {
     const float* sc = scores + t * E;
     uint32_t taken = 0;
+    float S = 0.0f, mine = 0.0f;
+    int my = 0;
     for (int k = 0; k < K; ++k) {
-      float bv = 0.0f;
-      int bi = 0x7fffffff;
-      for (int m = 0; m * 32 + lane < E; ++m) {
-        if ((taken >> m) & 1u) continue;
+      uint32_t bk = 0;
+      int bm = 0;
+      for (int m = 0; m < NM; ++m) {
         const int e = m * 32 + lane;
-        const float sv = __ldcg(sc + e);
-        const float v = bias ? __fadd_rn(sv, bias[e]) : sv;
-        if (bi == 0x7fffffff || v > bv) {
-          bv = v;
-          bi = e;
+        uint32_t key = 0;
+        if (e < E && !((taken >> m) & 1u)) {
+          const float sv = __ldcg(sc + e);
+          key = score_key(bias ? __fadd_rn(sv, bias[e]) : sv);
+        }
+        if (m == 0 || key > bk) {
+          bk = key;
+          bm = m;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(FULL, bv, off);
-        const int oi = __shfl_xor_sync(FULL, bi, off);
-        if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) ids_out[t * K + k] = bi;
+      const uint32_t top = __reduce_max_sync(FULL, bk);
+      uint32_t win = __reduce_min_sync(FULL, bk == top ? (uint32_t)(bm * 32 + lane) : 0xFFFFFFFFu);
+      win = win < (uint32_t)E ? win : 0u;
+      if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+      const float v = __ldcg(sc + win);
+      S = k == 0 ? v : __fadd_rn(S, v);
+      my = lane == k ? (int)win : my;
+      mine = lane == k ? v : mine;
+    }
+    if (lane < K) {
+      ids_out[t * K + lane] = my;
+      w_out[t * K + lane] = __fmul_rn(__fdiv_rn(mine, S), routed_scale);
     }
     __syncwarp();
-    if (lane == 0) {
-      float S = __ldcg(sc + ids_out[t * K]);
-      for (int k = 1; k < K; ++k) S = __fadd_rn(S, __ldcg(sc + ids_out[t * K + k]));
-      for (int k = 0; k < K; ++k)
-        w_out[t * K + k] = __fmul_rn(__fdiv_rn(__ldcg(sc + ids_out[t * K + k]), S), routed_scale);
-    }
   }
   if (threadIdx.x == 0) *ticket = 0;
 }
 
-// once per device, with that device current: resolve the array's device address
+// once per device, with that device current: resolve the array's device address.  The address
+// is kept for the life of the process, so calls after a cudaDeviceReset of that device (which
+// unloads the module that holds the array) are not supported.
 int scratch_for_current_device(float** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) return COLI_ECUDA;

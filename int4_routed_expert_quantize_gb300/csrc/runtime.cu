@@ -15,6 +15,10 @@
 
 using namespace coli;
 
+namespace {
+constexpr int kHostGraphMaxT = 8;  // token counts whose host-buffer forward runs as a cached graph
+}
+
 struct coli_moe {
   coli_moe_config cfg{};
   int device = 0;
@@ -23,6 +27,13 @@ struct coli_moe {
   Store st;
   Work w;
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
+  // coli_moe_forward_host for small batches: pinned staging for x, y and the status word, and
+  // one instantiated graph per token count (copy in, the forward's kernels, copy out, status)
+  float* pin_x = nullptr;
+  float* pin_y = nullptr;
+  int32_t* pin_status = nullptr;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t host_graph[kHostGraphMaxT + 1] = {};
   bool prefill = false;     // the tensor-core path is set up (max_tokens > kDecodeTmax)
   int prefill_min = kPrefillMinTokens;  // batches of at least this many tokens take it
   bool fused = false;       // one-token forwards use the fused expert kernel
@@ -61,7 +72,21 @@ int dalloc(coli_moe* h, T** p, size_t bytes) {
   return COLI_OK;
 }
 
+void drop_host_graphs(coli_moe* h) {
+  for (cudaGraphExec_t& g : h->host_graph)
+    if (g) {
+      cudaGraphExecDestroy(g);
+      g = nullptr;
+    }
+}
+
 void free_all(coli_moe* h) {
+  drop_host_graphs(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  h->cap_stream = nullptr;
+  if (h->pin_x) cudaFreeHost(h->pin_x);
+  h->pin_x = h->pin_y = nullptr;
+  h->pin_status = nullptr;
   for (void* p : h->allocs) cudaFree(p);
   h->allocs.clear();
 }
@@ -94,8 +119,22 @@ Shape shape_of(const coli_moe* h, int T) {
 
 int copy_dump(coli_moe* h, int T, const coli_moe_dump* dump, cudaStream_t stream);
 
-std::once_flag g_cfg_once;
-cudaError_t g_cfg_err = cudaSuccess;
+// The kernels' shared-memory attributes are set per device (cudaFuncSetAttribute applies to the
+// current device's context), once for each device a handle is created on.
+constexpr int kMaxDevices = 64;
+bool g_configured[kMaxDevices] = {};
+std::mutex g_cfg_mutex;
+
+cudaError_t configure_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  if (g_configured[dev]) return cudaSuccess;
+  cudaError_t e = configure_expert_kernels();
+  if (e == cudaSuccess) e = configure_route_kernels();
+  if (e == cudaSuccess) e = configure_fused_kernels();
+  if (e == cudaSuccess) g_configured[dev] = true;
+  return e;
+}
 
 int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump* dump,
                cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
@@ -136,7 +175,7 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
 }
 
 int run_prefill(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump* dump,
-                cudaStream_t stream) {
+                cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
   const Shape s = shape_of(h, T);
   ExpertDebug dbg;
   if (dump) {
@@ -148,10 +187,15 @@ int run_prefill(coli_moe* h, const float* x, int T, float* y, const coli_moe_dum
     if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
     if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
   }
-  cudaError_t e = launch_route_batch(x, s, h->st, h->w, h->maps.wr, h->maps.xnp, h->pw.tile_prefix,
-                                     kPrefillTileN, h->pw.xb, h->pw.dxp, stream);
+  cudaError_t e = ev ? cudaEventRecord(ev[0], stream) : cudaSuccess;
   if (e == cudaSuccess)
-    e = launch_prefill_experts(x, y, s, h->st, h->w, h->pw, h->maps, dbg, h->num_sms, stream);
+    e = launch_route_batch(x, s, h->st, h->w, h->maps.wr, h->maps.xnp, h->pw.tile_prefix,
+                           kPrefillTileN, h->pw.xb, h->pw.dxp, stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], stream);
+  if (e == cudaSuccess)
+    e = launch_prefill_experts(x, y, s, h->st, h->w, h->pw, h->maps, dbg, h->num_sms, stream,
+                               ev ? ev[2] : nullptr);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], stream);
   if (e != cudaSuccess) return COLI_ECUDA;
   if (dump) {
     const long P = (long)T * h->cfg.top_k + (h->cfg.n_shared ? T : 0);
@@ -222,6 +266,35 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   return COLI_OK;
 }
 
+// The instantiated host-buffer graph of T tokens, captured on first use on the handle's own
+// stream: copy of the pinned x into the device buffer, the forward's launches, copies of y and
+// the status word into the pinned staging.
+int host_graph_for(coli_moe* h, int T, float* dx, float* dy) {
+  if (h->host_graph[T]) return COLI_OK;
+  if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
+  const size_t n = (size_t)T * h->cfg.d;
+  cudaStream_t cs = h->cap_stream;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return COLI_ECUDA;
+  int rc = COLI_OK;
+  if (cudaMemcpyAsync(dx, h->pin_x, sizeof(float) * n, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    rc = COLI_ECUDA;
+  if (rc == COLI_OK) rc = forward_impl(h, dx, T, dy, nullptr, cs);
+  if (rc == COLI_OK &&
+      (cudaMemcpyAsync(h->pin_y, dy, sizeof(float) * n, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+       cudaMemcpyAsync(h->pin_status, h->w.status, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
+           cudaSuccess))
+    rc = COLI_ECUDA;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamEndCapture(cs, &g) != cudaSuccess && rc == COLI_OK) rc = COLI_ECUDA;
+  if (rc == COLI_OK && cudaGraphInstantiate(&h->host_graph[T], g, 0) != cudaSuccess) {
+    h->host_graph[T] = nullptr;
+    rc = COLI_ECUDA;
+  }
+  if (g) cudaGraphDestroy(g);
+  if (rc != COLI_OK) cudaGetLastError();
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,6 +302,7 @@ extern "C" {
 int coli_moe_set_prefill_min(coli_moe* h, int min_tokens) {
   if (!h || min_tokens <= kDecodeTmax) return COLI_EINVAL;
   h->prefill_min = min_tokens;
+  drop_host_graphs(h);  // the cached host-buffer graphs may have taken the other path
   return COLI_OK;
 }
 
@@ -277,12 +351,10 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
         down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst < 2)
       return COLI_EUNSUPPORTED;
   }
-  std::call_once(g_cfg_once, [] {
-    g_cfg_err = configure_expert_kernels();
-    if (g_cfg_err == cudaSuccess) g_cfg_err = configure_route_kernels();
-    if (g_cfg_err == cudaSuccess) g_cfg_err = configure_fused_kernels();
-  });
-  if (g_cfg_err != cudaSuccess) return COLI_ECUDA;
+  if (configure_device(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return COLI_ECUDA;
+  }
 
   coli_moe* h = new (std::nothrow) coli_moe();
   if (!h) return COLI_ENOMEM;
@@ -346,6 +418,20 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     }
   }
 #undef ALLOC
+  if (rc == COLI_OK) {
+    const size_t n = (size_t)(Tm < kHostGraphMaxT ? Tm : kHostGraphMaxT) * d;
+    void* p = nullptr;
+    if (cudaHostAlloc(&p, sizeof(float) * 2 * n + 64, cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      rc = COLI_ENOMEM;
+    } else {
+      h->pin_x = static_cast<float*>(p);
+      h->pin_y = h->pin_x + n;
+      h->pin_status = reinterpret_cast<int32_t*>(h->pin_y + n);
+      *h->pin_status = 0;
+      if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) rc = COLI_ECUDA;
+    }
+  }
   if (rc == COLI_OK && (cudaMemset(h->w.sel_flag, 0, 16) != cudaSuccess ||
                         cudaMemset(h->w.status, 0, 16) != cudaSuccess ||
                         cudaDeviceSynchronize() != cudaSuccess))
@@ -407,6 +493,7 @@ int coli_moe_load_router(coli_moe* h, const float* W_r, const float* bias, const
     h->st.bias = nullptr;
   }
   h->router_loaded = true;
+  drop_host_graphs(h);  // the cached host-buffer graphs hold the old bias pointer
   return COLI_OK;
 }
 
@@ -467,8 +554,9 @@ int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
 
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream) {
-  if (!h || !events || n_events < 4 || T < 1 || T > kDecodeTmax || T > h->cfg.max_tokens)
-    return COLI_EINVAL;
+  if (!h || !events || n_events < 4 || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
+  const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
+  if (T > kDecodeTmax && !batched) return COLI_EINVAL;
   for (int i = 0; i < 4; ++i)
     if (!events[i]) return COLI_EINVAL;
   if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15u) || ((uintptr_t)y_dev & 3u)) return COLI_EINVAL;
@@ -480,6 +568,7 @@ int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_d
   if (rc) return rc;
   cudaEvent_t ev[4];
   for (int i = 0; i < 4; ++i) ev[i] = (cudaEvent_t)events[i];
+  if (batched) return run_prefill(h, x_dev, T, y_dev, nullptr, (cudaStream_t)stream, ev);
   return run_decode(h, x_dev, T, y_dev, nullptr, (cudaStream_t)stream, ev);
 }
 
@@ -493,13 +582,28 @@ int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host
   const size_t n = (size_t)T * h->cfg.d;
   float* dx = h->dev_io;
   float* dy = h->cfg.has_norm ? h->dev_io : h->dev_io + (size_t)h->cfg.max_tokens * h->cfg.d;
+  if (T <= kHostGraphMaxT && !h->fault) {
+    // small batch: x into the pinned staging, one graph launch (copy in, kernels, copy out,
+    // status word), one synchronisation, y out of the staging
+    rc = host_graph_for(h, T, dx, dy);
+    if (rc) return rc;
+    memcpy(h->pin_x, x_host, sizeof(float) * n);
+    if (cudaGraphLaunch(h->host_graph[T], st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+      return COLI_ECUDA;
+    memcpy(y_host, h->pin_y, sizeof(float) * n);
+    // a bounded device wait that gave up leaves y undefined: report it (and clear it) here
+    return *h->pin_status == COLI_OK ? COLI_OK : coli_moe_status(h, stream);
+  }
   if (cudaMemcpyAsync(dx, x_host, sizeof(float) * n, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return COLI_ECUDA;
   rc = forward_impl(h, dx, T, dy, nullptr, stream);
   if (rc) return rc;
   if (cudaMemcpyAsync(y_host, dy, sizeof(float) * n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return COLI_ECUDA;
-  return cuda_status(cudaStreamSynchronize(st));
+  if (cudaStreamSynchronize(st) != cudaSuccess) return COLI_ECUDA;
+  // the call has synchronised anyway: report a bounded device wait that gave up (y_host is then
+  // undefined) instead of leaving it for coli_moe_status
+  return coli_moe_status(h, stream);
 }
 
 int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, int T,

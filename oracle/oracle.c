@@ -24,6 +24,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* threads the parallel loops use from now on (n >= 1); the results do not depend on it */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------------------------
  * Formats.  P1 §3.1 "int4 packed": two 4-bit values per byte, one f32 scale per row.
  * Readings (the pages are silent): symmetric scale s = max|w| / 7, codes round(w/s) clamped to

@@ -160,6 +160,7 @@ int orc_moe_dequant64(const orc_cfg* cfg, const float* xn, int T, const int32_t*
                       const float* x_resid, double* y);
 
 int orc_num_threads(void);
+void orc_set_num_threads(int n); /* threads of the parallel loops; results do not depend on it */
 
 #ifdef __cplusplus
 }

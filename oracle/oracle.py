@@ -100,6 +100,8 @@ def lib():
         L.orc_moe_dequant64.argtypes = [ctypes.POINTER(Cfg), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]
         L.orc_moe_dequant64.restype = _i
         L.orc_num_threads.restype = _i
+        L.orc_set_num_threads.argtypes = [_i]
+        L.orc_set_num_threads.restype = None
         _lib = L
     return _lib
 

@@ -1,8 +1,8 @@
-"""The routing entry point that allocates nothing (for callers that cannot call cudaMalloc,
-e.g. while a stream is being captured into a CUDA graph, or when another allocator owns the
-device memory).  Checked through the C ABI against the layer's own routing (the ids and
-weights coli_moe_forward_debug reports), bit for bit, on two calls in a row.  Kept in a file
-pytest collects last."""
+"""The routing entry point that allocates nothing, for callers that cannot call cudaMalloc
+(for example a process whose device memory belongs to another allocator's pool).  Checked
+through the C ABI against the layer's own routing (the ids and weights
+coli_moe_forward_debug reports), bit for bit, on two calls in a row.  Kept in a file pytest
+collects last."""
 import numpy as np
 import pytest
 import torch
@@ -35,6 +35,27 @@ def test_route_noalloc_matches_layer_routing_twice(name):
         torch.cuda.synchronize()
         assert np.array_equal(ids.cpu().numpy(), ref["ids"].cpu().numpy()), call
         assert np.array_equal(w.cpu().numpy(), ref["w"].cpu().numpy()), call
+    layer.close()
+
+
+def test_route_noalloc_ranks_non_finite_scores_like_the_layer():
+    """selection biases of NaN and +-inf: both sides rank by the same order-preserving key, so
+    the ids and weights still agree bit for bit, on two calls in a row"""
+    wl = W.WORKLOADS["tiny_t1"]
+    layer = synthetic.build_layer(wl, max_tokens=4)
+    Wr = torch.empty((wl.E, wl.d), dtype=torch.float32, device="cuda")
+    W.router_dev(wl, 0, Wr)
+    b = np.zeros(wl.E, dtype=np.float32)
+    b[3], b[5], b[7], b[20] = np.nan, -np.inf, np.inf, -np.nan
+    layer.load_router(Wr, b)
+    bias = torch.from_numpy(b).cuda()
+    for call, (T, token0) in enumerate([(4, 11), (2, 40)]):
+        x = synthetic.x_tokens(wl, T, token0=token0)
+        ref = layer.forward_debug(x)
+        ids, w = coli.route_noalloc(x, Wr, wl.K, bias=bias)
+        torch.cuda.synchronize()
+        assert np.array_equal(ids.cpu().numpy(), ref["ids"].cpu().numpy()), call
+        assert np.array_equal(w.cpu().numpy().view(np.uint32), ref["w"].cpu().numpy().view(np.uint32)), call
     layer.close()
 
 
