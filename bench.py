@@ -507,7 +507,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
     # end to end through the host-buffer entry point (copies inside the timed region)
     if want_e2e:
         xh = xpool[:64].cpu().pin_memory()
-        n_e2e = min(steps, 2000)
+        n_e2e = max(300, min(steps, 2000))  # enough calls for a stable host-side figure
         if not stacked:
             yh = torch.empty((T, wl.d), dtype=torch.float32).pin_memory()
             for i in range(min(20, max(3, warmup))):

@@ -57,6 +57,9 @@ WORKLOADS = {
     "glm_decode_t1": Workload("glm_decode_t1", d=6144, f=2048, E=256, K=8, n_shared=1, T=1),
     "glm_verify_t4": Workload("glm_verify_t4", d=6144, f=2048, E=256, K=8, n_shared=1, T=4,
                               bias="overlap"),
+    # speculative verify with 7 drafts: 1 + 7 tokens in one batch, the same overlap bias
+    "glm_verify_t8": Workload("glm_verify_t8", d=6144, f=2048, E=256, K=8, n_shared=1, T=8,
+                              bias="overlap"),
     "glm_stack16_t1": Workload("glm_stack16_t1", d=6144, f=2048, E=256, K=8, n_shared=1, T=1,
                                layers=16, has_norm=True),
     "glm_prefill_t512": Workload("glm_prefill_t512", d=6144, f=2048, E=256, K=8, n_shared=1,

@@ -12,7 +12,8 @@
 namespace coli {
 
 constexpr int kQB = 32;                         // activation block length
-constexpr int kDecodeTmax = 4;                  // tokens per call on the smem-staged path
+constexpr int kDecodeTmax = 8;                  // tokens per call on the smem-staged path
+constexpr int kRouteTgroup = 4;                 // tokens the router stages at a time
 constexpr int kNW = 8;                          // consumer warps per CTA of the expert kernels
 constexpr int kThreads = (kNW + 1) * 32;        // + one producer warp
 constexpr int kGuRps = 8;                       // gate/up row pairs per pipeline stage
@@ -142,9 +143,10 @@ cudaError_t configure_expert_kernels();
 struct GateupPlan {
   int nst, stage_bytes, xs_bytes, aux_bytes, hs_bytes, tab_bytes, sel_bytes, max_units, total;
 };
+// down kernel: a stage holds one chunk of a union expert's down rows, then the h codes, block
+// scales and code sums of that expert's pairs (at most T of them)
 struct DownPlan {
-  int nst, stage_bytes, hq_bytes, aux_bytes, es_bytes, tab_bytes, sel_bytes, max_rows, max_slots,
-      total;
+  int nst, stage_bytes, w_bytes, es_bytes, tab_bytes, sel_bytes, max_rows, max_slots, total;
 };
 // shared-memory plan of the fused one-token expert kernel (gate/up ring, a region used first by
 // the gate/up phase and then by the down phase, the selection)

@@ -1,4 +1,4 @@
-// Expert selection of a decode batch (T <= 4 tokens), computed inside the CTAs that need it:
+// Expert selection of a decode batch (T <= 8 tokens), computed inside the CTAs that need it:
 // top-K per token by score + selection bias (ties to the lower expert id), the weights
 // renormalised over the selected scores (summed in rank order), and the batch union -- the
 // distinct experts in ascending id order, each with its bucket of (token, rank) pairs in pair
@@ -16,9 +16,6 @@
 
 namespace coli {
 
-constexpr int kSelMaxPairs = kDecodeTmax * 32;     // T*K routed pairs (K <= 32)
-constexpr int kSelMaxSlots = kSelMaxPairs + 1;     // routed union slots + the shared expert
-
 // Selection state in shared memory
 struct Sel {
   float* sc;     // [T][E] scores
@@ -34,34 +31,38 @@ struct Sel {
   int* nu;       // [1] number of union slots
 };
 
-constexpr int kSelInts = 3 * kSelMaxPairs + kSelMaxSlots + (kSelMaxSlots + 1) +
-                         2 * (kSelMaxPairs + kDecodeTmax) + kSelMaxPairs + 4;
+// ints of the selection tables of a batch of T tokens (at most 32 routed pairs per token)
+__host__ __device__ inline int sel_ints(int T) {
+  const int mp = T * 32, ms = mp + 1;
+  return 3 * mp + ms + (ms + 1) + 2 * (mp + T) + mp + 4;
+}
 
 __host__ __device__ inline int sel_bytes(int T, int E) {
-  return ((T * E + E) * 4 + 15) / 16 * 16 + kSelInts * 4;
+  return ((T * E + E) * 4 + 15) / 16 * 16 + sel_ints(T) * 4;
 }
 
 __device__ inline Sel sel_carve(uint8_t* base, int T, int E) {
+  const int mp = T * 32, ms = mp + 1;
   Sel m;
   m.sc = reinterpret_cast<float*>(base);
   m.bias = m.sc + T * E;
   int* p = reinterpret_cast<int*>(base + ((T * E + E) * 4 + 15) / 16 * 16);
   m.ids = p;
-  p += kSelMaxPairs;
+  p += mp;
   m.wt = reinterpret_cast<float*>(p);
-  p += kSelMaxPairs;
+  p += mp;
   m.skey = p;
-  p += kSelMaxPairs;
+  p += mp;
   m.u_ids = p;
-  p += kSelMaxSlots;
+  p += ms;
   m.u_off = p;
-  p += kSelMaxSlots + 1;
+  p += ms + 1;
   m.p_tok = p;
-  p += kSelMaxPairs + kDecodeTmax;
+  p += mp + T;
   m.p_rank = p;
-  p += kSelMaxPairs + kDecodeTmax;
+  p += mp + T;
   m.inv = p;
-  p += kSelMaxPairs;
+  p += mp;
   m.nu = p;
   return m;
 }
@@ -258,7 +259,7 @@ __device__ inline void union_warp(const Shape& s, Sel& m, int lane) {
 // Selection from the scores (and, with has_bias, the bias) already in m.sc / m.bias and visible
 // to the whole CTA.
 // Every thread of the CTA calls it (it synchronises the CTA); results are visible on return.
-// The union of more than 32 pairs: pair i = t*K + k gets key (expert << 7) | i; its position in
+// The union of more than 32 pairs: pair i = t*K + k gets key (expert << 8) | i; its position in
 // the sorted keys is the number of smaller keys, which groups the pairs by expert in ascending id
 // and keeps pair order inside each group; a slot starts wherever the expert changes.
 __device__ inline void select_union(const Shape& s, Sel& m, bool has_bias) {
@@ -283,17 +284,17 @@ __device__ inline void select_union(const Shape& s, Sel& m, bool has_bias) {
     return;
   }
   for (int i = threadIdx.x; i < TK; i += blockDim.x) {
-    const int key = (m.ids[i] << 7) | i;
+    const int key = (m.ids[i] << 8) | i;
     int pos = 0;
-    for (int j = 0; j < TK; ++j) pos += ((m.ids[j] << 7) | j) < key;
+    for (int j = 0; j < TK; ++j) pos += ((m.ids[j] << 8) | j) < key;
     m.skey[pos] = key;
   }
   __syncthreads();
   for (int p = threadIdx.x; p < TK; p += blockDim.x) {
-    const int key = m.skey[p], e = key >> 7, i = key & 127;
+    const int key = m.skey[p], e = key >> 8, i = key & 255;
     int slot = 0;  // heads before p
-    for (int q = 1; q <= p; ++q) slot += (m.skey[q] >> 7) != (m.skey[q - 1] >> 7);
-    if (p == 0 || (m.skey[p - 1] >> 7) != e) {
+    for (int q = 1; q <= p; ++q) slot += (m.skey[q] >> 8) != (m.skey[q - 1] >> 8);
+    if (p == 0 || (m.skey[p - 1] >> 8) != e) {
       m.u_ids[slot] = e;
       m.u_off[slot] = p;
     }
@@ -303,7 +304,7 @@ __device__ inline void select_union(const Shape& s, Sel& m, bool has_bias) {
   }
   if (threadIdx.x == 0) {
     int nr = 1;
-    for (int q = 1; q < TK; ++q) nr += (m.skey[q] >> 7) != (m.skey[q - 1] >> 7);
+    for (int q = 1; q < TK; ++q) nr += (m.skey[q] >> 8) != (m.skey[q - 1] >> 8);
     int nu = nr;
     if (s.n_shared) {
       m.u_ids[nu] = E;

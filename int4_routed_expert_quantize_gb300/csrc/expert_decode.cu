@@ -42,15 +42,22 @@ static long max_union_slots(int T, int K, int E, int n_shared) {
 
 GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   GateupPlan p;
-  const int nbd = d / kQB;
+  const int nbd = d / kQB, nhb = f / 32;
   p.stage_bytes = kGuRps * d;
   p.xs_bytes = align16(T * d);
   p.aux_bytes = align16(T * nbd * 8);
   p.hs_bytes = align16(2 * 32 * T * 4);
-  // the cost split gives a CTA at most its share of the costliest layout in the cheapest units
-  const long units = max_union_slots(T, K, E, n_shared) * (f / 32);
+  // Units a CTA can receive.  The cost split hands CTA c the routed units whose cost prefix lies
+  // in [t_c, t_{c+1}) plus at most one unit past it, and t_{c+1} - t_c <= (total cost)/grid + 1;
+  // with gu_unit_cost(np) <= kGuCostPair*np + kGuCostBytes and at most P pairs over the slots,
+  // the total cost is at most nhb*(kGuCostPair*P + kGuCostBytes*slots).  So the routed units of a
+  // CTA are at most (that/grid + 2 + cost(T)) / cost(1) + 1, and its shared-expert units at most
+  // ceil(nhb/grid).
+  const long slots = max_union_slots(T, K, E, n_shared);
+  const long P = (long)T * K + (n_shared ? T : 0);
+  const long cmax = (long)nhb * (kGuCostPair * P + kGuCostBytes * slots);
   const long wmax = gu_unit_cost(T), wmin = gu_unit_cost(1);
-  p.max_units = (int)((units * wmax + wmin * grid - 1) / (wmin * grid)) + 4;
+  p.max_units = (int)((cmax / grid + 2 + wmax) / wmin + 1 + (nhb + grid - 1) / grid) + 2;
   p.tab_bytes = align16(p.max_units * kGuTabBytes);
   p.sel_bytes = align16(sel_bytes(T, E));
   const int fixed =
@@ -62,22 +69,22 @@ GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid
 }
 
 // per-CTA tables of the down kernel: the selection (coli_select.cuh) and the down-row scales of
-// this CTA's rows for every union slot
+// this CTA's rows for every union slot.  A ring stage holds one chunk of down rows of one union
+// expert (w_bytes at most) and then the h codes, block scales and code sums of that expert's
+// pairs (at most T pairs: a routed expert serves each token once, the shared one every token).
 DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid) {
   DownPlan p;
   const int P = T * K + (n_shared ? T : 0);
   const int nbf = f / kQB;
   p.max_rows = (d + grid - 1) / grid;  // rows of the largest CTA range
   const int chunk = p.max_rows < kDownChunk ? p.max_rows : kDownChunk;
-  p.stage_bytes = chunk * (f / 2);
-  p.hq_bytes = align16(P * f);
-  p.aux_bytes = 2 * align16(P * nbf * 4);
+  p.w_bytes = align16(chunk * (f / 2));
+  p.stage_bytes = p.w_bytes + T * (f + 8 * nbf);
   p.es_bytes = align16(chunk * P * 4);
   p.max_slots = (int)max_union_slots(T, K, E, n_shared);
   p.tab_bytes = align16(p.max_slots * p.max_rows * 4);
   p.sel_bytes = align16(sel_bytes(T, E));
-  const int fixed =
-      2 * kMaxStages * 8 + p.hq_bytes + p.aux_bytes + p.es_bytes + p.tab_bytes + p.sel_bytes;
+  const int fixed = 3 * kMaxStages * 8 + p.es_bytes + p.tab_bytes + p.sel_bytes;
   int nst = (kSmemLimit - fixed) / p.stage_bytes;
   p.nst = nst > kMaxStages ? kMaxStages : nst;
   p.total = p.nst * p.stage_bytes + fixed;
@@ -466,12 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         for (int q = 0; q < kDecodeTmax; ++q) toks[q] = q < np ? tu[5 + q] : 0;
         const GuRow r{grow, xs, dxs, nsx, d, nbd, A, lane, sg, su, row, f, p0,
                       hs + ((lu & 1) * 32 + rr) * T, DBG ? a.dbg : ExpertDebug{}};
-        if (np == 2)
-          gu_multi<G, 2, DBG>(r, toks);
-        else if (np == 3)
-          gu_multi<G, 3, DBG>(r, toks);
-        else
-          gu_multi<G, 4, DBG>(r, toks);
+        switch (np) {
+          case 2: gu_multi<G, 2, DBG>(r, toks); break;
+          case 3: gu_multi<G, 3, DBG>(r, toks); break;
+          case 4: gu_multi<G, 4, DBG>(r, toks); break;
+          case 5: gu_multi<G, 5, DBG>(r, toks); break;
+          case 6: gu_multi<G, 6, DBG>(r, toks); break;
+          case 7: gu_multi<G, 7, DBG>(r, toks); break;
+          default: gu_multi<G, 8, DBG>(r, toks); break;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with its row pair
@@ -504,25 +514,28 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
 // ------------------------------------------------------------------ down + combine --------
 // CTA c owns the output rows [d*c/grid, d*(c+1)/grid) -- about d/grid rows, so every CTA streams
 // the same number of bytes -- cut into chunks of at most kDownChunk rows.  A stage is one chunk
-// of one union expert's down matrix (one contiguous bulk copy).  The union is known when this
-// grid starts (the router finished before the gate/up grid let it launch), so the first stages
-// and the tables are loaded before waiting for the h codes.  Warp w owns rows w, w+8, ... of
-// the chunk: every lane folds its group's block dots for up to 8 rows, and one transposed
-// butterfly adds the 32 group partials of all 8 rows (the same pairwise tree per row as the
-// single-row butterfly).  Once a chunk has seen every union expert the warp combines its rows
-// for every token in the fixed order: shared expert first, then ranks 0..K-1.
+// of one union expert's down matrix (one contiguous bulk copy) followed by the h codes, block
+// scales and code sums of that expert's pairs (three more copies, issued once the gate/up grid
+// is complete).  The union is known when this grid starts (the router finished before the
+// gate/up grid let it launch), so the weights of the first stages and the tables are loaded
+// before waiting for the h codes.  Warp w owns rows w, w+8, ... of the chunk: every lane folds
+// its group's block dots for up to 8 rows, and one transposed butterfly adds the 32 group
+// partials of all 8 rows (the same pairwise tree per row as the single-row butterfly).  Once a
+// chunk has seen every union expert the warp combines its rows for every token in the fixed
+// order: shared expert first, then ranks 0..K-1.
 
 __host__ __device__ inline int down_rows_begin(int d, int c, int grid) {
   return (int)((long)d * c / grid);
 }
 
 // The down rows of one stage (warp `warp`'s rows of the chunk) dotted with the h codes of NP
-// consecutive pairs p, p+1, ...: each row block's weights are loaded and split once for all.
+// consecutive pairs of the stage's union expert: each row block's weights are loaded and split
+// once for all of them.
 struct DnRows {
   const uint8_t* sbase;  // the warp's first row in the stage
-  const uint8_t* hq;     // [P][f] h codes
-  const float* hd;       // [P][nbf] block scales
-  const int* hsum;       // [P][nbf] code sums
+  const uint8_t* hq;     // [np][f] h codes of the stage's pairs
+  const float* hd;       // [np][nbf] their block scales
+  const int* hsum;       // [np][nbf] their code sums
   const float* sdx;      // the warp's first down-row scale of the chunk (stride kNW)
   float* es;             // [chunk row][P] expert outputs
   int f, nbf, A, lane, warp, nj, jl, P, d, row0c;  // row0c: first output row of the chunk
@@ -530,8 +543,9 @@ struct DnRows {
   ExpertDebug dbg;
 };
 
+// q: the first of the NP pairs within the stage, p: its index among all pairs
 template <int GF, int NP, bool DBG>
-__device__ __forceinline__ void dn_rows(const DnRows& r, int p) {
+__device__ __forceinline__ void dn_rows(const DnRows& r, int q, int p) {
   const bool on = r.lane < r.A;
   const int rb = r.f >> 1;
   uint32_t hr[NP][GF][8];
@@ -542,13 +556,13 @@ __device__ __forceinline__ void dn_rows(const DnRows& r, int p) {
 #pragma unroll
     for (int i = 0; i < GF; ++i) {
       if (on) {
-        const uint8_t* base = r.hq + (long)(p + k) * r.f + (r.lane * GF + i) * 32;
+        const uint8_t* base = r.hq + (long)(q + k) * r.f + (r.lane * GF + i) * 32;
         const uint4 v0 = *reinterpret_cast<const uint4*>(base);
         const uint4 v1 = *reinterpret_cast<const uint4*>(base + 16);
         hr[k][i][0] = v0.x; hr[k][i][1] = v0.y; hr[k][i][2] = v0.z; hr[k][i][3] = v0.w;
         hr[k][i][4] = v1.x; hr[k][i][5] = v1.y; hr[k][i][6] = v1.z; hr[k][i][7] = v1.w;
-        hdr[k][i] = r.hd[(p + k) * r.nbf + r.lane * GF + i];
-        hnr[k][i] = -8 * r.hsum[(p + k) * r.nbf + r.lane * GF + i];
+        hdr[k][i] = r.hd[(q + k) * r.nbf + r.lane * GF + i];
+        hnr[k][i] = -8 * r.hsum[(q + k) * r.nbf + r.lane * GF + i];
       } else {
 #pragma unroll
         for (int t = 0; t < 8; ++t) hr[k][i][t] = 0u;
@@ -596,19 +610,16 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int abort_flag;
   __shared__ __align__(8) uint64_t selbar;
-  __shared__ __align__(8) uint64_t inbar;  // the h codes, scales and code sums are in
   const int d = a.s.d, f = a.s.f, T = a.s.T, K = a.s.K;
   const int nbf = f >> 5, A = nbf / GF, rb = f >> 1;
   const DownPlan& pl = a.pl;
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);
-  uint64_t* empty = full + kMaxStages;
-  uint8_t* hq = reinterpret_cast<uint8_t*>(empty + kMaxStages);  // [P][f] h codes
-  float* hd = reinterpret_cast<float*>(hq + pl.hq_bytes);          // [P][nbf] block scales
-  int* hsum = reinterpret_cast<int*>(hq + pl.hq_bytes + pl.aux_bytes / 2);  // [P][nbf] code sums
-  float* es = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes);  // [chunk row][Pm]
-  float* t_sd = reinterpret_cast<float*>(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes);
-  Sel sel = sel_carve(hq + pl.hq_bytes + pl.aux_bytes + pl.es_bytes + pl.tab_bytes, T, a.s.E);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.nst * pl.stage_bytes);  // weights in
+  uint64_t* hfull = full + kMaxStages;                                            // h inputs in
+  uint64_t* empty = hfull + kMaxStages;
+  float* es = reinterpret_cast<float*>(empty + kMaxStages);  // [chunk row][P]
+  float* t_sd = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(es) + pl.es_bytes);
+  Sel sel = sel_carve(reinterpret_cast<uint8_t*>(t_sd) + pl.tab_bytes, T, a.s.E);
   const int* t_ex = sel.u_ids;   // [slot] expert
   const int* t_off = sel.u_off;  // [slot] first pair
   const float* t_w = sel.wt;     // [T*K] routing weights
@@ -626,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   if (threadIdx.x == 0) {
     for (int i = 0; i < pl.nst; ++i) {
       mbar_init(&full[i], 1);
+      mbar_init(&hfull[i], 1);
       mbar_init(&empty[i], kNW);
     }
     mbar_init(&selbar, 1);
-    mbar_init(&inbar, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -666,65 +677,51 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
   const int nstage = nch * nu;
   const uint64_t pol = l2_evict_first_policy();
   const bool producer = (warp == kNW && lane == 0);
-  int issued = 0;
-  auto issue = [&](int s, int ci, int ex) {
-    int c0, cn;
-    chunk(ci, c0, cn);
-    const uint8_t* src = a.st.wd + ((long)ex * d + row0 + c0) * (long)rb;
-    mbar_expect_tx(&full[s], (uint32_t)(cn * rb));
-    bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)(cn * rb), &full[s], pol);
-  };
-  // prefetch the first stages before the wait for the gate/up grid
-  if (producer)
-    for (; issued < nstage && issued < pl.nst; ++issued) issue(issued, issued / nu, t_ex[issued % nu]);
-  // The consumers' inputs once the gate/up grid is complete (h codes visible): run by the
-  // consumer warps at their first real stage (see the consumer loop), not by the producer,
-  // which streams weights that do not depend on it.
   const int nthr = kNW * 32;
-  auto stage_inputs = [&]() {
-    // gate/up grid complete: h codes visible from here on.  Every pair's codes, block scales
-    // and code sums arrive as they lie in the workspace: three bulk copies, one round of memory
-    // latency (plain loads when a size is not a multiple of 16 bytes).
-    griddep_wait();
-    const uint32_t qbytes = (uint32_t)(P * f), sbytes = (uint32_t)(P * nbf * 4);
-    if ((sbytes & 15u) == 0) {
-      if (threadIdx.x == 0) {
-        mbar_expect_tx(&inbar, qbytes + 2 * sbytes);
-        bulk_g2s(hq, a.w.qh, qbytes, &inbar, pol);
-        bulk_g2s(hd, a.w.dh, sbytes, &inbar, pol);
-        bulk_g2s(hsum, a.w.sh, sbytes, &inbar, pol);
-      }
-      mbar_wait_bounded(&inbar, 0u, &abort_flag, a.w.status);
-    } else {
-      for (int i = threadIdx.x; i < P * f / 16; i += nthr)
-        reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(a.w.qh) + i);
-      for (int i = threadIdx.x; i < P * nbf; i += nthr) {
-        hd[i] = __ldcg(a.w.dh + i);
-        hsum[i] = __ldcg(a.w.sh + i);
-      }
-    }
-    named_bar_sync(1, nthr);
-  };
-
 
   if (warp == kNW) {
     if (producer) {
-      int s = issued % pl.nst, ci = issued / nu, slot = issued % nu;
-      uint32_t ph = (uint32_t)((issued / pl.nst) & 1);
-      for (int it = issued; it < nstage; ++it) {
-        if (it >= pl.nst && !mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
-        issue(s, ci, t_ex[slot]);
+      // stage it = (row chunk it / nu, union slot it % nu)
+      auto issue_w = [&](int s, int it) {
+        int c0, cn;
+        chunk(it / nu, c0, cn);
+        const uint8_t* src = a.st.wd + ((long)t_ex[it % nu] * d + row0 + c0) * (long)rb;
+        mbar_expect_tx(&full[s], (uint32_t)(cn * rb));
+        bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)(cn * rb), &full[s], pol);
+      };
+      // the slot's pairs are consecutive, so their h codes, scales and code sums are three
+      // contiguous ranges of the workspace
+      auto issue_h = [&](int s, int it) {
+        const int slot = it % nu, p0 = t_off[slot], np = t_off[slot + 1] - p0;
+        uint8_t* dst = ring + (long)s * pl.stage_bytes + pl.w_bytes;
+        const uint32_t qb = (uint32_t)(np * f), sb = (uint32_t)(np * nbf * 4);
+        mbar_expect_tx(&hfull[s], qb + 2 * sb);
+        bulk_g2s(dst, a.w.qh + (long)p0 * f, qb, &hfull[s], pol);
+        bulk_g2s(dst + qb, a.w.dh + (long)p0 * nbf, sb, &hfull[s], pol);
+        bulk_g2s(dst + qb + sb, a.w.sh + (long)p0 * nbf, sb, &hfull[s], pol);
+      };
+      // the first stages' weights before the wait for the gate/up grid, their h inputs after it
+      const int first = nstage < pl.nst ? nstage : pl.nst;
+      for (int it = 0; it < first; ++it) issue_w(it, it);
+      griddep_wait();  // gate/up grid complete: its h codes are visible from here on
+      for (int it = 0; it < first; ++it) issue_h(it, it);
+      int issued = first;
+      int s = first % pl.nst;
+      uint32_t ph = (uint32_t)((first / pl.nst) & 1);
+      for (int it = first; it < nstage; ++it) {
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1u, &abort_flag, a.w.status)) break;
+        issue_w(s, it);
+        issue_h(s, it);
         issued = it + 1;
         if (++s == pl.nst) {
           s = 0;
           ph ^= 1u;
         }
-        if (++slot == nu) {
-          slot = 0;
-          ++ci;
-        }
       }
-      if (abort_flag) drain_fills(full, pl.nst, issued);
+      if (abort_flag) {
+        drain_fills(full, pl.nst, issued);
+        drain_fills(hfull, pl.nst, issued);
+      }
     }
   } else {
     // this CTA's down-row scales for every union slot (they do not depend on the gate/up grid)
@@ -732,35 +729,40 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       const int sl = i / nrow, r = i - sl * nrow;
       t_sd[sl * pl.max_rows + r] = a.st.sc[(long)t_ex[sl] * (2 * f + d) + 2 * f + row0 + r];
     }
+    named_bar_sync(1, nthr);
     int s = 0, ci = 0, slot = 0, c0 = 0, cn = 0;
     uint32_t ph = 0;
     chunk(0, c0, cn);
     // rows of this warp in the current chunk: w, w+8, ... below cn
     int nj = cn > warp ? (cn - warp + kNW - 1) / kNW : 0;
     const int jl = 4 * (lane & 1) + 2 * ((lane >> 1) & 1) + ((lane >> 2) & 1);  // row of the sum
-    // Iteration -1 is a dry run of the stage code on whatever stage 0 and the h buffer hold
-    // (no wait, no result, no arrival): it brings the loop's instructions into the SM's caches
-    // while the CTA would otherwise wait for the gate/up grid, so the first real stage does not
-    // pay for fetching them.
+    // Iteration -1 is a dry run of the stage code on whatever stage 0 holds (no wait, no result,
+    // no arrival): it brings the loop's instructions into the SM's caches while the CTA would
+    // otherwise wait for the gate/up grid, so the first real stage does not pay for fetching them.
 #pragma unroll 1
     for (int it = -1; it < nstage; ++it) {
       const bool dry = it < 0;
-      if (it == 0) stage_inputs();
       const int p0 = t_off[slot], np = dry ? 1 : t_off[slot + 1] - p0;
-      if (!dry) mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
-      const uint8_t* sbase = ring + (long)s * pl.stage_bytes + (long)warp * rb;
+      if (!dry) {
+        mbar_wait_bounded(&full[s], ph, &abort_flag, a.w.status);
+        mbar_wait_bounded(&hfull[s], ph, &abort_flag, a.w.status);
+      }
+      const uint8_t* stage = ring + (long)s * pl.stage_bytes;
+      const uint8_t* hq = stage + pl.w_bytes;
+      const float* hd = reinterpret_cast<const float*>(hq + np * f);
+      const int* hsum = reinterpret_cast<const int*>(hd + np * nbf);
       const float* sdx = t_sd + slot * pl.max_rows + c0 + warp;
       // pairs two at a time (the pair count is a template argument, so both pairs' chains
       // interleave with no branch between them); each row block's weights are loaded and split
       // into nibble halves once for both
-      const DnRows r{sbase, hq, hd, hsum, sdx, es, f, nbf, A, lane, warp, nj, jl, P, d, row0 + c0,
-                     dry, DBG ? a.dbg : ExpertDebug{}};
+      const DnRows r{stage + (long)warp * rb, hq, hd, hsum, sdx, es, f, nbf, A, lane, warp, nj, jl, P,
+                     d, row0 + c0, dry, DBG ? a.dbg : ExpertDebug{}};
       for (int q = 0; q < np;) {
         if (np - q >= 2) {
-          dn_rows<GF, 2, DBG>(r, p0 + q);
+          dn_rows<GF, 2, DBG>(r, q, p0 + q);
           q += 2;
         } else {
-          dn_rows<GF, 1, DBG>(r, p0 + q);
+          dn_rows<GF, 1, DBG>(r, q, p0 + q);
           q += 1;
         }
       }

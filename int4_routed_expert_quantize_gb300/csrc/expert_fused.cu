@@ -27,7 +27,7 @@ namespace coli {
 
 static inline int align16f(int x) { return (x + 15) & ~15; }
 
-constexpr int kFuTabInts = 5 + kDecodeTmax;
+constexpr int kFuTabInts = 9;                 // expert, first pair, pairs, 32-row block, spare
 constexpr int kFuTabStride = kFuTabInts + 64;  // ints per unit table entry
 
 FusedPlan fused_plan(int d, int f, int K, int E, int n_shared, int grid) {

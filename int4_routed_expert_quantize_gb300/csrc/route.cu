@@ -29,24 +29,25 @@ __device__ __noinline__ void route_drain(uint64_t* bar) {
 
 // One launch does the routing half up to the scores.  Every CTA: one bulk copy brings its
 // kRouterEpc router rows into shared memory while all threads stage the tokens there (in the
-// router's chunk order) and the gate/up grid is let start its weight prefetch; then the optional
-// RMSNorm (one warp per token), the logits and sigmoid scores of its experts for every token
-// (one warp per (expert, token): lane g runs the fma chain over its d/32 contiguous elements,
-// the butterfly adds the 32 partials) and, on the other warps at the same time, this CTA's share
-// of the int8 activation blocks (one warp per block of 32).  The expert kernels select the
-// experts from the scores themselves (coli_select.cuh), so no CTA here waits for another.
+// router's chunk order, kRouteTgroup tokens at a time) and the gate/up grid is let start its
+// weight prefetch; then, for each group of tokens, the optional RMSNorm (one warp per token), the
+// logits and sigmoid scores of its experts (one warp per (expert, token): lane g runs the fma
+// chain over its d/32 contiguous elements, the butterfly adds the 32 partials) and, on the other
+// warps at the same time, this CTA's share of the group's int8 activation blocks (one warp per
+// block of 32).  The expert kernels select the experts from the scores themselves
+// (coli_select.cuh), so no CTA here waits for another.
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x, const Shape s,
                                                     const Store st, const Work w) {
   extern __shared__ __align__(128) float route_sm[];
   __shared__ __align__(8) uint64_t wbar;
-  __shared__ float rinv[kDecodeTmax];
+  __shared__ float rinv[kRouteTgroup];
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
   const int d = s.d, E = s.E, T = s.T, Gd = d >> 5, nbd = d >> 5;
   const int e0 = blockIdx.x * kRouterEpc;
   const int ne = min(kRouterEpc, E - e0);
   float* wrs = route_sm;                   // [kRouterEpc][d] router rows as stored
-  float* xsm = route_sm + kRouterEpc * d;  // [T][d] tokens
+  float* xsm = route_sm + kRouterEpc * d;  // [kRouteTgroup][d] tokens of the current group
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0) {  // this call's selection is not published yet; no CTA at the barrier
       w.sel_flag[0] = 0;
@@ -61,136 +62,145 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
       bulk_g2s(wrs + r * d, st.wr + (long)(e0 + r) * d, (uint32_t)d * 4u, &wbar, pol);
   }
   griddep_launch_dependents();
+  int rows = 0;  // this warp's view of the router rows: 0 not waited for, 1 in, -1 gave up
 
-  // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
-  // i4*32 + g (conflict-free reads by lane).  Work item w of a token is (i4 = 8*(w>>8) + (w&7),
-  // g = (w>>3)&31), so a warp reads four 128-byte runs of x and its shared-memory stores fall in
-  // 4 bank groups; each thread issues its loads in batches of 8 before storing any.
-  const int n_i4 = d / 128, per_t = 256 * ((n_i4 + 7) / 8), nw = T * per_t;
-  for (int c0 = threadIdx.x; c0 < nw; c0 += 8 * blockDim.x) {
-    float4 v[8];
-    int dst[8];
+  for (int t0 = 0; t0 < T; t0 += kRouteTgroup) {
+    const int Tg = min(kRouteTgroup, T - t0);
+    if (t0 > 0) __syncthreads();  // every warp is done with the previous group's tokens
+    // tokens into shared memory in router order: lane g's elements g*Gd + 4*i4 .. +3 at chunk
+    // i4*32 + g (conflict-free reads by lane).  Work item w of a token is (i4 = 8*(w>>8) +
+    // (w&7), g = (w>>3)&31), so a warp reads four 128-byte runs of x and its shared-memory
+    // stores fall in 4 bank groups; each thread issues its loads in batches of 8 before storing.
+    const int n_i4 = d / 128, per_t = 256 * ((n_i4 + 7) / 8), nw = Tg * per_t;
+    for (int c0 = threadIdx.x; c0 < nw; c0 += 8 * blockDim.x) {
+      float4 v[8];
+      int dst[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int c = c0 + k * blockDim.x;
-      const int t = c / per_t, w = c - t * per_t;
-      const int i4 = ((w >> 8) << 3) + (w & 7), g = (w >> 3) & 31;
-      dst[k] = c < nw && i4 < n_i4 ? t * (d / 4) + i4 * 32 + g : -1;
-      if (dst[k] >= 0)
-        v[k] = __ldg(reinterpret_cast<const float4*>(x + (long)t * d + g * Gd + 4 * i4));
+      for (int k = 0; k < 8; ++k) {
+        const int c = c0 + k * blockDim.x;
+        const int t = c / per_t, wi = c - t * per_t;
+        const int i4 = ((wi >> 8) << 3) + (wi & 7), g = (wi >> 3) & 31;
+        dst[k] = c < nw && i4 < n_i4 ? t * (d / 4) + i4 * 32 + g : -1;
+        if (dst[k] >= 0)
+          v[k] = __ldg(reinterpret_cast<const float4*>(x + (long)(t0 + t) * d + g * Gd + 4 * i4));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (dst[k] >= 0) reinterpret_cast<float4*>(xsm)[dst[k]] = v[k];
     }
+    __syncthreads();
+    if (s.has_norm) {
+      // mean of squares in the canonical order (lane g: fma chain over its d/32 elements)
+      for (int t = warp; t < Tg; t += nwarp) {
+        const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
+        float p = 0.0f;
+        for (int i4 = 0; i4 < d / 128; ++i4) {
+          const float4 v = xp[i4 * 32 + lane];
+          p = __fmaf_rn(v.x, v.x, p);
+          p = __fmaf_rn(v.y, v.y, p);
+          p = __fmaf_rn(v.z, v.z, p);
+          p = __fmaf_rn(v.w, v.w, p);
+        }
+        p = warp_tree_sum(p);
+        if (lane == 0) {
+          const float ms = __fdiv_rn(p, (float)d);
+          rinv[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, s.rms_eps)));
+        }
+      }
+      __syncthreads();
+      const int n4 = Tg * (d / 4);
+      for (int c0 = threadIdx.x; c0 < n4; c0 += 8 * blockDim.x) {
+        float4 gm[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (dst[k] >= 0) reinterpret_cast<float4*>(xsm)[dst[k]] = v[k];
-  }
-  __syncthreads();
-  if (s.has_norm) {
-    // mean of squares in the canonical order (lane g: fma chain over its d/32 elements)
-    for (int t = warp; t < T; t += nwarp) {
-      const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
+        for (int k = 0; k < 8; ++k) {
+          const int c = c0 + k * blockDim.x;
+          if (c < n4) {
+            const int pos = c % (d / 4);
+            gm[k] = __ldg(reinterpret_cast<const float4*>(st.gamma + (pos & 31) * Gd + 4 * (pos >> 5)));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = c0 + k * blockDim.x;
+          if (c < n4) {
+            const float r = rinv[c / (d / 4)];
+            float4 v = reinterpret_cast<float4*>(xsm)[c];
+            v.x = __fmul_rn(__fmul_rn(v.x, r), gm[k].x);
+            v.y = __fmul_rn(__fmul_rn(v.y, r), gm[k].y);
+            v.z = __fmul_rn(__fmul_rn(v.z, r), gm[k].z);
+            v.w = __fmul_rn(__fmul_rn(v.w, r), gm[k].w);
+            reinterpret_cast<float4*>(xsm)[c] = v;
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    // this CTA's share of the group's activation blocks: x_n (natural order), int8 codes,
+    // scale, code sum.  The warps that compute no logits take them (while the logits run);
+    // without such warps every warp takes its share first.
+    const int ndot = ne * Tg;
+    const int nq = ndot < nwarp ? nwarp - ndot : nwarp;
+    const int qw = ndot < nwarp ? warp - ndot : warp;
+    for (int b = qw >= 0 ? blockIdx.x * nq + qw : Tg * nbd; b < Tg * nbd; b += gridDim.x * nq) {
+      const int tl = b / nbd, bb = b - tl * nbd, t = t0 + tl;
+      const int j = bb * 32 + lane;
+      const int g = j / Gd, m = j - g * Gd;
+      const float v = xsm[(long)tl * d + ((m >> 2) * 32 + g) * 4 + (m & 3)];
+      w.xn[(long)t * d + j] = v;
+      const float dd = __fdiv_rn(warp_max(fabsf(v)), 127.0f);
+      const int q = q8_code(v, dd);
+      w.qx[(long)t * d + j] = (int8_t)q;
+      const int sq = warp_isum(q);
+      if (lane == 0) {
+        w.dx[(long)t * nbd + bb] = dd;
+        w.sx[(long)t * nbd + bb] = sq;
+      }
+    }
+
+    // logits: router rows and tokens both in shared memory, chunk i4*32 + g for lane g
+    for (int pi = warp; pi < ndot && rows >= 0; pi += nwarp) {
+      if (rows == 0) {
+        if (mbar_wait_bounded(&wbar, 0u, &abort_flag, w.status)) {
+          rows = 1;
+        } else {
+          rows = -1;
+          route_drain(&wbar);
+          break;
+        }
+      }
+      const int r = pi / Tg, tl = pi - r * Tg;
+      const float4* wp = reinterpret_cast<const float4*>(wrs + (long)r * d);
+      const float4* xp = reinterpret_cast<const float4*>(xsm + (long)tl * d);
       float p = 0.0f;
+#pragma unroll 4
       for (int i4 = 0; i4 < d / 128; ++i4) {
-        const float4 v = xp[i4 * 32 + lane];
-        p = __fmaf_rn(v.x, v.x, p);
-        p = __fmaf_rn(v.y, v.y, p);
-        p = __fmaf_rn(v.z, v.z, p);
-        p = __fmaf_rn(v.w, v.w, p);
+        const float4 a4 = wp[i4 * 32 + lane];
+        const float4 b4 = xp[i4 * 32 + lane];
+        p = __fmaf_rn(a4.x, b4.x, p);
+        p = __fmaf_rn(a4.y, b4.y, p);
+        p = __fmaf_rn(a4.z, b4.z, p);
+        p = __fmaf_rn(a4.w, b4.w, p);
       }
       p = warp_tree_sum(p);
       if (lane == 0) {
-        const float ms = __fdiv_rn(p, (float)d);
-        rinv[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, s.rms_eps)));
+        w.logits[(long)(t0 + tl) * E + e0 + r] = p;
+        w.scores[(long)(t0 + tl) * E + e0 + r] = canon_sigmoid(p);
       }
-    }
-    __syncthreads();
-    const int n4 = T * (d / 4);
-    for (int c0 = threadIdx.x; c0 < n4; c0 += 8 * blockDim.x) {
-      float4 gm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + k * blockDim.x;
-        if (c < n4) {
-          const int pos = c % (d / 4);
-          gm[k] = __ldg(reinterpret_cast<const float4*>(st.gamma + (pos & 31) * Gd + 4 * (pos >> 5)));
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + k * blockDim.x;
-        if (c < n4) {
-          const float r = rinv[c / (d / 4)];
-          float4 v = reinterpret_cast<float4*>(xsm)[c];
-          v.x = __fmul_rn(__fmul_rn(v.x, r), gm[k].x);
-          v.y = __fmul_rn(__fmul_rn(v.y, r), gm[k].y);
-          v.z = __fmul_rn(__fmul_rn(v.z, r), gm[k].z);
-          v.w = __fmul_rn(__fmul_rn(v.w, r), gm[k].w);
-          reinterpret_cast<float4*>(xsm)[c] = v;
-        }
-      }
-    }
-    __syncthreads();
-  }
-
-  // this CTA's share of the activation blocks: x_n (natural order), int8 codes, scale, code sum.
-  // The warps that compute no logits take them (while the logits run); without such warps
-  // every warp takes its share first.
-  const int ndot = ne * T;
-  const int nq = ndot < nwarp ? nwarp - ndot : nwarp;
-  const int qw = ndot < nwarp ? warp - ndot : warp;
-  for (int b = qw >= 0 ? blockIdx.x * nq + qw : T * nbd; b < T * nbd; b += gridDim.x * nq) {
-    const int t = b / nbd, bb = b - t * nbd;
-    const int j = bb * 32 + lane;
-    const int g = j / Gd, m = j - g * Gd;
-    const float v = xsm[(long)t * d + ((m >> 2) * 32 + g) * 4 + (m & 3)];
-    w.xn[(long)t * d + j] = v;
-    const float dd = __fdiv_rn(warp_max(fabsf(v)), 127.0f);
-    const int q = q8_code(v, dd);
-    w.qx[(long)t * d + j] = (int8_t)q;
-    const int sq = warp_isum(q);
-    if (lane == 0) {
-      w.dx[(long)t * nbd + bb] = dd;
-      w.sx[(long)t * nbd + bb] = sq;
     }
   }
-
-  // logits: router rows and tokens both in shared memory, chunk i4*32 + g for lane g
-  bool waited = false;
-  for (int pi = warp; pi < ndot; pi += nwarp) {
-    if (!waited) {
-      waited = true;
-      if (!mbar_wait_bounded(&wbar, 0u, &abort_flag, w.status)) {
-        route_drain(&wbar);
-        break;
-      }
-    }
-    const int r = pi / T, t = pi - r * T;
-    const float4* wp = reinterpret_cast<const float4*>(wrs + (long)r * d);
-    const float4* xp = reinterpret_cast<const float4*>(xsm + (long)t * d);
-    float p = 0.0f;
-#pragma unroll 4
-    for (int i4 = 0; i4 < d / 128; ++i4) {
-      const float4 a4 = wp[i4 * 32 + lane];
-      const float4 b4 = xp[i4 * 32 + lane];
-      p = __fmaf_rn(a4.x, b4.x, p);
-      p = __fmaf_rn(a4.y, b4.y, p);
-      p = __fmaf_rn(a4.z, b4.z, p);
-      p = __fmaf_rn(a4.w, b4.w, p);
-    }
-    p = warp_tree_sum(p);
-    if (lane == 0) {
-      w.logits[(long)t * E + e0 + r] = p;
-      w.scores[(long)t * E + e0 + r] = canon_sigmoid(p);
-    }
-  }
+  // a warp that computed no logits never waited for the router rows: wait (bounded) so that no
+  // bulk copy still writes shared memory when the CTA exits
+  if (rows == 0 && !mbar_wait_bounded(&wbar, 0u, &abort_flag, w.status)) route_drain(&wbar);
 }
 
 static size_t route_smem_bytes(int d, int T) {
-  return ((size_t)kRouterEpc * d + (size_t)T * d) * sizeof(float);
+  return ((size_t)kRouterEpc * d + (size_t)(T < kRouteTgroup ? T : kRouteTgroup) * d) * sizeof(float);
 }
 
 cudaError_t configure_route_kernels() {
   return cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)route_smem_bytes(8192, kDecodeTmax));
+                              (int)route_smem_bytes(8192, kRouteTgroup));
 }
 
 // ------------------------------------------------------------------ batched routing ------

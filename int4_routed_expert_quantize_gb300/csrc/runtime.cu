@@ -37,6 +37,7 @@ struct coli_moe {
   bool prefill = false;     // the tensor-core path is set up (max_tokens > kDecodeTmax)
   int prefill_min = kPrefillMinTokens;  // batches of at least this many tokens take it
   bool fused = false;       // one-token forwards use the fused expert kernel
+  int decode_tmax = 1;      // tokens per launch of the decode kernels (<= kDecodeTmax)
   int fault = 0;            // one-shot failure-path knob (coli_moe_inject_fault)
   PrefillWork pw;
   PrefillMaps maps;
@@ -250,16 +251,17 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
   if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
   const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
-  if (dump && T > kDecodeTmax && !batched) return COLI_EUNSUPPORTED;
+  if (dump && T > h->decode_tmax && !batched) return COLI_EUNSUPPORTED;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
   int rc = check_device(h);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   if (batched) return run_prefill(h, x, T, y, dump, st);
-  // the smem-staged kernels take up to kDecodeTmax tokens; larger batches run in chunks,
+  // the smem-staged kernels take up to decode_tmax tokens; larger batches run in chunks,
   // which gives the same result per token (each token's output depends on itself only)
-  for (int c0 = 0; c0 < T; c0 += kDecodeTmax) {
-    const int Tc = T - c0 < kDecodeTmax ? T - c0 : kDecodeTmax;
+  const int tm = h->decode_tmax;
+  for (int c0 = 0; c0 < T; c0 += tm) {
+    const int Tc = T - c0 < tm ? T - c0 : tm;
     rc = run_decode(h, x + (size_t)c0 * h->cfg.d, Tc, y + (size_t)c0 * h->cfg.d, dump, st);
     if (rc) return rc;
   }
@@ -316,7 +318,7 @@ int coli_moe_launches(const coli_moe* h, int T) {
   if (!h || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
   if (T == 1 && h->fused) return 2;
   if (T > kDecodeTmax && h->prefill && T >= h->prefill_min) return 8;
-  return 3 * ((T + kDecodeTmax - 1) / kDecodeTmax);
+  return 3 * ((T + h->decode_tmax - 1) / h->decode_tmax);
 }
 
 int64_t coli_moe_expert_record_bytes(int d, int f) {
@@ -341,16 +343,18 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     cudaGetLastError();
     return COLI_ECUDA;
   }
-  {
-    // the decode kernels' shared-memory plans for the grids they will launch with
-    const int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax;
+  // tokens per launch of the decode kernels: the largest count up to kDecodeTmax whose
+  // shared-memory plans (for the grids they will launch with) leave at least two ring stages
+  int decode_tmax = 0;
+  for (int Tc = c.max_tokens < kDecodeTmax ? c.max_tokens : kDecodeTmax; Tc >= 1 && !decode_tmax; --Tc) {
     const long slots = (long)(Tc * c.top_k < c.n_experts ? Tc * c.top_k : c.n_experts) + c.n_shared;
     const long gu_grid = slots * (c.f / 32) < sms ? slots * (c.f / 32) : sms;
     const int dn_grid = down_grid(c.d, sms);
-    if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid).nst < 2 ||
-        down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst < 2)
-      return COLI_EUNSUPPORTED;
+    if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid).nst >= 2 &&
+        down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst >= 2)
+      decode_tmax = Tc;
   }
+  if (!decode_tmax) return COLI_EUNSUPPORTED;
   if (configure_device(dev) != cudaSuccess) {
     cudaGetLastError();
     return COLI_ECUDA;
@@ -365,6 +369,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     return COLI_ECUDA;
   }
   h->slots = c.n_experts + c.n_shared;
+  h->decode_tmax = decode_tmax;
   h->loaded.assign(h->slots, 0);
   h->fused = fused_supported(c.d, c.f, c.top_k, c.n_experts, c.n_shared, h->num_sms);
   const long S = h->slots, d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
@@ -556,7 +561,7 @@ int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_d
                               void* const* events, int n_events, void* stream) {
   if (!h || !events || n_events < 4 || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
   const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
-  if (T > kDecodeTmax && !batched) return COLI_EINVAL;
+  if (T > h->decode_tmax && !batched) return COLI_EINVAL;
   for (int i = 0; i < 4; ++i)
     if (!events[i]) return COLI_EINVAL;
   if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15u) || ((uintptr_t)y_dev & 3u)) return COLI_EINVAL;

@@ -128,7 +128,7 @@ def test_tiny_batch_invariance(tiny):
 
 
 def test_tiny_chunked_batch(tiny):
-    """T above the per-call staging limit runs in chunks; each token still matches the oracle"""
+    """a 7-token batch in one union pass: each token still matches the oracle"""
     wl, L, OL = tiny
     x = W.x_host(wl, 7, token0=300)
     y = to_np(L.forward(torch.from_numpy(x).cuda()))
