@@ -86,12 +86,14 @@ def mutant_source(n):
 
 
 def write_mutant(n, directory):
-    """the patched source of mutant n, written next to a copy of oracle.h; returns its path"""
-    path = os.path.join(str(directory), f"oracle_m{n}.c")
+    """the patched source of mutant n, written next to a copy of oracle.h in a directory of its
+    own (so that mutants can be written and compiled in parallel); returns its path"""
+    sub = os.path.join(str(directory), f"m{n}")
+    os.makedirs(sub, exist_ok=True)
+    path = os.path.join(sub, "oracle.c")
     with open(path, "w") as fh:
         fh.write(mutant_source(n))
-    with open(os.path.join(O.HERE, "oracle.h")) as src, \
-            open(os.path.join(str(directory), "oracle.h"), "w") as dst:
+    with open(os.path.join(O.HERE, "oracle.h")) as src, open(os.path.join(sub, "oracle.h"), "w") as dst:
         dst.write(src.read())
     return path
 
