@@ -156,10 +156,11 @@ int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, 
  * of an earlier forward gave up (the word is then cleared).  Synchronises `stream`. */
 int coli_moe_status(coli_moe* h, void* stream);
 
-/* Batches of at least min_tokens tokens (min_tokens > 4) take the batched tensor-core path
- * (when the handle has it: max_tokens > 4); smaller batches run the decode kernels in chunks of
- * at most 4 tokens.  Both give the same result for every token.  The default, 256, is where the
- * two cost the same on the GLM-shaped layer.  EINVAL: min_tokens <= 4. */
+/* Batches of at least min_tokens tokens (min_tokens >= 2) take the batched tensor-core path
+ * (when the handle has it: max_tokens > 8); smaller batches run the decode kernels, in one union
+ * pass of up to 8 tokens or in chunks of 8.  Both give the same result for every token.  The
+ * default, 256, is where the two cost about the same on the GLM-shaped layer.  EINVAL:
+ * min_tokens < 2. */
 int coli_moe_set_prefill_min(coli_moe* h, int min_tokens);
 
 /* Failure-path test knob.  fault = COLI_FAULT_SKIP_ARRIVAL makes the next one-token forward on
@@ -174,9 +175,9 @@ int coli_moe_inject_fault(coli_moe* h, int fault);
 
 /* Number of kernel launches one coli_moe_forward of T tokens makes on this handle: 2 for one
  * token when the expert half runs as one fused kernel (router, then gate/up + down), 3 per
- * chunk of at most 4 tokens on the decode path, 8 on the batched tensor-core path (batches of at
- * least the coli_moe_set_prefill_min size, 256 by default).  Negative
- * status on error (EINVAL: T < 1 or T > max_tokens). */
+ * chunk of at most 8 tokens on the decode path (router, gate/up, down; one union pass per
+ * chunk), 8 on the batched tensor-core path (batches of at least the coli_moe_set_prefill_min
+ * size, 256 by default).  Negative status on error (EINVAL: T < 1 or T > max_tokens). */
 int coli_moe_launches(const coli_moe* h, int T);
 
 /* Bytes of one expert record in the canonical format (3*d*f/2 + 4*(2f+d)). */

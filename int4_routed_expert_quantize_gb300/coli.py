@@ -243,8 +243,8 @@ class MoeLayer:
         return int(lib().coli_moe_status(self.h, _stream(stream)))
 
     def set_prefill_min(self, min_tokens):
-        """batches of at least min_tokens (> 4) take the tensor-core path, smaller ones the
-        decode kernels in chunks of 4 (coli_moe_set_prefill_min)"""
+        """batches of at least min_tokens (>= 2) take the tensor-core path, smaller ones the
+        decode kernels in one pass of up to 8 tokens or chunks of 8 (coli_moe_set_prefill_min)"""
         _check(lib().coli_moe_set_prefill_min(self.h, min_tokens), "coli_moe_set_prefill_min")
 
     def inject_fault(self, fault):

@@ -112,6 +112,11 @@ int check_device(const coli_moe* h) {
   return dev == h->device ? COLI_OK : COLI_ESTATE;
 }
 
+// batches of at least prefill_min tokens (>= 2) take the tensor-core path when the handle has it
+bool takes_batched(const coli_moe* h, int T) {
+  return h->prefill && T >= 2 && T >= h->prefill_min;
+}
+
 Shape shape_of(const coli_moe* h, int T) {
   const coli_moe_config& c = h->cfg;
   return Shape{c.d, c.f, c.n_experts, c.top_k, c.n_shared, T, c.routed_scale, c.rms_eps,
@@ -250,7 +255,7 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
   if (x != y && overlap(x, bytes, y, bytes)) return COLI_EINVAL;
   if (x == y && !h->cfg.has_norm) return COLI_EINVAL;
-  const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
+  const bool batched = takes_batched(h, T);
   if (dump && T > h->decode_tmax && !batched) return COLI_EUNSUPPORTED;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
   int rc = check_device(h);
@@ -302,7 +307,7 @@ int host_graph_for(coli_moe* h, int T, float* dx, float* dy) {
 extern "C" {
 
 int coli_moe_set_prefill_min(coli_moe* h, int min_tokens) {
-  if (!h || min_tokens <= kDecodeTmax) return COLI_EINVAL;
+  if (!h || min_tokens < 2) return COLI_EINVAL;
   h->prefill_min = min_tokens;
   drop_host_graphs(h);  // the cached host-buffer graphs may have taken the other path
   return COLI_OK;
@@ -317,7 +322,7 @@ int coli_moe_inject_fault(coli_moe* h, int fault) {
 int coli_moe_launches(const coli_moe* h, int T) {
   if (!h || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
   if (T == 1 && h->fused) return 2;
-  if (T > kDecodeTmax && h->prefill && T >= h->prefill_min) return 8;
+  if (takes_batched(h, T)) return 8;
   return 3 * ((T + h->decode_tmax - 1) / h->decode_tmax);
 }
 
@@ -560,7 +565,7 @@ int coli_moe_forward_debug(coli_moe* h, const float* x_dev, int T, float* y_dev,
 int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_dev,
                               void* const* events, int n_events, void* stream) {
   if (!h || !events || n_events < 4 || T < 1 || T > h->cfg.max_tokens) return COLI_EINVAL;
-  const bool batched = h->prefill && T > kDecodeTmax && T >= h->prefill_min;
+  const bool batched = takes_batched(h, T);
   if (T > h->decode_tmax && !batched) return COLI_EINVAL;
   for (int i = 0; i < 4; ++i)
     if (!events[i]) return COLI_EINVAL;
