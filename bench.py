@@ -15,7 +15,8 @@ kernel for 2-4 tokens, the two tensor-core GEMMs for a prefill batch.
 The JSON line's top level is the headline workload (--workload, default glm_decode_t1: one
 GLM-5.2-shaped layer, one token).  `configs` holds a shorter timed run of each of the other
 layer configurations (tiny layer, 4-token verify batch, 16-layer stack, 512-token prefill), each
-with its own roofline and clock record.
+with its own roofline and clock record, and `spec_verify`: speculative verify forwards of
+1 + G tokens (G = 0..7 drafts) with simulated draft acceptance.
 
 With --gpus N under torchrun every rank runs its own replica on its own tokens (weak scaling, no
 collective on the data path) and the slowest rank's time is used.
@@ -47,7 +48,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 # the layer configurations the JSON line's `configs` object times besides the headline
-CONFIGS = ["tiny_t1", "glm_decode_t1", "glm_verify_t4", "glm_stack16_t1", "glm_prefill_t512"]
+CONFIGS = ["tiny_t1", "glm_decode_t1", "glm_verify_t4", "glm_stack16_t1", "glm_prefill_t512",
+           "spec_verify"]
 # steps of a `configs` entry are capped so the whole default run stays within a few minutes
 CONFIG_STEP_CAP = {"glm_prefill_t512": 60, "glm_stack16_t1": 300}
 
@@ -441,7 +443,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
         n_union = wl.K + wl.n_shared
     else:
         sizes = []
-        for i in range(min(steps, 64 if T <= 4 else 4)):
+        for i in range(min(steps, 64 if T <= 8 else 4)):
             dmp = layers[0].forward_debug(xpool[i % npool])
             sizes.append(int(dmp["n_union"].item()))
             del dmp
@@ -461,7 +463,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
            "expert_gbs": expert_gbs, "expert_hbm_frac": expert_gbs / B.hbm,
            "wall_s": wall, "gpu_launches": n_launch * steps + n_launch * n_prof, "kernel_ms": kern}
     hbm_src = f"{B.peak_kind} hbm_gbs (copy, burst)"
-    if T > 4:
+    if n_launch == 8 * wl.layers:
         # tensor-core path: the two GEMM launches (gate/up, then down + the combine)
         t_ms = kern["gateup"] + kern["down"]
         ach = expert_bytes(wl, n_union) / (t_ms / 1000.0) / 1e9
@@ -539,6 +541,88 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
     return out
 
 
+# per-draft acceptance of the simulated speculative decode: with 3 drafts it gives 2.5 tokens per
+# forward (1 + 0.7 + 0.49 + 0.343), inside the 2.2-2.8 the pages report for the int8 MTP head
+SPEC_ACCEPT = 0.7
+
+
+def emitted_tokens(accepted):
+    """tokens one verify forward yields: the verified token plus the drafts accepted before the
+    first rejected one.  accepted: bool [steps, G] (draft g accepted in isolation)"""
+    import numpy as np
+    accepted = np.asarray(accepted, dtype=bool)
+    if accepted.shape[1] == 0:
+        return np.ones(accepted.shape[0])
+    return 1 + np.cumprod(accepted, axis=1).sum(axis=1)
+
+
+def measure_spec(B, steps, warmup, max_drafts=7, seed=0):
+    """Speculative verify on the GLM layer with the overlap bias: for G = 0..max_drafts drafts a
+    forward of 1 + G tokens (one union pass), timed like measure(); acceptance is simulated per
+    step (each draft accepted with probability SPEC_ACCEPT while all before it were, from a
+    seeded generator), so a forward yields 1 + (accepted prefix) tokens.  -> dict"""
+    import numpy as np
+    import torch
+
+    from int4_routed_expert_quantize_gb300 import synthetic
+    wl = W.WORKLOADS["glm_verify_t8"]
+    L = synthetic.build_layer(wl, max_tokens=1 + max_drafts)
+    stream = torch.cuda.current_stream()
+    rng = np.random.default_rng(seed)
+    sweep = {}
+    for G in range(0, max_drafts + 1):
+        T = 1 + G
+        npool = 256
+        xpool = synthetic.x_tokens(wl, npool * T, token0=B.rank * npool * 8).view(npool, T, wl.d)
+        xin = xpool[0].clone()
+        y = torch.empty_like(xin)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            L.forward(xin, y)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            L.forward(xin, y)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(warmup + steps):
+            B.flush_l2(i)
+            xin.copy_(xpool[i % npool])
+            if i >= warmup:
+                evs[i - warmup][0].record(stream)
+            graph.replay()
+            if i >= warmup:
+                evs[i - warmup][1].record(stream)
+        torch.cuda.synchronize()
+        if L.status() != 0:
+            raise RuntimeError("device status")
+        t_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        emitted = emitted_tokens(rng.random((steps, G)) < SPEC_ACCEPT)
+        nus = [int(L.forward_debug(xpool[i])["n_union"].item()) for i in range(16)]
+        n_union = statistics.fmean(nus)
+        mean_s = reduce_max(sum(t_ms) / 1000.0, B.world) / steps
+        gbs = expert_bytes(wl, n_union) / mean_s / 1e9
+        sweep[f"G{G}"] = {"tokens_per_forward_batch": T, "ms_per_forward": 1000.0 * mean_s,
+                          "mean_union_experts": n_union, "expert_gbs": gbs,
+                          "expert_hbm_frac": gbs / B.hbm,
+                          "mean_emitted_per_forward": float(emitted.mean()),
+                          "accepted_tokens_per_s": B.world * float(emitted.sum()) / (mean_s * steps),
+                          "verified_tokens_per_s": B.world * T / mean_s, "launches": L.launches(T)}
+        del graph, xpool
+    L.close()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    best = max(sweep, key=lambda k: sweep[k]["accepted_tokens_per_s"])
+    return {"workload": "glm_verify_t8 layer, 1 + G tokens per forward (G = 0..%d drafts)" % max_drafts,
+            "acceptance": {"per_draft": SPEC_ACCEPT, "model": "a draft counts only if every draft before "
+                           "it was accepted; seeded draws; tokens per forward = 1 + accepted prefix"},
+            "steps": steps, "warmup": warmup, "sweep": sweep, "best": best,
+            "best_accepted_tokens_per_s": sweep[best]["accepted_tokens_per_s"],
+            "l2": "flushed between steps (256 MB write, outside the timed events)"}
+
+
 def run_coli(args):
     B = Bench(args)
     wl = W.WORKLOADS[args.workload]
@@ -553,6 +637,12 @@ def run_coli(args):
         cfgs = {}
         for name in names:
             if name == wl.name:
+                continue
+            if name == "spec_verify":
+                steps = max(1, min(args.steps, 300))
+                cfgs[name] = measure_spec(B, steps, max(3, min(args.warmup, 10)))
+                out["gpu_launches"] += sum(v["launches"] * (steps + max(3, min(args.warmup, 10)))
+                                           for v in cfgs[name]["sweep"].values())
                 continue
             cwl = W.WORKLOADS[name]
             steps = max(1, min(args.steps, CONFIG_STEP_CAP.get(name, args.steps)))

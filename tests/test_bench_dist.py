@@ -47,3 +47,18 @@ def test_bench_args_defaults():
     import bench
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and a.workload == "glm_decode_t1"
+
+
+def test_spec_accounting_counts_the_accepted_prefix():
+    """a forward yields its verified token plus the drafts accepted before the first rejection"""
+    import numpy as np
+
+    import bench
+    acc = np.array([[True, True, False, True], [False, True, True, True], [True] * 4, [False] * 4])
+    assert bench.emitted_tokens(acc).tolist() == [3, 1, 5, 1]
+    assert bench.emitted_tokens(np.zeros((3, 0), bool)).tolist() == [1, 1, 1]
+    # the simulated acceptance gives 1 + p + p^2 + p^3 tokens per forward with 3 drafts: 2.2..2.8
+    rng = np.random.default_rng(0)
+    m = bench.emitted_tokens(rng.random((200000, 3)) < bench.SPEC_ACCEPT).mean()
+    p = bench.SPEC_ACCEPT
+    assert abs(m - (1 + p + p * p + p ** 3)) < 0.01 and 2.2 <= m <= 2.8
