@@ -49,7 +49,7 @@ FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 # the layer configurations the JSON line's `configs` object times besides the headline
 CONFIGS = ["tiny_t1", "glm_decode_t1", "glm_verify_t4", "glm_stack16_t1", "glm_prefill_t512",
-           "spec_verify"]
+           "spec_verify", "glm_i8_decode_t1", "glm_i2_decode_t1"]
 # steps of a `configs` entry are capped so the whole default run stays within a few minutes
 CONFIG_STEP_CAP = {"glm_prefill_t512": 60, "glm_stack16_t1": 300}
 
@@ -83,7 +83,12 @@ def expert_bytes(wl, n_union_total):
 
 
 def gateup_bytes(wl, n_union_total):
-    return n_union_total * (wl.f * wl.d + 8 * wl.f)
+    """gate and up codes + their row scales of the union experts"""
+    return n_union_total * (2 * wl.f * wl.d * wl.wbits // 8 + 8 * wl.f)
+
+
+def down_bytes(wl, n_union_total):
+    return n_union_total * (wl.d * wl.f * wl.wbits // 8 + 4 * wl.d)
 
 
 def expert_ops(wl, T):
@@ -454,6 +459,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
     out = {"value": value, "unit": "tokens/s", "ms_per_step": 1000.0 * mean_s,
            "config": {"workload": wl.name, "d": wl.d, "f": wl.f, "E": wl.E, "K": wl.K,
                       "n_shared": wl.n_shared, "T": T, "layers": wl.layers, "bias": wl.bias,
+                      "weight_bits": wl.wbits,
                       "resident_expert_gb": round(wl.layers * (wl.E + wl.n_shared) * wl.expert_bytes / 1e9, 2),
                       "l2": "flushed between steps (256 MB write, outside the timed events)",
                       "tokens": f"pool of {npool} seeded batches, one per step",
@@ -502,8 +508,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
                            "frac": ach / B.hbm, "algorithmic_bytes": gb,
                            "traffic": recorded_traffic("gateup_decode_kernel", wl.name),
                            "timing": "CUDA events around the launch, profiled pass"}
-        db = n_union * (wl.d * wl.f // 2 + 4 * wl.d)
-        out["down_gbs"] = db / (kern["down"] / 1000.0) / 1e9
+        out["down_gbs"] = down_bytes(wl, n_union) / (kern["down"] / 1000.0) / 1e9
     if clk:
         out["clocks"] = clk
     # end to end through the host-buffer entry point (copies inside the timed region)
@@ -630,7 +635,7 @@ def run_coli(args):
     out = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": B.world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "i4xi8->i32,f32", "data": "synthetic"}
+           "dtype": f"i{wl.wbits}xi8->i32,f32", "data": "synthetic"}
     out.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step", "steps", "warmup")})
     if args.configs != "none":
         names = CONFIGS if args.configs == "all" else [n for n in args.configs.split(",") if n]

@@ -41,11 +41,12 @@ class Workload:
     w_sigma: float = 0.02
     router_sigma: float = 0.02
     x_sigma: float = 1.0
+    wbits: int = 4  # bits per expert weight: 4, or 8 / 2 for int8 / int2 experts
 
     @property
     def expert_bytes(self):
-        """packed int4 nibbles + f32 row scales of one expert (gate, up, down)"""
-        return 3 * self.d * self.f // 2 + 4 * (2 * self.f + self.d)
+        """packed codes + f32 row scales of one expert (gate, up, down)"""
+        return 3 * self.d * self.f * self.wbits // 8 + 4 * (2 * self.f + self.d)
 
     @property
     def n_slots(self):
@@ -64,6 +65,14 @@ WORKLOADS = {
                                layers=16, has_norm=True),
     "glm_prefill_t512": Workload("glm_prefill_t512", d=6144, f=2048, E=256, K=8, n_shared=1,
                                  T=512, bias="zipf"),
+    # int8 experts ("colibrì 架构概述" §3.1: int8 rows for the dense part and the MTP head) and
+    # int2 experts (int2 packed, experimental) on the same layers
+    "tiny_i8_t1": Workload("tiny_i8_t1", d=512, f=256, E=32, K=4, n_shared=1, T=1, wbits=8),
+    "tiny_i2_t1": Workload("tiny_i2_t1", d=512, f=256, E=32, K=4, n_shared=1, T=1, wbits=2),
+    "glm_i8_decode_t1": Workload("glm_i8_decode_t1", d=6144, f=2048, E=256, K=8, n_shared=1, T=1,
+                                 wbits=8),
+    "glm_i2_decode_t1": Workload("glm_i2_decode_t1", d=6144, f=2048, E=256, K=8, n_shared=1, T=1,
+                                 wbits=2),
     # the GLM layer's shapes with 32 routed experts: the same kernels and per-step bytes
     # (9 experts, 170 MB, more than L2) with 0.6 GB resident, for counter captures
     "glm_e32_decode_t1": Workload("glm_e32_decode_t1", d=6144, f=2048, E=32, K=8, n_shared=1, T=1),

@@ -23,7 +23,10 @@
  * major, two's complement, element 2i in the low nibble of byte i of its row, followed by
  * the f32 row scales [s_gate (f) | s_up (f) | s_down (d)] ("colibrì 架构概述" §3.1: two
  * 4-bit values per byte, one f32 scale per row; README: the three matrices of an expert
- * are stored next to each other).  The library repacks records into its own device layout
+ * are stored next to each other).  A layer created with wbits = 8 takes the same record with
+ * one int8 code per byte, with wbits = 2 four two's-complement 2-bit codes per byte (element
+ * 4i+k in bits 2k..2k+1 of byte i of its row) (§3.1 int8 rows for the dense part and the MTP
+ * head, int2 packed experimental).  The library repacks records into its own device layout
  * at load time; the weights are never expanded to floats.
  *
  * Conventions.  Every call returns COLI_OK (0) or a negative COLI_E* status; nothing aborts,
@@ -65,6 +68,8 @@ typedef struct {
   float routed_scale; /* multiplies every routing weight (1.0 = plain renormalisation)       */
   float rms_eps;    /* RMSNorm epsilon (used only with has_norm)                               */
   int has_norm;     /* 1: forward computes y = x + MoE(RMSNorm(x)) with the loaded gamma      */
+  int wbits;        /* bits per expert weight: 4 (int4, also when 0), 8 (int8 rows) or 2     */
+                    /* (int2 rows); int8 and int2 layers run the decode kernels for every T    */
 } coli_moe_config;
 
 /* Optional per-step outputs of coli_moe_forward_debug.  Device pointers owned by the caller;
@@ -183,10 +188,27 @@ int coli_moe_launches(const coli_moe* h, int T);
 /* Bytes of one expert record in the canonical format (3*d*f/2 + 4*(2f+d)). */
 int64_t coli_moe_expert_record_bytes(int d, int f);
 
+/* The same for wbits = 4, 8 or 2 bits per weight (3*d*f*wbits/8 + 4*(2f+d)); EINVAL for
+ * another width. */
+int64_t coli_moe_expert_record_bytes_w(int d, int f, int wbits);
+
 /* Standalone pack of fp32 rows into the canonical int4 format ("colibrì 架构概述" §3.1):
  * s[r] = max|w[r,:]|/7, q = round(w/s) clamped to [-7,7], two nibbles per byte.
  * w_dev [rows,cols] -> packed_dev [rows,cols/2], scales_dev [rows].  cols even, <= 65536. */
 int coli_quantize_i4_rows(const float* w_dev, int64_t rows, int cols, uint8_t* packed_dev,
+                          float* scales_dev, void* stream);
+
+/* Standalone pack of fp32 rows into int8 rows ("colibrì 架构概述" §3.1 int8, quantize_rows):
+ * s[r] = max|w[r,:]|/127, q = round(w/s) (half away from zero) clamped to [-127,127], one code
+ * per byte.  w_dev [rows,cols] -> q_dev [rows,cols], scales_dev [rows].  cols <= 65536. */
+int coli_quantize_i8_rows(const float* w_dev, int64_t rows, int cols, int8_t* q_dev,
+                          float* scales_dev, void* stream);
+
+/* Standalone pack of fp32 rows into int2 rows ("colibrì 架构概述" §3.1 int2 packed, pack_int2):
+ * s[r] = max|w[r,:]|, q = round(w/s) clamped to [-1,1], four two's-complement 2-bit codes per
+ * byte, element 4i+k in bits 2k..2k+1 of byte i.  w_dev [rows,cols] (16-byte aligned) ->
+ * packed_dev [rows,cols/4], scales_dev [rows].  cols a multiple of 4, <= 65536. */
+int coli_quantize_i2_rows(const float* w_dev, int64_t rows, int cols, uint8_t* packed_dev,
                           float* scales_dev, void* stream);
 
 /* Standalone Q8_0-style activation quantisation: blocks of 32, d = max|x|/127,

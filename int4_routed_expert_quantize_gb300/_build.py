@@ -10,7 +10,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "libcoli_moe.so")
-SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "expert_fused.cu", "expert_prefill.cu",
+SOURCES = ["pack.cu", "route.cu", "expert_decode.cu", "gateup_w4.cu", "down_w4.cu", "gateup_w8.cu",
+           "down_w8.cu", "gateup_w2.cu", "down_w2.cu", "expert_fused.cu", "expert_prefill.cu",
            "runtime.cu", "noalloc.cu", "tier.cpp", "status.cpp"]
 HOST_SOURCES = ["tier.cpp", "status.cpp"]  # the parts that need no CUDA
 

@@ -34,7 +34,7 @@ class ColiError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("d", _i), ("f", _i), ("n_experts", _i), ("top_k", _i), ("n_shared", _i),
                 ("qblock", _i), ("max_tokens", _i), ("routed_scale", _f), ("rms_eps", _f),
-                ("has_norm", _i)]
+                ("has_norm", _i), ("wbits", _i)]
 
 
 class TierConfig(ctypes.Structure):
@@ -95,6 +95,10 @@ def _bind_layer(L):
     L.coli_moe_status.argtypes = [_vp, _vp]
     L.coli_moe_expert_record_bytes.argtypes = [_i, _i]
     L.coli_moe_expert_record_bytes.restype = _i64
+    L.coli_moe_expert_record_bytes_w.argtypes = [_i, _i, _i]
+    L.coli_moe_expert_record_bytes_w.restype = _i64
+    L.coli_quantize_i8_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
+    L.coli_quantize_i2_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
     L.coli_moe_launches.argtypes = [_vp, _i]
     L.coli_moe_inject_fault.argtypes = [_vp, _i]
     L.coli_moe_set_prefill_min.argtypes = [_vp, _i]
@@ -150,17 +154,19 @@ def _stream(stream):
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else stream
 
 
-def expert_record_bytes(d, f):
-    return int(lib().coli_moe_expert_record_bytes(d, f))
+def expert_record_bytes(d, f, wbits=4):
+    return int(lib().coli_moe_expert_record_bytes_w(d, f, wbits))
 
 
 class MoeLayer:
-    """One int4 routed-expert MoE layer resident on the current CUDA device."""
+    """One routed-expert MoE layer (int4 experts, or int8 / int2 with wbits) resident on the
+    current CUDA device."""
 
     def __init__(self, d, f, n_experts, top_k, n_shared=1, max_tokens=4, routed_scale=1.0,
-                 rms_eps=1e-6, has_norm=False):
+                 rms_eps=1e-6, has_norm=False, wbits=4):
         self.cfg = Config(d, f, n_experts, top_k, n_shared, 32, max_tokens, routed_scale, rms_eps,
-                          int(has_norm))
+                          int(has_norm), wbits)
+        self.wbits = wbits
         h = _vp()
         _check(lib().coli_moe_create(ctypes.byref(self.cfg), ctypes.byref(h)), "coli_moe_create")
         self.h = h
@@ -170,7 +176,7 @@ class MoeLayer:
     @classmethod
     def for_workload(cls, wl, max_tokens=None):
         return cls(wl.d, wl.f, wl.E, wl.K, wl.n_shared, max_tokens or wl.T, 1.0, wl.rms_eps,
-                   wl.has_norm)
+                   wl.has_norm, wl.wbits)
 
     def close(self):
         if getattr(self, "h", None) is not None and self.h.value:
@@ -276,6 +282,41 @@ def quantize_i4_rows(w, packed=None, scales=None, stream=None):
     _check(lib().coli_quantize_i4_rows(_ptr(w), rows, cols, _ptr(packed), _ptr(scales), _stream(stream)),
            "coli_quantize_i4_rows")
     return packed, scales
+
+
+def quantize_i8_rows(w, q=None, scales=None, stream=None):
+    """int8 rows (one code per byte) and one f32 scale per row (coli_quantize_i8_rows)"""
+    rows, cols = w.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.int8, device=w.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().coli_quantize_i8_rows(_ptr(w), rows, cols, _ptr(q), _ptr(scales), _stream(stream)),
+           "coli_quantize_i8_rows")
+    return q, scales
+
+
+def quantize_i2_rows(w, packed=None, scales=None, stream=None):
+    """int2 rows (four codes per byte) and one f32 scale per row (coli_quantize_i2_rows)"""
+    rows, cols = w.shape
+    if packed is None:
+        packed = torch.empty((rows, cols // 4), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().coli_quantize_i2_rows(_ptr(w), rows, cols, _ptr(packed), _ptr(scales), _stream(stream)),
+           "coli_quantize_i2_rows")
+    return packed, scales
+
+
+def quantize_rows(w, wbits, out=None, scales=None, stream=None):
+    """rows of `wbits` bits per weight into `out` (a uint8 view of the record's bytes)"""
+    if wbits == 4:
+        return quantize_i4_rows(w, out, scales, stream)
+    if wbits == 8:
+        return quantize_i8_rows(w, None if out is None else out.view(torch.int8), scales, stream)
+    if wbits == 2:
+        return quantize_i2_rows(w, out, scales, stream)
+    raise ValueError(f"no {wbits}-bit rows")
 
 
 def route_noalloc(x, W_r, K, bias=None, routed_scale=1.0, stream=None):

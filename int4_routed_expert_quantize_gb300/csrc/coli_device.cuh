@@ -124,10 +124,106 @@ __device__ __forceinline__ int block_dot_split(const uint32_t (&lo)[4], const ui
 // Position, within a stored row, of block b = g*G + i (G blocks per lane group): the groups are
 // contiguous and a group's blocks are rotated by one for groups 4..7 mod 8, so that the
 // 16-byte loads of 8 consecutive lanes fall in distinct shared-memory banks.
-__device__ __forceinline__ int store_chunk(int g, int i, int G) {
+__host__ __device__ __forceinline__ int store_chunk(int g, int i, int G) {
   int c = i + ((g >> 2) & 1);
   if (c >= G) c -= G;
   return g * G + c;
+}
+
+// The same for 8-byte units (int2 blocks): rotated by one for groups 8..15 mod 16, so that the
+// 8-byte loads of 16 consecutive lanes fall in distinct banks.
+__host__ __device__ __forceinline__ int store_chunk8(int g, int i, int G) {
+  int c = i + ((g >> 3) & 1);
+  if (c >= G) c -= G;
+  return g * G + c;
+}
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// ------------------------------------------------------------------ weight widths ---------
+// One 32-element weight block of a stored row, prepared as 8 words for dp4a against the block's
+// activation codes x[0..7] (x[j] = elements 4j..4j+3), for WB = 4, 8 or 2 bits per weight:
+//  * int4 (store: 16 bytes, word k = elements 8k..8k+7, byte m = element 8k+m low nibble and
+//    8k+m+4 high nibble, each code + 8): w[2k] = word & 0x0F0F0F0F pairs with x[2k], w[2k+1] =
+//    word & 0xF0F0F0F0 (16 x code) with x[2k+1];
+//  * int8 (store: the block's two 16-byte halves in two planes of the row, nb chunks apart,
+//    codes as they are): w[j] = word j, signed;
+//  * int2 (store: 8 bytes, word h = elements 16h..16h+15, element 16h+4k+m in bits 2k..2k+1 of
+//    byte m, each code + 2): w[4h+k] = (word h >> 2k) & 0x03030303.
+// The offset codes (+8, +2) are removed by the block's correction -off * sum(x).
+template <int WB>
+struct Wfmt {
+  static constexpr int off = WB == 4 ? 8 : (WB == 2 ? 2 : 0);  // code offset in the store
+  static constexpr int row_bytes(int n) { return n * WB / 8; }
+};
+
+// row: the stored row; g: the lane's group; i: block within the group; G blocks per group; nb
+// blocks in the row.  Lanes outside the active groups pass on = false and get zeros.
+template <int WB>
+__device__ __forceinline__ void wload(const uint8_t* row, int g, int i, int G, int nb, bool on,
+                                      uint32_t (&w)[8]) {
+  if constexpr (WB == 4) {
+    uint4 c = make_uint4(0, 0, 0, 0);
+    if (on) c = *reinterpret_cast<const uint4*>(row + store_chunk(g, i, G) * 16);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[2 * k] = cw[k] & 0x0F0F0F0Fu;
+      w[2 * k + 1] = cw[k] & 0xF0F0F0F0u;
+    }
+  } else if constexpr (WB == 8) {
+    uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+    if (on) {
+      const int o = store_chunk(g, i, G) * 16;
+      c0 = *reinterpret_cast<const uint4*>(row + o);
+      c1 = *reinterpret_cast<const uint4*>(row + nb * 16 + o);
+    }
+    w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
+    w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
+  } else {
+    uint2 c = make_uint2(0, 0);
+    if (on) c = *reinterpret_cast<const uint2*>(row + store_chunk8(g, i, G) * 8);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = (c.x >> (2 * k)) & 0x03030303u;
+      w[4 + k] = (c.y >> (2 * k)) & 0x03030303u;
+    }
+  }
+}
+
+// exact int32 dot of a prepared weight block with the block's activation codes; corr = -off *
+// (sum of the 32 activation codes)
+template <int WB>
+__device__ __forceinline__ int wdot(const uint32_t (&w)[8], const uint32_t (&x)[8], int corr) {
+  if constexpr (WB == 4) {
+    int a1 = 0, a16 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      a1 = dp4a_us(w[2 * k], x[2 * k], a1);
+      a16 = dp4a_us(w[2 * k + 1], x[2 * k + 1], a16);
+    }
+    return a1 + (a16 >> 4) + corr;
+  } else if constexpr (WB == 8) {
+    int a = 0, b = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      a = dp4a_ss(w[k], x[k], a);
+      b = dp4a_ss(w[4 + k], x[4 + k], b);
+    }
+    return a + b + corr;
+  } else {
+    int a = 0, b = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      a = dp4a_us(w[k], x[k], a);
+      b = dp4a_us(w[4 + k], x[4 + k], b);
+    }
+    return a + b + corr;
+  }
 }
 
 // ------------------------------------------------------------------ mbarrier / bulk copy ---

@@ -92,6 +92,7 @@ struct Shape {
   int d, f, E, K, n_shared, T;
   float routed_scale, rms_eps;
   int has_norm;
+  int wbits;  // bits per expert weight: 4, 8 or 2
 };
 
 // optional debug outputs of the expert kernels (device pointers, may be null)
@@ -130,7 +131,11 @@ cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, con
                                    const ExpertDebug& dbg, int num_sms, cudaStream_t stream,
                                    cudaEvent_t after_gateup = nullptr);
 cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
-                                 int64_t dst_row_stride, cudaStream_t stream);
+                                 int64_t dst_row_stride, cudaStream_t stream, int wbits);
+cudaError_t launch_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q,
+                                    float* scales, cudaStream_t stream);
+cudaError_t launch_quantize_i2_rows(const float* w, int64_t rows, int cols, uint8_t* packed,
+                                    float* scales, cudaStream_t stream);
 cudaError_t launch_permute_router(const float* src, float* dst, int E, int d,
                                   cudaStream_t stream);
 cudaError_t launch_quantize_i4_rows(const float* w, int64_t rows, int cols, uint8_t* packed,
@@ -138,6 +143,29 @@ cudaError_t launch_quantize_i4_rows(const float* w, int64_t rows, int cols, uint
 cudaError_t launch_quantize_q8(const float* x, int64_t n, int8_t* q, float* d,
                                cudaStream_t stream);
 cudaError_t configure_expert_kernels();
+
+// per-CTA unit table of the gate/up kernel: slot, expert, first pair, pair count, the pairs'
+// tokens (T at most) and the 32 gate + 32 up row scales
+constexpr int kGuTabInts = 5 + kDecodeTmax;  // slot, expert, first pair, pairs, hb, tokens
+constexpr int kGuTabBytes = (kGuTabInts + 64) * 4;
+// Relative cost of one gate/up unit whose union slot serves np tokens: its bytes take the same
+// time whatever np (kGuCostBytes), its dots grow with np (kGuCostPair each); the larger bounds
+// the unit.  The routed units are split over the CTAs by this cost, not by count.  Calibrated
+// on the four-token int4 GLM layer: a four-token unit measured about 3.6 times a one-token unit,
+// and the step time keeps improving up to a model ratio of about 4.4, flat beyond.
+constexpr int kGuCostBytes = 20, kGuCostPair = 22;
+__host__ __device__ constexpr int gu_unit_cost(int np) {
+  return kGuCostPair * np > kGuCostBytes ? kGuCostPair * np : kGuCostBytes;
+}
+
+// Gate/up row pairs per ring stage: 8 (one per consumer warp, each warp reduces the gate and the
+// up row of its pair) for int4 and int2; 4 for int8, whose rows are twice the int4 bytes: warp w
+// then reduces one row, the gate row of pair w%4 (w < 4) or its up row, and SwiGLU is applied
+// when the unit's 32 rows are in.
+__host__ __device__ constexpr int gu_rows_per_stage(int wb) { return wb == 8 ? 4 : 8; }
+// Down rows per stage chunk: at most 8 per warp, and half that for int8 so that a stage keeps the
+// bytes of an int4 one.
+__host__ __device__ constexpr int dn_chunk_cap(int wb) { return wb == 8 ? kDownChunk / 2 : kDownChunk; }
 
 // shared-memory plans (host and device agree on the carve-up)
 struct GateupPlan {
@@ -161,8 +189,19 @@ cudaError_t configure_fused_kernels();
 cudaError_t launch_expert_fused(const float* x, float* y, const Shape& s, const Store& st,
                                 const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                 bool skip_arrival, cudaStream_t stream);
-GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
-DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid);
+GateupPlan gateup_plan(int d, int f, int T, int K, int E, int n_shared, int grid, int wbits);
+DownPlan down_plan(int d, int f, int T, int K, int E, int n_shared, int grid, int wbits);
 int down_grid(int d, int num_sms);  // CTAs of the down kernel
+// the decode kernels of one weight width (expert_decode.cuh, instantiated per width)
+template <int WB> cudaError_t configure_gateup_kernels_wb();
+template <int WB> cudaError_t configure_down_kernels_wb();
+template <int WB>
+cudaError_t launch_gateup_decode_wb(const Shape& s, const Store& st, const Work& w,
+                                    const ExpertDebug& dbg, int num_sms, bool pdl,
+                                    cudaStream_t stream);
+template <int WB>
+cudaError_t launch_down_decode_wb(const float* x, float* y, const Shape& s, const Store& st,
+                                  const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
+                                  cudaStream_t stream);
 
 }  // namespace coli

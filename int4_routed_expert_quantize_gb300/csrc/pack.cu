@@ -1,6 +1,7 @@
-// Format kernels: the canonical int4 row packer ("colibrì 架构概述" §3.1: two 4-bit values per
-// byte, one f32 scale per row), the standalone Q8_0-style activation quantiser, and the
-// load-time repack of canonical records into the store layout the expert kernels stream.
+// Format kernels: the canonical int4, int8 and int2 row packers ("colibrì 架构概述" §3.1: two
+// 4-bit values per byte, one value per byte, four 2-bit values per byte; one f32 scale per
+// row), the standalone Q8_0-style activation quantiser, and the load-time repack of canonical
+// records into the store layout the expert kernels stream.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,74 @@ cudaError_t launch_quantize_i4_rows(const float* w, int64_t rows, int cols, uint
   if (rows <= 0) return cudaSuccess;
   const long blocks = (rows + 7) / 8;
   quantize_i4_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(w, rows, cols, packed, scales);
+  return cudaGetLastError();
+}
+
+// int8 rows ("colibrì 架构概述" §3.1 int8, quantize_rows): one warp per row, s = max|w| / 127,
+// code = round(w / s) half away from zero clamped to [-127, 127], one code per byte
+__global__ void __launch_bounds__(256) quantize_i8_rows_kernel(const float* __restrict__ w,
+                                                               long rows, int cols,
+                                                               int8_t* __restrict__ q,
+                                                               float* __restrict__ scales) {
+  const long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* wr = w + row * cols;
+  float amax = 0.0f;
+  for (int i = lane; i < cols; i += 32) amax = fmaxf(amax, fabsf(wr[i]));
+  const float s = __fdiv_rn(warp_max(amax), 127.0f);
+  for (int i = lane; i < cols; i += 32) {
+    int v = 0;
+    if (s != 0.0f) v = max(-127, min(127, (int)roundf(__fdiv_rn(wr[i], s))));
+    q[row * cols + i] = (int8_t)v;
+  }
+  if (lane == 0) scales[row] = s;
+}
+
+// int2 rows ("colibrì 架构概述" §3.1 int2 packed, pack_int2): one warp per row, s = max|w|,
+// code = round(w / s) half away from zero clamped to [-1, 1], four two's-complement 2-bit codes
+// per byte with element 4i+k in bits 2k..2k+1 of byte i
+__global__ void __launch_bounds__(256) quantize_i2_rows_kernel(const float* __restrict__ w,
+                                                               long rows, int cols,
+                                                               uint8_t* __restrict__ packed,
+                                                               float* __restrict__ scales) {
+  const long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float4* wr = reinterpret_cast<const float4*>(w + row * cols);
+  float amax = 0.0f;
+  for (int i = lane; i < cols / 4; i += 32) {
+    const float4 v = wr[i];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  const float s = warp_max(amax);  // max|w| / 1
+  uint8_t* pr = packed + row * (cols / 4);
+  for (int i = lane; i < cols / 4; i += 32) {
+    const float4 v = wr[i];
+    const float e[4] = {v.x, v.y, v.z, v.w};
+    int byte = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int c = 0;
+      if (s != 0.0f) c = max(-1, min(1, (int)roundf(__fdiv_rn(e[k], s))));
+      byte |= (c & 3) << (2 * k);
+    }
+    pr[i] = (uint8_t)byte;
+  }
+  if (lane == 0) scales[row] = s;
+}
+
+cudaError_t launch_quantize_i8_rows(const float* w, int64_t rows, int cols, int8_t* q,
+                                    float* scales, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  quantize_i8_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(w, rows, cols, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_i2_rows(const float* w, int64_t rows, int cols, uint8_t* packed,
+                                    float* scales, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  quantize_i2_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(w, rows, cols, packed, scales);
   return cudaGetLastError();
 }
 
@@ -103,11 +172,64 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__
       make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Canonical int8 row -> store layout: the two 16-byte halves of block b = g*G + i go to two
+// planes of the row (nb chunks apart), each at chunk store_chunk(g, i, G); codes unchanged.
+__global__ void __launch_bounds__(256) repack_i8_kernel(const uint8_t* __restrict__ src,
+                                                        uint8_t* __restrict__ dst, int rows, int cols,
+                                                        long dst_row_stride) {
+  const int nb = cols / 32;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)rows * nb) return;
+  const long r = idx / nb;
+  const int b = (int)(idx - r * nb);
+  const int G = (nb + 31) / 32;
+  const int g = b / G, i = b - g * G;
+  const uint4* c = reinterpret_cast<const uint4*>(src + r * cols + (long)b * 32);
+  uint8_t* row = dst + r * dst_row_stride + (long)store_chunk(g, i, G) * 16;
+  *reinterpret_cast<uint4*>(row) = c[0];
+  *reinterpret_cast<uint4*>(row + (long)nb * 16) = c[1];
+}
+
+// Canonical int2 row (element 4i+k in bits 2k..2k+1 of byte i) -> store layout: block b = g*G +
+// i (8 bytes) goes to 8-byte unit store_chunk8(g, i, G); inside it word h holds elements
+// 16h..16h+15 with element 16h+4k+m in bits 2k..2k+1 of byte m, as code + 2 (for a 2-bit two's
+// complement field, code + 2 is the field with its top bit flipped).
+__global__ void __launch_bounds__(256) repack_i2_kernel(const uint8_t* __restrict__ src,
+                                                        uint8_t* __restrict__ dst, int rows, int cols,
+                                                        long dst_row_stride) {
+  const int nb = cols / 32;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)rows * nb) return;
+  const long r = idx / nb;
+  const int b = (int)(idx - r * nb);
+  const int G = (nb + 31) / 32;
+  const int g = b / G, i = b - g * G;
+  const uint2 c = *reinterpret_cast<const uint2*>(src + r * (cols / 4) + (long)b * 8);
+  const uint32_t cw[2] = {c.x, c.y};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    // canonical: element e of the block in byte e >> 2, bits 2*(e & 3)
+    const uint32_t field = (cw[e >> 4] >> (8 * ((e >> 2) & 3) + 2 * (e & 3))) & 3u;
+    const int h = e >> 4, k = (e & 15) >> 2, m = e & 3;
+    out[h] |= (field ^ 2u) << (8 * m + 2 * k);
+  }
+  *reinterpret_cast<uint2*>(dst + r * dst_row_stride + (long)store_chunk8(g, i, G) * 8) =
+      make_uint2(out[0], out[1]);
+}
+
 cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int cols,
-                                 int64_t dst_row_stride, cudaStream_t stream) {
+                                 int64_t dst_row_stride, cudaStream_t stream, int wbits) {
   const long n = (long)rows * (cols / 32);
-  repack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(src, dst, rows, cols,
-                                                                 dst_row_stride);
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  if (wbits == 4)
+    repack_kernel<<<grid, 256, 0, stream>>>(src, dst, rows, cols, dst_row_stride);
+  else if (wbits == 8)
+    repack_i8_kernel<<<grid, 256, 0, stream>>>(src, dst, rows, cols, dst_row_stride);
+  else if (wbits == 2)
+    repack_i2_kernel<<<grid, 256, 0, stream>>>(src, dst, rows, cols, dst_row_stride);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

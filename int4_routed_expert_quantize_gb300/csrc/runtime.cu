@@ -49,7 +49,8 @@ struct coli_moe {
 
 namespace {
 
-int64_t rec_bytes(int d, int f) { return 3LL * d * f / 2; }
+// bytes of the codes of one expert record: gate, up and down at wb bits per weight
+int64_t rec_bytes(int d, int f, int wb) { return 3LL * d * f * wb / 8; }
 
 bool shape_ok(int n) {
   if (n < 128 || n > 8192 || n % 128) return false;
@@ -120,7 +121,7 @@ bool takes_batched(const coli_moe* h, int T) {
 Shape shape_of(const coli_moe* h, int T) {
   const coli_moe_config& c = h->cfg;
   return Shape{c.d, c.f, c.n_experts, c.top_k, c.n_shared, T, c.routed_scale, c.rms_eps,
-               c.has_norm};
+               c.has_norm, c.wbits};
 }
 
 int copy_dump(coli_moe* h, int T, const coli_moe_dump* dump, cudaStream_t stream);
@@ -327,15 +328,21 @@ int coli_moe_launches(const coli_moe* h, int T) {
 }
 
 int64_t coli_moe_expert_record_bytes(int d, int f) {
-  return rec_bytes(d, f) + 4LL * (2LL * f + d);
+  return rec_bytes(d, f, 4) + 4LL * (2LL * f + d);
+}
+
+int64_t coli_moe_expert_record_bytes_w(int d, int f, int wbits) {
+  if (wbits != 4 && wbits != 8 && wbits != 2) return COLI_EINVAL;
+  return rec_bytes(d, f, wbits) + 4LL * (2LL * f + d);
 }
 
 int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   if (!out) return COLI_EINVAL;
   *out = nullptr;
   if (!cfg) return COLI_EINVAL;
-  const coli_moe_config c = *cfg;
-  if (c.qblock != 32 || c.n_experts < 1 || c.n_experts > 1024 || c.top_k < 1 ||
+  coli_moe_config c = *cfg;
+  if (c.wbits == 0) c.wbits = 4;  // int4 experts unless the caller asks for another width
+  if ((c.wbits != 4 && c.wbits != 8 && c.wbits != 2) || c.qblock != 32 || c.n_experts < 1 || c.n_experts > 1024 || c.top_k < 1 ||
       c.top_k > c.n_experts || c.top_k > 32 || (c.n_shared != 0 && c.n_shared != 1) ||
       c.max_tokens < 1 || c.max_tokens > 4096 || !std::isfinite(c.routed_scale) ||
       !(c.rms_eps >= 0.0f) || !std::isfinite(c.rms_eps) || c.d <= 0 || c.f <= 0)
@@ -355,8 +362,8 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
     const long slots = (long)(Tc * c.top_k < c.n_experts ? Tc * c.top_k : c.n_experts) + c.n_shared;
     const long gu_grid = slots * (c.f / 32) < sms ? slots * (c.f / 32) : sms;
     const int dn_grid = down_grid(c.d, sms);
-    if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid).nst >= 2 &&
-        down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid).nst >= 2)
+    if (gateup_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)gu_grid, c.wbits).nst >= 2 &&
+        down_plan(c.d, c.f, Tc, c.top_k, c.n_experts, c.n_shared, (int)dn_grid, c.wbits).nst >= 2)
       decode_tmax = Tc;
   }
   if (!decode_tmax) return COLI_EUNSUPPORTED;
@@ -376,14 +383,16 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   h->slots = c.n_experts + c.n_shared;
   h->decode_tmax = decode_tmax;
   h->loaded.assign(h->slots, 0);
-  h->fused = fused_supported(c.d, c.f, c.top_k, c.n_experts, c.n_shared, h->num_sms);
+  // the fused one-token kernel and the tensor-core path take int4 experts
+  h->fused = c.wbits == 4 && fused_supported(c.d, c.f, c.top_k, c.n_experts, c.n_shared, h->num_sms);
   const long S = h->slots, d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
   const long Pm = Tm * K + (c.n_shared ? Tm : 0);
   int rc = COLI_OK;
 #define ALLOC(ptr, bytes) \
   if (rc == COLI_OK) rc = dalloc(h, &(ptr), (size_t)(bytes));
-  ALLOC(h->st.wgu, S * f * d)
-  ALLOC(h->st.wd, S * d * (f / 2))
+  const long wb = c.wbits;
+  ALLOC(h->st.wgu, S * f * (2 * d * wb / 8))
+  ALLOC(h->st.wd, S * d * (f * wb / 8))
   ALLOC(h->st.sc, sizeof(float) * S * (2 * f + d))
   ALLOC(h->st.wr, sizeof(float) * E * d)
   if (c.has_norm) ALLOC(h->st.gamma, sizeof(float) * d)
@@ -409,7 +418,7 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.sel_flag, sizeof(int32_t) * 4)
   ALLOC(h->w.status, sizeof(int32_t) * 4)
   ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
-  if (rc == COLI_OK && Tm > kDecodeTmax && d % 256 == 0 &&
+  if (rc == COLI_OK && c.wbits == 4 && Tm > kDecodeTmax && d % 256 == 0 &&
       configure_prefill_kernels((int)d, (int)f, (int)E) == cudaSuccess &&
       configure_route_batch_kernels((int)E) == cudaSuccess) {
     const long prow = Pm + kPrefillTileN;
@@ -515,8 +524,10 @@ int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* pack
   int rc = check_device(h);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  const int d = h->cfg.d, f = h->cfg.f;
-  const size_t rb = (size_t)rec_bytes(d, f);
+  const int d = h->cfg.d, f = h->cfg.f, wb = h->cfg.wbits;
+  const size_t rb = (size_t)rec_bytes(d, f, wb);
+  const size_t rbd = (size_t)d * wb / 8, rbf = (size_t)f * wb / 8;  // bytes of a gate/up, a down row
+  const size_t mat = (size_t)f * rbd;                                 // bytes of a gate or up matrix
   const bool on_device = is_device_ptr(packed);
   uint8_t* staging = nullptr;
   if (!on_device && cudaMalloc(&staging, rb) != cudaSuccess) {
@@ -532,11 +543,12 @@ int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* pack
       if (e == cudaSuccess) e = cudaStreamSynchronize(st);
       rec = staging;
     }
-    uint8_t* gu = h->st.wgu + (size_t)slot * f * d;
-    uint8_t* dn = h->st.wd + (size_t)slot * d * (f / 2);
-    if (e == cudaSuccess) e = launch_repack_matrix(rec, gu, f, d, d, st);
-    if (e == cudaSuccess) e = launch_repack_matrix(rec + (size_t)f * d / 2, gu + d / 2, f, d, d, st);
-    if (e == cudaSuccess) e = launch_repack_matrix(rec + (size_t)f * d, dn, d, f, f / 2, st);
+    // gate row r and up row r side by side (row pairs), then the down rows
+    uint8_t* gu = h->st.wgu + (size_t)slot * 2 * mat;
+    uint8_t* dn = h->st.wd + (size_t)slot * d * rbf;
+    if (e == cudaSuccess) e = launch_repack_matrix(rec, gu, f, d, 2 * rbd, st, wb);
+    if (e == cudaSuccess) e = launch_repack_matrix(rec + mat, gu + rbd, f, d, 2 * rbd, st, wb);
+    if (e == cudaSuccess) e = launch_repack_matrix(rec + 2 * mat, dn, d, f, rbf, st, wb);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(h->st.sc + (size_t)slot * (2 * f + d), scales + (size_t)i * (2 * f + d),
                           sizeof(float) * (2 * f + d), cudaMemcpyDefault, st);
@@ -656,6 +668,24 @@ int coli_quantize_i4_rows(const float* w_dev, int64_t rows, int cols, uint8_t* p
   if (!w_dev || !packed_dev || !scales_dev) return COLI_EINVAL;
   return cuda_status(
       launch_quantize_i4_rows(w_dev, rows, cols, packed_dev, scales_dev, (cudaStream_t)stream));
+}
+
+int coli_quantize_i8_rows(const float* w_dev, int64_t rows, int cols, int8_t* q_dev,
+                          float* scales_dev, void* stream) {
+  if (rows < 0 || cols <= 0 || cols > 65536) return COLI_EINVAL;
+  if (rows == 0) return COLI_OK;
+  if (!w_dev || !q_dev || !scales_dev) return COLI_EINVAL;
+  return cuda_status(
+      launch_quantize_i8_rows(w_dev, rows, cols, q_dev, scales_dev, (cudaStream_t)stream));
+}
+
+int coli_quantize_i2_rows(const float* w_dev, int64_t rows, int cols, uint8_t* packed_dev,
+                          float* scales_dev, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 4 || cols > 65536) return COLI_EINVAL;
+  if (rows == 0) return COLI_OK;
+  if (!w_dev || !packed_dev || !scales_dev || ((uintptr_t)w_dev & 15u)) return COLI_EINVAL;
+  return cuda_status(
+      launch_quantize_i2_rows(w_dev, rows, cols, packed_dev, scales_dev, (cudaStream_t)stream));
 }
 
 int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_dev,

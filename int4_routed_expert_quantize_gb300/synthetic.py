@@ -1,5 +1,6 @@
 """Resident layers filled from the seeded generator (gen/): the float weights are drawn on
-the device, packed by the library's own int4 packer and loaded into the expert store.
+the device, packed by the library's own row packer of the layer's width (int4, int8 or int2)
+and loaded into the expert store.
 Used by the benchmark, the smoke check and the tests; nothing here computes the layer."""
 import torch
 
@@ -22,17 +23,18 @@ def build_layer(wl, layer=0, max_tokens=None, batch=8, stream=None):
     gate = torch.empty((f, d), dtype=torch.float32, device=dev)
     up = torch.empty((f, d), dtype=torch.float32, device=dev)
     down = torch.empty((d, f), dtype=torch.float32, device=dev)
-    rb = 3 * d * f // 2
-    rec = torch.empty((batch, rb), dtype=torch.uint8, device=dev)
+    wb = wl.wbits
+    mat = f * d * wb // 8  # bytes of the gate, the up or the down codes
+    rec = torch.empty((batch, 3 * mat), dtype=torch.uint8, device=dev)
     sc = torch.empty((batch, 2 * f + d), dtype=torch.float32, device=dev)
     n = E + wl.n_shared
     for first in range(0, n, batch):
         count = min(batch, n - first)
         for j in range(count):
             workloads.expert_float_dev(wl, layer, first + j, gate, up, down)
-            coli.quantize_i4_rows(gate, rec[j, : f * d // 2].view(f, d // 2), sc[j, :f])
-            coli.quantize_i4_rows(up, rec[j, f * d // 2: f * d].view(f, d // 2), sc[j, f: 2 * f])
-            coli.quantize_i4_rows(down, rec[j, f * d:].view(d, f // 2), sc[j, 2 * f:])
+            coli.quantize_rows(gate, wb, rec[j, :mat].view(f, d * wb // 8), sc[j, :f])
+            coli.quantize_rows(up, wb, rec[j, mat: 2 * mat].view(f, d * wb // 8), sc[j, f: 2 * f])
+            coli.quantize_rows(down, wb, rec[j, 2 * mat:].view(d, f * wb // 8), sc[j, 2 * f:])
         torch.cuda.synchronize()
         L.load_experts(first, count, rec, sc, stream=stream)
     del gate, up, down, rec, sc

@@ -282,20 +282,20 @@ def expert_ffn(rec, sc, d, f, qx, dx, want_A=False):
 
 # ---------------- expert records from the generator ----------------
 
-def expert_record_from_float(gate, up, down):
-    """[gate | up | down] packed nibbles and [s_g | s_u | s_d] scales, the three matrices of an
-    expert stored adjacently"""
-    pg, sg = quantize_i4_rows(gate)
-    pu, su = quantize_i4_rows(up)
-    pd, sd = quantize_i4_rows(down)
-    rec = np.concatenate([pg.ravel(), pu.ravel(), pd.ravel()])
-    sc = np.concatenate([sg, su, sd])
+def expert_record_from_float(gate, up, down, wbits=4):
+    """[gate | up | down] packed codes (int4 nibbles, int8 bytes or int2 fields, by the oracle's
+    own packers) and [s_g | s_u | s_d] scales, the three matrices of an expert stored adjacently"""
+    quant = {4: quantize_i4_rows, 8: quantize_i8_rows, 2: quantize_i2_rows}[wbits]
+    parts = [quant(m) for m in (gate, up, down)]
+    rec = np.concatenate([np.ascontiguousarray(p).view(np.uint8).ravel() for p, _ in parts])
+    sc = np.concatenate([s for _, s in parts])
     return rec, sc
 
 
 def expert_record(wl, layer, expert):
     from gen import workloads
-    return expert_record_from_float(*workloads.expert_float_host(wl, layer, expert))
+    return expert_record_from_float(*workloads.expert_float_host(wl, layer, expert),
+                                    wbits=getattr(wl, "wbits", 4))
 
 
 # ---------------- full layer ----------------
@@ -404,4 +404,5 @@ class Layer:
         if self.wl.n_shared:
             need.add(self.wl.E)
         self.ensure(sorted(need))
+        kw.setdefault("wbits", getattr(self.wl, "wbits", 4))
         return forward(self.wl, x, self.Wr, self.bias, self.gamma, self.recs, **kw)
