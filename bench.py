@@ -49,7 +49,7 @@ FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 # the layer configurations the JSON line's `configs` object times besides the headline
 CONFIGS = ["tiny_t1", "glm_decode_t1", "glm_verify_t4", "glm_stack16_t1", "glm_prefill_t512",
-           "spec_verify", "glm_i8_decode_t1", "glm_i2_decode_t1"]
+           "spec_verify", "glm_i8_decode_t1", "glm_i2_decode_t1", "tiered"]
 # steps of a `configs` entry are capped so the whole default run stays within a few minutes
 CONFIG_STEP_CAP = {"glm_prefill_t512": 60, "glm_stack16_t1": 300}
 
@@ -628,6 +628,66 @@ def measure_spec(B, steps, warmup, max_drafts=7, seed=0):
             "l2": "flushed between steps (256 MB write, outside the timed events)"}
 
 
+def measure_tiered(B, steps, warmup, hbm_slots=64, n_pin=16):
+    """The GLM layer with the prefill workload's Zipf selection bias, one token per forward, with
+    only hbm_slots of its 256 routed experts in HBM: each forward routes on the GPU, lets the tier
+    manager place its union (pinned, LRU, load) and copies the misses from pinned host memory
+    over the host link before the expert kernels run.  Timed on the host clock (the call
+    synchronises once to read the union).  Also times plain copies of expert records from pinned
+    host memory into HBM (the host link's rate).  -> dict"""
+    import torch
+
+    from int4_routed_expert_quantize_gb300 import coli, synthetic
+    wl = W.Workload("glm_zipf_t1", d=6144, f=2048, E=256, K=8, n_shared=1, T=1, bias="zipf")
+    L = synthetic.build_layer(wl, max_tokens=1, hbm_slots=hbm_slots)
+    tier = coli.Tier(1, wl.E, n_pin, hbm_slots - n_pin)
+    xs = synthetic.x_tokens(wl, warmup + steps, token0=B.rank * (warmup + steps))
+    y = torch.empty((1, wl.d), dtype=torch.float32, device="cuda")
+    for i in range(warmup):
+        L.forward_tiered(tier, 0, xs[i:i + 1], y)
+    L.repin_tiered(tier, 0)  # pin the experts the warm-up found hottest
+    torch.cuda.synchronize()
+    st0, (r0, b0) = tier.stats(), L.tier_copies()
+    t0 = time.perf_counter()
+    for i in range(warmup, warmup + steps):
+        L.forward_tiered(tier, 0, xs[i:i + 1], y)
+    torch.cuda.synchronize()
+    el = reduce_max(time.perf_counter() - t0, B.world)
+    st1, (r1, b1) = tier.stats(), L.tier_copies()
+    if L.status() != 0:
+        raise RuntimeError("device status")
+    # the host link: copies of whole records from pinned host memory into HBM, CUDA events
+    nrec = 16
+    src = torch.empty(nrec * wl.expert_bytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nrec * wl.expert_bytes, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dst.copy_(src, non_blocking=True)
+    e0.record()
+    for k in range(nrec):
+        dst[k * wl.expert_bytes:(k + 1) * wl.expert_bytes].copy_(
+            src[k * wl.expert_bytes:(k + 1) * wl.expert_bytes], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    link_gbs = nrec * wl.expert_bytes / (e0.elapsed_time(e1) / 1000.0) / 1e9
+    L.close()
+    tier.close()
+    del xs, src, dst
+    torch.cuda.empty_cache()
+    calls = steps
+    used = (st1["pin_hits"] - st0["pin_hits"]) + (st1["lru_hits"] - st0["lru_hits"]) + (st1["misses"] - st0["misses"])
+    return {"workload": "glm layer (d=6144, f=2048, E=256, K=8), prefill's Zipf(1.1) selection bias, T=1",
+            "hbm_slots": hbm_slots, "n_pin": n_pin, "n_lru": hbm_slots - n_pin,
+            "resident_fraction": hbm_slots / wl.E, "steps": steps, "warmup": warmup,
+            "ms_per_forward_wall": 1000.0 * el / calls,
+            "tokens_per_s": B.world * calls / el,
+            "miss_rate": (st1["misses"] - st0["misses"]) / max(1, used),
+            "records_copied_per_forward": (r1 - r0) / calls,
+            "host_link_bytes_per_forward": (b1 - b0) / calls,
+            "host_link_gbs_records": link_gbs,
+            "host_link_ms_per_forward_est": (b1 - b0) / calls / (link_gbs * 1e9) * 1000.0,
+            "timing": "host clock around coli_moe_forward_tiered (one union read-back per call)"}
+
+
 def run_coli(args):
     B = Bench(args)
     wl = W.WORKLOADS[args.workload]
@@ -642,6 +702,10 @@ def run_coli(args):
         cfgs = {}
         for name in names:
             if name == wl.name:
+                continue
+            if name == "tiered":
+                steps = max(1, min(args.steps, 300))
+                cfgs[name] = measure_tiered(B, steps, max(3, min(args.warmup, 50)))
                 continue
             if name == "spec_verify":
                 steps = max(1, min(args.steps, 300))

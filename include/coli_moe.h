@@ -70,6 +70,10 @@ typedef struct {
   int has_norm;     /* 1: forward computes y = x + MoE(RMSNorm(x)) with the loaded gamma      */
   int wbits;        /* bits per expert weight: 4 (int4, also when 0), 8 (int8 rows) or 2     */
                     /* (int2 rows); int8 and int2 layers run the decode kernels for every T    */
+  int hbm_slots;    /* 0 (or >= n_experts): every expert record resident in HBM.  Otherwise a   */
+                    /* tiered layer: HBM holds hbm_slots routed records (>= top_k) plus the    */
+                    /* shared one, every record also sits in pinned host memory, and           */
+                    /* coli_tier.h's coli_moe_forward_tiered places the experts a forward needs */
 } coli_moe_config;
 
 /* Optional per-step outputs of coli_moe_forward_debug.  Device pointers owned by the caller;

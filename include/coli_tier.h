@@ -134,6 +134,9 @@ int coli_tier_heat(const coli_tier* t, int layer, int64_t* heat);
 int coli_tier_session_heat(const coli_tier* t, int layer, int64_t* heat);
 int coli_tier_set_heat(coli_tier* t, int layer, const int64_t* heat);
 
+/* The configuration the tier was created with.  EINVAL: NULL argument. */
+int coli_tier_config_of(const coli_tier* t, coli_tier_config* out);
+
 /* stats[COLI_TIER_N_STATS], the counters listed above, summed over all layers since create. */
 int coli_tier_stats(const coli_tier* t, int64_t* stats);
 
@@ -146,6 +149,45 @@ int coli_tier_stats(const coli_tier* t, int64_t* stats);
  * read or written in full. */
 int coli_tier_save_usage(const coli_tier* t, const char* path);
 int coli_tier_load_usage(coli_tier* t, const char* path);
+
+/* ---- The device side: tiered coli_moe layers (created with 0 < hbm_slots < n_experts) ----
+ *
+ * Such a layer keeps every expert record in pinned host (Grace) memory, in the layout its
+ * kernels stream, and hbm_slots routed records plus the shared expert in HBM; its kernels find
+ * each record through a slot table on the device.  Where an expert sits changes how fast a
+ * forward runs, never what it computes: the tiered forward is bit-identical to the all-resident
+ * layer's.  The tier passed to these calls must have n_experts equal to the layer's experts and
+ * n_pin + n_lru equal to its hbm_slots; `layer` is the layer's index in the tier.  Placements
+ * copy each record with one copy per part (gate/up rows, down rows, scales) and then update the
+ * slot table, in the order of the given stream. */
+
+/* Forward of T tokens with host-decided placement ("colibrì 架构概述" §5: pin, then LRU, then
+ * load; README "統一記憶體階層"): the routing runs on `stream`, the call waits for its union,
+ * coli_tier_lookup decides the loads and evictions, the missing records are copied to their
+ * slots, and the expert kernels run.  Batches run in chunks of at most n_lru / top_k tokens so
+ * that a chunk's union fits the LRU slots.  The call synchronises `stream` once per chunk (to
+ * read the union); it waits (on the device) for placements made by the two calls below.
+ * Arguments and errors as coli_moe_forward, plus EINVAL for a tier that does not match the
+ * layer and EUNSUPPORTED when n_lru < top_k. */
+int coli_moe_forward_tiered(coli_moe* h, coli_tier* tier, int layer, const float* x_dev, int T,
+                            float* y_dev, void* stream);
+
+/* Router-lookahead read-ahead ("colibrì 架构概述" §4 pilot_prefetch; README: the next layer's
+ * router predicts its experts one layer ahead): coli_tier_prefetch on ids[n] (host memory, as
+ * that call takes them), then the copies on `stream`, after the layer's last forward (an event
+ * wait) and before its next one (the next forward waits for them).  Use one stream for the
+ * prefetch and repin calls of a layer. */
+int coli_moe_prefetch_tiered(coli_moe* h, coli_tier* tier, int layer, const int32_t* ids, int n,
+                             void* stream);
+
+/* coli_tier_repin (by_usage = 0: session heat, the live repin) or coli_tier_autopin (by_usage =
+ * 1: usage heat, at start-up) of the layer, carried out like a prefetch: dropped experts leave
+ * the slot table, entering ones are copied in. */
+int coli_moe_repin_tiered(coli_moe* h, coli_tier* tier, int layer, int by_usage, void* stream);
+
+/* Records and bytes copied from host memory into the layer's HBM slots since it was created
+ * (the traffic over the host link that the placements caused).  EINVAL: NULL argument. */
+int coli_moe_tier_copies(const coli_moe* h, int64_t* records, int64_t* bytes);
 
 #ifdef __cplusplus
 }

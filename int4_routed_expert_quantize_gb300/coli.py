@@ -34,7 +34,7 @@ class ColiError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("d", _i), ("f", _i), ("n_experts", _i), ("top_k", _i), ("n_shared", _i),
                 ("qblock", _i), ("max_tokens", _i), ("routed_scale", _f), ("rms_eps", _f),
-                ("has_norm", _i), ("wbits", _i)]
+                ("has_norm", _i), ("wbits", _i), ("hbm_slots", _i)]
 
 
 class TierConfig(ctypes.Structure):
@@ -74,6 +74,7 @@ def _bind_host(L):
     L.coli_tier_heat.argtypes = [_vp, _i, _vp]
     L.coli_tier_set_heat.argtypes = [_vp, _i, _vp]
     L.coli_tier_stats.argtypes = [_vp, _vp]
+    L.coli_tier_config_of.argtypes = [_vp, ctypes.POINTER(TierConfig)]
     L.coli_tier_save_usage.argtypes = [_vp, ctypes.c_char_p]
     L.coli_tier_load_usage.argtypes = [_vp, ctypes.c_char_p]
     L.coli_moe_strerror.argtypes = [_i]
@@ -105,6 +106,10 @@ def _bind_layer(L):
     L.coli_quantize_i4_rows.argtypes = [_vp, _i64, _i, _vp, _vp, _vp]
     L.coli_quantize_act_q8.argtypes = [_vp, _i64, _vp, _vp, _vp]
     L.coli_route_noalloc.argtypes = [_vp, _i, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]
+    L.coli_moe_forward_tiered.argtypes = [_vp, _vp, _i, _vp, _i, _vp, _vp]
+    L.coli_moe_prefetch_tiered.argtypes = [_vp, _vp, _i, _vp, _i, _vp]
+    L.coli_moe_repin_tiered.argtypes = [_vp, _vp, _i, _i, _vp]
+    L.coli_moe_tier_copies.argtypes = [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
 
 
 def lib():
@@ -163,10 +168,10 @@ class MoeLayer:
     current CUDA device."""
 
     def __init__(self, d, f, n_experts, top_k, n_shared=1, max_tokens=4, routed_scale=1.0,
-                 rms_eps=1e-6, has_norm=False, wbits=4):
+                 rms_eps=1e-6, has_norm=False, wbits=4, hbm_slots=0):
         self.cfg = Config(d, f, n_experts, top_k, n_shared, 32, max_tokens, routed_scale, rms_eps,
-                          int(has_norm), wbits)
-        self.wbits = wbits
+                          int(has_norm), wbits, hbm_slots)
+        self.wbits, self.hbm_slots = wbits, hbm_slots
         h = _vp()
         _check(lib().coli_moe_create(ctypes.byref(self.cfg), ctypes.byref(h)), "coli_moe_create")
         self.h = h
@@ -174,9 +179,33 @@ class MoeLayer:
         self.max_tokens, self.has_norm = max_tokens, has_norm
 
     @classmethod
-    def for_workload(cls, wl, max_tokens=None):
+    def for_workload(cls, wl, max_tokens=None, hbm_slots=0):
         return cls(wl.d, wl.f, wl.E, wl.K, wl.n_shared, max_tokens or wl.T, 1.0, wl.rms_eps,
-                   wl.has_norm, wl.wbits)
+                   wl.has_norm, wl.wbits, hbm_slots)
+
+    def forward_tiered(self, tier, layer, x, y=None, stream=None):
+        """forward of a tiered layer with the tier manager placing its experts
+        (coli_moe_forward_tiered)"""
+        if y is None:
+            y = torch.empty_like(x)
+        _check(lib().coli_moe_forward_tiered(self.h, tier.h, layer, _ptr(x), x.shape[0], _ptr(y),
+                                             _stream(stream)), "coli_moe_forward_tiered")
+        return y
+
+    def prefetch_tiered(self, tier, layer, ids, stream=None):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().coli_moe_prefetch_tiered(self.h, tier.h, layer, ids.ctypes.data, ids.size,
+                                              _stream(stream)), "coli_moe_prefetch_tiered")
+
+    def repin_tiered(self, tier, layer, by_usage=False, stream=None):
+        _check(lib().coli_moe_repin_tiered(self.h, tier.h, layer, int(by_usage), _stream(stream)),
+               "coli_moe_repin_tiered")
+
+    def tier_copies(self):
+        """(records, bytes) copied from host memory into the HBM slots since creation"""
+        r, b = _i64(), _i64()
+        _check(lib().coli_moe_tier_copies(self.h, ctypes.byref(r), ctypes.byref(b)), "coli_moe_tier_copies")
+        return r.value, b.value
 
     def close(self):
         if getattr(self, "h", None) is not None and self.h.value:

@@ -341,6 +341,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Store slot of expert `ex`: the slot table of a tiered layer, else the id itself.  An expert
+// that is not resident (a forward on a tiered layer before its experts were placed) reads slot 0
+// and records COLI_ESTATE in the status word, so no copy addresses outside the store.
+__device__ __forceinline__ long store_slot(const Store& st, int ex, int* status) {
+  if (!st.slot_of) return ex;
+  const int s = __ldcg(st.slot_of + ex);
+  if (s < 0) {
+    atomicExch(status, COLI_ESTATE);
+    return 0;
+  }
+  return s;
+}
+
 // ------------------------------------------------------------------ shared by the expert kernels
 // Sum over the warp of 8 values per lane, one per row: the exchange at distance o keeps half
 // of the rows on each side, so after distances 1, 2, 4 lane l holds one row's partial, and

@@ -47,6 +47,9 @@ struct Store {
   float* wr = nullptr;
   float* bias = nullptr;   // nullptr: no selection bias
   float* gamma = nullptr;  // has_norm only
+  // tiered layers (fewer HBM slots than experts): the store slot of each expert id, -1 when not
+  // resident; nullptr: every expert sits in the slot of its own id
+  const int32_t* slot_of = nullptr;
 };
 
 struct Work {
@@ -117,6 +120,16 @@ cudaError_t launch_down_decode(const float* x, float* y, const Shape& s, const S
                                const Work& w, const ExpertDebug& dbg, int num_sms, bool pdl,
                                cudaStream_t stream);
 cudaError_t configure_route_kernels();
+cudaError_t launch_select_publish(const Shape& s, const Store& st, const Work& w,
+                                  cudaStream_t stream);
+// up to kSlotUpdateMax slot-table entries of a tiered layer, passed by value to one launch
+constexpr int kSlotUpdateMax = 64;
+struct SlotUpdate {
+  int n;
+  int32_t ids[kSlotUpdateMax];
+  int32_t slots[kSlotUpdateMax];
+};
+cudaError_t launch_set_slots(int32_t* slot_of, const SlotUpdate& u, cudaStream_t stream);
 cudaError_t configure_route_batch_kernels(int E);
 cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, const Work& w,
                                const CUtensorMap& map_wr, const CUtensorMap& map_x,

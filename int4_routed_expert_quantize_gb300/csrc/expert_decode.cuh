@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
     for (; issued < na * SPU && issued < pl.nst; ++issued) {
       const int unit = a0 + issued / SPU;
       const int sub = issued % SPU;
-      const uint8_t* src = a.st.wgu + ((long)a.s.E * f + unit * 32 + sub * R) * (long)rpb;
+      const uint8_t* src =
+          a.st.wgu + (store_slot(a.st, a.s.E, a.w.status) * f + unit * 32 + sub * R) * (long)rpb;
       mbar_expect_tx(&full[issued], (uint32_t)pl.stage_bytes);
       bulk_g2s(ring + issued * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[issued], pol);
     }
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         int slot, hb;
         unit_of(it / SPU, slot, hb);
         const uint8_t* src =
-            a.st.wgu + ((long)sel.u_ids[slot] * f + hb * 32 + (it % SPU) * R) * (long)rpb;
+            a.st.wgu + (store_slot(a.st, sel.u_ids[slot], a.w.status) * f + hb * 32 + (it % SPU) * R) * (long)rpb;
         mbar_expect_tx(&full[s], (uint32_t)pl.stage_bytes);
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[s], pol);
         issued = it + 1;
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(const Gateup
         tu[4] = hb;
       }
       if (lane < np && lane < kDecodeTmax) tu[5 + lane] = sel.p_tok[p0 + lane];
-      const float* scx = a.st.sc + (long)ex * (2 * f + d);
+      const float* scx = a.st.sc + store_slot(a.st, ex, a.w.status) * (2 * f + d);
       float* tsc = reinterpret_cast<float*>(tu + kGuTabInts);
       tsc[lane] = scx[hb * 32 + lane];
       tsc[32 + lane] = scx[f + hb * 32 + lane];
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
       auto issue_w = [&](int s, int it) {
         int c0, cn;
         chunk(it / nu, c0, cn);
-        const uint8_t* src = a.st.wd + ((long)t_ex[it % nu] * d + row0 + c0) * (long)rb;
+        const uint8_t* src = a.st.wd + (store_slot(a.st, t_ex[it % nu], a.w.status) * d + row0 + c0) * (long)rb;
         mbar_expect_tx(&full[s], (uint32_t)(cn * rb));
         bulk_g2s(ring + (long)s * pl.stage_bytes, src, (uint32_t)(cn * rb), &full[s], pol);
       };
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(const DownArgs
     // this CTA's down-row scales for every union slot (they do not depend on the gate/up grid)
     for (int i = threadIdx.x; i < nu * nrow; i += nthr) {
       const int sl = i / nrow, r = i - sl * nrow;
-      t_sd[sl * pl.max_rows + r] = a.st.sc[(long)t_ex[sl] * (2 * f + d) + 2 * f + row0 + r];
+      t_sd[sl * pl.max_rows + r] = a.st.sc[store_slot(a.st, t_ex[sl], a.w.status) * (2 * f + d) + 2 * f + row0 + r];
     }
     named_bar_sync(1, nthr);
     int s = 0, ci = 0, slot = 0, c0 = 0, cn = 0;

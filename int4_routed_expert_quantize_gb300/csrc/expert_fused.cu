@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
     for (; issued < na * SPU && issued < pl.nst; ++issued) {
       const int unit = a0 + issued / SPU;
       const int sub = issued % SPU;
-      const uint8_t* src = a.st.wgu + ((long)a.s.E * f + unit * 32 + sub * kGuRps) * (long)d;
+      const uint8_t* src =
+          a.st.wgu + (store_slot(a.st, a.s.E, a.w.status) * f + unit * 32 + sub * kGuRps) * (long)d;
       mbar_expect_tx(&full[issued], (uint32_t)pl.stage_bytes);
       bulk_g2s(ring + issued * pl.stage_bytes, src, (uint32_t)pl.stage_bytes, &full[issued], pol);
     }
@@ -236,13 +237,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
         if (it < nst_gu) {
           int slot, hb;
           unit_of(it / SPU, slot, hb);
-          src = a.st.wgu + ((long)sel.u_ids[slot] * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
+          src = a.st.wgu +
+                (store_slot(a.st, sel.u_ids[slot], a.w.status) * f + hb * 32 + (it % SPU) * kGuRps) * (long)d;
           bytes = (uint32_t)pl.stage_bytes;
         } else {
           const int j = it - nst_gu, ci = j / nu, slot = j - ci * nu;
           int c0, cn;
           chunk(ci, c0, cn);
-          src = a.st.wd + ((long)sel.u_ids[slot] * d + row0 + c0) * (long)rb;
+          src = a.st.wd + (store_slot(a.st, sel.u_ids[slot], a.w.status) * d + row0 + c0) * (long)rb;
           bytes = (uint32_t)(cn * rb);
         }
         mbar_expect_tx(&full[s], bytes);
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
         tu[3] = np;
         tu[4] = hb;
       }
-      const float* scx = a.st.sc + (long)ex * (2 * f + d);
+      const float* scx = a.st.sc + store_slot(a.st, ex, a.w.status) * (2 * f + d);
       float* tsc = reinterpret_cast<float*>(tu + kFuTabInts);
       tsc[lane] = scx[hb * 32 + lane];
       tsc[32 + lane] = scx[f + hb * 32 + lane];
@@ -279,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
     // gate/up stages run (each thread waits for its own before the grid barrier)
     for (int i = threadIdx.x; i < nu * nrow; i += kNW * 32) {
       const int sl = i / nrow, r = i - sl * nrow;
-      cp_async4(t_sd + sl * pl.max_rows + r, a.st.sc + (long)sel.u_ids[sl] * (2 * f + d) + 2 * f + row0 + r);
+      cp_async4(t_sd + sl * pl.max_rows + r,
+                a.st.sc + store_slot(a.st, sel.u_ids[sl], a.w.status) * (2 * f + d) + 2 * f + row0 + r);
     }
     named_bar_sync(1, kNW * 32);
 

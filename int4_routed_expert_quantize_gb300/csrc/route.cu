@@ -502,6 +502,38 @@ cudaError_t launch_route_batch(const float* x, const Shape& s, const Store& st, 
   return cudaGetLastError();
 }
 
+// The batch's selection published to the workspace by one CTA (top-K, weights, union and
+// buckets, the same values the expert kernels compute for themselves): a tiered layer reads the
+// union back to the host to place the experts before the expert kernels run.
+__global__ void __launch_bounds__(kThreads) select_publish_kernel(const Shape s, const Store st,
+                                                                  const Work w) {
+  extern __shared__ __align__(16) uint8_t sel_sm[];
+  Sel sel = sel_carve(sel_sm, s.T, s.E);
+  for (int i = threadIdx.x; i < s.T * s.E; i += blockDim.x) sel.sc[i] = __ldcg(w.scores + i);
+  if (st.bias)
+    for (int i = threadIdx.x; i < s.E; i += blockDim.x) sel.bias[i] = st.bias[i];
+  __syncthreads();
+  select_union(s, sel, st.bias != nullptr);
+  sel_publish(s, sel, w);
+}
+
+cudaError_t launch_select_publish(const Shape& s, const Store& st, const Work& w,
+                                  cudaStream_t stream) {
+  select_publish_kernel<<<1, kThreads, (size_t)sel_bytes(s.T, s.E), stream>>>(s, st, w);
+  return cudaGetLastError();
+}
+
+// slot table updates of a tiered layer: slot_of[ids[i]] = slots[i] in order (-1: not resident)
+__global__ void set_slots_kernel(int32_t* slot_of, const SlotUpdate u) {
+  if (threadIdx.x == 0)
+    for (int i = 0; i < u.n; ++i) slot_of[u.ids[i]] = u.slots[i];
+}
+
+cudaError_t launch_set_slots(int32_t* slot_of, const SlotUpdate& u, cudaStream_t stream) {
+  set_slots_kernel<<<1, 32, 0, stream>>>(slot_of, u);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const Work& w,
                          cudaStream_t stream) {
   // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work

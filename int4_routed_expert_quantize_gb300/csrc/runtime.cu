@@ -12,6 +12,7 @@
 
 #include "coli_internal.h"
 #include "coli_moe.h"
+#include "coli_tier.h"
 
 using namespace coli;
 
@@ -45,6 +46,22 @@ struct coli_moe {
   std::vector<uint8_t> loaded;
   int n_loaded = 0;
   std::vector<void*> allocs;
+  // Tiered layer (0 < hbm_slots < E): HBM holds hbm_slots routed records and, in the slot after
+  // them, the shared one; every record also sits in pinned host memory in the store layout,
+  // from where the placements copy it.  The kernels address records through the device slot
+  // table; slot_owner mirrors it on the host.
+  int hbm_slots = 0;  // 0: every expert resident in the slot of its own id
+  uint8_t* host_wgu = nullptr;
+  uint8_t* host_wd = nullptr;
+  float* host_sc = nullptr;
+  int32_t* slot_of = nullptr;         // device [E+1]
+  std::vector<int32_t> slot_owner;    // expert in each device slot (-1: free)
+  int32_t* pin_union = nullptr;       // pinned [E+2]: n_union, then the union's expert ids
+  cudaEvent_t copy_done = nullptr;    // after the last placement made outside a forward
+  cudaEvent_t fwd_done = nullptr;     // after the last forward's kernels
+  bool copy_pending = false;          // a forward must wait for copy_done first
+  int64_t copied_records = 0, copied_bytes = 0;
+  std::vector<void*> host_allocs;
 };
 
 namespace {
@@ -84,6 +101,11 @@ void drop_host_graphs(coli_moe* h) {
 
 void free_all(coli_moe* h) {
   drop_host_graphs(h);
+  for (void* p : h->host_allocs) cudaFreeHost(p);
+  h->host_allocs.clear();
+  if (h->copy_done) cudaEventDestroy(h->copy_done);
+  if (h->fwd_done) cudaEventDestroy(h->fwd_done);
+  h->copy_done = h->fwd_done = nullptr;
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   h->cap_stream = nullptr;
   if (h->pin_x) cudaFreeHost(h->pin_x);
@@ -262,6 +284,10 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
   int rc = check_device(h);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
+  if (h->hbm_slots && h->copy_pending) {  // placements made outside a forward land first
+    if (cudaStreamWaitEvent(st, h->copy_done, 0) != cudaSuccess) return COLI_ECUDA;
+    h->copy_pending = false;
+  }
   if (batched) return run_prefill(h, x, T, y, dump, st);
   // the smem-staged kernels take up to decode_tmax tokens; larger batches run in chunks,
   // which gives the same result per token (each token's output depends on itself only)
@@ -271,7 +297,99 @@ int forward_impl(coli_moe* h, const float* x, int T, float* y, const coli_moe_du
     rc = run_decode(h, x + (size_t)c0 * h->cfg.d, Tc, y + (size_t)c0 * h->cfg.d, dump, st);
     if (rc) return rc;
   }
+  if (h->hbm_slots && cudaEventRecord(h->fwd_done, st) != cudaSuccess) return COLI_ECUDA;
   return COLI_OK;
+}
+
+// Carries out a placement decided by the tier manager on stream `st`: the evicted (or dropped)
+// experts leave the slot table; each fetched record is copied from its pinned host copy into
+// its HBM slot (gate/up rows, down rows, scales: one copy each) and enters the slot table.  The
+// table changes follow the copies in stream order, in launches of up to kSlotUpdateMax entries.
+int place(coli_moe* h, const int32_t* out_ids, const int32_t* out_slots, int n_out,
+          const int32_t* in_ids, const int32_t* in_slots, int n_in, cudaStream_t st) {
+  const size_t d = h->cfg.d, f = h->cfg.f, wb = h->cfg.wbits;
+  const size_t gu = f * (2 * d * wb / 8), dn = d * (f * wb / 8), scn = 2 * f + d;
+  SlotUpdate u{};
+  bool ok = true;
+  auto flush = [&]() {
+    if (ok && u.n) ok = launch_set_slots(h->slot_of, u, st) == cudaSuccess;
+    u.n = 0;
+  };
+  auto add = [&](int32_t id, int32_t slot) {
+    if (u.n == kSlotUpdateMax) flush();
+    u.ids[u.n] = id;
+    u.slots[u.n] = slot;
+    ++u.n;
+  };
+  for (int i = 0; i < n_out; ++i) {
+    const int32_t sl = out_slots[i];
+    if (sl < 0 || sl >= h->hbm_slots || h->slot_owner[sl] != out_ids[i]) return COLI_ESTATE;
+    h->slot_owner[sl] = -1;
+    add(out_ids[i], -1);
+  }
+  for (int i = 0; i < n_in && ok; ++i) {
+    const int32_t id = in_ids[i], sl = in_slots[i];
+    if (id < 0 || id >= h->cfg.n_experts || sl < 0 || sl >= h->hbm_slots) return COLI_ESTATE;
+    if (h->slot_owner[sl] >= 0) add(h->slot_owner[sl], -1);  // not expected: the tier frees first
+    ok = cudaMemcpyAsync(h->st.wgu + sl * gu, h->host_wgu + id * gu, gu, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+         cudaMemcpyAsync(h->st.wd + sl * dn, h->host_wd + id * dn, dn, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+         cudaMemcpyAsync(h->st.sc + sl * scn, h->host_sc + id * scn, sizeof(float) * scn,
+                         cudaMemcpyHostToDevice, st) == cudaSuccess;
+    h->slot_owner[sl] = id;
+    add(id, sl);
+    ++h->copied_records;
+    h->copied_bytes += (int64_t)(gu + dn + sizeof(float) * scn);
+  }
+  flush();
+  return ok ? COLI_OK : COLI_ECUDA;
+}
+
+// The tier's shape must match the tiered layer: its experts, and n_pin + n_lru HBM slots.
+int tier_matches(const coli_moe* h, const coli_tier* tier, int layer, coli_tier_config* tc) {
+  if (!h || !tier || !h->hbm_slots) return COLI_EINVAL;
+  if (coli_tier_config_of(tier, tc) != COLI_OK || tc->n_experts != h->cfg.n_experts ||
+      tc->n_pin + tc->n_lru != h->hbm_slots || layer < 0 || layer >= tc->n_layers)
+    return COLI_EINVAL;
+  return COLI_OK;
+}
+
+// One tiered forward of T <= decode_tmax tokens whose union fits the LRU slots: route and
+// publish the selection, read the union back, let the tier manager place its experts, copy the
+// misses, then run the expert kernels against the updated slot table.
+int run_tiered(coli_moe* h, coli_tier* tier, int layer, const float* x, int T, float* y,
+               cudaStream_t st) {
+  const Shape s = shape_of(h, T);
+  const int E = h->cfg.n_experts;
+  cudaError_t e = launch_route(x, s, h->st, h->w, st);
+  if (e == cudaSuccess) e = launch_select_publish(s, h->st, h->w, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->pin_union, h->w.n_union, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->pin_union + 1, h->w.union_ids, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return COLI_ECUDA;
+  const int nr = h->pin_union[0] - h->cfg.n_shared;  // routed union experts, ascending ids
+  if (nr < 1 || nr > E) return COLI_ECUDA;
+  std::vector<int32_t> buf(4 * (size_t)nr);
+  int32_t *fi = buf.data(), *fs = fi + nr, *ei = fs + nr, *es = ei + nr;
+  int nf = 0, ne = 0;
+  int rc = coli_tier_lookup(tier, layer, h->pin_union + 1, nr, nullptr, nullptr, fi, fs, &nf, ei, es, &ne);
+  if (rc) return rc;
+  if (h->copy_pending) {  // placements made outside a forward land first
+    if (cudaStreamWaitEvent(st, h->copy_done, 0) != cudaSuccess) return COLI_ECUDA;
+    h->copy_pending = false;
+  }
+  rc = place(h, ei, es, ne, fi, fs, nf, st);
+  if (rc) return rc;
+  // the first expert kernel is an ordinary launch: it starts after the slot table update
+  ExpertDebug dbg;
+  if (T == 1 && h->fused) {
+    e = launch_expert_fused(x, y, s, h->st, h->w, dbg, h->num_sms, false, false, st);
+  } else {
+    e = launch_gateup_decode(s, h->st, h->w, dbg, h->num_sms, false, st);
+    if (e == cudaSuccess) e = launch_down_decode(x, y, s, h->st, h->w, dbg, h->num_sms, true, st);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(h->fwd_done, st);
+  return e == cudaSuccess ? COLI_OK : COLI_ECUDA;
 }
 
 // The instantiated host-buffer graph of T tokens, captured on first use on the handle's own
@@ -345,8 +463,11 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   if ((c.wbits != 4 && c.wbits != 8 && c.wbits != 2) || c.qblock != 32 || c.n_experts < 1 || c.n_experts > 1024 || c.top_k < 1 ||
       c.top_k > c.n_experts || c.top_k > 32 || (c.n_shared != 0 && c.n_shared != 1) ||
       c.max_tokens < 1 || c.max_tokens > 4096 || !std::isfinite(c.routed_scale) ||
-      !(c.rms_eps >= 0.0f) || !std::isfinite(c.rms_eps) || c.d <= 0 || c.f <= 0)
+      !(c.rms_eps >= 0.0f) || !std::isfinite(c.rms_eps) || c.d <= 0 || c.f <= 0 ||
+      c.hbm_slots < 0)
     return COLI_EINVAL;
+  if (c.hbm_slots >= c.n_experts) c.hbm_slots = 0;  // every expert fits: not tiered
+  if (c.hbm_slots && c.hbm_slots < c.top_k) return COLI_EINVAL;
   if (!shape_ok(c.d) || !shape_ok(c.f)) return COLI_EUNSUPPORTED;
 
   int dev = 0, sms = 0;
@@ -382,10 +503,13 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   }
   h->slots = c.n_experts + c.n_shared;
   h->decode_tmax = decode_tmax;
+  h->hbm_slots = c.hbm_slots;
   h->loaded.assign(h->slots, 0);
   // the fused one-token kernel and the tensor-core path take int4 experts
   h->fused = c.wbits == 4 && fused_supported(c.d, c.f, c.top_k, c.n_experts, c.n_shared, h->num_sms);
-  const long S = h->slots, d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
+  // device store slots: every expert, or a tiered layer's routed slots and the shared one
+  const long S = h->hbm_slots ? h->hbm_slots + c.n_shared : h->slots;
+  const long d = c.d, f = c.f, E = c.n_experts, K = c.top_k, Tm = c.max_tokens;
   const long Pm = Tm * K + (c.n_shared ? Tm : 0);
   int rc = COLI_OK;
 #define ALLOC(ptr, bytes) \
@@ -418,7 +542,40 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   ALLOC(h->w.sel_flag, sizeof(int32_t) * 4)
   ALLOC(h->w.status, sizeof(int32_t) * 4)
   ALLOC(h->dev_io, sizeof(float) * 2 * Tm * d)
-  if (rc == COLI_OK && c.wbits == 4 && Tm > kDecodeTmax && d % 256 == 0 &&
+  if (h->hbm_slots) {
+    // tiered: the slot table (nothing routed resident yet, the shared expert in the slot after
+    // the routed ones), every record's pinned host copy, the union read-back buffer, events
+    ALLOC(h->slot_of, sizeof(int32_t) * (E + 1))
+    std::vector<int32_t> init((size_t)E + 1, -1);
+    if (c.n_shared) init[E] = h->hbm_slots;
+    if (rc == COLI_OK && cudaMemcpy(h->slot_of, init.data(), sizeof(int32_t) * (E + 1),
+                                    cudaMemcpyHostToDevice) != cudaSuccess)
+      rc = COLI_ECUDA;
+    h->st.slot_of = h->slot_of;
+    h->slot_owner.assign((size_t)S, -1);
+    if (c.n_shared) h->slot_owner[h->hbm_slots] = (int32_t)E;
+    const size_t n1 = (size_t)h->slots;
+    const size_t sizes[4] = {n1 * f * (2 * d * wb / 8), n1 * d * (f * wb / 8), sizeof(float) * n1 * (2 * f + d),
+                             sizeof(int32_t) * (E + 2)};
+    void* ptrs[4] = {};
+    for (int i = 0; i < 4 && rc == COLI_OK; ++i) {
+      if (cudaHostAlloc(&ptrs[i], sizes[i], cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        rc = COLI_ENOMEM;
+      } else {
+        h->host_allocs.push_back(ptrs[i]);
+      }
+    }
+    h->host_wgu = static_cast<uint8_t*>(ptrs[0]);
+    h->host_wd = static_cast<uint8_t*>(ptrs[1]);
+    h->host_sc = static_cast<float*>(ptrs[2]);
+    h->pin_union = static_cast<int32_t*>(ptrs[3]);
+    if (rc == COLI_OK && (cudaEventCreateWithFlags(&h->copy_done, cudaEventDisableTiming) != cudaSuccess ||
+                          cudaEventCreateWithFlags(&h->fwd_done, cudaEventDisableTiming) != cudaSuccess))
+      rc = COLI_ECUDA;
+  }
+  // the tensor-core path takes int4 layers whose every expert is resident
+  if (rc == COLI_OK && c.wbits == 4 && !h->hbm_slots && Tm > kDecodeTmax && d % 256 == 0 &&
       configure_prefill_kernels((int)d, (int)f, (int)E) == cudaSuccess &&
       configure_route_batch_kernels((int)E) == cudaSuccess) {
     const long prow = Pm + kPrefillTileN;
@@ -529,32 +686,66 @@ int coli_moe_load_experts(coli_moe* h, int first, int count, const uint8_t* pack
   const size_t rbd = (size_t)d * wb / 8, rbf = (size_t)f * wb / 8;  // bytes of a gate/up, a down row
   const size_t mat = (size_t)f * rbd;                                 // bytes of a gate or up matrix
   const bool on_device = is_device_ptr(packed);
-  uint8_t* staging = nullptr;
+  const bool tiered = h->hbm_slots > 0;
+  const size_t scn = (size_t)(2 * f + d);  // scales of a record
+  uint8_t* staging = nullptr;  // a host record on the device
+  uint8_t* rstage = nullptr;   // tiered: one record in the store layout, on its way to the host
   if (!on_device && cudaMalloc(&staging, rb) != cudaSuccess) {
     cudaGetLastError();
     return COLI_ENOMEM;
   }
+  if (tiered && cudaMalloc(&rstage, 2 * mat + (size_t)d * rbf) != cudaSuccess) {
+    cudaGetLastError();
+    if (staging) cudaFree(staging);
+    return COLI_ENOMEM;
+  }
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < count && e == cudaSuccess; ++i) {
-    const int slot = first + i;
+    const int id = first + i;
     const uint8_t* rec = packed + (size_t)i * rb;
     if (!on_device) {
       e = cudaMemcpyAsync(staging, rec, rb, cudaMemcpyHostToDevice, st);
       if (e == cudaSuccess) e = cudaStreamSynchronize(st);
       rec = staging;
     }
-    // gate row r and up row r side by side (row pairs), then the down rows
-    uint8_t* gu = h->st.wgu + (size_t)slot * 2 * mat;
-    uint8_t* dn = h->st.wd + (size_t)slot * d * rbf;
+    // gate row r and up row r side by side (row pairs), then the down rows: into the expert's
+    // device slot, or (tiered) into the staging record that then goes to the pinned host copy
+    uint8_t* gu = tiered ? rstage : h->st.wgu + (size_t)id * 2 * mat;
+    uint8_t* dn = tiered ? rstage + 2 * mat : h->st.wd + (size_t)id * d * rbf;
     if (e == cudaSuccess) e = launch_repack_matrix(rec, gu, f, d, 2 * rbd, st, wb);
     if (e == cudaSuccess) e = launch_repack_matrix(rec + mat, gu + rbd, f, d, 2 * rbd, st, wb);
     if (e == cudaSuccess) e = launch_repack_matrix(rec + 2 * mat, dn, d, f, rbf, st, wb);
+    if (!tiered) {
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->st.sc + (size_t)id * scn, scales + (size_t)i * scn, sizeof(float) * scn,
+                            cudaMemcpyDefault, st);
+      continue;
+    }
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(h->st.sc + (size_t)slot * (2 * f + d), scales + (size_t)i * (2 * f + d),
-                          sizeof(float) * (2 * f + d), cudaMemcpyDefault, st);
+      e = cudaMemcpyAsync(h->host_wgu + (size_t)id * 2 * mat, rstage, 2 * mat, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->host_wd + (size_t)id * d * rbf, rstage + 2 * mat, (size_t)d * rbf,
+                          cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->host_sc + (size_t)id * scn, scales + (size_t)i * scn, sizeof(float) * scn,
+                          cudaMemcpyDefault, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the staging record is reused
+    // a record that is resident (the shared expert always is) gets the new bytes in HBM too
+    for (size_t sl = 0; sl < h->slot_owner.size() && e == cudaSuccess; ++sl) {
+      if (h->slot_owner[sl] != id) continue;
+      e = cudaMemcpyAsync(h->st.wgu + sl * 2 * mat, h->host_wgu + (size_t)id * 2 * mat, 2 * mat,
+                          cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->st.wd + sl * d * rbf, h->host_wd + (size_t)id * d * rbf, (size_t)d * rbf,
+                            cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->st.sc + sl * scn, h->host_sc + (size_t)id * scn, sizeof(float) * scn,
+                            cudaMemcpyHostToDevice, st);
+    }
   }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (staging) cudaFree(staging);
+  if (rstage) cudaFree(rstage);
   if (e != cudaSuccess) return COLI_ECUDA;
   for (int i = 0; i < count; ++i)
     if (!h->loaded[first + i]) {
@@ -604,7 +795,7 @@ int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host
   const size_t n = (size_t)T * h->cfg.d;
   float* dx = h->dev_io;
   float* dy = h->cfg.has_norm ? h->dev_io : h->dev_io + (size_t)h->cfg.max_tokens * h->cfg.d;
-  if (T <= kHostGraphMaxT && !h->fault) {
+  if (T <= kHostGraphMaxT && !h->fault && !h->hbm_slots) {
     // small batch: x into the pinned staging, one graph launch (copy in, kernels, copy out,
     // status word), one synchronisation, y out of the staging
     rc = host_graph_for(h, T, dx, dy);
@@ -626,6 +817,82 @@ int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host
   // the call has synchronised anyway: report a bounded device wait that gave up (y_host is then
   // undefined) instead of leaving it for coli_moe_status
   return coli_moe_status(h, stream);
+}
+
+int coli_moe_forward_tiered(coli_moe* h, coli_tier* tier, int layer, const float* x_dev, int T,
+                            float* y_dev, void* stream) {
+  coli_tier_config tc;
+  int rc = tier_matches(h, tier, layer, &tc);
+  if (rc) return rc;
+  if (T < 0 || T > h->cfg.max_tokens) return COLI_EINVAL;
+  if (T == 0) return COLI_OK;
+  if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15u) || ((uintptr_t)y_dev & 3u)) return COLI_EINVAL;
+  const size_t bytes = sizeof(float) * (size_t)T * h->cfg.d;
+  if (x_dev != y_dev && overlap(x_dev, bytes, y_dev, bytes)) return COLI_EINVAL;
+  if (x_dev == y_dev && !h->cfg.has_norm) return COLI_EINVAL;
+  if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
+  if ((rc = check_device(h))) return rc;
+  // a chunk's routed union must fit the LRU slots: at most n_lru / K tokens at a time
+  int tm = tc.n_lru / h->cfg.top_k;
+  if (tm > h->decode_tmax) tm = h->decode_tmax;
+  if (tm < 1) return COLI_EUNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int c0 = 0; c0 < T; c0 += tm) {
+    const int Tc = T - c0 < tm ? T - c0 : tm;
+    rc = run_tiered(h, tier, layer, x_dev + (size_t)c0 * h->cfg.d, Tc, y_dev + (size_t)c0 * h->cfg.d, st);
+    if (rc) return rc;
+  }
+  return COLI_OK;
+}
+
+int coli_moe_prefetch_tiered(coli_moe* h, coli_tier* tier, int layer, const int32_t* ids, int n,
+                             void* stream) {
+  coli_tier_config tc;
+  int rc = tier_matches(h, tier, layer, &tc);
+  if (rc) return rc;
+  if (n < 0 || (n > 0 && !ids)) return COLI_EINVAL;
+  if (n == 0) return COLI_OK;
+  if ((rc = check_device(h))) return rc;
+  std::vector<int32_t> buf(4 * (size_t)n);
+  int32_t *fi = buf.data(), *fs = fi + n, *ei = fs + n, *es = ei + n;
+  int nf = 0, ne = 0;
+  if ((rc = coli_tier_prefetch(tier, layer, ids, n, fi, fs, &nf, ei, es, &ne))) return rc;
+  if (nf + ne == 0) return COLI_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  // no copy may overwrite a slot that an earlier forward still reads
+  if (cudaStreamWaitEvent(st, h->fwd_done, 0) != cudaSuccess) return COLI_ECUDA;
+  if ((rc = place(h, ei, es, ne, fi, fs, nf, st))) return rc;
+  if (cudaEventRecord(h->copy_done, st) != cudaSuccess) return COLI_ECUDA;
+  h->copy_pending = true;
+  return COLI_OK;
+}
+
+int coli_moe_repin_tiered(coli_moe* h, coli_tier* tier, int layer, int by_usage, void* stream) {
+  coli_tier_config tc;
+  int rc = tier_matches(h, tier, layer, &tc);
+  if (rc) return rc;
+  if ((rc = check_device(h))) return rc;
+  const int m = tc.n_pin > 0 ? tc.n_pin : 1;
+  std::vector<int32_t> buf(4 * (size_t)m);
+  int32_t *fi = buf.data(), *fs = fi + m, *di = fs + m, *ds = di + m;
+  int nf = 0, nd = 0;
+  rc = by_usage ? coli_tier_autopin(tier, layer, fi, fs, &nf, di, ds, &nd)
+                : coli_tier_repin(tier, layer, fi, fs, &nf, di, ds, &nd);
+  if (rc) return rc;
+  if (nf + nd == 0) return COLI_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamWaitEvent(st, h->fwd_done, 0) != cudaSuccess) return COLI_ECUDA;
+  if ((rc = place(h, di, ds, nd, fi, fs, nf, st))) return rc;
+  if (cudaEventRecord(h->copy_done, st) != cudaSuccess) return COLI_ECUDA;
+  h->copy_pending = true;
+  return COLI_OK;
+}
+
+int coli_moe_tier_copies(const coli_moe* h, int64_t* records, int64_t* bytes) {
+  if (!h || !records || !bytes) return COLI_EINVAL;
+  *records = h->copied_records;
+  *bytes = h->copied_bytes;
+  return COLI_OK;
 }
 
 int coli_moe_stack_forward(coli_moe* const* layers, int n_layers, float* x_dev, int T,

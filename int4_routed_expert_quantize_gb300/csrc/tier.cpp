@@ -385,6 +385,12 @@ int coli_tier_set_heat(coli_tier* t, int layer, const int64_t* heat) {
   return COLI_OK;
 }
 
+int coli_tier_config_of(const coli_tier* t, coli_tier_config* out) {
+  if (!t || !out) return COLI_EINVAL;
+  *out = coli_tier_config{t->n_layers, t->n_experts, t->n_pin, t->n_lru};
+  return COLI_OK;
+}
+
 int coli_tier_stats(const coli_tier* t, int64_t* stats) {
   if (!t || !stats) return COLI_EINVAL;
   std::memcpy(stats, t->stats, sizeof(t->stats));

@@ -9,9 +9,9 @@ from gen import workloads
 from . import coli
 
 
-def build_layer(wl, layer=0, max_tokens=None, batch=8, stream=None):
+def build_layer(wl, layer=0, max_tokens=None, batch=8, stream=None, hbm_slots=0):
     dev = torch.device("cuda")
-    L = coli.MoeLayer.for_workload(wl, max_tokens)
+    L = coli.MoeLayer.for_workload(wl, max_tokens, hbm_slots)
     d, f, E = wl.d, wl.f, wl.E
     Wr = torch.empty((E, d), dtype=torch.float32, device=dev)
     workloads.router_dev(wl, layer, Wr)
