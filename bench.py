@@ -524,8 +524,8 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
             for i in range(n_e2e):
                 layers[0].forward_host(xh[i % len(xh)], yh)
             el = reduce_max(time.perf_counter() - t0, world)
-            note = ("coli_moe_forward_host: x into the handle's pinned staging, one graph launch "
-                    "(H2D x, forward, D2H y), sync")
+            note = ("coli_moe_forward_host: x into the handle's mapped pinned staging, one graph "
+                    "launch (the GPU reads x from host memory, forward, the GPU writes y back), sync")
         else:
             barrier(world)
             t0 = time.perf_counter()
@@ -705,7 +705,8 @@ def run_coli(args):
                 continue
             if name == "tiered":
                 steps = max(1, min(args.steps, 300))
-                cfgs[name] = measure_tiered(B, steps, max(3, min(args.warmup, 50)))
+                cfgs[name] = {f"slots{n}": measure_tiered(B, steps, 100, hbm_slots=n, n_pin=n // 4)
+                              for n in (64, 128, 192)}
                 continue
             if name == "spec_verify":
                 steps = max(1, min(args.steps, 300))

@@ -233,6 +233,39 @@ cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int
   return cudaGetLastError();
 }
 
+// Host-buffer forwards: the input read from, and the output and status word written to, mapped
+// pinned host memory by the GPU itself (over the host link, no copy-engine transfer).  The loads
+// bypass the caches (the host rewrites the buffer between calls); the stores write through.
+__global__ void __launch_bounds__(256) host_in_kernel(const float4* __restrict__ hx,
+                                                      float4* __restrict__ dx, int n4) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) dx[i] = __ldcv(hx + i);
+}
+
+__global__ void __launch_bounds__(256) host_out_kernel(const float4* __restrict__ dy,
+                                                       float4* __restrict__ hy, int n4,
+                                                       const int* __restrict__ status,
+                                                       int* __restrict__ hstatus) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) __stwt(hy + i, __ldcg(dy + i));
+  if (i == 0) __stwt(hstatus, __ldcg(status));
+}
+
+cudaError_t launch_host_in(const float* hx, float* dx, int n, cudaStream_t stream) {
+  const int n4 = n / 4;
+  host_in_kernel<<<(n4 + 255) / 256, 256, 0, stream>>>(reinterpret_cast<const float4*>(hx),
+                                                       reinterpret_cast<float4*>(dx), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_host_out(const float* dy, float* hy, int n, const int* status, int* hstatus,
+                            cudaStream_t stream) {
+  const int n4 = n / 4;
+  host_out_kernel<<<(n4 + 255) / 256, 256, 0, stream>>>(reinterpret_cast<const float4*>(dy),
+                                                        reinterpret_cast<float4*>(hy), n4, status, hstatus);
+  return cudaGetLastError();
+}
+
 // router rows: lane g's contiguous elements g*(d/32) .. in 4-float chunks at i4*32 + g
 __global__ void __launch_bounds__(256) permute_router_kernel(const float* __restrict__ src,
                                                              float* __restrict__ dst, int E, int d) {

@@ -30,9 +30,12 @@ struct coli_moe {
   float* dev_io = nullptr;  // [2][Tm][d] buffers of coli_moe_forward_host
   // coli_moe_forward_host for small batches: pinned staging for x, y and the status word, and
   // one instantiated graph per token count (copy in, the forward's kernels, copy out, status)
-  float* pin_x = nullptr;
+  float* pin_x = nullptr;          // host addresses
   float* pin_y = nullptr;
   int32_t* pin_status = nullptr;
+  float* map_x = nullptr;          // the same memory as the device addresses it
+  float* map_y = nullptr;
+  int32_t* map_status = nullptr;
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t host_graph[kHostGraphMaxT + 1] = {};
   bool prefill = false;     // the tensor-core path is set up (max_tokens > kDecodeTmax)
@@ -393,8 +396,10 @@ int run_tiered(coli_moe* h, coli_tier* tier, int layer, const float* x, int T, f
 }
 
 // The instantiated host-buffer graph of T tokens, captured on first use on the handle's own
-// stream: copy of the pinned x into the device buffer, the forward's launches, copies of y and
-// the status word into the pinned staging.
+// stream: a kernel that reads x from the mapped pinned staging into the device buffer, the
+// forward's launches, and a kernel that writes y and the status word back to the staging (the
+// GPU reaches the host memory itself: no copy-engine transfer, whose start-up dominates for a
+// few tokens).
 int host_graph_for(coli_moe* h, int T, float* dx, float* dy) {
   if (h->host_graph[T]) return COLI_OK;
   if (!h->router_loaded || h->n_loaded < h->slots) return COLI_ESTATE;
@@ -402,13 +407,9 @@ int host_graph_for(coli_moe* h, int T, float* dx, float* dy) {
   cudaStream_t cs = h->cap_stream;
   if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return COLI_ECUDA;
   int rc = COLI_OK;
-  if (cudaMemcpyAsync(dx, h->pin_x, sizeof(float) * n, cudaMemcpyHostToDevice, cs) != cudaSuccess)
-    rc = COLI_ECUDA;
+  if (launch_host_in(h->map_x, dx, (int)n, cs) != cudaSuccess) rc = COLI_ECUDA;
   if (rc == COLI_OK) rc = forward_impl(h, dx, T, dy, nullptr, cs);
-  if (rc == COLI_OK &&
-      (cudaMemcpyAsync(h->pin_y, dy, sizeof(float) * n, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
-       cudaMemcpyAsync(h->pin_status, h->w.status, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
-           cudaSuccess))
+  if (rc == COLI_OK && launch_host_out(dy, h->map_y, (int)n, h->w.status, h->map_status, cs) != cudaSuccess)
     rc = COLI_ECUDA;
   cudaGraph_t g = nullptr;
   if (cudaStreamEndCapture(cs, &g) != cudaSuccess && rc == COLI_OK) rc = COLI_ECUDA;
@@ -597,7 +598,8 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
   if (rc == COLI_OK) {
     const size_t n = (size_t)(Tm < kHostGraphMaxT ? Tm : kHostGraphMaxT) * d;
     void* p = nullptr;
-    if (cudaHostAlloc(&p, sizeof(float) * 2 * n + 64, cudaHostAllocDefault) != cudaSuccess) {
+    void* q = nullptr;
+    if (cudaHostAlloc(&p, sizeof(float) * 2 * n + 64, cudaHostAllocMapped) != cudaSuccess) {
       cudaGetLastError();
       rc = COLI_ENOMEM;
     } else {
@@ -605,7 +607,15 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
       h->pin_y = h->pin_x + n;
       h->pin_status = reinterpret_cast<int32_t*>(h->pin_y + n);
       *h->pin_status = 0;
-      if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) rc = COLI_ECUDA;
+      if (cudaHostGetDevicePointer(&q, p, 0) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        rc = COLI_ECUDA;
+      } else {
+        h->map_x = static_cast<float*>(q);
+        h->map_y = h->map_x + n;
+        h->map_status = reinterpret_cast<int32_t*>(h->map_y + n);
+      }
     }
   }
   if (rc == COLI_OK && (cudaMemset(h->w.sel_flag, 0, 16) != cudaSuccess ||
