@@ -104,7 +104,8 @@ typedef struct {
 } coli_moe_dump;
 
 /* Validates cfg and allocates, on the current device, the expert store ((E+n_shared) expert
- * records in the library's layout), the router and the workspace for max_tokens.
+ * records in the library's layout), the router and the workspace for max_tokens.  Layers with
+ * d > 7168 or f > 5120 run kernel instances that spill registers (correct, slower).
  * EINVAL: bad cfg or out == NULL.  EUNSUPPORTED: a shape rule above is broken.  ENOMEM.
  * ECUDA: no usable device.  On error *out is left NULL. */
 int coli_moe_create(const coli_moe_config* cfg, coli_moe** out);
@@ -233,9 +234,10 @@ int coli_quantize_act_q8(const float* x_dev, int64_t n, int8_t* q_dev, float* d_
  * and W_r_dev 16-byte aligned.  Limits: T <= 4, T*E <= 4096, E <= 1024, K <= min(E, 32), d a
  * multiple of 128 up to 8192 (EINVAL beyond them).  Its scratch (16 KB) is a fixed array in the
  * library's device memory, present on every device that loads the library until the process
- * exits; the first call on a device looks up that array's address and keeps it, so calls after
- * a cudaDeviceReset of that device are not supported.  Every call shares the array: calls that
- * overlap on the GPU (for example on two streams) race on it. */
+ * exits; the first call on a device looks up that array's address and keeps it (make that first
+ * call before any stream capture), so calls after a cudaDeviceReset of that device are not
+ * supported.  Every call shares the array: calls that overlap on the GPU (for example on two
+ * streams) race on it. */
 int coli_route_noalloc(const float* x_dev, int T, const float* W_r_dev, const float* bias_dev,
                        int E, int d, int K, float routed_scale, int32_t* ids_dev, float* w_dev,
                        void* stream);

@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(256) route_noalloc_kernel(const float* __restr
   if (threadIdx.x == 0) *ticket = 0;
 }
 
-// once per device, with that device current: resolve the array's device address.  The address
-// is kept for the life of the process, so calls after a cudaDeviceReset of that device (which
+// once per device, with that device current: resolve the array's device address (the first call
+// on a device does this set-up, so it should come before any stream capture).  The address is
+// kept for the life of the process, so calls after a cudaDeviceReset of that device (which
 // unloads the module that holds the array) are not supported.
 int scratch_for_current_device(float** out) {
   int dev = -1;
