@@ -26,7 +26,7 @@ constexpr int kMaxStages = 8;
 constexpr int kPrefillMinTokens = 256;
 constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
-constexpr int kPrefillTileN = 64;               // pairs per tensor-core tile
+constexpr int kPrefillTileN = 32;               // pairs per tensor-core tile
 
 // Store layout (built by the repack kernel at load time):
 //  * a matrix row of n int4 values is n/32 blocks of 16 bytes.  With nb = n/32 blocks and
@@ -84,7 +84,7 @@ struct PrefillWork {
   float* dxp = nullptr;         // [Pm+64][d/32] their block scales
   __nv_bfloat16* hb = nullptr;  // [Pm+64][f] h codes as bf16 (down projection operand)
   float* e = nullptr;           // [Pm][d] expert outputs per pair
-  int32_t* tile_prefix = nullptr;  // [E+2] per union slot: 64-pair tiles before it
+  int32_t* tile_prefix = nullptr;  // [E+2] per union slot: tiles of kPrefillTileN pairs before it
 };
 
 struct PrefillMaps {

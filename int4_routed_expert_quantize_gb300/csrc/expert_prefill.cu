@@ -29,16 +29,19 @@
 
 namespace coli {
 
-constexpr int kPfM = 128;
-constexpr int kPfN = kPrefillTileN;
-constexpr int kPfStages = 4;      // bf16 A / B ring (one 32-element K-block each)
-constexpr int kPfRawStages = 6;   // raw int4 weight ring (one lane group of blocks each)
+constexpr int kPfM = 128;               // weight rows per tile
+constexpr int kPfP = kPrefillTileN;     // pairs per tile
+constexpr int kPfR = 4;                 // 32-element blocks per MMA burst
+constexpr int kPfN = kPfR * kPfP;       // MMA width: block-diagonal columns (block, pair)
+constexpr int kPfBurstK = kPfR * 32;    // K elements of a burst
+constexpr int kPfStages = 2;            // operand stages, and accumulator buffers, in flight
+constexpr int kPfRawStages = 4;         // raw int4 weight ring (one lane group of blocks each)
 constexpr int kPfWarps = 15;
 constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kPfAStage = kPfM * 32 * 2;  // 8 KB
-constexpr int kPfBStage = kPfN * 32 * 2;  // 4 KB
-constexpr int kPfAcc = 3;                 // accumulator buffers: K-blocks in flight between MMA and epilogue
-constexpr uint32_t kTmemCols = 512;       // acc[3] x 64 + stack[5] x 64 = 512 used
+constexpr int kPfAStage = kPfM * kPfBurstK * 2;   // 32 KB of bf16 weights
+constexpr int kPfBStage = kPfBurstK * kPfN * 2;   // 32 KB of bf16 activations, block-diagonal
+constexpr uint32_t kTmemCols = 512;     // accumulators 2 x 128 columns, tree stack 5 x 32
+constexpr uint32_t kStackCol = kPfStages * kPfN;
 
 struct PfArgs {
   Shape s;
@@ -55,14 +58,14 @@ struct PfSmem {
   uint8_t* raw;
   uint8_t* a;
   uint8_t* b;
-  float* dxs;  // [nb][64]
-  float* us;   // [64][64] u values, column-major (gate/up only)
+  float* dxs;  // [nb][kPfP]
+  float* us;   // [kPfP][64] u values (gate/up only)
   uint64_t* raw_full;
   uint64_t* raw_empty;
-  uint64_t* a_full;    // the K-block's converted weights and activation block are in
-  uint64_t* ab_empty;
-  uint64_t* acc_full;
-  uint64_t* acc_empty;
+  uint64_t* a_full;     // a burst's converted weights and activation blocks are in
+  uint64_t* done;       // a burst's MMAs are complete: its operand stage is free and its
+                        // accumulator readable
+  uint64_t* acc_empty;  // the epilogue has read a burst's accumulator
   uint32_t* tmem_slot;
   int* tp;    // [nu+1] tile prefix per union slot
   int* tex;   // [nu]   expert id per union slot
@@ -81,15 +84,14 @@ __device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
   m.dxs = reinterpret_cast<float*>(p);
   p += a.dx_bytes;
   m.us = reinterpret_cast<float*>(p);
-  p += a.down ? 0 : kPfN * 64 * 4;
+  p += a.down ? 0 : kPfP * 64 * 4;
   uint64_t* bars = reinterpret_cast<uint64_t*>(p);
   m.raw_full = bars;
   m.raw_empty = bars + kPfRawStages;
   m.a_full = m.raw_empty + kPfRawStages;
-  m.ab_empty = m.a_full + kPfStages;
-  m.acc_full = m.ab_empty + kPfStages;
-  m.acc_empty = m.acc_full + kPfAcc;
-  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfAcc);
+  m.done = m.a_full + kPfStages;
+  m.acc_empty = m.done + kPfStages;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfStages);
   m.tp = reinterpret_cast<int*>(m.tmem_slot + 4);
   m.tex = m.tp + a.s.E + 2;
   m.toff = m.tex + a.s.E + 2;
@@ -100,10 +102,10 @@ int prefill_smem_bytes(int d, int f, int E, int down) {
   const int K = down ? f : d;
   const int nb = K / kQB, G = (nb + 31) / 32;
   const int raw = kPfM * G * 16;
-  const int dx = nb * kPfN * 4;
-  const int bars = (2 * kPfRawStages + 2 * kPfStages + 2 * kPfAcc) * 8 + 16;
+  const int dx = nb * kPfP * 4;
+  const int bars = (2 * kPfRawStages + 3 * kPfStages) * 8 + 16;
   const int tabs = 3 * (E + 2) * 4;
-  return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfN * 64 * 4) +
+  return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfP * 64 * 4) +
          bars + tabs;
 }
 
@@ -145,6 +147,12 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
   }
 }
 
+// One tile = 128 weight rows x 32 pairs of one union slot, its K range walked in bursts of 4
+// blocks of 32.  A burst is 8 MMAs (K = 16 each, M = 128, N = 128) into one accumulator: the
+// activation operand is block-diagonal -- column (b, p) holds pair p's codes in the K rows of
+// block b and zeros elsewhere -- so column (b, p) of the accumulator is the exact block dot of
+// block b and pair p.  One commit per burst both frees the burst's operand stage and hands its
+// accumulator to the epilogue.
 __global__ void __launch_bounds__(kPfThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                        const PfArgs a) {
@@ -156,6 +164,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const bool down = a.down != 0;
   const int K = down ? f : d;
   const int nb = K / kQB, G = (nb + 31) / 32, ngrp = nb / G;
+  const int nburst = nb / kPfR;  // d and f are multiples of 128
   const int n_mt = down ? d / kPfM : f / (kPfM / 2);
   const int raw_bytes = kPfM * G * 16;
   const int nu = __ldcg(a.w.n_union);
@@ -169,10 +178,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(&m.a_full[i], 5);  // 4 converter warps + the activation loader (expect_tx)
-      mbar_init(&m.ab_empty[i], 1);
-    }
-    for (int i = 0; i < kPfAcc; ++i) {
-      mbar_init(&m.acc_full[i], 1);
+      mbar_init(&m.done[i], 1);
       mbar_init(&m.acc_empty[i], 8);
     }
     abort_flag = 0;
@@ -183,6 +189,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     m.toff[i] = __ldcg(a.w.offsets + i);
     m.tex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
   }
+  // the activation stages' off-diagonal blocks stay zero: only the diagonal is ever copied in
+  for (int i = threadIdx.x; i < kPfStages * kPfBStage / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(m.b)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (warp == 6) tmem_alloc(m.tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -215,190 +225,180 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- bf16 activation block (64 pairs x 32) of every K-step
+    // ---------------- the activation blocks of every burst, each on the diagonal: block j of
+    // the burst -> K rows 32j..32j+31 (core-matrix columns 4j..4j+3) x columns 32j..32j+31
     if (lane == 0) {
       long kb = 0;
       for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
         int u, mt, nt;
         pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
-        const int row0 = m.toff[u] + nt * kPfN;
-        for (int b = 0; b < nb; ++b, ++kb) {
+        const int row0 = m.toff[u] + nt * kPfP;
+        for (int bu = 0; bu < nburst; ++bu, ++kb) {
           const int s = (int)(kb % kPfStages);
           const long n = kb / kPfStages;
-          if (n > 0 && !mbar_wait_bounded(&m.ab_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
+          if (n > 0 && !mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
             break;
           uint8_t* dst = m.b + (long)s * kPfBStage;
-          mbar_expect_tx(&m.a_full[s], (uint32_t)kPfBStage);
+          mbar_expect_tx(&m.a_full[s], (uint32_t)(kPfR * 4 * kPfP * 16));
 #pragma unroll
-          for (int kc = 0; kc < 4; ++kc)
-            tma_load_2d(dst + kc * (kPfN * 16), &map_x, b * 32 + kc * 8, row0, &m.a_full[s]);
+          for (int j = 0; j < kPfR; ++j)
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc)
+              tma_load_2d(dst + ((4 * j + kc) * (kPfN / 8) + 4 * j) * 128, &map_x,
+                          (bu * kPfR + j) * 32 + kc * 8, row0, &m.a_full[s]);
         }
       }
     }
   } else if (warp >= 2 && warp <= 5) {
-    // ---------------- int4 -> bf16 conversion: thread r owns weight row r of the tile
+    // ---------------- int4 -> bf16: thread r owns weight row r of the tile; block j of a burst
+    // goes to core-matrix columns 4j..4j+3 of the burst's weight stage
     const int r = threadIdx.x - 64;
-    long kb = 0, kg = 0;
+    long kbl = 0, kg = 0;  // blocks and groups so far
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       for (int gi = 0; gi < ngrp; ++gi, ++kg) {
         const int rs = (int)(kg % kPfRawStages);
         mbar_wait_bounded(&m.raw_full[rs], (uint32_t)((kg / kPfRawStages) & 1), &abort_flag, status);
         const uint8_t* rrow = m.raw + (long)rs * a.raw_stage_bytes + r * G * 16;
-        for (int i = 0; i < G; ++i, ++kb) {
+        for (int i = 0; i < G; ++i, ++kbl) {
+          const long kb = kbl / kPfR;
+          const int j = (int)(kbl % kPfR);
           const int s = (int)(kb % kPfStages);
           const long n = kb / kPfStages;
-          if (n > 0) mbar_wait_bounded(&m.ab_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
+          if (j == 0 && n > 0) mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
           const uint4 c = *reinterpret_cast<const uint4*>(rrow + (store_chunk(gi, i, G) - gi * G) * 16);
           uint4 o[4];
           int4_chunk_to_bf16(c, o);
           uint8_t* ast = m.a + (long)s * kPfAStage;
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc)
-            *reinterpret_cast<uint4*>(ast + (kc * 16 + (r >> 3)) * 128 + (r & 7) * 16) = o[kc];
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&m.a_full[s]);
+            *reinterpret_cast<uint4*>(ast + ((4 * j + kc) * (kPfM / 8) + (r >> 3)) * 128 + (r & 7) * 16) = o[kc];
+          if (j == kPfR - 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&m.a_full[s]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.raw_empty[rs]);
       }
     }
   } else if (warp == 6) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: one burst of 8 MMAs and one commit per 4 blocks
     if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kPfM, kPfN);
       long kb = 0;
-      int ab = 0;          // accumulator buffer of K-block kb
-      uint32_t aph = 0;    // parity of its current use
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        int u, mt, nt;
-        pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
-        // MMA width: the tile's valid pairs rounded up to 16 (padding columns are discarded)
-        const int nv = min(kPfN, m.toff[u + 1] - (m.toff[u] + nt * kPfN));
-        const int nmma = (nv + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(kPfM, nmma);
-        for (int b = 0; b < nb; ++b, ++kb) {
+        for (int bu = 0; bu < nburst; ++bu, ++kb) {
           const int s = (int)(kb % kPfStages);
-          const uint32_t ph = (uint32_t)((kb / kPfStages) & 1);
-          // both operands of the K-block: the converted weights and the activation block
-          bool ok = mbar_wait_bounded(&m.a_full[s], ph, &abort_flag, status);
-          if (kb >= kPfAcc) ok = mbar_wait_bounded(&m.acc_empty[ab], aph ^ 1u, &abort_flag, status) && ok;
-          const int abuf = ab;
-          if (++ab == kPfAcc) {
-            ab = 0;
-            aph ^= 1u;
-          }
+          const long n = kb / kPfStages;
+          bool ok = mbar_wait_bounded(&m.a_full[s], (uint32_t)(n & 1), &abort_flag, status);
+          if (n > 0) ok = mbar_wait_bounded(&m.acc_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status) && ok;
           if (!ok) continue;
           tc_fence_after();
           const uint8_t* as = m.a + (long)s * kPfAStage;
           const uint8_t* bs = m.b + (long)s * kPfBStage;
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
+          for (int ks = 0; ks < kPfBurstK / 16; ++ks) {
             const uint64_t da = smem_desc(as + ks * 2 * (kPfM / 8) * 128, (kPfM / 8) * 128, 128);
             const uint64_t db = smem_desc(bs + ks * 2 * (kPfN / 8) * 128, (kPfN / 8) * 128, 128);
-            tc_mma_bf16(tmem + abuf * kPfN, da, db, idesc, ks > 0);
+            tc_mma_bf16(tmem + (uint32_t)(s * kPfN), da, db, idesc, ks > 0);
           }
-          tc_commit(&m.ab_empty[s]);
-          tc_commit(&m.acc_full[abuf]);
+          tc_commit(&m.done[s]);
         }
       }
     }
   } else {
-    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half*32..
+    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., pairs half*16..half*16+15
     const int q = warp & 3;
     const int half = (warp - 7) >> 2;
     const int row = q * 32 + lane;
     const int etid = threadIdx.x - 7 * 32;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    int ab = 0;          // accumulator buffer of the next K-block
-    uint32_t aph = 0;    // parity of its current use
+    long kb = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int u, mt, nt;
       pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
       const int ex = m.tex[u];
-      const int pb = m.toff[u] + nt * kPfN;  // first pair of the tile
+      const int pb = m.toff[u] + nt * kPfP;  // first pair of the tile
       const int pe = m.toff[u + 1];          // end of the slot's pairs
-      const int nv = min(kPfN, pe - pb);       // valid pairs of the tile
-      const bool active = half * 32 < nv;       // this warp has columns to finish
-      // this tile's activation block scales, [block][column]
+      const int nv = min(kPfP, pe - pb);       // valid pairs of the tile
+      const bool active = half * 16 < nv;       // this warp has columns to finish
+      // this tile's activation block scales, [block][pair]
       named_bar_sync(2, 8 * 32);
       const float* dsrc = down ? a.w.dh : a.pw.dxp;
 #pragma unroll 4
-      for (int idx = etid; idx < nb * kPfN; idx += 8 * 32) {
-        const int b = idx / kPfN, col = idx - b * kPfN;
+      for (int idx = etid; idx < nb * kPfP; idx += 8 * 32) {
+        const int b = idx / kPfP, col = idx - b * kPfP;
         m.dxs[idx] = col < nv ? __ldcg(dsrc + (long)(pb + col) * nb + b) : 0.0f;
       }
       named_bar_sync(2, 8 * 32);
 
-      float chain[32];
+      float chain[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+      for (int c = 0; c < 16; ++c) chain[c] = 0.0f;
       int gi = 0, gb = 0;  // current group and block within it
-      for (int b = 0; b < nb; ++b) {
-        mbar_wait_bounded(&m.acc_full[ab], aph, &abort_flag, status);
+      auto push_group = [&](void) {
+        // group leaf gi complete: merge it into the pairwise-tree stack (levels in TMEM); after
+        // the last leaf `chain` holds the whole sum
+        float lv[16];
+        int l = 0;
+        for (; (gi >> l) & 1; ++l) {
+          tmem_ld16(tl + kStackCol + l * kPfP + half * 16, lv);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) chain[c] = __fadd_rn(lv[c], chain[c]);
+        }
+        if (l < 5) {
+          tmem_st16(tl + kStackCol + l * kPfP + half * 16, chain);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) chain[c] = 0.0f;
+        }
+        ++gi;
+      };
+      for (int bu = 0; bu < nburst; ++bu, ++kb) {
+        const int s = (int)(kb % kPfStages);
+        const long n = kb / kPfStages;
+        mbar_wait_bounded(&m.done[s], (uint32_t)(n & 1), &abort_flag, status);
         tc_fence_after();
-        float acc[32];
-        if (active) tmem_ld32(tl + ab * kPfN + half * 32, acc);
+        float acc[kPfR][16];
+        if (active) {
+#pragma unroll
+          for (int j = 0; j < kPfR; ++j) tmem_ld16(tl + s * kPfN + j * kPfP + half * 16, acc[j]);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&m.acc_empty[ab]);
-        if (++ab == kPfAcc) {
-          ab = 0;
-          aph ^= 1u;
-        }
+        if (lane == 0) mbar_arrive(&m.acc_empty[s]);
         if (!active) continue;
-        const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfN + half * 32);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dv = dxb[c4];
-          chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[4 * c4 + 0], chain[4 * c4 + 0]);
-          chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[4 * c4 + 1], chain[4 * c4 + 1]);
-          chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[4 * c4 + 2], chain[4 * c4 + 2]);
-          chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[4 * c4 + 3], chain[4 * c4 + 3]);
-        }
-        int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
-        if (Adump != nullptr) {
-          const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
-          int32_t* dump = (!down && row >= 64) ? a.dbg.Au : Adump;
-          const int nrow = down ? d : f;
-          for (int c = 0; c < 32; ++c) {
-            const int p = pb + half * 32 + c;
-            if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[c];
-          }
-        }
-        if (++gb == G) {
-          // group leaf gi complete: merge it into the pairwise-tree stack (levels in TMEM);
-          // after the last leaf `chain` holds the whole sum
-          gb = 0;
-          int l = 0;
-          for (; (gi >> l) & 1; ++l) {
-            tmem_ld32(tl + kPfAcc * kPfN + l * kPfN + half * 32, acc);
+        for (int j = 0; j < kPfR; ++j) {
+          const int b = bu * kPfR + j;
+          const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfP + half * 16);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 dv = dxb[c4];
+            chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[j][4 * c4 + 0], chain[4 * c4 + 0]);
+            chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[j][4 * c4 + 1], chain[4 * c4 + 1]);
+            chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[j][4 * c4 + 2], chain[4 * c4 + 2]);
+            chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[j][4 * c4 + 3], chain[4 * c4 + 3]);
           }
-          if (l < 5) {
-            tmem_st32(tl + kPfAcc * kPfN + l * kPfN + half * 32, chain);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
+          int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
+          if (Adump != nullptr) {
+            const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
+            int32_t* dump = (!down && row >= 64) ? a.dbg.Au : Adump;
+            const int nrow = down ? d : f;
+            for (int c = 0; c < 16; ++c) {
+              const int p = pb + half * 16 + c;
+              if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[j][c];
+            }
           }
-          ++gi;
+          if (++gb == G) {
+            gb = 0;
+            push_group();
+          }
         }
       }
       if (active) {
         // empty groups ngrp..31 are +0 leaves of the tree
-        for (int gz = ngrp; gz < 32; ++gz) {
-          float acc[32];
-          int l = 0;
-          for (; (gz >> l) & 1; ++l) {
-            tmem_ld32(tl + kPfAcc * kPfN + l * kPfN + half * 32, acc);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) chain[c] = __fadd_rn(acc[c], chain[c]);
-          }
-          if (l < 5) {
-            tmem_st32(tl + kPfAcc * kPfN + l * kPfN + half * 32, chain);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) chain[c] = 0.0f;
-          }
-        }
+        while (gi < 32) push_group();
       }
       // chain = the canonical sum of every (row, pair) of this thread
       const float* scx = a.st.sc + (long)ex * (2 * f + d);
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!active) continue;
         const int r = mt * kPfM + row;
         const float sd = scx[2 * f + r];
-        for (int c = 0; c < 32; ++c) {
-          const int p = pb + half * 32 + c;
+        for (int c = 0; c < 16; ++c) {
+          const int p = pb + half * 16 + c;
           if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, chain[c]);
         }
       } else {
@@ -416,25 +416,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float sr = is_up ? scx[f + r] : scx[r];
         float* o = chain;  // the row-scaled projection, in place
 #pragma unroll
-        for (int c = 0; c < 32; ++c) o[c] = __fmul_rn(sr, chain[c]);
+        for (int c = 0; c < 16; ++c) o[c] = __fmul_rn(sr, chain[c]);
         if (a.dbg.g != nullptr && active) {
           float* dst = is_up ? a.dbg.u : a.dbg.g;
-          for (int c = 0; c < 32; ++c) {
-            const int p = pb + half * 32 + c;
+          for (int c = 0; c < 16; ++c) {
+            const int p = pb + half * 16 + c;
             if (p < pe) dst[(long)p * f + r] = o[c];
           }
         }
         if (is_up && active) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) m.us[(half * 32 + c) * 64 + (row - 64)] = o[c];
+          for (int c = 0; c < 16; ++c) m.us[(half * 16 + c) * 64 + (row - 64)] = o[c];
         }
         named_bar_sync(2, 8 * 32);
         if (!is_up && active) {
           // h = SiLU(g) * u; the warp's 32 rows are one int8 block of h for each pair
           const int nhb = f >> 5, hbk = r >> 5;
-          for (int c = 0; c < 32; ++c) {
-            const int p = pb + half * 32 + c;
-            const float hv = canon_silu_mul(o[c], m.us[(half * 32 + c) * 64 + row]);
+          for (int c = 0; c < 16; ++c) {
+            const int p = pb + half * 16 + c;
+            const float hv = canon_silu_mul(o[c], m.us[(half * 16 + c) * 64 + row]);
             const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
             const int code = q8_code(hv, dd);
             const int sq = warp_isum(code);
@@ -525,9 +525,9 @@ bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const 
   ok = ok && make_map(&maps->wd, st.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(f / 2),
                       (uint64_t)slots * d, (uint32_t)(Gf * 16), (uint32_t)kPfM);
   ok = ok && make_map(&maps->xb, pw.xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)prow,
-                      8u, (uint32_t)kPfN);
+                      8u, (uint32_t)kPfP);
   ok = ok && make_map(&maps->hb, pw.hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)f, (uint64_t)prow,
-                      8u, (uint32_t)kPfN);
+                      8u, (uint32_t)kPfP);
   // router rows and normalised tokens (both in the router's chunk order), 256-float boxes
   ok = ok && make_map(&maps->wr, st.wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)d, (uint64_t)E,
                       256u, 16u);
@@ -554,7 +554,7 @@ cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, con
     const int K = down ? s.f : s.d;
     const int nb = K / kQB, G = (nb + 31) / 32;
     args.raw_stage_bytes = kPfM * G * 16;
-    args.dx_bytes = nb * kPfN * 4;
+    args.dx_bytes = nb * kPfP * 4;
     const int smem = prefill_smem_bytes(s.d, s.f, s.E, down);
     expert_gemm_kernel<<<num_sms, kPfThreads, smem, stream>>>(down ? maps.wd : maps.wgu,
                                                               down ? maps.hb : maps.xb, args);
