@@ -2,21 +2,24 @@
 //
 // For a batch the union experts see many tokens each (up to a few hundred), so the expert
 // projections are genuinely dense grouped GEMMs: per union slot, [rows of W] x [K] x [pairs of
-// the slot's bucket].  GB300's int8 tensor rate is low, so the int8 x int4 products run as
-// kind::f16 with bf16 operands holding the exact integers (|code| <= 127, products <= 1016, a
-// 32-term block sum < 2^24: every partial is exact in the f32 accumulator).  Each K-block of 32
-// (one activation scale) is its own MMA accumulation in TMEM, so the epilogue sees the exact
-// int32 block dot and applies the canonical fp32 order of the decode path: an fma chain over
+// the slot's bucket].  sm_103a has no int8 MMA (ptxas refuses tcgen05.mma kind::i8 for it),
+// so the int8 x int4 products run as kind::f16 with bf16 operands holding the exact integers
+// (|code| <= 127, products <= 1016, a 32-term block sum < 2^24: every partial is exact in the
+// f32 accumulator).  Each K-block of 32 (one activation scale) gets accumulator columns of its
+// own (a block-diagonal activation operand, below), so the epilogue sees the exact int32 block
+// dot and applies the canonical fp32 order of the decode path: an fma chain over
 // the blocks of each of 32 contiguous groups (registers) and the pairwise tree over the groups
 // (a 5-level stack kept in TMEM columns).  Results are therefore bit-identical to the decode
 // kernels and the CPU oracle ("colibrì 架构概述" §5 gate/up/SiLU/down; README batch union).
 //
-// CTA: 15 warps, one tile (128 weight rows x 64 pairs) at a time, persistent over tiles:
-//   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream, deep ring)
-//   warp 1      bulk-tensor copies of the bf16 activation block of each K-step (completing on
-//               the same barrier as the converted weights, so the MMA issuer waits once)
-//   warps 2-5   int4 -> bf16 conversion of the weight block into the MMA's shared layout
-//   warp 6      TMEM owner and single MMA issuer (2 x K16 MMAs per K-block, 3 accumulator buffers)
+// CTA: 15 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
+//   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream)
+//   warp 1      bulk-tensor copies of the bf16 activation blocks of each burst of 4 blocks, on
+//               the diagonal of a zeroed operand (completing on the same barrier as the
+//               converted weights, so the MMA issuer waits once)
+//   warp 2      TMEM owner and single MMA issuer (8 x K16 MMAs and one commit per burst, two
+//               accumulator buffers)
+//   warps 3-6   int4 -> bf16 conversion of the weight blocks into the MMA's shared layout
 //   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,7 +39,10 @@ constexpr int kPfN = kPfR * kPfP;       // MMA width: block-diagonal columns (bl
 constexpr int kPfBurstK = kPfR * 32;    // K elements of a burst
 constexpr int kPfStages = 2;            // operand stages, and accumulator buffers, in flight
 constexpr int kPfRawStages = 4;         // raw int4 weight ring (one lane group of blocks each)
-constexpr int kPfWarps = 15;
+constexpr int kPfConv = 4;              // int4 -> bf16 converter warps
+constexpr int kPfEpi0 = 3 + kPfConv;    // first of the 8 epilogue warps
+static_assert(kPfConv == 4 || kPfConv == 8, "converter warps: one or two per row");
+constexpr int kPfWarps = kPfEpi0 + 8;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfAStage = kPfM * kPfBurstK * 2;   // 32 KB of bf16 weights
 constexpr int kPfBStage = kPfBurstK * kPfN * 2;   // 32 KB of bf16 activations, block-diagonal
@@ -147,6 +153,23 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
   }
 }
 
+// group leaf gi complete: merge it into the pairwise-tree stack (levels in TMEM); after the last
+// leaf `chain` holds the whole sum
+#define COLI_PF_PUSH_GROUP()                                                   \
+  {                                                                            \
+    float lv[16];                                                              \
+    int l = 0;                                                                 \
+    for (; (gi >> l) & 1; ++l) {                                               \
+      tmem_ld16(tl + kStackCol + l * kPfP + half * 16, lv);                    \
+      _Pragma("unroll") for (int c = 0; c < 16; ++c) chain[c] = __fadd_rn(lv[c], chain[c]); \
+    }                                                                          \
+    if (l < 5) {                                                               \
+      tmem_st16(tl + kStackCol + l * kPfP + half * 16, chain);                 \
+      _Pragma("unroll") for (int c = 0; c < 16; ++c) chain[c] = 0.0f;         \
+    }                                                                          \
+    ++gi;                                                                      \
+  }
+
 // One tile = 128 weight rows x 32 pairs of one union slot, its K range walked in bursts of 4
 // blocks of 32.  A burst is 8 MMAs (K = 16 each, M = 128, N = 128) into one accumulator: the
 // activation operand is block-diagonal -- column (b, p) holds pair p's codes in the K rows of
@@ -174,10 +197,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfRawStages; ++i) {
       mbar_init(&m.raw_full[i], 1);
-      mbar_init(&m.raw_empty[i], 4);
+      mbar_init(&m.raw_empty[i], kPfConv);
     }
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&m.a_full[i], 5);  // 4 converter warps + the activation loader (expect_tx)
+      mbar_init(&m.a_full[i], kPfConv + 1);  // the converter warps + the activation loader (expect_tx)
       mbar_init(&m.done[i], 1);
       mbar_init(&m.acc_empty[i], 8);
     }
@@ -193,7 +216,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   for (int i = threadIdx.x; i < kPfStages * kPfBStage / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(m.b)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
-  if (warp == 6) tmem_alloc(m.tmem_slot, kTmemCols);
+  if (warp == 2) tmem_alloc(m.tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -249,10 +272,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     }
-  } else if (warp >= 2 && warp <= 5) {
-    // ---------------- int4 -> bf16: thread r owns weight row r of the tile; block j of a burst
-    // goes to core-matrix columns 4j..4j+3 of the burst's weight stage
-    const int r = threadIdx.x - 64;
+  } else if (warp >= 3 && warp < kPfEpi0) {
+    // ---------------- int4 -> bf16: thread r owns weight row r % 128 of the tile and, with more
+    // than 4 converter warps, its share of a burst's blocks (j % (kPfConv / 4) == r / 128);
+    // block j of a burst goes to core-matrix columns 4j..4j+3 of the burst's weight stage
+    const int r = (threadIdx.x - 96) & (kPfM - 1);
+    const int hf = (threadIdx.x - 96) >> 7;
     long kbl = 0, kg = 0;  // blocks and groups so far
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       for (int gi = 0; gi < ngrp; ++gi, ++kg) {
@@ -265,6 +290,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int s = (int)(kb % kPfStages);
           const long n = kb / kPfStages;
           if (j == 0 && n > 0) mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
+          if (j % (kPfConv / 4) == hf) {
           const uint4 c = *reinterpret_cast<const uint4*>(rrow + (store_chunk(gi, i, G) - gi * G) * 16);
           uint4 o[4];
           int4_chunk_to_bf16(c, o);
@@ -272,6 +298,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc)
             *reinterpret_cast<uint4*>(ast + ((4 * j + kc) * (kPfM / 8) + (r >> 3)) * 128 + (r & 7) * 16) = o[kc];
+          }
           if (j == kPfR - 1) {
             fence_proxy_async_smem();
             __syncwarp();
@@ -282,7 +309,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) mbar_arrive(&m.raw_empty[rs]);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == 2) {
     // ---------------- MMA issuer: one burst of 8 MMAs and one commit per 4 blocks
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kPfM, kPfN);
@@ -310,9 +337,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., pairs half*16..half*16+15
     const int q = warp & 3;
-    const int half = (warp - 7) >> 2;
+    const int half = (warp - kPfEpi0) >> 2;
     const int row = q * 32 + lane;
-    const int etid = threadIdx.x - 7 * 32;
+    const int etid = threadIdx.x - kPfEpi0 * 32;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     long kb = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -337,32 +364,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int c = 0; c < 16; ++c) chain[c] = 0.0f;
       int gi = 0, gb = 0;  // current group and block within it
-      auto push_group = [&](void) {
-        // group leaf gi complete: merge it into the pairwise-tree stack (levels in TMEM); after
-        // the last leaf `chain` holds the whole sum
-        float lv[16];
-        int l = 0;
-        for (; (gi >> l) & 1; ++l) {
-          tmem_ld16(tl + kStackCol + l * kPfP + half * 16, lv);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) chain[c] = __fadd_rn(lv[c], chain[c]);
-        }
-        if (l < 5) {
-          tmem_st16(tl + kStackCol + l * kPfP + half * 16, chain);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) chain[c] = 0.0f;
-        }
-        ++gi;
-      };
       for (int bu = 0; bu < nburst; ++bu, ++kb) {
         const int s = (int)(kb % kPfStages);
         const long n = kb / kPfStages;
         mbar_wait_bounded(&m.done[s], (uint32_t)(n & 1), &abort_flag, status);
         tc_fence_after();
-        float acc[kPfR][16];
+        // the burst's 4 blocks (16 columns each) in one round of loads, then the accumulator goes
+        // back to the MMA issuer before they are folded
+        float acc4[kPfR][16];
         if (active) {
 #pragma unroll
-          for (int j = 0; j < kPfR; ++j) tmem_ld16(tl + s * kPfN + j * kPfP + half * 16, acc[j]);
+          for (int j = 0; j < kPfR; ++j) tmem_ld16(tl + s * kPfN + j * kPfP + half * 16, acc4[j]);
         }
         tc_fence_before();
         __syncwarp();
@@ -370,42 +382,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!active) continue;
 #pragma unroll
         for (int j = 0; j < kPfR; ++j) {
+          const float (&acc)[16] = acc4[j];
           const int b = bu * kPfR + j;
           const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfP + half * 16);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const float4 dv = dxb[c4];
-            chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[j][4 * c4 + 0], chain[4 * c4 + 0]);
-            chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[j][4 * c4 + 1], chain[4 * c4 + 1]);
-            chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[j][4 * c4 + 2], chain[4 * c4 + 2]);
-            chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[j][4 * c4 + 3], chain[4 * c4 + 3]);
+            chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[4 * c4 + 0], chain[4 * c4 + 0]);
+            chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[4 * c4 + 1], chain[4 * c4 + 1]);
+            chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[4 * c4 + 2], chain[4 * c4 + 2]);
+            chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[4 * c4 + 3], chain[4 * c4 + 3]);
           }
           int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
           if (Adump != nullptr) {
             const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
             int32_t* dump = (!down && row >= 64) ? a.dbg.Au : Adump;
             const int nrow = down ? d : f;
+#pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int p = pb + half * 16 + c;
-              if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[j][c];
+              if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[c];
             }
           }
           if (++gb == G) {
             gb = 0;
-            push_group();
+            COLI_PF_PUSH_GROUP()
           }
         }
       }
       if (active) {
         // empty groups ngrp..31 are +0 leaves of the tree
-        while (gi < 32) push_group();
+        while (gi < 32) COLI_PF_PUSH_GROUP()
       }
-      // chain = the canonical sum of every (row, pair) of this thread
+      // chain = the canonical sum of every (row, pair) of this thread (every loop over the 16
+      // pairs is unrolled, so chain stays in registers)
       const float* scx = a.st.sc + (long)ex * (2 * f + d);
       if (down) {
         if (!active) continue;
         const int r = mt * kPfM + row;
         const float sd = scx[2 * f + r];
+#pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int p = pb + half * 16 + c;
           if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, chain[c]);
@@ -414,27 +430,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int r = mt * (kPfM / 2) + (row & 63);
         const bool is_up = row >= 64;
         const float sr = is_up ? scx[f + r] : scx[r];
-        float* o = chain;  // the row-scaled projection, in place
 #pragma unroll
-        for (int c = 0; c < 16; ++c) o[c] = __fmul_rn(sr, chain[c]);
+        for (int c = 0; c < 16; ++c) chain[c] = __fmul_rn(sr, chain[c]);  // the row-scaled projection
         if (a.dbg.g != nullptr && active) {
           float* dst = is_up ? a.dbg.u : a.dbg.g;
+#pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int p = pb + half * 16 + c;
-            if (p < pe) dst[(long)p * f + r] = o[c];
+            if (p < pe) dst[(long)p * f + r] = chain[c];
           }
         }
         if (is_up && active) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) m.us[(half * 16 + c) * 64 + (row - 64)] = o[c];
+          for (int c = 0; c < 16; ++c) m.us[(half * 16 + c) * 64 + (row - 64)] = chain[c];
         }
         named_bar_sync(2, 8 * 32);
         if (!is_up && active) {
           // h = SiLU(g) * u; the warp's 32 rows are one int8 block of h for each pair
           const int nhb = f >> 5, hbk = r >> 5;
+#pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int p = pb + half * 16 + c;
-            const float hv = canon_silu_mul(o[c], m.us[(half * 16 + c) * 64 + row]);
+            const float hv = canon_silu_mul(chain[c], m.us[(half * 16 + c) * 64 + row]);
             const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
             const int code = q8_code(hv, dd);
             const int sq = warp_isum(code);
@@ -454,7 +471,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 6) {
+  if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
