@@ -320,6 +320,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// hint: bring the 128-byte line holding p into L2
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // asynchronous 4-byte copy global -> shared through the load path (not the bulk-copy engine,
 // whose queue may hold weight stages); the thread's copies are complete after
 // cp_async_wait_all()

@@ -12,7 +12,7 @@
 // (a 5-level stack kept in TMEM columns).  Results are therefore bit-identical to the decode
 // kernels and the CPU oracle ("colibrì 架构概述" §5 gate/up/SiLU/down; README batch union).
 //
-// CTA: 15 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
+// CTA: 23 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
 //   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream)
 //   warp 1      bulk-tensor copies of the bf16 activation blocks of each burst of 4 blocks, on
 //               the diagonal of a zeroed operand (completing on the same barrier as the
@@ -20,7 +20,8 @@
 //   warp 2      TMEM owner and single MMA issuer (8 x K16 MMAs and one commit per burst, two
 //               accumulator buffers)
 //   warps 3-6   int4 -> bf16 conversion of the weight blocks into the MMA's shared layout
-//   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
+//   warps 7-22  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
+//               (warp w: TMEM lanes 32*(w%4).., 8 of the tile's 32 pairs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,9 +41,13 @@ constexpr int kPfBurstK = kPfR * 32;    // K elements of a burst
 constexpr int kPfStages = 2;            // operand stages, and accumulator buffers, in flight
 constexpr int kPfRawStages = 4;         // raw int4 weight ring (one lane group of blocks each)
 constexpr int kPfConv = 4;              // int4 -> bf16 converter warps
-constexpr int kPfEpi0 = 3 + kPfConv;    // first of the 8 epilogue warps
+constexpr int kPfEpi0 = 3 + kPfConv;    // first epilogue warp
 static_assert(kPfConv == 4 || kPfConv == 8, "converter warps: one or two per row");
-constexpr int kPfWarps = kPfEpi0 + 8;
+constexpr int kPfEpiW = 16;             // epilogue warps: 4 per TMEM lane quadrant
+constexpr int kPfEpiC = kPfP * 4 / kPfEpiW;  // pairs (accumulator columns per block) per epilogue warp
+constexpr int kPfWarps = kPfEpi0 + kPfEpiW;
+constexpr int kDxS = kPfP + 4;          // row stride (floats) of the staged block scales: 16-byte rows,
+                                        // and 8 blocks x 4 pairs of one copy round hit 32 banks
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfAStage = kPfM * kPfBurstK * 2;   // 32 KB of bf16 weights
 constexpr int kPfBStage = kPfBurstK * kPfN * 2;   // 32 KB of bf16 activations, block-diagonal
@@ -64,7 +69,7 @@ struct PfSmem {
   uint8_t* raw;
   uint8_t* a;
   uint8_t* b;
-  float* dxs;  // [nb][kPfP]
+  float* dxs;  // [nb][kDxS]: block scales of the tile's pairs
   float* us;   // [kPfP][64] u values (gate/up only)
   uint64_t* raw_full;
   uint64_t* raw_empty;
@@ -108,7 +113,7 @@ int prefill_smem_bytes(int d, int f, int E, int down) {
   const int K = down ? f : d;
   const int nb = K / kQB, G = (nb + 31) / 32;
   const int raw = kPfM * G * 16;
-  const int dx = nb * kPfP * 4;
+  const int dx = nb * kDxS * 4;
   const int bars = (2 * kPfRawStages + 3 * kPfStages) * 8 + 16;
   const int tabs = 3 * (E + 2) * 4;
   return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfP * 64 * 4) +
@@ -157,15 +162,15 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
 // leaf `chain` holds the whole sum
 #define COLI_PF_PUSH_GROUP()                                                   \
   {                                                                            \
-    float lv[16];                                                              \
+    float lv[kPfEpiC];                                                         \
     int l = 0;                                                                 \
     for (; (gi >> l) & 1; ++l) {                                               \
-      tmem_ld16(tl + kStackCol + l * kPfP + half * 16, lv);                    \
-      _Pragma("unroll") for (int c = 0; c < 16; ++c) chain[c] = __fadd_rn(lv[c], chain[c]); \
+      tmem_ld8(tl + kStackCol + l * kPfP + e8, lv);                            \
+      _Pragma("unroll") for (int c = 0; c < kPfEpiC; ++c) chain[c] = __fadd_rn(lv[c], chain[c]); \
     }                                                                          \
     if (l < 5) {                                                               \
-      tmem_st16(tl + kStackCol + l * kPfP + half * 16, chain);                 \
-      _Pragma("unroll") for (int c = 0; c < 16; ++c) chain[c] = 0.0f;         \
+      tmem_st8(tl + kStackCol + l * kPfP + e8, chain);                         \
+      _Pragma("unroll") for (int c = 0; c < kPfEpiC; ++c) chain[c] = 0.0f;    \
     }                                                                          \
     ++gi;                                                                      \
   }
@@ -176,6 +181,7 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
 // block b and zeros elsewhere -- so column (b, p) of the accumulator is the exact block dot of
 // block b and pair p.  One commit per burst both frees the burst's operand stage and hands its
 // accumulator to the epilogue.
+template <bool kDown>
 __global__ void __launch_bounds__(kPfThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                        const PfArgs a) {
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const PfSmem m = pf_carve(smem, a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.s.d, f = a.s.f;
-  const bool down = a.down != 0;
+  constexpr bool down = kDown;
   const int K = down ? f : d;
   const int nb = K / kQB, G = (nb + 31) / 32, ngrp = nb / G;
   const int nburst = nb / kPfR;  // d and f are multiples of 128
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(&m.a_full[i], kPfConv + 1);  // the converter warps + the activation loader (expect_tx)
       mbar_init(&m.done[i], 1);
-      mbar_init(&m.acc_empty[i], 8);
+      mbar_init(&m.acc_empty[i], kPfEpiW);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -275,38 +281,52 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp >= 3 && warp < kPfEpi0) {
     // ---------------- int4 -> bf16: thread r owns weight row r % 128 of the tile and, with more
     // than 4 converter warps, its share of a burst's blocks (j % (kPfConv / 4) == r / 128);
-    // block j of a burst goes to core-matrix columns 4j..4j+3 of the burst's weight stage
+    // block j of a burst goes to core-matrix columns 4j..4j+3 of the burst's weight stage.  A
+    // burst's raw chunks are all read before any is converted, so the four conversions overlap.
     const int r = (threadIdx.x - 96) & (kPfM - 1);
     const int hf = (threadIdx.x - 96) >> 7;
-    long kbl = 0, kg = 0;  // blocks and groups so far
+    long kb = 0, kg = 0;  // bursts and raw groups so far
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      for (int gi = 0; gi < ngrp; ++gi, ++kg) {
-        const int rs = (int)(kg % kPfRawStages);
-        mbar_wait_bounded(&m.raw_full[rs], (uint32_t)((kg / kPfRawStages) & 1), &abort_flag, status);
-        const uint8_t* rrow = m.raw + (long)rs * a.raw_stage_bytes + r * G * 16;
-        for (int i = 0; i < G; ++i, ++kbl) {
-          const long kb = kbl / kPfR;
-          const int j = (int)(kbl % kPfR);
-          const int s = (int)(kb % kPfStages);
-          const long n = kb / kPfStages;
-          if (j == 0 && n > 0) mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
-          if (j % (kPfConv / 4) == hf) {
-          const uint4 c = *reinterpret_cast<const uint4*>(rrow + (store_chunk(gi, i, G) - gi * G) * 16);
+      int gi = 0, ci = 0;  // group of the next block, and its chunk within the group
+      for (int bu = 0; bu < nburst; ++bu, ++kb) {
+        const int s = (int)(kb % kPfStages);
+        const long n = kb / kPfStages;
+        if (n > 0) mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
+        uint4 c[kPfR];
+        int rel = 0;  // raw stages released by this burst: count, first one is (kg0 % ring)
+        const long kg0 = kg;
+#pragma unroll
+        for (int j = 0; j < kPfR; ++j) {
+          const int rs = (int)(kg % kPfRawStages);
+          if (ci == 0) mbar_wait_bounded(&m.raw_full[rs], (uint32_t)((kg / kPfRawStages) & 1), &abort_flag, status);
+          int cc = ci + ((gi >> 2) & 1);  // the store's chunk rotation within a group
+          if (cc >= G) cc -= G;
+          c[j] = make_uint4(0, 0, 0, 0);
+          if (j % (kPfConv / 4) == hf)
+            c[j] = *reinterpret_cast<const uint4*>(m.raw + (long)rs * a.raw_stage_bytes + (r * G + cc) * 16);
+          if (++ci == G) {
+            ci = 0;
+            ++gi;
+            ++kg;
+            ++rel;
+          }
+        }
+        uint8_t* ast = m.a + (long)s * kPfAStage;
+#pragma unroll
+        for (int j = 0; j < kPfR; ++j) {
+          if (j % (kPfConv / 4) != hf) continue;
           uint4 o[4];
-          int4_chunk_to_bf16(c, o);
-          uint8_t* ast = m.a + (long)s * kPfAStage;
+          int4_chunk_to_bf16(c[j], o);
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc)
             *reinterpret_cast<uint4*>(ast + ((4 * j + kc) * (kPfM / 8) + (r >> 3)) * 128 + (r & 7) * 16) = o[kc];
-          }
-          if (j == kPfR - 1) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&m.a_full[s]);
-          }
         }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&m.raw_empty[rs]);
+        if (lane == 0) {
+          mbar_arrive(&m.a_full[s]);
+          for (int i = 0; i < rel; ++i) mbar_arrive(&m.raw_empty[(int)((kg0 + i) % kPfRawStages)]);
+        }
       }
     }
   } else if (warp == 2) {
@@ -335,12 +355,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., pairs half*16..half*16+15
+    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).. and the columns of pairs
+    // e8..e8+7 of every block
     const int q = warp & 3;
-    const int half = (warp - kPfEpi0) >> 2;
+    const int e8 = ((warp - kPfEpi0) >> 2) * kPfEpiC;
     const int row = q * 32 + lane;
-    const int etid = threadIdx.x - kPfEpi0 * 32;
+    const int ew = warp - kPfEpi0;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    int32_t* const Adump = down ? a.dbg.Ad : a.dbg.Ag;
     long kb = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int u, mt, nt;
@@ -349,32 +371,58 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int pb = m.toff[u] + nt * kPfP;  // first pair of the tile
       const int pe = m.toff[u + 1];          // end of the slot's pairs
       const int nv = min(kPfP, pe - pb);       // valid pairs of the tile
-      const bool active = half * 16 < nv;       // this warp has columns to finish
-      // this tile's activation block scales, [block][pair]
-      named_bar_sync(2, 8 * 32);
-      const float* dsrc = down ? a.w.dh : a.pw.dxp;
-#pragma unroll 4
-      for (int idx = etid; idx < nb * kPfP; idx += 8 * 32) {
-        const int b = idx / kPfP, col = idx - b * kPfP;
-        m.dxs[idx] = col < nv ? __ldcg(dsrc + (long)(pb + col) * nb + b) : 0.0f;
+      const bool active = e8 < nv;             // this warp has columns to finish
+      // this tile's activation block scales -> dxs[block][pair], all copies in flight at once: a
+      // copy round is 8 consecutive blocks (32 contiguous bytes of a pair's row) x 4 pairs
+      named_bar_sync(2, kPfEpiW * 32);
+      {
+        const float* dsrc = down ? a.w.dh : a.pw.dxp;
+        const int col = (lane >> 3), bi = lane & 7;
+        const int nbb = (nb + 7) >> 3;
+        for (int g = ew; g < nbb * (kPfP / 4); g += kPfEpiW) {
+          const int c = (g % (kPfP / 4)) * 4 + col, b = (g / (kPfP / 4)) * 8 + bi;
+          if (b < nb) {
+            float* dst = m.dxs + b * kDxS + c;
+            if (c < nv) cp_async4(dst, dsrc + (long)(pb + c) * nb + b);
+            else *dst = 0.0f;
+          }
+        }
+        cp_async_wait_all();
       }
-      named_bar_sync(2, 8 * 32);
+      named_bar_sync(2, kPfEpiW * 32);
+      {
+        // the next tile's block scales: pull their lines into L2 while this tile runs
+        const int tn = t + gridDim.x;
+        if (tn < total) {
+          int un, mtn, ntn;
+          pf_tile(m.tp, nu, n_mt, tn, un, mtn, ntn);
+          const int pbn = m.toff[un] + ntn * kPfP;
+          const int nvn = min(kPfP, m.toff[un + 1] - pbn);
+          const float* dsrc = down ? a.w.dh : a.pw.dxp;
+          const int lines = (nb * 4 + 127) >> 7;  // 128-byte lines per pair row (rows need not align)
+          for (int i = threadIdx.x - kPfEpi0 * 32; i < nvn * (lines + 1); i += kPfEpiW * 32) {
+            const int pr = i / (lines + 1), li = i - pr * (lines + 1);
+            const float* row = dsrc + (long)(pbn + pr) * nb;
+            prefetch_l2(reinterpret_cast<const char*>(row) + min(li * 128, nb * 4 - 4));
+          }
+        }
+      }
 
-      float chain[16];
+      float chain[kPfEpiC];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) chain[c] = 0.0f;
+      for (int c = 0; c < kPfEpiC; ++c) chain[c] = 0.0f;
       int gi = 0, gb = 0;  // current group and block within it
       for (int bu = 0; bu < nburst; ++bu, ++kb) {
         const int s = (int)(kb % kPfStages);
         const long n = kb / kPfStages;
         mbar_wait_bounded(&m.done[s], (uint32_t)(n & 1), &abort_flag, status);
         tc_fence_after();
-        // the burst's 4 blocks (16 columns each) in one round of loads, then the accumulator goes
-        // back to the MMA issuer before they are folded
-        float acc4[kPfR][16];
+        // the burst's 4 blocks in one round of loads, then the accumulator goes back to the MMA
+        // issuer before they are folded
+        uint32_t acc4[kPfR][kPfEpiC];
         if (active) {
-#pragma unroll
-          for (int j = 0; j < kPfR; ++j) tmem_ld16(tl + s * kPfN + j * kPfP + half * 16, acc4[j]);
+          const uint32_t t0 = tl + s * kPfN + e8;
+          tmem_ld8x4(t0, t0 + kPfP, t0 + 2 * kPfP, t0 + 3 * kPfP, acc4);
         }
         tc_fence_before();
         __syncwarp();
@@ -382,26 +430,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!active) continue;
 #pragma unroll
         for (int j = 0; j < kPfR; ++j) {
-          const float (&acc)[16] = acc4[j];
           const int b = bu * kPfR + j;
-          const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kPfP + half * 16);
+          const float4* dxb = reinterpret_cast<const float4*>(m.dxs + b * kDxS + e8);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < kPfEpiC / 4; ++c4) {
             const float4 dv = dxb[c4];
-            chain[4 * c4 + 0] = __fmaf_rn(dv.x, acc[4 * c4 + 0], chain[4 * c4 + 0]);
-            chain[4 * c4 + 1] = __fmaf_rn(dv.y, acc[4 * c4 + 1], chain[4 * c4 + 1]);
-            chain[4 * c4 + 2] = __fmaf_rn(dv.z, acc[4 * c4 + 2], chain[4 * c4 + 2]);
-            chain[4 * c4 + 3] = __fmaf_rn(dv.w, acc[4 * c4 + 3], chain[4 * c4 + 3]);
+            chain[4 * c4 + 0] = __fmaf_rn(dv.x, __uint_as_float(acc4[j][4 * c4 + 0]), chain[4 * c4 + 0]);
+            chain[4 * c4 + 1] = __fmaf_rn(dv.y, __uint_as_float(acc4[j][4 * c4 + 1]), chain[4 * c4 + 1]);
+            chain[4 * c4 + 2] = __fmaf_rn(dv.z, __uint_as_float(acc4[j][4 * c4 + 2]), chain[4 * c4 + 2]);
+            chain[4 * c4 + 3] = __fmaf_rn(dv.w, __uint_as_float(acc4[j][4 * c4 + 3]), chain[4 * c4 + 3]);
           }
-          int32_t* Adump = down ? a.dbg.Ad : a.dbg.Ag;
           if (Adump != nullptr) {
             const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
             int32_t* dump = (!down && row >= 64) ? a.dbg.Au : Adump;
             const int nrow = down ? d : f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int p = pb + half * 16 + c;
-              if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)acc[c];
+            for (int c = 0; c < kPfEpiC; ++c) {
+              const int p = pb + e8 + c;
+              if (p < pe) dump[((long)p * nrow + wrow) * nb + b] = (int32_t)__uint_as_float(acc4[j][c]);
             }
           }
           if (++gb == G) {
@@ -414,7 +460,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // empty groups ngrp..31 are +0 leaves of the tree
         while (gi < 32) COLI_PF_PUSH_GROUP()
       }
-      // chain = the canonical sum of every (row, pair) of this thread (every loop over the 16
+      // chain = the canonical sum of every (row, pair) of this thread (every loop over the
       // pairs is unrolled, so chain stays in registers)
       const float* scx = a.st.sc + (long)ex * (2 * f + d);
       if (down) {
@@ -422,8 +468,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int r = mt * kPfM + row;
         const float sd = scx[2 * f + r];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int p = pb + half * 16 + c;
+        for (int c = 0; c < kPfEpiC; ++c) {
+          const int p = pb + e8 + c;
           if (p < pe) a.pw.e[(long)p * d + r] = __fmul_rn(sd, chain[c]);
         }
       } else {
@@ -431,27 +477,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool is_up = row >= 64;
         const float sr = is_up ? scx[f + r] : scx[r];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) chain[c] = __fmul_rn(sr, chain[c]);  // the row-scaled projection
+        for (int c = 0; c < kPfEpiC; ++c) chain[c] = __fmul_rn(sr, chain[c]);  // the row-scaled projection
         if (a.dbg.g != nullptr && active) {
           float* dst = is_up ? a.dbg.u : a.dbg.g;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int p = pb + half * 16 + c;
+          for (int c = 0; c < kPfEpiC; ++c) {
+            const int p = pb + e8 + c;
             if (p < pe) dst[(long)p * f + r] = chain[c];
           }
         }
         if (is_up && active) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) m.us[(half * 16 + c) * 64 + (row - 64)] = chain[c];
+          for (int c = 0; c < kPfEpiC; ++c) m.us[(e8 + c) * 64 + (row - 64)] = chain[c];
         }
-        named_bar_sync(2, 8 * 32);
+        named_bar_sync(2, kPfEpiW * 32);
         if (!is_up && active) {
           // h = SiLU(g) * u; the warp's 32 rows are one int8 block of h for each pair
           const int nhb = f >> 5, hbk = r >> 5;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int p = pb + half * 16 + c;
-            const float hv = canon_silu_mul(chain[c], m.us[(half * 16 + c) * 64 + row]);
+          for (int c = 0; c < kPfEpiC; ++c) {
+            const int p = pb + e8 + c;
+            const float hv = canon_silu_mul(chain[c], m.us[(e8 + c) * 64 + row]);
             const float dd = __fdiv_rn(warp_max(fabsf(hv)), 127.0f);
             const int code = q8_code(hv, dd);
             const int sq = warp_isum(code);
@@ -531,7 +577,10 @@ cudaError_t configure_prefill_kernels(int d, int f, int E) {
                        ? prefill_smem_bytes(d, f, E, 0)
                        : prefill_smem_bytes(d, f, E, 1);
   if (need > kSmemLimit) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  const cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(expert_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const PrefillWork& pw, int d,
@@ -571,10 +620,12 @@ cudaError_t launch_prefill_experts(const float* x, float* y, const Shape& s, con
     const int K = down ? s.f : s.d;
     const int nb = K / kQB, G = (nb + 31) / 32;
     args.raw_stage_bytes = kPfM * G * 16;
-    args.dx_bytes = nb * kPfP * 4;
+    args.dx_bytes = nb * kDxS * 4;
     const int smem = prefill_smem_bytes(s.d, s.f, s.E, down);
-    expert_gemm_kernel<<<num_sms, kPfThreads, smem, stream>>>(down ? maps.wd : maps.wgu,
-                                                              down ? maps.hb : maps.xb, args);
+    if (down)
+      expert_gemm_kernel<true><<<num_sms, kPfThreads, smem, stream>>>(maps.wd, maps.hb, args);
+    else
+      expert_gemm_kernel<false><<<num_sms, kPfThreads, smem, stream>>>(maps.wgu, maps.xb, args);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
