@@ -320,6 +320,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Two lanes of fp32 at once (sm_100 and later): each lane rounds exactly as the scalar
+// fma.rn / add.rn does, so a pair of these is bit-identical to two scalar operations.
+// c = a * b + c on (c0, c1)
+__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float& c0, float& c1) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// c = a + c on (c0, c1)
+__device__ __forceinline__ void add2_rn(float a0, float a1, float& c0, float& c1) {
+  asm("{\n\t.reg .b64 a, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 c, {%0, %1};\n\t"
+      "add.rn.f32x2 c, a, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1));
+}
+
 // hint: bring the 128-byte line holding p into L2
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

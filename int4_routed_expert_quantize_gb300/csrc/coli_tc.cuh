@@ -131,6 +131,31 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// four 16-column loads (columns at t0..t3) with one wait for all of them
+#define COLI_TMEM_LD16(taddr, r)                                                              \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, "   \
+               "%9, %10, %11, %12, %13, %14, %15}, [%16];"                                   \
+               : "=r"((r)[0]), "=r"((r)[1]), "=r"((r)[2]), "=r"((r)[3]), "=r"((r)[4]),       \
+                 "=r"((r)[5]), "=r"((r)[6]), "=r"((r)[7]), "=r"((r)[8]), "=r"((r)[9]),       \
+                 "=r"((r)[10]), "=r"((r)[11]), "=r"((r)[12]), "=r"((r)[13]), "=r"((r)[14]),  \
+                 "=r"((r)[15])                                                               \
+               : "r"(taddr)                                                                  \
+               : "memory")
+#define COLI_R16(r) "+r"((r)[0]), "+r"((r)[1]), "+r"((r)[2]), "+r"((r)[3]), "+r"((r)[4]), \
+    "+r"((r)[5]), "+r"((r)[6]), "+r"((r)[7]), "+r"((r)[8]), "+r"((r)[9]), "+r"((r)[10]), \
+    "+r"((r)[11]), "+r"((r)[12]), "+r"((r)[13]), "+r"((r)[14]), "+r"((r)[15])
+__device__ __forceinline__ void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3,
+                                            uint32_t (&r)[4][16]) {
+  COLI_TMEM_LD16(t0, r[0]);
+  COLI_TMEM_LD16(t1, r[1]);
+  COLI_TMEM_LD16(t2, r[2]);
+  COLI_TMEM_LD16(t3, r[3]);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : COLI_R16(r[0]), COLI_R16(r[1]), COLI_R16(r[2]), COLI_R16(r[3])
+               :
+               : "memory");
+}
+
 // 16 consecutive columns of this warp's 32 lanes: thread i gets lane (base lane + i), columns
 // col..col+15 of it
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {

@@ -12,7 +12,7 @@
 // (a 5-level stack kept in TMEM columns).  Results are therefore bit-identical to the decode
 // kernels and the CPU oracle ("colibrì 架构概述" §5 gate/up/SiLU/down; README batch union).
 //
-// CTA: 23 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
+// CTA: 15 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
 //   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream)
 //   warp 1      bulk-tensor copies of the bf16 activation blocks of each burst of 4 blocks, on
 //               the diagonal of a zeroed operand (completing on the same barrier as the
@@ -20,8 +20,8 @@
 //   warp 2      TMEM owner and single MMA issuer (8 x K16 MMAs and one commit per burst, two
 //               accumulator buffers)
 //   warps 3-6   int4 -> bf16 conversion of the weight blocks into the MMA's shared layout
-//   warps 7-22  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
-//               (warp w: TMEM lanes 32*(w%4).., 8 of the tile's 32 pairs)
+//   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
+//               (warp w: TMEM lanes 32*(w%4).., 16 of the tile's 32 pairs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,7 +43,7 @@ constexpr int kPfRawStages = 4;         // raw int4 weight ring (one lane group 
 constexpr int kPfConv = 4;              // int4 -> bf16 converter warps
 constexpr int kPfEpi0 = 3 + kPfConv;    // first epilogue warp
 static_assert(kPfConv == 4 || kPfConv == 8, "converter warps: one or two per row");
-constexpr int kPfEpiW = 16;             // epilogue warps: 4 per TMEM lane quadrant
+constexpr int kPfEpiW = 8;              // epilogue warps: 2 per TMEM lane quadrant
 constexpr int kPfEpiC = kPfP * 4 / kPfEpiW;  // pairs (accumulator columns per block) per epilogue warp
 constexpr int kPfWarps = kPfEpi0 + kPfEpiW;
 constexpr int kDxS = kPfP + 4;          // row stride (floats) of the staged block scales: 16-byte rows,
@@ -162,14 +162,15 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
 // leaf `chain` holds the whole sum
 #define COLI_PF_PUSH_GROUP()                                                   \
   {                                                                            \
-    float lv[kPfEpiC];                                                         \
     int l = 0;                                                                 \
     for (; (gi >> l) & 1; ++l) {                                               \
-      tmem_ld8(tl + kStackCol + l * kPfP + e8, lv);                            \
-      _Pragma("unroll") for (int c = 0; c < kPfEpiC; ++c) chain[c] = __fadd_rn(lv[c], chain[c]); \
+      float lv[kPfEpiC];                                                       \
+      tmem_ld16(tl + kStackCol + l * kPfP + e8, lv);                           \
+      _Pragma("unroll") for (int c = 0; c < kPfEpiC; c += 2)                   \
+        add2_rn(lv[c], lv[c + 1], chain[c], chain[c + 1]);                     \
     }                                                                          \
     if (l < 5) {                                                               \
-      tmem_st8(tl + kStackCol + l * kPfP + e8, chain);                         \
+      tmem_st16(tl + kStackCol + l * kPfP + e8, chain);                        \
       _Pragma("unroll") for (int c = 0; c < kPfEpiC; ++c) chain[c] = 0.0f;    \
     }                                                                          \
     ++gi;                                                                      \
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t acc4[kPfR][kPfEpiC];
         if (active) {
           const uint32_t t0 = tl + s * kPfN + e8;
-          tmem_ld8x4(t0, t0 + kPfP, t0 + 2 * kPfP, t0 + 3 * kPfP, acc4);
+          tmem_ld16x4(t0, t0 + kPfP, t0 + 2 * kPfP, t0 + 3 * kPfP, acc4);
         }
         tc_fence_before();
         __syncwarp();
@@ -435,10 +436,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < kPfEpiC / 4; ++c4) {
             const float4 dv = dxb[c4];
-            chain[4 * c4 + 0] = __fmaf_rn(dv.x, __uint_as_float(acc4[j][4 * c4 + 0]), chain[4 * c4 + 0]);
-            chain[4 * c4 + 1] = __fmaf_rn(dv.y, __uint_as_float(acc4[j][4 * c4 + 1]), chain[4 * c4 + 1]);
-            chain[4 * c4 + 2] = __fmaf_rn(dv.z, __uint_as_float(acc4[j][4 * c4 + 2]), chain[4 * c4 + 2]);
-            chain[4 * c4 + 3] = __fmaf_rn(dv.w, __uint_as_float(acc4[j][4 * c4 + 3]), chain[4 * c4 + 3]);
+            fma2_rn(dv.x, dv.y, __uint_as_float(acc4[j][4 * c4 + 0]), __uint_as_float(acc4[j][4 * c4 + 1]),
+                    chain[4 * c4 + 0], chain[4 * c4 + 1]);
+            fma2_rn(dv.z, dv.w, __uint_as_float(acc4[j][4 * c4 + 2]), __uint_as_float(acc4[j][4 * c4 + 3]),
+                    chain[4 * c4 + 2], chain[4 * c4 + 3]);
           }
           if (Adump != nullptr) {
             const int wrow = down ? mt * kPfM + row : mt * (kPfM / 2) + (row & 63);
