@@ -209,6 +209,15 @@ __device__ __forceinline__ uint64_t smem_desc(const void* p, uint32_t lbo, uint3
          (1ull << 46);
 }
 
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: rows of 128 bytes (64 bf16 of K)
+// in 1024-byte atoms of 8 rows, as a tensor copy with 128-byte swizzle writes them (the atom
+// must start on a 1024-byte boundary).  p = the atom's start plus the byte offset of the MMA's
+// K slice within the 128-byte row; sbo = 1024 between 8-row groups; layout code 2 in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
+  const uint64_t a = (smem_addr(p) >> 4) & 0x3FFFu;
+  return a | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T ; accumulate = false overwrites D
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, bool accumulate) {

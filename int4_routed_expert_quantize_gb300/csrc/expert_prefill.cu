@@ -38,7 +38,8 @@ constexpr int kPfP = kPrefillTileN;     // pairs per tile
 constexpr int kPfR = 4;                 // 32-element blocks per MMA burst
 constexpr int kPfN = kPfR * kPfP;       // MMA width: block-diagonal columns (block, pair)
 constexpr int kPfBurstK = kPfR * 32;    // K elements of a burst
-constexpr int kPfStages = 2;            // operand stages, and accumulator buffers, in flight
+constexpr int kPfOpStages = 3;          // operand stages (converted weights + activations) in flight
+constexpr int kPfAccStages = 2;         // accumulator buffers in flight
 constexpr int kPfRawStages = 4;         // raw int4 weight ring (one lane group of blocks each)
 constexpr int kPfConv = 4;              // int4 -> bf16 converter warps
 constexpr int kPfEpi0 = 3 + kPfConv;    // first epilogue warp
@@ -50,9 +51,9 @@ constexpr int kDxS = kPfP + 4;          // row stride (floats) of the staged blo
                                         // and 8 blocks x 4 pairs of one copy round hit 32 banks
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfAStage = kPfM * kPfBurstK * 2;   // 32 KB of bf16 weights
-constexpr int kPfBStage = kPfBurstK * kPfN * 2;   // 32 KB of bf16 activations, block-diagonal
+constexpr int kPfBStage = kPfBurstK * kPfP * 2;   // 8 KB of bf16 activations: 2 x [32 pairs][64 K], 128-byte swizzle
 constexpr uint32_t kTmemCols = 512;     // accumulators 2 x 128 columns, tree stack 5 x 32
-constexpr uint32_t kStackCol = kPfStages * kPfN;
+constexpr uint32_t kStackCol = kPfAccStages * kPfN;
 
 struct PfArgs {
   Shape s;
@@ -74,8 +75,8 @@ struct PfSmem {
   uint64_t* raw_full;
   uint64_t* raw_empty;
   uint64_t* a_full;     // a burst's converted weights and activation blocks are in
-  uint64_t* done;       // a burst's MMAs are complete: its operand stage is free and its
-                        // accumulator readable
+  uint64_t* op_free;    // a burst's MMAs are complete: its operand stage is free
+  uint64_t* acc_full;   // ... and its accumulator is readable
   uint64_t* acc_empty;  // the epilogue has read a burst's accumulator
   uint32_t* tmem_slot;
   int* tp;    // [nu+1] tile prefix per union slot
@@ -86,12 +87,12 @@ struct PfSmem {
 __device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
   PfSmem m;
   uint8_t* p = smem;
+  m.b = p;  // first: the swizzled activation stages need 1024-byte alignment
+  p += kPfOpStages * kPfBStage;
   m.raw = p;
   p += kPfRawStages * a.raw_stage_bytes;
   m.a = p;
-  p += kPfStages * kPfAStage;
-  m.b = p;
-  p += kPfStages * kPfBStage;
+  p += kPfOpStages * kPfAStage;
   m.dxs = reinterpret_cast<float*>(p);
   p += a.dx_bytes;
   m.us = reinterpret_cast<float*>(p);
@@ -100,9 +101,10 @@ __device__ __forceinline__ PfSmem pf_carve(uint8_t* smem, const PfArgs& a) {
   m.raw_full = bars;
   m.raw_empty = bars + kPfRawStages;
   m.a_full = m.raw_empty + kPfRawStages;
-  m.done = m.a_full + kPfStages;
-  m.acc_empty = m.done + kPfStages;
-  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfStages);
+  m.op_free = m.a_full + kPfOpStages;
+  m.acc_full = m.op_free + kPfOpStages;
+  m.acc_empty = m.acc_full + kPfAccStages;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(m.acc_empty + kPfAccStages);
   m.tp = reinterpret_cast<int*>(m.tmem_slot + 4);
   m.tex = m.tp + a.s.E + 2;
   m.toff = m.tex + a.s.E + 2;
@@ -114,9 +116,9 @@ int prefill_smem_bytes(int d, int f, int E, int down) {
   const int nb = K / kQB, G = (nb + 31) / 32;
   const int raw = kPfM * G * 16;
   const int dx = nb * kDxS * 4;
-  const int bars = (2 * kPfRawStages + 3 * kPfStages) * 8 + 16;
+  const int bars = (2 * kPfRawStages + 2 * kPfOpStages + 2 * kPfAccStages) * 8 + 16;
   const int tabs = 3 * (E + 2) * 4;
-  return kPfRawStages * raw + kPfStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfP * 64 * 4) +
+  return kPfRawStages * raw + kPfOpStages * (kPfAStage + kPfBStage) + dx + (down ? 0 : kPfP * 64 * 4) +
          bars + tabs;
 }
 
@@ -201,14 +203,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int total = n_mt * __ldcg(a.pw.tile_prefix + nu);
   int* status = a.w.status;
 
+  if ((smem_addr(m.b) & 1023u) != 0) {  // the swizzled activation stages need 1024-byte alignment
+    if (threadIdx.x == 0) atomicExch(a.w.status, COLI_EUNSUPPORTED);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfRawStages; ++i) {
       mbar_init(&m.raw_full[i], 1);
       mbar_init(&m.raw_empty[i], kPfConv);
     }
-    for (int i = 0; i < kPfStages; ++i) {
+    for (int i = 0; i < kPfOpStages; ++i) {
       mbar_init(&m.a_full[i], kPfConv + 1);  // the converter warps + the activation loader (expect_tx)
-      mbar_init(&m.done[i], 1);
+      mbar_init(&m.op_free[i], 1);
+    }
+    for (int i = 0; i < kPfAccStages; ++i) {
+      mbar_init(&m.acc_full[i], 1);
       mbar_init(&m.acc_empty[i], kPfEpiW);
     }
     abort_flag = 0;
@@ -219,10 +228,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     m.toff[i] = __ldcg(a.w.offsets + i);
     m.tex[i] = i < nu ? __ldcg(a.w.union_ids + i) : 0;
   }
-  // the activation stages' off-diagonal blocks stay zero: only the diagonal is ever copied in
-  for (int i = threadIdx.x; i < kPfStages * kPfBStage / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(m.b)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
   if (warp == 2) tmem_alloc(m.tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -264,18 +269,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         pf_tile(m.tp, nu, n_mt, t, u, mt, nt);
         const int row0 = m.toff[u] + nt * kPfP;
         for (int bu = 0; bu < nburst; ++bu, ++kb) {
-          const int s = (int)(kb % kPfStages);
-          const long n = kb / kPfStages;
-          if (n > 0 && !mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
+          const int s = (int)(kb % kPfOpStages);
+          const long n = kb / kPfOpStages;
+          if (n > 0 && !mbar_wait_bounded(&m.op_free[s], (uint32_t)((n - 1) & 1), &abort_flag, status))
             break;
           uint8_t* dst = m.b + (long)s * kPfBStage;
-          mbar_expect_tx(&m.a_full[s], (uint32_t)(kPfR * 4 * kPfP * 16));
-#pragma unroll
-          for (int j = 0; j < kPfR; ++j)
-#pragma unroll
-            for (int kc = 0; kc < 4; ++kc)
-              tma_load_2d(dst + ((4 * j + kc) * (kPfN / 8) + 4 * j) * 128, &map_x,
-                          (bu * kPfR + j) * 32 + kc * 8, row0, &m.a_full[s]);
+          mbar_expect_tx(&m.a_full[s], (uint32_t)kPfBStage);
+          // two boxes of 64 K x 32 pairs (128-byte rows, swizzled): blocks 0-1 and 2-3
+          tma_load_2d(dst, &map_x, bu * kPfBurstK, row0, &m.a_full[s]);
+          tma_load_2d(dst + kPfBStage / 2, &map_x, bu * kPfBurstK + kPfBurstK / 2, row0, &m.a_full[s]);
         }
       }
     }
@@ -290,9 +292,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int gi = 0, ci = 0;  // group of the next block, and its chunk within the group
       for (int bu = 0; bu < nburst; ++bu, ++kb) {
-        const int s = (int)(kb % kPfStages);
-        const long n = kb / kPfStages;
-        if (n > 0) mbar_wait_bounded(&m.done[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
+        const int s = (int)(kb % kPfOpStages);
+        const long n = kb / kPfOpStages;
+        if (n > 0) mbar_wait_bounded(&m.op_free[s], (uint32_t)((n - 1) & 1), &abort_flag, status);
         uint4 c[kPfR];
         int rel = 0;  // raw stages released by this burst: count, first one is (kg0 % ring)
         const long kg0 = kg;
@@ -333,25 +335,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 2) {
     // ---------------- MMA issuer: one burst of 8 MMAs and one commit per 4 blocks
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kPfM, kPfN);
+      const uint32_t idesc = idesc_bf16_f32(kPfM, kPfP);
       long kb = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
         for (int bu = 0; bu < nburst; ++bu, ++kb) {
-          const int s = (int)(kb % kPfStages);
-          const long n = kb / kPfStages;
+          const int s = (int)(kb % kPfOpStages), sa = (int)(kb % kPfAccStages);
+          const long n = kb / kPfOpStages, na = kb / kPfAccStages;
           bool ok = mbar_wait_bounded(&m.a_full[s], (uint32_t)(n & 1), &abort_flag, status);
-          if (n > 0) ok = mbar_wait_bounded(&m.acc_empty[s], (uint32_t)((n - 1) & 1), &abort_flag, status) && ok;
+          if (na > 0) ok = mbar_wait_bounded(&m.acc_empty[sa], (uint32_t)((na - 1) & 1), &abort_flag, status) && ok;
           if (!ok) continue;
           tc_fence_after();
           const uint8_t* as = m.a + (long)s * kPfAStage;
           const uint8_t* bs = m.b + (long)s * kPfBStage;
 #pragma unroll
           for (int ks = 0; ks < kPfBurstK / 16; ++ks) {
+            const int j = ks >> 1, kk = ks & 1;  // block j of the burst -> accumulator columns 32j..
             const uint64_t da = smem_desc(as + ks * 2 * (kPfM / 8) * 128, (kPfM / 8) * 128, 128);
-            const uint64_t db = smem_desc(bs + ks * 2 * (kPfN / 8) * 128, (kPfN / 8) * 128, 128);
-            tc_mma_bf16(tmem + (uint32_t)(s * kPfN), da, db, idesc, ks > 0);
+            const uint64_t db = smem_desc_sw128(bs + (j >> 1) * (kPfBStage / 2) + (j & 1) * 64 + kk * 32);
+            tc_mma_bf16(tmem + (uint32_t)(sa * kPfN + j * kPfP), da, db, idesc, kk > 0);
           }
-          tc_commit(&m.done[s]);
+          tc_commit(&m.op_free[s]);
+          tc_commit(&m.acc_full[sa]);
         }
       }
     }
@@ -414,9 +418,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int c = 0; c < kPfEpiC; ++c) chain[c] = 0.0f;
       int gi = 0, gb = 0;  // current group and block within it
       for (int bu = 0; bu < nburst; ++bu, ++kb) {
-        const int s = (int)(kb % kPfStages);
-        const long n = kb / kPfStages;
-        mbar_wait_bounded(&m.done[s], (uint32_t)(n & 1), &abort_flag, status);
+        const int s = (int)(kb % kPfAccStages);
+        const long n = kb / kPfAccStages;
+        mbar_wait_bounded(&m.acc_full[s], (uint32_t)(n & 1), &abort_flag, status);
         tc_fence_after();
         // the burst's 4 blocks in one round of loads, then the accumulator goes back to the MMA
         // issuer before they are folded
@@ -561,7 +565,8 @@ static EncodeTiledFn encode_fn() {
 
 // 2-D map over a row-major [rows][cols] array (elem_bytes 1 or 2), box {box_cols, box_rows}
 static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes,
-                     uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+                     uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -569,7 +574,7 @@ static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -591,10 +596,11 @@ bool prefill_make_maps(PrefillMaps* maps, const Store& st, const Work& w, const 
                      (uint64_t)slots * f, (uint32_t)(Gd * 16), (uint32_t)(kPfM / 2));
   ok = ok && make_map(&maps->wd, st.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(f / 2),
                       (uint64_t)slots * d, (uint32_t)(Gf * 16), (uint32_t)kPfM);
+  // activation codes: boxes of 64 bf16 (one 128-byte swizzled row) x 32 pairs
   ok = ok && make_map(&maps->xb, pw.xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)prow,
-                      8u, (uint32_t)kPfP);
+                      (uint32_t)(kPfBurstK / 2), (uint32_t)kPfP, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&maps->hb, pw.hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)f, (uint64_t)prow,
-                      8u, (uint32_t)kPfP);
+                      (uint32_t)(kPfBurstK / 2), (uint32_t)kPfP, CU_TENSOR_MAP_SWIZZLE_128B);
   // router rows and normalised tokens (both in the router's chunk order), 256-float boxes
   ok = ok && make_map(&maps->wr, st.wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)d, (uint64_t)E,
                       256u, 16u);
