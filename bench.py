@@ -109,17 +109,24 @@ def peaks():
         return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
 
 
-def recorded_traffic(kernel, workload):
-    """per-launch DRAM bytes from the committed ncu summary of this kernel, if it is current"""
+def recorded_traffic(kernel, workload, n_union=None, pairs=None):
+    """per-launch DRAM bytes from the committed ncu summary of this kernel, if it is current.
+    A record taken on a smaller case of the same kernel and layer shapes carries a linear model
+    (bytes per union expert, bytes per token-expert pair) measured there; the figure for this
+    workload is that model at its own union size and pair count."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh).get(f"{kernel}:{workload}")
     except Exception:
         return None
-    if not rec:
+    if not rec or source_digest(rec["sources"]) != rec["sources_sha256_16"]:
         return None
-    return rec["bytes_per_launch"] if source_digest(rec["sources"]) == rec["sources_sha256_16"] else None
+    if "bytes_per_launch" in rec:
+        return rec["bytes_per_launch"]
+    if n_union is None:
+        return None
+    return rec["bytes_per_union_expert"] * n_union + rec.get("bytes_per_pair", 0.0) * (pairs or 0)
 
 
 def source_digest(names):
@@ -479,7 +486,8 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
                            "bound": "hbm", "achieved": ach, "peak": B.hbm, "peak_source": hbm_src,
                            "unit": "GB/s", "frac": ach / B.hbm,
                            "algorithmic_bytes": expert_bytes(wl, n_union),
-                           "traffic": recorded_traffic("expert_gemm_kernel", wl.name),
+                           "traffic": recorded_traffic("expert_gemm_kernel", wl.name, n_union,
+                                                       T * (wl.K + wl.n_shared)),
                            "tensor": {"achieved": tf, "peak": B.bf16, "unit": "TFLOP/s",
                                       "frac": tf / B.bf16, "algorithmic_flops": flops,
                                       "peak_source": f"{B.peak_kind} bf16_tflops (burst); the MMAs "
@@ -506,7 +514,7 @@ def measure(B, wl, steps, warmup, want_e2e, pool):
         out["roofline"] = {"kernel": "gateup_decode_kernel", "bound": "hbm", "achieved": ach,
                            "peak": B.hbm, "peak_source": hbm_src, "unit": "GB/s",
                            "frac": ach / B.hbm, "algorithmic_bytes": gb,
-                           "traffic": recorded_traffic("gateup_decode_kernel", wl.name),
+                           "traffic": recorded_traffic("gateup_decode_kernel", wl.name, n_union),
                            "timing": "CUDA events around the launch, profiled pass"}
         out["down_gbs"] = down_bytes(wl, n_union) / (kern["down"] / 1000.0) / 1e9
     if clk:
