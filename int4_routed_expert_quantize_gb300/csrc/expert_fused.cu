@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_fused_kernel(const FusedAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int SPU = 32 / kGuRps;
   const int G_ = gridDim.x, c = blockIdx.x;
+  // the grid after this one (the copy of y to the caller, or the next forward's router) may be
+  // scheduled once every CTA of this grid has started; it waits for this grid to complete
+  griddep_launch_dependents();
 
   // shared-expert units of this CTA: [a0, a1) of the nhb units of store slot E
   const int UA = a.s.n_shared ? nhb : 0;

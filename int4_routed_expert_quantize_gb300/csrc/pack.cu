@@ -238,6 +238,7 @@ cudaError_t launch_repack_matrix(const uint8_t* src, uint8_t* dst, int rows, int
 // bypass the caches (the host rewrites the buffer between calls); the stores write through.
 __global__ void __launch_bounds__(256) host_in_kernel(const float4* __restrict__ hx,
                                                       float4* __restrict__ dx, int n4) {
+  griddep_launch_dependents();  // the router may be scheduled; it waits for this grid
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n4) dx[i] = __ldcv(hx + i);
 }
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(256) host_out_kernel(const float4* __restrict_
                                                        float4* __restrict__ hy, int n4,
                                                        const int* __restrict__ status,
                                                        int* __restrict__ hstatus) {
+  griddep_wait();  // a programmatic dependent of the forward's last grid
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n4) __stwt(hy + i, __ldcg(dy + i));
   if (i == 0) __stwt(hstatus, __ldcg(status));
@@ -261,9 +263,17 @@ cudaError_t launch_host_in(const float* hx, float* dx, int n, cudaStream_t strea
 cudaError_t launch_host_out(const float* dy, float* hy, int n, const int* status, int* hstatus,
                             cudaStream_t stream) {
   const int n4 = n / 4;
-  host_out_kernel<<<(n4 + 255) / 256, 256, 0, stream>>>(reinterpret_cast<const float4*>(dy),
-                                                        reinterpret_cast<float4*>(hy), n4, status, hstatus);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n4 + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, host_out_kernel, reinterpret_cast<const float4*>(dy),
+                            reinterpret_cast<float4*>(hy), n4, status, hstatus);
 }
 
 // router rows: lane g's contiguous elements g*(d/32) .. in 4-float chunks at i4*32 + g

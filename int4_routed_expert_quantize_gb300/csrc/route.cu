@@ -48,6 +48,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ x,
   const int ne = min(kRouterEpc, E - e0);
   float* wrs = route_sm;                   // [kRouterEpc][d] router rows as stored
   float* xsm = route_sm + kRouterEpc * d;  // [kRouteTgroup][d] tokens of the current group
+  // launched as a programmatic dependent: the preceding grid (the previous forward, or the
+  // copy of x into device memory) is complete and its writes visible from here on
+  griddep_wait();
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0) {  // this call's selection is not published yet; no CTA at the barrier
       w.sel_flag[0] = 0;
@@ -536,10 +539,20 @@ cudaError_t launch_set_slots(int32_t* slot_of, const SlotUpdate& u, cudaStream_t
 
 cudaError_t launch_route(const float* x, const Shape& s, const Store& st, const Work& w,
                          cudaStream_t stream) {
-  // an ordinary launch: it reads the caller's x, so it stays ordered after all earlier work
+  // a programmatic dependent launch: its CTAs may be scheduled while the preceding grid
+  // finishes, and wait for that grid (griddepcontrol.wait) before touching anything
   const int grid = (s.E + kRouterEpc - 1) / kRouterEpc;
-  route_kernel<<<grid, 256, route_smem_bytes(s.d, s.T), stream>>>(x, s, st, w);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = route_smem_bytes(s.d, s.T);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_kernel, x, s, st, w);
 }
 
 }  // namespace coli
