@@ -149,13 +149,17 @@ int coli_moe_forward_profiled(coli_moe* h, const float* x_dev, int T, float* y_d
                               void* const* events, int n_events, void* stream);
 
 /* Host-buffer form: copies x_host [T,d] to the device, runs forward, copies y back to
- * y_host [T,d] and synchronises `stream`; any host memory (pageable or pinned).  Batches of up to
- * 8 tokens go through the handle's own mapped pinned staging and one CUDA graph per token count
- * (a kernel that reads x from the staging, the forward's kernels, a kernel that writes y and the
- * status word back), captured on the handle's stream on the first call with that count and
- * launched on `stream`; larger batches, and tiered layers, copy directly.  Returns COLI_ETIMEOUT
- * (and clears it, as coli_moe_status does) when a bounded device wait of this forward gave up;
- * y_host is then undefined. */
+ * y_host [T,d] and returns once y_host holds the result; any host memory (pageable or pinned).
+ * Batches of up to 8 tokens go through the handle's own mapped pinned staging and one CUDA graph
+ * per token count (a kernel that reads x from the staging, the forward's kernels, a kernel that
+ * writes y and the status word back and then raises a completion counter in the staging),
+ * captured on the handle's stream on the first call with that count and launched on `stream`;
+ * the call waits by polling that counter (falling back to synchronising `stream` after a
+ * second), so on return the graph's last kernel may still be exiting on `stream` -- later work
+ * on `stream` is ordered after it as usual, and other streams must synchronise with `stream`
+ * before relying on the call's device-side effects.  Larger batches, and tiered layers, copy
+ * directly and synchronise `stream`.  Returns COLI_ETIMEOUT (and clears it, as coli_moe_status
+ * does) when a bounded device wait of this forward gave up; y_host is then undefined. */
 int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host, void* stream);
 
 /* Runs n_layers has_norm layers in sequence on x_dev [T,d] in place:

@@ -156,6 +156,9 @@ cudaError_t launch_quantize_i4_rows(const float* w, int64_t rows, int cols, uint
 cudaError_t launch_quantize_q8(const float* x, int64_t n, int8_t* q, float* d,
                                cudaStream_t stream);
 // host-buffer forwards: n floats (a multiple of 4) from / to mapped pinned host memory
+// the host-buffer forward's staging tail: word 0 = the status word, word kHostDoneWord = a
+// completion counter the last kernel of each call raises by one
+constexpr int kHostDoneWord = 4;
 cudaError_t launch_host_in(const float* hx, float* dx, int n, cudaStream_t stream);
 cudaError_t launch_host_out(const float* dy, float* hy, int n, const int* status, int* hstatus,
                             cudaStream_t stream);

@@ -243,14 +243,21 @@ __global__ void __launch_bounds__(256) host_in_kernel(const float4* __restrict__
   if (i < n4) dx[i] = __ldcv(hx + i);
 }
 
-__global__ void __launch_bounds__(256) host_out_kernel(const float4* __restrict__ dy,
-                                                       float4* __restrict__ hy, int n4,
-                                                       const int* __restrict__ status,
-                                                       int* __restrict__ hstatus) {
+// One CTA: y and the status word, then the completion counter (hstatus[kHostDoneWord]) one up,
+// after every thread's writes are ordered before it at system scope; the host polls it.
+__global__ void __launch_bounds__(1024) host_out_kernel(const float4* __restrict__ dy,
+                                                        float4* __restrict__ hy, int n4,
+                                                        const int* __restrict__ status,
+                                                        int* __restrict__ hstatus) {
   griddep_wait();  // a programmatic dependent of the forward's last grid
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n4) __stwt(hy + i, __ldcg(dy + i));
-  if (i == 0) __stwt(hstatus, __ldcg(status));
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) __stwt(hy + i, __ldcg(dy + i));
+  if (threadIdx.x == 0) __stwt(hstatus, __ldcg(status));
+  __threadfence_system();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* done = hstatus + kHostDoneWord;
+    *done = *done + 1;
+  }
 }
 
 cudaError_t launch_host_in(const float* hx, float* dx, int n, cudaStream_t stream) {
@@ -264,8 +271,8 @@ cudaError_t launch_host_out(const float* dy, float* hy, int n, const int* status
                             cudaStream_t stream) {
   const int n4 = n / 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n4 + 255) / 256);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

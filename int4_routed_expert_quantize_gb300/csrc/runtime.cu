@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <chrono>
 #include <cmath>
 #include <mutex>
 #include <new>
@@ -32,7 +33,8 @@ struct coli_moe {
   // one instantiated graph per token count (copy in, the forward's kernels, copy out, status)
   float* pin_x = nullptr;          // host addresses
   float* pin_y = nullptr;
-  int32_t* pin_status = nullptr;
+  int32_t* pin_status = nullptr;    // [0] status word, [kHostDoneWord] completion counter
+  int32_t host_done = 0;             // the counter's value after the last completed call
   float* map_x = nullptr;          // the same memory as the device addresses it
   float* map_y = nullptr;
   int32_t* map_status = nullptr;
@@ -95,6 +97,9 @@ int dalloc(coli_moe* h, T** p, size_t bytes) {
 }
 
 void drop_host_graphs(coli_moe* h) {
+  bool any = false;
+  for (cudaGraphExec_t g : h->host_graph) any = any || g;
+  if (any) cudaDeviceSynchronize();  // a call may still be finishing its last kernel
   for (cudaGraphExec_t& g : h->host_graph)
     if (g) {
       cudaGraphExecDestroy(g);
@@ -607,6 +612,8 @@ int coli_moe_create(const coli_moe_config* cfg, coli_moe** out) {
       h->pin_y = h->pin_x + n;
       h->pin_status = reinterpret_cast<int32_t*>(h->pin_y + n);
       *h->pin_status = 0;
+      h->pin_status[kHostDoneWord] = 0;
+      h->host_done = 0;
       if (cudaHostGetDevicePointer(&q, p, 0) != cudaSuccess ||
           cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
         cudaGetLastError();
@@ -811,8 +818,26 @@ int coli_moe_forward_host(coli_moe* h, const float* x_host, int T, float* y_host
     rc = host_graph_for(h, T, dx, dy);
     if (rc) return rc;
     memcpy(h->pin_x, x_host, sizeof(float) * n);
-    if (cudaGraphLaunch(h->host_graph[T], st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
-      return COLI_ECUDA;
+    if (cudaGraphLaunch(h->host_graph[T], st) != cudaSuccess) return COLI_ECUDA;
+    // the graph's last kernel writes y and the status word, then raises the completion counter:
+    // poll it (an acquire load, so y is read after it) instead of a stream synchronisation; past
+    // a second, or on any mismatch, fall back to the synchronisation and resume from the counter
+    const int32_t want = h->host_done + 1;
+    const auto t0 = std::chrono::steady_clock::now();
+    bool seen = false;
+    for (uint32_t it = 1;; ++it) {
+      if (__atomic_load_n(h->pin_status + kHostDoneWord, __ATOMIC_ACQUIRE) == want) {
+        seen = true;
+        break;
+      }
+      if ((it & 1023u) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::seconds(1)) break;
+    }
+    if (!seen) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return COLI_ECUDA;
+      h->host_done = __atomic_load_n(h->pin_status + kHostDoneWord, __ATOMIC_ACQUIRE);
+    } else {
+      h->host_done = want;
+    }
     memcpy(y_host, h->pin_y, sizeof(float) * n);
     // a bounded device wait that gave up leaves y undefined: report it (and clear it) here
     return *h->pin_status == COLI_OK ? COLI_OK : coli_moe_status(h, stream);
