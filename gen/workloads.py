@@ -76,6 +76,12 @@ WORKLOADS = {
     # the GLM layer's shapes with 32 routed experts: the same kernels and per-step bytes
     # (9 experts, 170 MB, more than L2) with 0.6 GB resident, for counter captures
     "glm_e32_decode_t1": Workload("glm_e32_decode_t1", d=6144, f=2048, E=32, K=8, n_shared=1, T=1),
+    "glm_e32_stack2_t1": Workload("glm_e32_stack2_t1", d=6144, f=2048, E=32, K=8, n_shared=1, T=1,
+                                  layers=2, has_norm=True),
+    "glm_e32_i8_decode_t1": Workload("glm_e32_i8_decode_t1", d=6144, f=2048, E=32, K=8, n_shared=1,
+                                     T=1, wbits=8),
+    "glm_e32_i2_decode_t1": Workload("glm_e32_i2_decode_t1", d=6144, f=2048, E=32, K=8, n_shared=1,
+                                     T=1, wbits=2),
     "glm_e32_verify_t4": Workload("glm_e32_verify_t4", d=6144, f=2048, E=32, K=8, n_shared=1, T=4,
                                   bias="overlap"),
     # 256 tokens (the batched tensor-core path), zipf selection: ~33 union experts, 0.4 GB of
