@@ -549,7 +549,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// the driver's tensor-map encoder, looked up through the runtime (no link against libcuda)
+// the CUDA driver API's tensor-map encoder, looked up through the runtime (no link against libcuda)
 static EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
