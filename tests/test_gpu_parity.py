@@ -279,4 +279,12 @@ def test_glm_verify_t4_union(glm):
     sizes = np.diff(offs)
     assert (sizes[:-1] == 4).sum() >= 4  # biased experts shared by all tokens
     assert nu - 1 < 4 * wl.K  # union smaller than the pair count
+    # the production kernel instances (the ones the verify benchmark times) on further batches
+    for token0 in (4, 64, 400):
+        x = W.x_host(wl, 4, token0)
+        y = to_np(L.forward(torch.from_numpy(x).cuda()))
+        ref = OL.forward(x, want_dump=False)
+        assert np.array_equal(y, ref["y"]), token0
+        assert normwise_rel(y, ref["y64"]) <= TOL
+    assert L.status() == 0
     L.close()
