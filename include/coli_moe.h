@@ -174,7 +174,7 @@ int coli_moe_status(coli_moe* h, void* stream);
 /* Batches of at least min_tokens tokens (min_tokens >= 2) take the batched tensor-core path
  * (when the handle has it: max_tokens > 8); smaller batches run the decode kernels, in one union
  * pass of up to 8 tokens or in chunks of 8.  Both give the same result for every token.  The
- * default, 256, is where the two cost about the same on the GLM-shaped layer.  EINVAL:
+ * default, 128, is where the two cost about the same on the GLM-shaped layer.  EINVAL:
  * min_tokens < 2. */
 int coli_moe_set_prefill_min(coli_moe* h, int min_tokens);
 
@@ -192,7 +192,7 @@ int coli_moe_inject_fault(coli_moe* h, int fault);
  * token when the expert half runs as one fused kernel (router, then gate/up + down), 3 per
  * chunk of at most 8 tokens on the decode path (router, gate/up, down; one union pass per
  * chunk), 8 on the batched tensor-core path (batches of at least the coli_moe_set_prefill_min
- * size, 256 by default).  Negative status on error (EINVAL: T < 1 or T > max_tokens). */
+ * size, 128 by default).  Negative status on error (EINVAL: T < 1 or T > max_tokens). */
 int coli_moe_launches(const coli_moe* h, int T);
 
 /* Bytes of one expert record in the canonical format (3*d*f/2 + 4*(2f+d)). */

@@ -23,7 +23,7 @@ constexpr int kMaxStages = 8;
 // Default batch size from which the tensor-core path is taken: below it the decode kernels in
 // chunks of 4 tokens are faster (measured on the GLM layer: 188 vs 1178 us at 5 tokens, 4.4 vs
 // 8.4 ms at 128, even at 256, 17.5 vs 9.1 ms at 512)
-constexpr int kPrefillMinTokens = 256;
+constexpr int kPrefillMinTokens = 128;
 constexpr int kSmemLimit = 232448 - 1024;       // 227 KB per CTA minus room for static smem
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits give up after 2 s
 constexpr int kPrefillTileN = 32;               // pairs per tensor-core tile

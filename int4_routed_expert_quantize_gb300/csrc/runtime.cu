@@ -187,9 +187,9 @@ int run_decode(coli_moe* h, const float* x, int T, float* y, const coli_moe_dump
     if ((dbg.g || dbg.u) && !(dbg.g && dbg.u)) return COLI_EINVAL;
     if ((dbg.Ag || dbg.Au) && !(dbg.Ag && dbg.Au)) return COLI_EINVAL;
   }
-  // route (ordinary launch) -> gate/up -> down, or for one token route -> the fused expert
-  // kernel; the expert kernels are programmatic dependents that prefetch weights before
-  // waiting, unless events are recorded between the launches (with the fused kernel the
+  // route -> gate/up -> down, or for one token route -> the fused expert kernel; every launch
+  // after the first is a programmatic dependent that prefetches weights before waiting (the
+  // router itself waits for the preceding grid before it reads anything), unless events are recorded between the launches (with the fused kernel the
   // events bracket route | fused | nothing)
   const bool pdl = (ev == nullptr);
   cudaError_t e = ev ? cudaEventRecord(ev[0], stream) : cudaSuccess;
