@@ -6,19 +6,19 @@
 // so the int8 x int4 products run as kind::f16 with bf16 operands holding the exact integers
 // (|code| <= 127, products <= 1016, a 32-term block sum < 2^24: every partial is exact in the
 // f32 accumulator).  Each K-block of 32 (one activation scale) gets accumulator columns of its
-// own (a block-diagonal activation operand, below), so the epilogue sees the exact int32 block
-// dot and applies the canonical fp32 order of the decode path: an fma chain over
+// own (its two MMAs write only those, below), so the epilogue sees the exact int32 block dot
+// and applies the canonical fp32 order of the decode path: an fma chain over
 // the blocks of each of 32 contiguous groups (registers) and the pairwise tree over the groups
 // (a 5-level stack kept in TMEM columns).  Results are therefore bit-identical to the decode
 // kernels and the CPU oracle ("colibrì 架构概述" §5 gate/up/SiLU/down; README batch union).
 //
 // CTA: 15 warps, one tile (128 weight rows x 32 pairs) at a time, persistent over tiles:
 //   warp 0      bulk-tensor copies of raw int4 weight groups (HBM stream)
-//   warp 1      bulk-tensor copies of the bf16 activation blocks of each burst of 4 blocks, on
-//               the diagonal of a zeroed operand (completing on the same barrier as the
-//               converted weights, so the MMA issuer waits once)
-//   warp 2      TMEM owner and single MMA issuer (8 x K16 MMAs and one commit per burst, two
-//               accumulator buffers)
+//   warp 1      bulk-tensor copies of each burst's activation codes (bf16): two boxes of 64 K x
+//               32 pairs with 128-byte swizzle
+//   warp 2      TMEM owner (512 columns: two accumulator buffers, the tree stack) and the single
+//               MMA issuer: per burst 8 MMAs (K = 16, N = 32 per block) and two commits (operand
+//               stage free; accumulator ready)
 //   warps 3-6   int4 -> bf16 conversion of the weight blocks into the MMA's shared layout
 //   warps 7-14  epilogue: TMEM -> registers, block scales, canonical sums, SwiGLU / outputs
 //               (warp w: TMEM lanes 32*(w%4).., 16 of the tile's 32 pairs)
@@ -179,11 +179,10 @@ __device__ __forceinline__ void int4_chunk_to_bf16(const uint4 c, uint4 (&out)[4
   }
 
 // One tile = 128 weight rows x 32 pairs of one union slot, its K range walked in bursts of 4
-// blocks of 32.  A burst is 8 MMAs (K = 16 each, M = 128, N = 128) into one accumulator: the
-// activation operand is block-diagonal -- column (b, p) holds pair p's codes in the K rows of
-// block b and zeros elsewhere -- so column (b, p) of the accumulator is the exact block dot of
-// block b and pair p.  One commit per burst both frees the burst's operand stage and hands its
-// accumulator to the epilogue.
+// blocks of 32.  A burst is 8 MMAs (K = 16 each, M = 128, N = 32) into one accumulator buffer of
+// 128 columns: block j of the burst accumulates into columns 32j..32j+31 only, so column
+// (j, p) holds the exact int32 dot of block j with pair p.  After the burst one commit frees its
+// operand stage and another hands the accumulator to the epilogue.
 template <bool kDown>
 __global__ void __launch_bounds__(kPfThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
